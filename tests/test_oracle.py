@@ -1,0 +1,313 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks one step of the oracle against something independent:
+numpy's float16 casts (a library routine), hand-packed words, hand-derived
+worked examples, closed forms, brute-force sums, and invariants of the
+method (trivial g_idx == no g_idx; act-order is a row permutation).  A few
+tests plant a plausible mistake (a dropped "+1", a reversed nibble order) in
+a copy of the oracle's inputs and check that the tolerance catches it.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers
+
+def pack_rows(q: np.ndarray) -> np.ndarray:
+    """Test-side packer: q [K, N] codes -> [K/8, N] int32, code 8i+r in bits 4r..4r+3."""
+    K, N = q.shape
+    words = np.zeros((K // 8, N), np.uint64)
+    for r in range(8):
+        words |= q[r::8, :].astype(np.uint64) << np.uint64(4 * r)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def pack_cols(z: np.ndarray) -> np.ndarray:
+    """Test-side packer: z [G, N] codes -> [G, N/8] int32, code 8j+r in bits 4r..4r+3."""
+    G, N = z.shape
+    words = np.zeros((G, N // 8), np.uint64)
+    for r in range(8):
+        words |= z[:, r::8].astype(np.uint64) << np.uint64(4 * r)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def h(v) -> np.ndarray:
+    return np.asarray(v, np.float16)
+
+
+# ------------------------------------------------------------------- fp16
+
+def test_half_to_double_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = oracle.half_bits_to_f64(bits)
+    lib = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], lib[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(mine[~nan]), np.signbit(lib[~nan]))
+
+
+def test_double_to_half_matches_numpy_rounding():
+    g = np.random.default_rng(1234)
+    vals = [g.standard_normal(200000) * 10.0 ** g.uniform(-9, 5, 200000)]
+    # every fp16 value, the midpoints between neighbours (ties) and points
+    # just either side of them
+    allh = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    finite = np.sort(allh[np.isfinite(allh)])
+    mid = (finite[:-1] + finite[1:]) / 2.0
+    vals += [finite, mid, np.nextafter(mid, np.inf), np.nextafter(mid, -np.inf)]
+    # overflow edge and tiny subnormals
+    vals.append(np.array([65504.0, 65519.0, 65519.999, 65520.0, 65536.0, 1e6, -65520.0,
+                          2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26,
+                          2.0 ** -14, 2.0 ** -14 - 2.0 ** -25, 0.0, -0.0, np.inf, -np.inf]))
+    v = np.concatenate(vals)
+    mine = oracle.f64_to_half_bits(v)
+    with np.errstate(over="ignore"):
+        lib = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(mine, lib)
+
+
+def test_double_to_half_nan():
+    out = oracle.f64_to_half_bits(np.array([np.nan]))
+    assert np.isnan(out.view(np.float16)[0])
+
+
+# ----------------------------------------------------------------- unpack
+
+def _golden_words():
+    rows = []
+    with open(os.path.join(GOLDEN, "unpack_words.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            rows.append((int(parts[0], 16), [int(p) for p in parts[1:]]))
+    return rows
+
+
+@pytest.mark.parametrize("word,codes", _golden_words())
+def test_unpack_hand_packed_words(word, codes):
+    w = np.array([word], np.uint32).view(np.int32)
+    # qweight: one word per column, the eight codes run down K
+    q = oracle.unpack_qweight(np.tile(w, (1, 8)).reshape(1, 8), 8, 8)
+    assert q[:, 0].tolist() == codes
+    assert (q == q[:, :1]).all()
+    # qzeros: the eight codes run along N
+    z = oracle.unpack_qzeros(w.reshape(1, 1), 1, 8)
+    assert z[0].tolist() == codes
+
+
+def test_unpack_round_trip_all_values_all_positions():
+    g = np.random.default_rng(5)
+    K, N, G = 64, 48, 4
+    q = g.integers(0, 16, size=(K, N)).astype(np.uint8)
+    q[:16, 0] = np.arange(16)            # every value ...
+    for r in range(8):                   # ... at every nibble position
+        q[r::8, 1] = (np.arange(K // 8) + r) % 16
+    z = g.integers(0, 16, size=(G, N)).astype(np.uint8)
+    z[0, :16] = np.arange(16)
+    assert np.array_equal(oracle.unpack_qweight(pack_rows(q), K, N), q)
+    assert np.array_equal(oracle.unpack_qzeros(pack_cols(z), G, N), z)
+
+
+# ----------------------------------------------------------- group map
+
+def test_row_groups_trivial_and_errors():
+    gr, G = oracle.row_groups(None, 256, 64)
+    assert G == 4 and np.array_equal(gr, np.arange(256) // 64)
+    gr, G = oracle.row_groups(None, 256, -1)
+    assert G == 1 and not gr.any()
+    with pytest.raises(ValueError):
+        oracle.row_groups(None, 256, 48)          # does not divide K
+    with pytest.raises(ValueError):
+        oracle.row_groups(None, 256, 0)
+    bad = np.arange(256, dtype=np.int32) // 64
+    bad[7] = 4
+    with pytest.raises(ValueError):
+        oracle.row_groups(bad, 256, 64)
+    bad[7] = -1
+    with pytest.raises(ValueError):
+        oracle.row_groups(bad, 256, 64)
+
+
+# ---------------------------------------------------------------- dequant
+
+def test_dequant_unit_scale_is_exact_integer():
+    g = np.random.default_rng(7)
+    K, N = 32, 16
+    q = g.integers(0, 16, (K, N)).astype(np.uint8)
+    z = g.integers(0, 16, (1, N)).astype(np.uint8)
+    s = np.ones((1, N), np.float16).view(np.uint16)
+    w16, w64 = oracle.dequant(q, z, s, np.zeros(K, np.int32), K, N)
+    expect = q.astype(np.int64) - z.astype(np.int64) - 1
+    assert np.array_equal(w64, expect.astype(np.float64))
+    assert np.array_equal(w16.view(np.float16).astype(np.float64), expect.astype(np.float64))
+
+
+def test_dequant_power_of_two_scale_and_numpy_cast():
+    g = np.random.default_rng(8)
+    K, N, G = 64, 32, 2
+    q = g.integers(0, 16, (K, N)).astype(np.uint8)
+    z = g.integers(0, 16, (G, N)).astype(np.uint8)
+    gr = (np.arange(K) // 32).astype(np.int32)
+    # powers of two scale exactly
+    s2 = (2.0 ** g.integers(-20, 3, (G, N))).astype(np.float16)
+    w16, w64 = oracle.dequant(q, z, s2.view(np.uint16), gr, K, N)
+    iq = q.astype(np.float64) - z[gr].astype(np.float64) - 1
+    assert np.array_equal(w64, s2.astype(np.float64)[gr] * iq)
+    # arbitrary fp16 scales: one rounding of the exact product, as numpy casts it
+    s = g.uniform(1e-4, 3.0, (G, N)).astype(np.float16)
+    w16, w64 = oracle.dequant(q, z, s.view(np.uint16), gr, K, N)
+    exact = s.astype(np.float64)[gr] * iq
+    assert np.array_equal(w64, exact)
+    assert np.array_equal(w16, exact.astype(np.float16).view(np.uint16))
+
+
+# --------------------------------------------------------------- products
+
+def test_linear_matches_numpy_matmul():
+    g = np.random.default_rng(9)
+    M, K, N = 5, 96, 40
+    x = g.standard_normal((M, K))
+    w = g.standard_normal((K, N))
+    b = g.standard_normal(N)
+    y = oracle.linear_f64(x, w, b, nthreads=3)
+    ref = x @ w + b
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(x).sum() * np.abs(w).max())
+
+
+def test_linear_brute_force_tiny():
+    g = np.random.default_rng(10)
+    M, K, N = 3, 16, 8
+    x = g.standard_normal((M, K))
+    w = g.standard_normal((K, N))
+    b = g.standard_normal(N)
+    y = oracle.linear_f64(x, w, b, nthreads=2)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):            # ascending k, then bias
+                acc += x[m, k] * w[k, n]
+            acc += b[n]
+            assert y[m, n] == acc         # same order, so bitwise equal
+
+
+def test_one_hot_x_selects_dequantized_row():
+    layer = synthetic.make_layer(128, 64, 32, bias=True, key=(11,))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, None, 128, 64, 32)
+    for k in (0, 1, 31, 32, 77, 127):
+        x = np.zeros((1, 128), np.float16)
+        x[0, k] = 1.0
+        y = oracle.reference_output(x, dq, layer.bias)
+        expect = dq.w16.view(np.float16).astype(np.float64)[k] + layer.bias.astype(np.float64)
+        assert np.array_equal(y[0], expect)
+
+
+def test_closed_form_all_equal_codes():
+    K, N, c, z0 = 256, 16, 11, 4
+    q = np.full((K, N), c, np.uint8)
+    z = np.full((2, N), z0, np.uint8)
+    g = np.random.default_rng(12)
+    # dyadic x so every partial sum is exact in fp64
+    x = (g.integers(-64, 64, (3, K)) / 16.0).astype(np.float16)
+    bias = (g.integers(-8, 8, N) / 4.0).astype(np.float16)
+    dq = oracle.dequantize_layer(pack_rows(q), pack_cols(z), np.ones((2, N), np.float16),
+                                 None, K, N, 128)
+    y = oracle.reference_output(x, dq, bias)
+    expect = (c - z0 - 1) * x.astype(np.float64).sum(axis=1, keepdims=True) + bias.astype(np.float64)
+    assert np.array_equal(y, expect)
+
+
+def test_golden_worked_examples():
+    with open(os.path.join(GOLDEN, "worked_examples.json")) as f:
+        spec = json.load(f)
+    for case in spec["cases"]:
+        def arr(key, dt):
+            v = case[key]
+            return None if v is None else np.array([[int(s, 16) for s in row] for row in v] if isinstance(v[0], list)
+                                                    else [int(s, 16) for s in v], dtype=np.uint64)
+        K, N, gs = case["K"], case["N"], case["groupsize"]
+        qw = arr("qweight_hex", None).astype(np.uint32).view(np.int32)
+        qz = arr("qzeros_hex", None).astype(np.uint32).view(np.int32)
+        sc = arr("scales_fp16_hex", None).astype(np.uint16)
+        xb = arr("x_fp16_hex", None).astype(np.uint16)
+        bb = case["bias_fp16_hex"]
+        bias = None if bb is None else np.array([int(s, 16) for s in bb], np.uint16)
+        gidx = None if "g_idx" not in case else np.array(case["g_idx"], np.int32)
+        dq = oracle.dequantize_layer(qw, qz, sc, gidx, K, N, gs)
+        assert [int(v) for v in dq.w16[0]] == [int(s, 16) for s in case["w16_row0_hex"]]
+        y = oracle.reference_output(xb, dq, bias)
+        assert np.array_equal(y, np.array(case["y"], np.float64)), case["comment"]
+
+
+# ---------------------------------------------------------------- g_idx
+
+def test_trivial_gidx_equals_none():
+    layer = synthetic.make_layer(256, 64, 64, key=(13,))
+    x = synthetic.activations(4, 256, key=(13, 4))
+    gi = (np.arange(256) // 64).astype(np.int32)
+    a = oracle.linear_layer(layer.qweight, layer.qzeros, layer.scales, None, None, x, 256, 64, 64)
+    b = oracle.linear_layer(layer.qweight, layer.qzeros, layer.scales, gi, None, x, 256, 64, 64)
+    assert np.array_equal(a[0].w16, b[0].w16)
+    assert np.array_equal(a[1], b[1])
+
+
+def test_act_order_is_a_row_permutation():
+    """y(x, W, g_idx) == y(x[:, P], W[P, :], g_idx[P]); with g_idx[P] sorted
+    this is the plain grouped layer on the permuted operands."""
+    K, N, gs = 256, 32, 64
+    layer = synthetic.make_layer(K, N, gs, act_order=True, key=(14,))
+    x = synthetic.activations(3, K, key=(14, 3))
+    q = oracle.unpack_qweight(layer.qweight, K, N)
+    P = np.argsort(layer.g_idx, kind="stable")
+    assert np.array_equal(layer.g_idx[P], np.arange(K) // gs)
+    dq_a, y_a, _, _ = oracle.linear_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx,
+                                          None, x, K, N, gs)
+    dq_b, y_b, _, _ = oracle.linear_layer(pack_rows(q[P]), layer.qzeros, layer.scales, None,
+                                          None, np.ascontiguousarray(x[:, P]), K, N, gs)
+    assert np.array_equal(dq_a.w16[P], dq_b.w16)
+    assert np.allclose(y_a, y_b, rtol=1e-12, atol=1e-12 * np.abs(y_a).max())
+
+
+# ------------------------------------------------------------ tolerance
+
+def test_single_layer_reference_within_tolerance_of_exact():
+    layer, x = synthetic.single_layer()
+    dq, y_ref, y_exact, tol = oracle.linear_layer(layer.qweight, layer.qzeros, layer.scales, None,
+                                                  None, x, 1024, 1024, 128)
+    assert np.all(np.abs(y_ref - y_exact) <= tol)
+    assert np.all(tol > 0)
+
+
+def test_tolerance_catches_planted_mistakes():
+    """Plant two plausible errors in the oracle's inputs and make sure the
+    stated tolerance rejects them: dropping the +1 on the zero point, and
+    reading the nibbles high-first."""
+    K, N, gs = 1024, 256, 128
+    layer = synthetic.make_layer(K, N, gs, key=(15,))
+    x = synthetic.activations(2, K, key=(15, 2))
+    dq, y_ref, _, tol = oracle.linear_layer(layer.qweight, layer.qzeros, layer.scales, None,
+                                            None, x, K, N, gs)
+    # (a) no +1: equivalent to an effective zero one smaller
+    z = oracle.unpack_qzeros(layer.qzeros, dq.G, N).astype(np.int64)
+    # z - 1 would go negative for z = 0: emulate through the weights instead
+    w_wrong = dq.w64 + layer.scales.astype(np.float64)[dq.gr]
+    y_wrong = oracle.linear_f64(oracle.half_bits_to_f64(x.view(np.uint16)), w_wrong)
+    assert np.any(np.abs(y_wrong - y_ref) > tol)
+    # (b) nibbles read high-first
+    q = oracle.unpack_qweight(layer.qweight, K, N)
+    q_rev = q.reshape(K // 8, 8, N)[:, ::-1, :].reshape(K, N)
+    dq_rev = oracle.dequantize_layer(pack_rows(q_rev), layer.qzeros, layer.scales, None, K, N, gs)
+    y_rev = oracle.reference_output(x, dq_rev)
+    assert np.any(np.abs(y_rev - y_ref) > tol)
+    del z
