@@ -1,0 +1,370 @@
+"""Benchmark of the fused GPTQ W4A16 linear layer on one GB300 (or N replicas).
+
+Workload (decode_7b): Llama-7B-shaped projection layers (K,N) in
+{(4096,4096), (4096,11008), (11008,4096), (4096,12288)}, groupsize 128,
+trivial g_idx, fp16 bias, x ~ N(0,1) fp16, with M in {1,2,4,8} rows.  One
+step runs every (shape, M) case once on each of R weight replicas, so that a
+weight set is touched once per step and the per-step working set (R * 81.7 MB)
+is several times the 129 MB L2: every call streams its weights from HBM.
+
+Metric: effective HBM bandwidth of decode, algorithmic bytes (qweight +
+qzeros + scales as stored) per second, whole job.  Also reported: the
+decode kernel's roofline fraction (per-launch CUDA events), the end-to-end
+figure through the C ABI with host buffers, the CPU oracle timed on this
+host, SM clocks during the run, and the prefill_7b tensor-core numbers.
+
+--impl reference times the CPU oracle (the plain dequantize-then-matmul
+route) on the same workload, one shape per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "W4A16 GEMM: decode eff. HBM TB/s (% roofline), prefill TFLOPS (% FP16 peak)"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--replicas", type=int, default=8)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--soak-s", type=float, default=1.0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The CPU oracle on the decode_7b workload: one shape (all four M) per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    shapes = synthetic.DECODE_7B_SHAPES
+    layers = {s: synthetic.workload_layer("decode_7b", s[0], s[1], 128, False) for s in shapes}
+    xs = {(s, M): synthetic.workload_x("decode_7b", s[0], s[1], 128, False, M) for s in shapes
+          for M in synthetic.DECODE_7B_M}
+
+    def step(i):
+        s = shapes[i % len(shapes)]
+        L = layers[s]
+        dq = oracle.dequantize_layer(L.qweight, L.qzeros, L.scales, None, s[0], s[1], 128)
+        for M in synthetic.DECODE_7B_M:
+            oracle.reference_output(xs[(s, M)], dq, L.bias, nthreads=cores)
+        return L.weight_bytes * len(synthetic.DECODE_7B_M)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode_7b", "shapes": [list(s) for s in shapes], "M": synthetic.DECODE_7B_M,
+                   "groupsize": 128, "step": "one shape, all four M, dequantize once then fp64 products"},
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: one decode_7b shape, all four M (shapes in turn)"},
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_sample(budget_s: float = 25.0):
+    """The oracle as it stands on the decode_7b cases, shape by shape, within a time budget."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    nbytes, ncases, shapes_done = 0, 0, []
+    for (K, N) in synthetic.DECODE_7B_SHAPES:
+        L = synthetic.workload_layer("decode_7b", K, N, 128, False)
+        dq = oracle.dequantize_layer(L.qweight, L.qzeros, L.scales, None, K, N, 128)
+        for M in synthetic.DECODE_7B_M:
+            x = synthetic.workload_x("decode_7b", K, N, 128, False, M)
+            oracle.reference_output(x, dq, L.bias, nthreads=cores)
+            nbytes += L.weight_bytes
+            ncases += 1
+        shapes_done.append([K, N])
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{ncases} decode_7b cases (shapes {shapes_done}, M 1/2/4/8; dequantize once per shape, "
+                      f"fp64 products on {cores} threads), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ native
+
+def run_native(args):
+    import torch
+
+    import gptq_bit_weight_gb300 as q4
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
+
+    shapes = synthetic.DECODE_7B_SHAPES
+    Ms = synthetic.DECODE_7B_M
+    R = args.replicas
+    mats, wbytes = {}, {}
+    for (K, N) in shapes:
+        L = synthetic.workload_layer("decode_7b", K, N, 128, False)
+        qw = torch.from_numpy(L.qweight).to(dev)
+        qz = torch.from_numpy(L.qzeros).to(dev)
+        sc = torch.from_numpy(L.scales).to(dev)
+        b = torch.from_numpy(L.bias).to(dev)
+        mats[(K, N)] = [q4.Q4Matrix(qw, qz, sc, None, b, 128) for _ in range(R)]
+        for m in mats[(K, N)]:
+            m.reserve(max(Ms))
+        wbytes[(K, N)] = L.weight_bytes
+        del qw, qz, sc
+    xs = {(s, M): torch.from_numpy(synthetic.workload_x("decode_7b", s[0], s[1], 128, False, M)).to(dev)
+          for s in shapes for M in Ms}
+    outs = {(s, M): torch.empty((M, s[1]), dtype=torch.float16, device=dev) for s in shapes for M in Ms}
+    calls = [(s, M, r) for r in range(R) for M in Ms for s in shapes]
+    step_bytes = sum(wbytes[s] for (s, M, r) in calls)
+    assert R * sum(wbytes.values()) > 2 * L2_BYTES
+
+    def step():
+        for (s, M, r) in calls:
+            q4.gptq_q4_matmul(mats[s][r].handle, xs[(s, M)].data_ptr(), M, outs[(s, M)].data_ptr(), sptr)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        import torch.distributed as dist
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    with ClockSampler(local) as clk:
+        t_end = time.perf_counter() + args.soak_s
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        while time.perf_counter() < t_end:      # clock soak: more untimed warm-up
+            step()
+            torch.cuda.synchronize()
+        # ---- timed region: exactly K steps
+        barrier()
+        n0 = q4.gptq_q4_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+        launches = q4.gptq_q4_launch_count() - n0
+        ms = max_over_ranks(e0.elapsed_time(e1))
+        # ---- per-launch durations of the decode kernel (same steps, events around each call)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+        per_call = []
+        for _ in range(max(1, min(args.steps, 5))):
+            for (s, M, r), (a, b) in zip(calls, evs):
+                a.record(stream)
+                q4.gptq_q4_matmul(mats[s][r].handle, xs[(s, M)].data_ptr(), M, outs[(s, M)].data_ptr(), sptr)
+                b.record(stream)
+            torch.cuda.synchronize()
+            per_call.append([a.elapsed_time(b) for (a, b) in evs])
+    clocks = clk.summary()
+
+    value = step_bytes * args.steps * world / (ms * 1e-3) / 1e12
+    kern_ms = float(np.sum(np.median(np.array(per_call), axis=0)))
+    achieved_gbs = step_bytes / (kern_ms * 1e-3) / 1e9
+    launches_per_step = len(calls)
+
+    # per-case figures (median over repetitions) for the record
+    med = np.median(np.array(per_call), axis=0)
+    per_case = {}
+    for (s, M, r), t in zip(calls, med):
+        per_case.setdefault(f"{s[0]}x{s[1]} M={M}", []).append(float(t))
+    per_case = {k: {"us": round(1e3 * float(np.median(v)), 2),
+                    "TB/s": round(wbytes[tuple(int(a) for a in k.split()[0].split('x'))] / (float(np.median(v)) * 1e-3) / 1e12, 3)}
+                for k, v in per_case.items()}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    ho = {k: torch.empty(v.shape, dtype=torch.float16).pin_memory() for k, v in outs.items()}
+    dx = {k: torch.empty_like(v) for k, v in xs.items()}
+    h2d = sum(hx[(s, M)].numel() * 2 for (s, M, r) in calls)
+    d2h = sum(ho[(s, M)].numel() * 2 for (s, M, r) in calls)
+
+    def e2e_step():
+        for (s, M, r) in calls:
+            dx[(s, M)].copy_(hx[(s, M)], non_blocking=True)
+            q4.gptq_q4_matmul(mats[s][r].handle, dx[(s, M)].data_ptr(), M, outs[(s, M)].data_ptr(), sptr)
+            ho[(s, M)].copy_(outs[(s, M)], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    barrier()
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e_value = step_bytes * args.steps * world / e2e_s / 1e12
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(q4, torch, dev, stream, bf16_tf, peak_src)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 x int4 -> f32 accumulate", "data": "synthetic",
+            "config": {"workload": "decode_7b", "shapes": [list(s) for s in shapes], "M": Ms, "groupsize": 128,
+                       "g_idx": "trivial", "bias": True, "replicas": R,
+                       "calls_per_step": launches_per_step,
+                       "l2": f"inputs larger than L2: {R} weight replicas, {R * sum(wbytes.values()) / 1e6:.0f} MB "
+                             f"per step vs 129 MB L2, each replica touched once per step",
+                       "bytes_per_step": step_bytes, "soak_s": args.soak_s,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved_gbs / hbm_gbs, "traffic": None,
+                         "kernel": "decode_kernel", "peak_source": peak_src,
+                         "how": "algorithmic bytes of all calls of a step / sum of per-call CUDA-event durations"},
+            "per_case": per_case,
+            "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if prefill:
+            line["prefill"] = prefill
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src):
+    """prefill_7b: M in {512, 2048} on the three 7B shapes, fused tensor-core path."""
+    return None
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,537 @@
+// C ABI of the fused GPTQ W4A16 linear layer: argument checks, the handle
+// (the Q4Matrix of "Implementation: Predibase Lorax GPTQ Exllama V1",
+// "Description"), act-order permutation, path selection and status
+// reporting.  Every failure returns a status with the specific reason kept
+// for gptq_q4_last_error ("Inference Backends", "Hardware, dependency, and
+// format requirements": validation errors keep their specific reason); there
+// is no fallback route.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/gptq_q4.h"
+#include "q4_internal.cuh"
+
+namespace q4 {
+cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
+                            uint16_t *out, int *status, cudaStream_t s);
+cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
+int prefill_default_min_m();
+}  // namespace q4
+
+struct gptq_q4_s {
+    int device = -1;
+    int K = 0, N = 0, groupsize = 0, geff = 0, G = 0;
+    int act_order = 0;
+    uint32_t *wp = nullptr;
+    uint32_t *s2 = nullptr;
+    uint32_t *zeros = nullptr;
+    int32_t *perm = nullptr;
+    uint16_t *bias = nullptr;
+    int *status = nullptr;
+    float *ws = nullptr;
+    size_t ws_floats = 0;
+    int *tickets = nullptr;
+    int n_tickets = 0;
+    uint16_t *temp_state = nullptr;
+    size_t temp_state_elems = 0;
+    int path = GPTQ_Q4_PATH_AUTO;
+    int prefill_min_m = 0;
+    size_t device_bytes = 0;
+};
+
+namespace {
+
+thread_local int t_status = GPTQ_Q4_OK;
+thread_local char t_msg[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+int set_status(int code, const char *fmt, ...) {
+    t_status = code;
+    if (fmt) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+        va_end(ap);
+    } else {
+        t_msg[0] = '\0';
+    }
+    return code;
+}
+
+int ok() { return set_status(GPTQ_Q4_OK, nullptr); }
+
+int cuda_fail(cudaError_t e, const char *what) {
+    cudaGetLastError();   // clear a sticky-free error so the next call starts clean
+    if (e == cudaErrorMemoryAllocation)
+        return set_status(GPTQ_Q4_OUT_OF_MEMORY, "%s: %s", what, cudaGetErrorString(e));
+    return set_status(GPTQ_Q4_CUDA_ERROR, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define Q4_CUDA(expr, what)                               \
+    do {                                                  \
+        cudaError_t e_ = (expr);                          \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device memory of the current device (or managed)?
+int check_device_ptr(const void *p, int dev, const char *name) {
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "%s is not a CUDA pointer", name);
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "%s is not device memory", name);
+    if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "%s lives on device %d, current device is %d", name,
+                          attr.device, dev);
+    return GPTQ_Q4_OK;
+}
+
+int check_device_sm103(int *dev_out) {
+    int dev = 0;
+    Q4_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    int major = 0, minor = 0;
+    Q4_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute");
+    Q4_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+        return set_status(GPTQ_Q4_UNSUPPORTED,
+                          "kernels are built for sm_103a only; device %d has compute capability %d.%d", dev,
+                          major, minor);
+    *dev_out = dev;
+    return GPTQ_Q4_OK;
+}
+
+template <typename T>
+int dev_alloc(T **p, size_t count, gptq_q4_s *h, const char *what) {
+    if (count == 0) {
+        *p = nullptr;
+        return GPTQ_Q4_OK;
+    }
+    void *v = nullptr;
+    cudaError_t e = cudaMalloc(&v, count * sizeof(T));
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    *p = static_cast<T *>(v);
+    if (h) h->device_bytes += count * sizeof(T);
+    return GPTQ_Q4_OK;
+}
+
+void release(gptq_q4_s *h) {
+    if (!h) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (h->device >= 0) cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    cudaFree(h->wp);
+    cudaFree(h->s2);
+    cudaFree(h->zeros);
+    cudaFree(h->perm);
+    cudaFree(h->bias);
+    cudaFree(h->status);
+    cudaFree(h->ws);
+    cudaFree(h->tickets);
+    cudaFree(h->temp_state);
+    if (cur >= 0) cudaSetDevice(cur);
+    delete h;
+}
+
+q4::HandleView view(const gptq_q4_s *h) {
+    q4::HandleView v{};
+    v.K = h->K;
+    v.N = h->N;
+    v.G = h->G;
+    v.geff = h->geff;
+    v.groupsize = h->groupsize;
+    v.wp = reinterpret_cast<const uint4 *>(h->wp);
+    v.s2 = h->s2;
+    v.zeros = h->zeros;
+    v.perm = h->act_order ? h->perm : nullptr;
+    v.bias = h->bias;
+    v.status = h->status;
+    return v;
+}
+
+int check_handle(gptq_q4_handle h) {
+    if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
+    int dev = -1;
+    Q4_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != h->device)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle was made on device %d, current device is %d",
+                          h->device, dev);
+    return GPTQ_Q4_OK;
+}
+
+// Grow the split-K workspace / tickets (stream-ordered when a stream is given).
+int ensure_decode_work(gptq_q4_s *h, size_t ws_floats, int n_tickets, cudaStream_t s, bool sync_alloc) {
+    if (ws_floats > h->ws_floats) {
+        if (h->ws) {
+            if (sync_alloc) cudaFree(h->ws);
+            else Q4_CUDA(cudaFreeAsync(h->ws, s), "cudaFreeAsync(workspace)");
+            h->device_bytes -= h->ws_floats * sizeof(float);
+            h->ws = nullptr;
+            h->ws_floats = 0;
+        }
+        void *v = nullptr;
+        cudaError_t e = sync_alloc ? cudaMalloc(&v, ws_floats * sizeof(float))
+                                   : cudaMallocAsync(&v, ws_floats * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e, "allocating split-K workspace");
+        h->ws = static_cast<float *>(v);
+        h->ws_floats = ws_floats;
+        h->device_bytes += ws_floats * sizeof(float);
+    }
+    if (n_tickets > h->n_tickets) {
+        if (h->tickets) {
+            if (sync_alloc) cudaFree(h->tickets);
+            else Q4_CUDA(cudaFreeAsync(h->tickets, s), "cudaFreeAsync(tickets)");
+            h->device_bytes -= static_cast<size_t>(h->n_tickets) * sizeof(int);
+            h->tickets = nullptr;
+            h->n_tickets = 0;
+        }
+        void *v = nullptr;
+        cudaError_t e = sync_alloc ? cudaMalloc(&v, n_tickets * sizeof(int))
+                                   : cudaMallocAsync(&v, n_tickets * sizeof(int), s);
+        if (e != cudaSuccess) return cuda_fail(e, "allocating split-K tickets");
+        h->tickets = static_cast<int *>(v);
+        h->n_tickets = n_tickets;
+        h->device_bytes += static_cast<size_t>(n_tickets) * sizeof(int);
+        if (sync_alloc) Q4_CUDA(cudaMemset(h->tickets, 0, n_tickets * sizeof(int)), "cudaMemset(tickets)");
+        else Q4_CUDA(cudaMemsetAsync(h->tickets, 0, n_tickets * sizeof(int), s), "cudaMemsetAsync(tickets)");
+    }
+    return GPTQ_Q4_OK;
+}
+
+int ensure_temp_state(gptq_q4_s *h, int M, cudaStream_t s, bool sync_alloc) {
+    const size_t need = static_cast<size_t>(M) * h->K;
+    if (!h->act_order || need <= h->temp_state_elems) return GPTQ_Q4_OK;
+    if (h->temp_state) {
+        if (sync_alloc) cudaFree(h->temp_state);
+        else Q4_CUDA(cudaFreeAsync(h->temp_state, s), "cudaFreeAsync(temp_state)");
+        h->device_bytes -= h->temp_state_elems * 2;
+        h->temp_state = nullptr;
+        h->temp_state_elems = 0;
+    }
+    void *v = nullptr;
+    cudaError_t e = sync_alloc ? cudaMalloc(&v, need * 2) : cudaMallocAsync(&v, need * 2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "allocating temp_state");
+    h->temp_state = static_cast<uint16_t *>(v);
+    h->temp_state_elems = need;
+    h->device_bytes += need * 2;
+    return GPTQ_Q4_OK;
+}
+
+int decode_max_ws_rows() { return 16; }
+
+}  // namespace
+
+extern "C" {
+
+gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                            const int32_t *g_idx, int K, int N, int groupsize) {
+    if (!qweight || !qzeros || !scales) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "qweight, qzeros and scales must not be NULL");
+        return nullptr;
+    }
+    if (K <= 0 || N <= 0 || K % 8 || N % 8) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "K=%d and N=%d must be positive multiples of 8 (eight codes per word)",
+                   K, N);
+        return nullptr;
+    }
+    if (!(groupsize == -1 || (groupsize > 0 && K % groupsize == 0))) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "groupsize=%d must be -1 or a positive divisor of K=%d", groupsize, K);
+        return nullptr;
+    }
+    const int geff = groupsize == -1 ? K : groupsize;
+    const int G = K / geff;
+    int dev = -1;
+    if (check_device_sm103(&dev) != GPTQ_Q4_OK) return nullptr;
+    if (check_device_ptr(qweight, dev, "qweight") || check_device_ptr(qzeros, dev, "qzeros") ||
+        check_device_ptr(scales, dev, "scales") || (g_idx && check_device_ptr(g_idx, dev, "g_idx")))
+        return nullptr;
+    if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, 2) || (g_idx && !aligned(g_idx, 4))) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "misaligned input pointer");
+        return nullptr;
+    }
+
+    // act-order: one stable argsort of g_idx (a counting sort by group keeps
+    // the original order inside each group), identity -> no act-order.
+    std::vector<int32_t> perm;
+    bool act = false;
+    if (g_idx) {
+        std::vector<int32_t> gi(K);
+        cudaError_t e = cudaMemcpy(gi.data(), g_idx, sizeof(int32_t) * K, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) {
+            cuda_fail(e, "copying g_idx to the host");
+            return nullptr;
+        }
+        std::vector<int> count(G + 1, 0);
+        for (int k = 0; k < K; ++k) {
+            if (gi[k] < 0 || gi[k] >= G) {
+                set_status(GPTQ_Q4_INVALID_ARGUMENT, "g_idx[%d]=%d is outside [0, %d)", k, gi[k], G);
+                return nullptr;
+            }
+            ++count[gi[k] + 1];
+        }
+        for (int g = 0; g < G; ++g) {
+            if (count[g + 1] != geff) {
+                set_status(GPTQ_Q4_UNSUPPORTED,
+                           "group %d holds %d rows; the GPU layout needs every group to hold exactly %d", g,
+                           count[g + 1], geff);
+                return nullptr;
+            }
+            count[g + 1] += count[g];
+        }
+        perm.resize(K);
+        for (int k = 0; k < K; ++k) perm[count[gi[k]]++] = k;
+        for (int k = 0; k < K; ++k)
+            if (perm[k] != k) {
+                act = true;
+                break;
+            }
+    }
+    if (K % 64 || N % 64 || geff % 32) {
+        set_status(GPTQ_Q4_UNSUPPORTED,
+                   "the GPU kernels need K %% 64 == 0, N %% 64 == 0 and a group size that is a multiple of 32 "
+                   "(K=%d N=%d group=%d)",
+                   K, N, geff);
+        return nullptr;
+    }
+
+    gptq_q4_s *h = new (std::nothrow) gptq_q4_s();
+    if (!h) {
+        set_status(GPTQ_Q4_OUT_OF_MEMORY, "host allocation of the handle failed");
+        return nullptr;
+    }
+    h->device = dev;
+    h->K = K;
+    h->N = N;
+    h->groupsize = groupsize;
+    h->geff = geff;
+    h->G = G;
+    h->act_order = act ? 1 : 0;
+    h->prefill_min_m = q4::prefill_default_min_m();
+
+    cudaStream_t s = nullptr;
+    auto fail = [&](int) -> gptq_q4_handle {
+        int code = t_status;
+        char msg[512];
+        std::memcpy(msg, t_msg, sizeof(msg));
+        if (s) cudaStreamDestroy(s);
+        release(h);
+        t_status = code;
+        std::memcpy(t_msg, msg, sizeof(msg));
+        return nullptr;
+    };
+    const size_t words = static_cast<size_t>(K / 8) * N;
+    if (dev_alloc(&h->wp, words, h, "allocating packed weights") ||
+        dev_alloc(&h->s2, static_cast<size_t>(G) * (N / 16) * 8, h, "allocating scales") ||
+        dev_alloc(&h->zeros, static_cast<size_t>(G) * (N / 8), h, "allocating zeros") ||
+        dev_alloc(&h->status, 1, h, "allocating status word") ||
+        (act && dev_alloc(&h->perm, static_cast<size_t>(K), h, "allocating permutation")))
+        return fail(0);
+    cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
+    if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), s)) != cudaSuccess) return fail(cuda_fail(e, "memset"));
+    if (act && (e = cudaMemcpyAsync(h->perm, perm.data(), sizeof(int32_t) * K, cudaMemcpyHostToDevice, s)) !=
+                   cudaSuccess)
+        return fail(cuda_fail(e, "copying the permutation"));
+    if ((e = cudaMemcpyAsync(h->zeros, qzeros, sizeof(uint32_t) * G * (N / 8), cudaMemcpyDeviceToDevice, s)) !=
+        cudaSuccess)
+        return fail(cuda_fail(e, "copying qzeros"));
+    if ((e = q4::launch_repack_codes(qweight, act ? h->perm : nullptr, K, N, h->wp, s)) != cudaSuccess)
+        return fail(cuda_fail(e, "repack launch"));
+    if ((e = q4::launch_repack_scales(scales, G, N, h->s2, s)) != cudaSuccess)
+        return fail(cuda_fail(e, "scale repack launch"));
+    g_launches += 2;
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(cuda_fail(e, "repack"));
+    cudaStreamDestroy(s);
+    s = nullptr;
+    const q4::DecodePlan p = q4::plan_decode(decode_max_ws_rows(), K, N);
+    if (ensure_decode_work(h, p.ws_floats, p.n_tickets, nullptr, true)) return fail(0);
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail(cuda_fail(e, "make"));
+    ok();
+    return h;
+}
+
+int gptq_q4_set_bias(gptq_q4_handle h, const uint16_t *bias) {
+    if (int r = check_handle(h)) return r;
+    if (!bias) {
+        cudaDeviceSynchronize();
+        cudaFree(h->bias);
+        if (h->bias) h->device_bytes -= static_cast<size_t>(h->N) * 2;
+        h->bias = nullptr;
+        return ok();
+    }
+    if (int r = check_device_ptr(bias, h->device, "bias")) return r;
+    if (!aligned(bias, 2)) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "misaligned bias");
+    if (!h->bias && dev_alloc(&h->bias, static_cast<size_t>(h->N), h, "allocating bias")) return t_status;
+    Q4_CUDA(cudaMemcpy(h->bias, bias, static_cast<size_t>(h->N) * 2, cudaMemcpyDeviceToDevice), "copying bias");
+    Q4_CUDA(cudaDeviceSynchronize(), "set_bias");
+    return ok();
+}
+
+int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
+    if (int r = check_handle(h)) return r;
+    if (max_m < 0) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "max_m=%d < 0", max_m);
+    Q4_CUDA(cudaDeviceSynchronize(), "reserve");
+    size_t ws = 0;
+    int nt = 0;
+    for (int m = 1; m <= std::min(max_m, 64); ++m) {
+        const q4::DecodePlan p = q4::plan_decode(m, h->K, h->N);
+        ws = std::max(ws, p.ws_floats);
+        nt = std::max(nt, p.n_tickets);
+    }
+    if (max_m > 64) {
+        const q4::DecodePlan p = q4::plan_decode(max_m, h->K, h->N);
+        ws = std::max(ws, p.ws_floats);
+        nt = std::max(nt, p.n_tickets);
+    }
+    if (int r = ensure_decode_work(h, ws, nt, nullptr, true)) return r;
+    if (int r = ensure_temp_state(h, max_m, nullptr, true)) return r;
+    Q4_CUDA(cudaDeviceSynchronize(), "reserve");
+    return ok();
+}
+
+static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out, cudaStream_t stream,
+                      int path) {
+    const uint16_t *xin = x;
+    if (h->act_order) {
+        if (int r = ensure_temp_state(h, M, stream, false)) return r;
+        Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->K, h->temp_state, stream), "xreorder launch");
+        ++g_launches;
+        xin = h->temp_state;
+    }
+    const q4::HandleView v = view(h);
+    if (path == GPTQ_Q4_PATH_PREFILL) {
+        Q4_CUDA(q4::launch_prefill(v, xin, M, out, stream), "prefill launch");
+        ++g_launches;
+        return ok();
+    }
+    const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N);
+    if (int r = ensure_decode_work(h, p.ws_floats, p.n_tickets, stream, false)) return r;
+    q4::DecodeWork w{h->ws, h->ws_floats, h->tickets, h->n_tickets};
+    Q4_CUDA(q4::launch_decode(v, p, w, xin, M, out, stream), "decode launch");
+    ++g_launches;
+    return ok();
+}
+
+static int check_matmul_args(gptq_q4_handle h, const void *x, int M, const void *out) {
+    if (int r = check_handle(h)) return r;
+    if (M < 0) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "M=%d < 0", M);
+    if (M == 0) return GPTQ_Q4_OK;
+    if (!x || !out) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "x and out must not be NULL when M > 0");
+    if (!aligned(x, 16) || !aligned(out, 16))
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "x and out must be 16-byte aligned");
+    return GPTQ_Q4_OK;
+}
+
+int gptq_q4_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out, cudaStream_t stream) {
+    if (int r = check_matmul_args(h, x, M, out)) return r;
+    if (M == 0) return ok();
+    int path = h->path;
+    if (path == GPTQ_Q4_PATH_AUTO) path = (M >= h->prefill_min_m) ? GPTQ_Q4_PATH_PREFILL : GPTQ_Q4_PATH_DECODE;
+    return run_matmul(h, x, M, out, stream, path);
+}
+
+int gptq_q4_dequant(gptq_q4_handle h, uint16_t *temp_dq, cudaStream_t stream) {
+    if (int r = check_handle(h)) return r;
+    if (!temp_dq) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must not be NULL");
+    if (!aligned(temp_dq, 16)) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must be 16-byte aligned");
+    Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
+    ++g_launches;
+    return ok();
+}
+
+int gptq_q4_debug_unpack(gptq_q4_handle h, uint8_t *q, uint8_t *z, cudaStream_t stream) {
+    if (int r = check_handle(h)) return r;
+    if (!q && !z) return ok();
+    Q4_CUDA(q4::launch_debug_unpack(view(h), q, z, stream), "unpack launch");
+    ++g_launches;
+    return ok();
+}
+
+int gptq_q4_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
+                     uint16_t *out, cudaStream_t stream) {
+    if (M < 0 || K <= 0 || N <= 0) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "bad sizes M=%d K=%d N=%d", M, K, N);
+    if (K % 64 || N % 64)
+        return set_status(GPTQ_Q4_UNSUPPORTED, "the tensor-core GEMM needs K %% 64 == 0 and N %% 64 == 0");
+    if (M == 0) return ok();
+    if (!a || !b || !out) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "a, b and out must not be NULL");
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16) || (bias && !aligned(bias, 2)))
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "a, b and out must be 16-byte aligned");
+    Q4_CUDA(q4::launch_gemm_f16(a, b, bias, M, K, N, out, nullptr, stream), "gemm launch");
+    ++g_launches;
+    return ok();
+}
+
+int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *temp_dq, uint16_t *out,
+                           cudaStream_t stream) {
+    if (int r = check_matmul_args(h, x, M, out)) return r;
+    if (M == 0) return ok();
+    if (!temp_dq || !aligned(temp_dq, 16))
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must be a 16-byte aligned device buffer");
+    Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
+    ++g_launches;
+    Q4_CUDA(q4::launch_gemm_f16(x, temp_dq, h->bias, M, h->K, h->N, out, h->status, stream), "gemm launch");
+    ++g_launches;
+    return ok();
+}
+
+int gptq_q4_set_path(gptq_q4_handle h, int path) {
+    if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
+    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_PREFILL)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "unknown path %d", path);
+    h->path = path;
+    return ok();
+}
+
+int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m) {
+    if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
+    if (min_m < 0) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "min_m=%d < 0", min_m);
+    h->prefill_min_m = min_m;
+    return ok();
+}
+
+int gptq_q4_info(gptq_q4_handle h, int *K, int *N, int *groupsize, int *G, int *act_order, size_t *device_bytes) {
+    if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
+    if (K) *K = h->K;
+    if (N) *N = h->N;
+    if (groupsize) *groupsize = h->groupsize;
+    if (G) *G = h->G;
+    if (act_order) *act_order = h->act_order;
+    if (device_bytes) *device_bytes = h->device_bytes;
+    return ok();
+}
+
+int gptq_q4_device_error(gptq_q4_handle h) {
+    if (int r = check_handle(h)) return r;
+    Q4_CUDA(cudaDeviceSynchronize(), "synchronize");
+    int flag = 0;
+    Q4_CUDA(cudaMemcpy(&flag, h->status, sizeof(int), cudaMemcpyDeviceToHost), "reading status word");
+    if (flag) {
+        Q4_CUDA(cudaMemset(h->status, 0, sizeof(int)), "clearing status word");
+        return set_status(GPTQ_Q4_DEVICE_FAULT, "a kernel reported status 0x%x", flag);
+    }
+    return ok();
+}
+
+void gptq_q4_free(gptq_q4_handle h) {
+    release(h);
+    ok();
+}
+
+int gptq_q4_last_status(void) { return t_status; }
+const char *gptq_q4_last_error(void) { return t_msg; }
+uint64_t gptq_q4_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,338 @@
+// Decode (small-M) fused GPTQ W4A16 matmul.
+//
+// "GPTQ's 'Exllama Kernel Not Installed' Warning", "What the fallback
+// actually does": the fused kernel reads packed 4-bit weights from memory,
+// unpacks and dequantizes them in registers and multiplies against fp16
+// activations without ever writing a dequantized matrix; weight-bound
+// decoding is limited by memory bandwidth.
+// "Inference Backends", "Numeric epilogues and input gradients": fp32
+// accumulation, fp32 split reductions, bias added to the fp32 sum before the
+// one final cast, and no atomic partial-output reduction.
+//
+// Work split.  A CTA (8 warps) owns 32 output columns (two 16-column tiles),
+// up to 8*MT rows of x, and one K slice.  Its warps split the slice into
+// contiguous runs of 64-row chunks.  For each chunk a lane issues one 16-byte
+// streaming load per column tile; a ring of DEPTH chunks keeps loads in
+// flight while earlier chunks are computed.
+//
+// Arithmetic.  Each packed word gives, with one LOP3 and one HFMA2 per pair,
+// the exact integers (q - z - 1) of eight consecutive rows of one column as
+// four half2 registers.  Those are the A operand of m16n8k16 tensor-core MMAs
+// (rows = output columns n, k = weight rows) against x as the B operand
+// (columns = rows of x), accumulating in fp32.  The K index inside a 32-row
+// block is permuted identically for A and B (lane tq owns rows 8tq..8tq+7),
+// which lets both operands come from single 16-byte loads; a sum does not
+// depend on the order of its terms beyond rounding.  The scale is factored
+// out of each group: a fresh fp32 partial per group, then acc += s * partial.
+//
+// Reduction.  Warps of a CTA are summed in a fixed order through shared
+// memory.  With more than one K slice, each CTA writes its fp32 partial tile
+// to the workspace, and the last CTA of a column tile to arrive (an atomic
+// ticket; nobody waits) adds the slices in slice order, adds bias and rounds
+// once to fp16.  The result is deterministic.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "q4_internal.cuh"
+
+namespace q4 {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kNTW = 2;             // 16-column tiles per CTA
+constexpr int kNB = 16 * kNTW;      // columns per CTA
+constexpr int kDepth = 4;           // chunks in the load ring
+
+struct DecodeArgs {
+    const uint16_t *x;
+    uint16_t *out;
+    float *ws;
+    int *tickets;
+    int M;
+    int splits;
+    int slice_chunks;
+};
+
+__host__ __device__ inline int x_row_stride(int slice_chunks) { return slice_chunks * 64 + 32; }
+
+template <int MT>
+__host__ __device__ inline size_t smem_bytes(int slice_chunks, int max_groups) {
+    return static_cast<size_t>(8 * MT) * x_row_stride(slice_chunks) * 2     // x slice
+           + static_cast<size_t>(kWarps) * kNTW * MT * 128 * 4              // warp partials
+           + static_cast<size_t>(max_groups) * kNTW * 10 * 4;              // scale pairs + zero words
+}
+
+__host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
+    return (slice_chunks * 64 + geff - 1) / geff + 1;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int K = h.K, N = h.N, KC = K >> 6, NT16 = N >> 4;
+    const int nt0 = blockIdx.x * kNTW;
+    const int split = blockIdx.y;
+    const int m0 = blockIdx.z * (8 * MT);
+    const int mrows = min(8 * MT, a.M - m0);
+    const int c_beg = split * a.slice_chunks;
+    const int c_end = min(KC, c_beg + a.slice_chunks);
+    const int nch = c_end - c_beg;
+    const int XS = x_row_stride(a.slice_chunks);
+    const int geff = h.geff;
+    const int bpg = geff >> 5;                          // 32-row blocks per group
+
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
+    float *red = reinterpret_cast<float *>(smem + static_cast<size_t>(8 * MT) * XS * 2);
+    uint32_t *gsz = reinterpret_cast<uint32_t *>(red + kWarps * kNTW * MT * 128);
+
+    // ---- stage x[m0 : m0 + 8MT][slice] (zero rows past M) and the slice's
+    //      scale pairs / zero words for this CTA's two column tiles.
+    {
+        const int vpr = nch * 8;                        // 16-byte vectors per row
+        for (int i = threadIdx.x; i < 8 * MT * vpr; i += kThreads) {
+            const int r = i / vpr, c = i - r * vpr;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < mrows)
+                v = __ldg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64 + c * 8));
+            *reinterpret_cast<uint4 *>(xs + r * XS + c * 8) = v;
+        }
+        const int g_beg = (c_beg * 64) / geff;
+        const int g_end = (c_end * 64 - 1) / geff + 1;
+        const int ng = g_end - g_beg;
+        for (int i = threadIdx.x; i < ng * kNTW * 10; i += kThreads) {
+            const int gl = i / (kNTW * 10), rest = i - gl * (kNTW * 10);
+            const int nt = rest / 10, w = rest - nt * 10;
+            const size_t gr = static_cast<size_t>(g_beg + gl);
+            uint32_t v;
+            if (w < 8) v = __ldg(h.s2 + (gr * NT16 + nt0 + nt) * 8 + w);
+            else v = __ldg(h.zeros + gr * (N >> 3) + (nt0 + nt) * 2 + (w - 8));
+            gsz[i] = v;
+        }
+    }
+    __syncthreads();
+
+    const int wc_beg = c_beg + (nch * warp) / kWarps;
+    const int wc_end = c_beg + (nch * (warp + 1)) / kWarps;
+    const int wn = wc_end - wc_beg;
+    const int g_base = (c_beg * 64) / geff;
+
+    float acc[kNTW][MT][4], accg[kNTW][MT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][mt][i] = 0.f, accg[nt][mt][i] = 0.f;
+
+    if (wn > 0) {
+        uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
+        float sc[kNTW][2];
+        int blk = 2 * wc_beg;
+        int grp = blk / bpg;
+        int left = bpg - (blk - grp * bpg);
+
+        auto load_group = [&](int g) {
+            const uint32_t *base = gsz + (g - g_base) * kNTW * 10;
+#pragma unroll
+            for (int nt = 0; nt < kNTW; ++nt) {
+                const uint32_t sp = base[nt * 10 + gq];
+                const uint32_t zw0 = base[nt * 10 + 8], zw1 = base[nt * 10 + 9];
+                sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
+                sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
+                const uint32_t z0 = (zw0 >> (4 * gq)) & 0xFu, z1 = (zw1 >> (4 * gq)) & 0xFu;
+                nzlo[nt][0] = neg_zlo(z0);
+                nzhi[nt][0] = neg_zhi(z0);
+                nzlo[nt][1] = neg_zlo(z1);
+                nzhi[nt][1] = neg_zhi(z1);
+            }
+        };
+        auto flush = [&]() {
+#pragma unroll
+            for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[nt][mt][i] = fmaf(sc[nt][i >> 1], accg[nt][mt][i], acc[nt][mt][i]);
+                        accg[nt][mt][i] = 0.f;
+                    }
+        };
+        load_group(grp);
+
+        const uint4 *wbase[kNTW];
+#pragma unroll
+        for (int nt = 0; nt < kNTW; ++nt)
+            wbase[nt] = h.wp + (static_cast<size_t>(nt0 + nt) * KC + wc_beg) * 32 + lane;
+
+        uint4 buf[kDepth][kNTW];
+#pragma unroll
+        for (int i = 0; i < kDepth; ++i)
+            if (i < wn)
+#pragma unroll
+                for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(i) * 32);
+
+        for (int base = 0; base < wn; base += kDepth) {
+#pragma unroll
+            for (int i = 0; i < kDepth; ++i) {
+                const int c = base + i;
+                if (c < wn) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (left == 0) {
+                            flush();
+                            ++grp;
+                            load_group(grp);
+                            left = bpg;
+                        }
+                        const int kk = (2 * (wc_beg + c - c_beg) + hh) * 32 + 8 * tq;
+                        uint4 xb[MT];
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt)
+                            xb[mt] = *reinterpret_cast<const uint4 *>(xs + (mt * 8 + gq) * XS + kk);
+#pragma unroll
+                        for (int nt = 0; nt < kNTW; ++nt) {
+                            const uint32_t lo = hh ? buf[i][nt].z : buf[i][nt].x;
+                            const uint32_t hi = hh ? buf[i][nt].w : buf[i][nt].y;
+                            uint32_t al[4], ah[4];
+                            unpack_qz(lo, nzlo[nt][0], nzhi[nt][0], al);
+                            unpack_qz(hi, nzlo[nt][1], nzhi[nt][1], ah);
+                            const uint32_t A0[4] = {al[0], ah[0], al[1], ah[1]};
+                            const uint32_t A1[4] = {al[2], ah[2], al[3], ah[3]};
+#pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                mma_16816(accg[nt][mt], A0, xb[mt].x, xb[mt].y);
+                                mma_16816(accg[nt][mt], A1, xb[mt].z, xb[mt].w);
+                            }
+                        }
+                        --left;
+                    }
+                    if (c + kDepth < wn)
+#pragma unroll
+                        for (int nt = 0; nt < kNTW; ++nt)
+                            buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(c + kDepth) * 32);
+                }
+            }
+        }
+        flush();
+    }
+
+    // ---- fixed-order reduction over the CTA's warps
+    constexpr int E = kNTW * MT * 128;                 // partial elements per CTA
+#pragma unroll
+    for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            *reinterpret_cast<float4 *>(red + warp * E + (nt * MT + mt) * 128 + lane * 4) =
+                make_float4(acc[nt][mt][0], acc[nt][mt][1], acc[nt][mt][2], acc[nt][mt][3]);
+    __syncthreads();
+
+    auto element_mn = [&](int e, int &m, int &n) {
+        const int ntm = e >> 7, l = (e >> 2) & 31, i = e & 3;
+        const int nt = ntm / MT, mt = ntm - nt * MT;
+        n = 16 * (nt0 + nt) + (l >> 2) + 8 * (i >> 1);
+        m = m0 + mt * 8 + 2 * (l & 3) + (i & 1);
+    };
+
+    const int tile_id = blockIdx.z * gridDim.x + blockIdx.x;
+    if (a.splits == 1) {
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += red[w * E + e];
+            int m, n;
+            element_mn(e, m, n);
+            if (m < a.M) {
+                if (h.bias) v += __half2float(__ushort_as_half(h.bias[n]));
+                a.out[static_cast<size_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
+            }
+        }
+        return;
+    }
+
+    float *my_ws = a.ws + (static_cast<size_t>(tile_id) * a.splits + split) * E;
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += red[w * E + e];
+        __stcg(my_ws + e, v);
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        const int prev = atomicAdd(a.tickets + tile_id, 1);
+        s_last = (prev == a.splits - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float *tile_ws = a.ws + static_cast<size_t>(tile_id) * a.splits * E;
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int m, n;
+        element_mn(e, m, n);
+        float v = 0.f;
+        for (int s = 0; s < a.splits; ++s) v += __ldcg(tile_ws + static_cast<size_t>(s) * E + e);
+        if (m < a.M) {
+            if (h.bias) v += __half2float(__ushort_as_half(h.bias[n]));
+            a.out[static_cast<size_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
+        }
+    }
+    if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
+}
+
+template <int MT>
+cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
+                      uint16_t *out, cudaStream_t s) {
+    const size_t smem = smem_bytes<MT>(p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
+    static bool configured = false;   // per template instance; attribute is per-function
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks};
+    dim3 grid(p.ctas_n, p.splits, p.zdim);
+    decode_kernel<MT><<<grid, kThreads, smem, s>>>(h, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int M, int K, int N) {
+    DecodePlan p{};
+    p.mt = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+    p.zdim = (M + 8 * p.mt - 1) / (8 * p.mt);
+    p.ctas_n = N / kNB;
+    const int KC = K / 64;
+    const int max_slice = 64 / p.mt;                    // x slice <= 64 KB of shared memory
+    const int min_slice = std::min(KC, 16);             // at least two chunks per warp
+    const int base = p.ctas_n * p.zdim;
+    const int target = 4 * kSMs;
+    int splits = (target + base - 1) / base;
+    splits = std::min(splits, std::max(1, KC / min_slice));
+    splits = std::max(splits, (KC + max_slice - 1) / max_slice);
+    splits = std::max(1, std::min(splits, KC));
+    p.slice_chunks = (KC + splits - 1) / splits;
+    p.splits = (KC + p.slice_chunks - 1) / p.slice_chunks;
+    p.n_tickets = base;
+    p.ws_floats = p.splits > 1 ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
+    return p;
+}
+
+size_t decode_ws_floats_for(int M, int K, int N) { return plan_decode(M, K, N).ws_floats; }
+
+cudaError_t launch_decode(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
+                          uint16_t *out, cudaStream_t s) {
+    switch (p.mt) {
+        case 1: return launch_mt<1>(h, p, w, x, M, out, s);
+        case 2: return launch_mt<2>(h, p, w, x, M, out, s);
+        default: return launch_mt<4>(h, p, w, x, M, out, s);
+    }
+}
+
+}  // namespace q4

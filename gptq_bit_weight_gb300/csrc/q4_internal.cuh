@@ -1,0 +1,144 @@
+// Internal definitions shared by the kernels and the C-ABI layer.
+//
+// Private execution layout of the packed weights ("Inference Backends",
+// "Packing, conversion, and runtime initialization": runtime init may repack
+// into a private layout).  Rows are taken in act-order permutation order P
+// (identity when there is no act-order), so that every group is a contiguous
+// run of rows and groups never need gathering at run time.
+//
+//   Wp word (nt, kc, lane, j), nt = n/16, kc = k/64, lane = 4*gq + tq:
+//     column  n = 16*nt + gq + 8*(j & 1)
+//     rows    j' = 64*kc + 32*(j >> 1) + 8*tq + r,  r = 0..7   (permuted order)
+//     code of row r sits in nibble  pos(r) = (r >> 1) + 4*(r & 1),
+//     i.e. nibbles 0..7 hold rows r = 0,2,4,6,1,3,5,7.
+//   Word index ((nt*KC + kc)*32 + lane)*4 + j: each lane owns one aligned
+//   16-byte vector per (nt, kc), and a warp reads one contiguous 512-byte run.
+//
+// Why this shape: (1) one 16-byte load gives a lane exactly the A-operand
+// codes of two m16n8k16 MMAs for rows n = gq and gq+8 over 64 values of k;
+// (2) one word holds eight consecutive k of one column, which is one 16-byte
+// row segment of a K-major fp16 operand tile for the prefill tensor cores;
+// (3) the nibble order lets the 0x6400 fp16 "magic number" (the exponent
+// pattern of 1024) turn two codes into a half2 with one LOP3: codes of rows r
+// and r+1 land in the low and high half of the same 32-bit register
+// (Kim et al. 2022, "Who Says Elephants Can't Run", fast int4 -> fp16).
+//
+// Scales: S2 word (gr, nt, gq) = half2(scales[gr][16nt+gq], scales[gr][16nt+gq+8]).
+// Zero points keep the checkpoint layout [G][N/8].
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace q4 {
+
+constexpr int kSMs = 152;
+
+__host__ __device__ inline int nib_pos(int r) { return (r >> 1) + 4 * (r & 1); }
+
+__host__ __device__ inline size_t wp_index(int nt, int kc, int lane, int j, int KC) {
+    return ((static_cast<size_t>(nt) * KC + kc) * 32 + lane) * 4 + j;
+}
+
+// ----------------------------------------------------------- device helpers
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Streaming 16-byte load of packed weights: read once per call, so it skips
+// L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Four codes pairs of one packed word -> four half2 registers holding
+// (q - z - 1) exactly for rows (0,1), (2,3), (4,5), (6,7) of the word.
+//   nzlo = half2 splat of -(1025 + z)  : (1024 + q) - (1025 + z)
+//   nzhi = half2 splat of -(65 + z)    : (1024 + 16 q) / 16 - (65 + z)
+// Every intermediate is a small integer, so each fp16 step is exact.
+__device__ __forceinline__ void unpack_qz(uint32_t w, uint32_t nzlo, uint32_t nzhi, uint32_t (&a)[4]) {
+    const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
+    const uint32_t kOne = 0x3C003C00u, kSixteenth = 0x2C002C00u;
+    uint32_t t0 = lop3_and_or(w, kLo, kMagic);
+    uint32_t t1 = lop3_and_or(w, kHi, kMagic);
+    uint32_t w8 = w >> 8;
+    uint32_t t2 = lop3_and_or(w8, kLo, kMagic);
+    uint32_t t3 = lop3_and_or(w8, kHi, kMagic);
+    a[0] = hfma2(t0, kOne, nzlo);
+    a[1] = hfma2(t1, kSixteenth, nzhi);
+    a[2] = hfma2(t2, kOne, nzlo);
+    a[3] = hfma2(t3, kSixteenth, nzhi);
+}
+
+// Zero-point constants for unpack_qz from a stored zero z (0..15).
+__device__ __forceinline__ uint32_t neg_zlo(uint32_t z) { return (0xE401u + z) * 0x00010001u; }
+__device__ __forceinline__ uint32_t neg_zhi(uint32_t z) { return (0xD410u + 16u * z) * 0x00010001u; }
+
+// D += A . B on the tensor cores, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------ launchers
+struct HandleView {
+    int K, N, G, geff, groupsize;
+    const uint4 *wp;        // private packed codes
+    const uint32_t *s2;     // scale pairs
+    const uint32_t *zeros;  // checkpoint-layout zero points
+    const int32_t *perm;    // P (device) or nullptr
+    const uint16_t *bias;   // device fp16 [N] or nullptr
+    int *status;            // device status word
+};
+
+struct DecodeWork {
+    float *ws;              // split-K partials
+    size_t ws_floats;
+    int *tickets;           // one per output tile, all zero between calls
+    int n_tickets;
+};
+
+// repack / unpack / dequant / reorder (q4_repack.cu)
+cudaError_t launch_repack_codes(const int32_t *qweight, const int32_t *perm, int K, int N,
+                                uint32_t *wp, cudaStream_t s);
+cudaError_t launch_repack_scales(const uint16_t *scales, int G, int N, uint32_t *s2, cudaStream_t s);
+cudaError_t launch_debug_unpack(const HandleView &h, uint8_t *q, uint8_t *z, cudaStream_t s);
+cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t s);
+cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K,
+                            uint16_t *temp_state, cudaStream_t s);
+
+// decode (q4_decode.cu)
+struct DecodePlan {
+    int mt;            // 8-row m tiles per CTA (1, 2 or 4)
+    int zdim;          // row blocks
+    int ctas_n;        // column tiles of 32
+    int splits;        // K slices
+    int slice_chunks;  // 64-row chunks per slice
+    size_t ws_floats;  // workspace needed
+    int n_tickets;
+};
+DecodePlan plan_decode(int M, int K, int N);
+size_t decode_ws_floats_for(int M, int K, int N);
+cudaError_t launch_decode(const HandleView &h, const DecodePlan &plan, const DecodeWork &w,
+                          const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
+
+}  // namespace q4

@@ -1,0 +1,217 @@
+// One-time repack of a GPTQ checkpoint into the private execution layout,
+// and the read-back kernels (codes, dequantized weights) plus the act-order
+// activation gather.
+//
+// "Inference Backends", "Packing, conversion, and runtime initialization":
+// runtime initialization repacks loaded tensors into a kernel's private
+// layout and shuffles scales/zeros.  "Implementation: Predibase Lorax GPTQ
+// Exllama V1", "Description": temp_state reorders activations for act-order
+// and temp_dq receives dequantized weights.
+#include <cuda_fp16.h>
+
+#include "q4_internal.cuh"
+
+namespace q4 {
+
+// ---------------------------------------------------------------- codes
+// One thread per private word.  Each of its eight rows (permuted order) is
+// looked up in the checkpoint through P, its nibble extracted and placed at
+// nib_pos(r).  Rows of one act-order word come from different checkpoint
+// words, so the codes are unpacked and repacked one by one.
+__global__ void repack_codes_kernel(const int32_t *__restrict__ qweight, const int32_t *__restrict__ perm,
+                                    int K, int N, uint32_t *__restrict__ wp) {
+    const int KC = K / 64;
+    const size_t total = static_cast<size_t>(N / 16) * KC * 128;
+    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(idx & 3);
+        const int lane = static_cast<int>((idx >> 2) & 31);
+        const size_t tile = idx >> 7;
+        const int kc = static_cast<int>(tile % KC);
+        const int nt = static_cast<int>(tile / KC);
+        const int gq = lane >> 2, tq = lane & 3;
+        const int n = 16 * nt + gq + 8 * (j & 1);
+        const int kb = 64 * kc + 32 * (j >> 1) + 8 * tq;
+        uint32_t out = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int k = perm ? perm[kb + r] : kb + r;
+            const uint32_t word = static_cast<uint32_t>(qweight[static_cast<size_t>(k >> 3) * N + n]);
+            const uint32_t code = (word >> (4 * (k & 7))) & 0xFu;
+            out |= code << (4 * nib_pos(r));
+        }
+        wp[idx] = out;
+    }
+}
+
+cudaError_t launch_repack_codes(const int32_t *qweight, const int32_t *perm, int K, int N, uint32_t *wp,
+                                cudaStream_t s) {
+    const size_t total = static_cast<size_t>(N / 16) * (K / 64) * 128;
+    const int threads = 256;
+    const size_t want = (total + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 65535u * 16u ? want : 65535u * 16u);
+    repack_codes_kernel<<<blocks, threads, 0, s>>>(qweight, perm, K, N, wp);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- scales
+__global__ void repack_scales_kernel(const uint16_t *__restrict__ scales, int G, int N, uint32_t *__restrict__ s2) {
+    const size_t total = static_cast<size_t>(G) * (N / 16) * 8;
+    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int gq = static_cast<int>(idx & 7);
+        const size_t rest = idx >> 3;
+        const int nt = static_cast<int>(rest % (N / 16));
+        const int gr = static_cast<int>(rest / (N / 16));
+        const size_t base = static_cast<size_t>(gr) * N + 16 * nt + gq;
+        s2[idx] = static_cast<uint32_t>(scales[base]) | (static_cast<uint32_t>(scales[base + 8]) << 16);
+    }
+}
+
+cudaError_t launch_repack_scales(const uint16_t *scales, int G, int N, uint32_t *s2, cudaStream_t s) {
+    const size_t total = static_cast<size_t>(G) * (N / 16) * 8;
+    const int threads = 256;
+    const size_t want = (total + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 65535u * 16u ? want : 65535u * 16u);
+    repack_scales_kernel<<<blocks, threads, 0, s>>>(scales, G, N, s2);
+    return cudaGetLastError();
+}
+
+// -------------------------------------------------- unpack (read-back)
+// q[k][n] in original row order from the private words; z from the zeros.
+__global__ void debug_unpack_kernel(HandleView h, uint8_t *__restrict__ q, uint8_t *__restrict__ z) {
+    const int K = h.K, N = h.N, KC = K / 64;
+    const uint32_t *wp = reinterpret_cast<const uint32_t *>(h.wp);
+    const size_t total_words = static_cast<size_t>(N / 16) * KC * 128;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    if (q) {
+        for (size_t idx = tid; idx < total_words; idx += stride) {
+            const int j = static_cast<int>(idx & 3);
+            const int lane = static_cast<int>((idx >> 2) & 31);
+            const size_t tile = idx >> 7;
+            const int kc = static_cast<int>(tile % KC);
+            const int nt = static_cast<int>(tile / KC);
+            const int n = 16 * nt + (lane >> 2) + 8 * (j & 1);
+            const int kb = 64 * kc + 32 * (j >> 1) + 8 * (lane & 3);
+            const uint32_t w = wp[idx];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int k = h.perm ? h.perm[kb + r] : kb + r;
+                q[static_cast<size_t>(k) * N + n] = static_cast<uint8_t>((w >> (4 * nib_pos(r))) & 0xFu);
+            }
+        }
+    }
+    if (z) {
+        const size_t total_z = static_cast<size_t>(h.G) * N;
+        for (size_t idx = tid; idx < total_z; idx += stride) {
+            const int n = static_cast<int>(idx % N);
+            const size_t gr = idx / N;
+            const uint32_t w = h.zeros[gr * (N / 8) + n / 8];
+            z[idx] = static_cast<uint8_t>((w >> (4 * (n & 7))) & 0xFu);
+        }
+    }
+}
+
+cudaError_t launch_debug_unpack(const HandleView &h, uint8_t *q, uint8_t *z, cudaStream_t s) {
+    debug_unpack_kernel<<<kSMs * 8, 256, 0, s>>>(h, q, z);
+    return cudaGetLastError();
+}
+
+// -------------------------------------------------------------- dequant
+// temp_dq[k][n] = fp16(s * (q - (z + 1))), original row order.
+// A CTA takes 64 columns x 64 (permuted) rows at a time: 256 threads each
+// dequantize two private words (16 values) into a shared tile, then the tile
+// is written out one 128-byte row per 8 threads, each row to its original
+// position P[j].  The product s * (q - z - 1) is exact in fp32 (11-bit times
+// 5-bit integer), so __float2half_rn rounds it exactly once.
+__global__ void __launch_bounds__(256) dequant_kernel(HandleView h, uint16_t *__restrict__ out) {
+    constexpr int kPad = 8;
+    __shared__ __align__(16) uint16_t tile[64][64 + kPad];
+    const int K = h.K, N = h.N, KC = K / 64, NT64 = N / 64;
+    const int tid = threadIdx.x;
+    const int bpg = h.geff / 32;
+    const uint32_t *wp = reinterpret_cast<const uint32_t *>(h.wp);
+    const size_t ntiles = static_cast<size_t>(NT64) * KC;
+    for (size_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int kc = static_cast<int>(t % KC);
+        const int n64 = static_cast<int>(t / KC);
+#pragma unroll
+        for (int rep = 0; rep < 2; ++rep) {
+            const int widx = tid + 256 * rep;          // 0..511 within the 64x64 tile
+            const int j = widx & 3;
+            const int lane = (widx >> 2) & 31;
+            const int ntl = widx >> 7;                 // n16 tile within the 64 columns
+            const int nt = 4 * n64 + ntl;
+            const int gq = lane >> 2, tq = lane & 3;
+            const int n = 16 * nt + gq + 8 * (j & 1);
+            const int kl = 32 * (j >> 1) + 8 * tq;     // local row of r = 0
+            const int gr = (64 * kc + kl) / 32 / bpg;  // group of these eight rows
+            const uint32_t w = wp[wp_index(nt, kc, lane, j, KC)];
+            const uint32_t zw = h.zeros[static_cast<size_t>(gr) * (N / 8) + n / 8];
+            const int zeff = static_cast<int>((zw >> (4 * (n & 7))) & 0xFu) + 1;
+            const uint32_t sp = h.s2[(static_cast<size_t>(gr) * (N / 16) + nt) * 8 + gq];
+            const uint16_t sbits = static_cast<uint16_t>((j & 1) ? (sp >> 16) : (sp & 0xFFFFu));
+            const float s = __half2float(__ushort_as_half(sbits));
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int code = static_cast<int>((w >> (4 * nib_pos(r))) & 0xFu);
+                const float v = s * static_cast<float>(code - zeff);
+                tile[kl + r][n - 64 * n64] = __half_as_ushort(__float2half_rn(v));
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int rep = 0; rep < 2; ++rep) {
+            const int row = (tid >> 3) + 32 * rep;
+            const int c8 = tid & 7;
+            const int jrow = 64 * kc + row;
+            const int k = h.perm ? h.perm[jrow] : jrow;
+            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[row][8 * c8]);
+            *reinterpret_cast<uint4 *>(out + static_cast<size_t>(k) * N + 64 * n64 + 8 * c8) = v;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t s) {
+    const size_t ntiles = static_cast<size_t>(h.N / 64) * (h.K / 64);
+    const size_t want = ntiles;
+    const int blocks = static_cast<int>(want < static_cast<size_t>(kSMs) * 8 ? want : static_cast<size_t>(kSMs) * 8);
+    dequant_kernel<<<blocks, 256, 0, s>>>(h, temp_dq);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- xreorder
+// temp_state[m][j] = x[m][P[j]]: eight consecutive j per thread, written as
+// one 16-byte store; the gathered reads come from the small x (L2-resident).
+__global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int K,
+                                uint16_t *__restrict__ ts) {
+    const size_t total = static_cast<size_t>(M) * (K / 8);
+    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t m = idx / (K / 8);
+        const int j0 = static_cast<int>(idx % (K / 8)) * 8;
+        const uint16_t *xr = x + m * K;
+        const int4 p0 = *reinterpret_cast<const int4 *>(perm + j0);
+        const int4 p1 = *reinterpret_cast<const int4 *>(perm + j0 + 4);
+        uint4 v;
+        v.x = static_cast<uint32_t>(xr[p0.x]) | (static_cast<uint32_t>(xr[p0.y]) << 16);
+        v.y = static_cast<uint32_t>(xr[p0.z]) | (static_cast<uint32_t>(xr[p0.w]) << 16);
+        v.z = static_cast<uint32_t>(xr[p1.x]) | (static_cast<uint32_t>(xr[p1.y]) << 16);
+        v.w = static_cast<uint32_t>(xr[p1.z]) | (static_cast<uint32_t>(xr[p1.w]) << 16);
+        *reinterpret_cast<uint4 *>(ts + m * K + j0) = v;
+    }
+}
+
+cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K, uint16_t *temp_state,
+                            cudaStream_t s) {
+    const size_t total = static_cast<size_t>(M) * (K / 8);
+    const int threads = 256;
+    const size_t want = (total + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < static_cast<size_t>(kSMs) * 16 ? want : static_cast<size_t>(kSMs) * 16);
+    xreorder_kernel<<<blocks > 0 ? blocks : 1, threads, 0, s>>>(x, perm, M, K, temp_state);
+    return cudaGetLastError();
+}
+
+}  // namespace q4

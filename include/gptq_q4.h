@@ -1,0 +1,215 @@
+/*
+ * gptq_q4.h -- C ABI of the GB300 (sm_103a) fused GPTQ W4A16 linear layer.
+ *
+ *     y[M][N] = x[M][K] . W[K][N] + bias[N]
+ *
+ * W is a GPTQ (v1) 4-bit weight matrix:
+ *   qweight  int32 [K/8][N]   eight 4-bit codes per word along K, code k%8 in
+ *                             bits 4(k%8) .. 4(k%8)+3 (lowest nibble first)
+ *   qzeros   int32 [G][N/8]   eight 4-bit zero points per word along N, same
+ *                             nibble order
+ *   scales   fp16  [G][N]     one scale per (group, column)
+ *   g_idx    int32 [K]        group of each row (act-order), or NULL
+ *   w[k][n] = scales[g][n] * (q[k][n] - (z[g][n] + 1)),  g = g_idx[k]
+ *             (g = k / groupsize when g_idx is NULL; G = K / groupsize, or
+ *              G = 1 and one group over all of K when groupsize == -1)
+ *
+ * Sources (web pages; sections named):
+ *   "GPTQ's 'Exllama Kernel Not Installed' Warning" -- "Why the kernel is
+ *     missing" (4-bit integers packed in 32-bit words, a scale and a zero per
+ *     group) and "What the fallback actually does" (the fused kernel reads
+ *     packed weights, dequantizes in registers and never writes a dequantized
+ *     matrix; the fallback rebuilds W and runs an ordinary matmul, reaching the
+ *     same answer with several times the memory traffic).
+ *   "Implementation: Predibase Lorax GPTQ Exllama V1" -- "Description" (a
+ *     Q4Matrix handle built from qweight, qzeros, scales and optional g_idx;
+ *     q4_matmul computes x @ q4 into a (batch, width) fp16 output; temp_state
+ *     reorders activations for act-order; temp_dq holds dequantized weights
+ *     for the prefill matmul; create_exllama_buffers sizes both) and "I/O
+ *     Contract" (dtypes; bits must be 4; None or trivial g_idx = no act-order).
+ *   "Inference Backends" -- "Packing, conversion, and runtime initialization"
+ *     (runtime init repacks into a private execution layout and builds native
+ *     handles), "Numeric epilogues and input gradients" (bias joins the fp32
+ *     accumulator before the one final cast; split reductions stay fp32;
+ *     no atomic partial-output reduction), "Strided tensor operands" (one
+ *     stable argsort gives the reorder; an identity permutation skips the
+ *     gather), "Runtime cache lifetime" (no dense weight cache is kept
+ *     between operations).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" must be CUDA device (or managed) memory of the
+ *     device that is current when the call is made; "host" means host memory.
+ *     Arrays are dense and row-major; fp16 values are passed as their 16-bit
+ *     patterns (uint16_t).
+ *   - Every call except gptq_q4_make returns GPTQ_Q4_OK (0) or a negative
+ *     status.  gptq_q4_make returns NULL on failure.  The status and a message
+ *     with the specific reason are kept per host thread and read back with
+ *     gptq_q4_last_status() / gptq_q4_last_error().  Nothing is ever printed,
+ *     and no call silently falls back to another route: there is no CPU path.
+ *   - Work is enqueued on the caller's stream and the calls return without
+ *     waiting, except gptq_q4_make, gptq_q4_reserve, gptq_q4_free and
+ *     gptq_q4_device_error, which synchronize as stated.
+ *   - A handle may be used from one stream at a time (its workspaces are
+ *     reused by every call).  Distinct handles are independent.
+ */
+#ifndef GPTQ_Q4_H
+#define GPTQ_Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define GPTQ_Q4_OK                 0
+#define GPTQ_Q4_INVALID_ARGUMENT (-1) /* NULL, bad sizes, g_idx out of range, misalignment */
+#define GPTQ_Q4_UNSUPPORTED      (-2) /* valid GPTQ data outside what the GPU kernels take,
+                                         or a device that is not sm_103 */
+#define GPTQ_Q4_CUDA_ERROR       (-3) /* a CUDA runtime call failed; message holds its text */
+#define GPTQ_Q4_OUT_OF_MEMORY    (-4) /* a device allocation failed */
+#define GPTQ_Q4_DEVICE_FAULT     (-5) /* a kernel reported an error through its status word */
+
+/* Paths gptq_q4_matmul can take (see gptq_q4_set_path). */
+#define GPTQ_Q4_PATH_AUTO      0  /* decode below the prefill threshold, fused prefill above */
+#define GPTQ_Q4_PATH_DECODE    1  /* always the register-dequant split-K kernel */
+#define GPTQ_Q4_PATH_PREFILL   2  /* always the fused shared-memory-dequant tensor-core kernel */
+
+typedef struct gptq_q4_s *gptq_q4_handle;   /* opaque; owns device memory */
+
+/* Build a handle (the Q4Matrix of the Lorax page's "Description": make_q4).
+ *
+ *   qweight  device int32 [K/8][N]
+ *   qzeros   device int32 [G][N/8]
+ *   scales   device fp16  [G][N]
+ *   g_idx    device int32 [K], or NULL for the trivial map k / groupsize
+ *   groupsize  > 0 dividing K, or -1 for one group over all of K
+ *
+ * Validates the arguments; copies g_idx to the host, checks every entry is in
+ * [0, G), and derives the act-order row permutation P with one stable argsort
+ * (rows sorted by group, original order kept within a group).  An identity P
+ * means no act-order.  Then repacks the codes, in P order, into a private
+ * tile-ordered layout (same byte count as qweight), and the scales into a
+ * private pairing; zero points keep the checkpoint layout.  All of it is
+ * copied into handle-owned device memory, so the caller may free or change its
+ * tensors afterwards.  Also sizes the split-K workspace for M <= 16.
+ * Synchronizes the device before returning.  The caller must have finished
+ * writing the input tensors (e.g. synchronized its stream) before the call.
+ *
+ * Errors (NULL return; reason in gptq_q4_last_error):
+ *   INVALID_ARGUMENT  NULL qweight/qzeros/scales, K or N <= 0, K % 8 or N % 8
+ *                     != 0, groupsize not -1 and not a positive divisor of K,
+ *                     a g_idx entry outside [0, G), a pointer that is not
+ *                     device memory of the current device
+ *   UNSUPPORTED       K % 64, N % 64 or (groupsize or K) % 32 != 0; an
+ *                     act-order g_idx whose groups do not all hold exactly
+ *                     groupsize rows; current device is not compute 10.3
+ *   OUT_OF_MEMORY, CUDA_ERROR */
+gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros,
+                            const uint16_t *scales, const int32_t *g_idx,
+                            int K, int N, int groupsize);
+
+/* Attach (or with NULL, detach) a bias: device fp16 [N], copied into the
+ * handle.  Bias is added to the fp32 accumulator before the single rounding
+ * to fp16 ("Inference Backends", "Numeric epilogues and input gradients").
+ * Enqueued on the legacy default stream and synchronized before returning.
+ * Errors: INVALID_ARGUMENT (NULL handle), OUT_OF_MEMORY, CUDA_ERROR. */
+int gptq_q4_set_bias(gptq_q4_handle h, const uint16_t *bias);
+
+/* Size the handle's work buffers for calls with up to max_m rows: the
+ * act-order activation buffer temp_state [max_m][K] fp16 and the split-K
+ * partial sums.  The counterpart of the Lorax page's create_exllama_buffers
+ * (max_total_tokens).  A later gptq_q4_matmul with more rows grows the buffers
+ * itself (stream-ordered allocation on the caller's stream); calling this
+ * first keeps allocation out of gptq_q4_matmul.  Synchronizes the device.
+ * Errors: INVALID_ARGUMENT (NULL handle, max_m < 0), OUT_OF_MEMORY. */
+int gptq_q4_reserve(gptq_q4_handle h, int max_m);
+
+/* out = x . W + bias  (q4_matmul; the Lorax page's "Description").
+ *
+ *   x    device fp16 [M][K], 16-byte aligned
+ *   out  device fp16 [M][N], 16-byte aligned; written entirely, never read
+ *   M    rows; 0 is a valid no-op
+ *
+ * With act-order, x is first gathered into temp_state (temp_state[m][j] =
+ * x[m][P[j]]).  Rows below the prefill threshold run the decode kernel: packed
+ * weights streamed with 128-bit loads, dequantized in registers, fp32
+ * accumulation on the tensor cores (mma.sync), split-K across CTAs with a
+ * fixed-order fp32 reduction by the last CTA to finish each column tile.
+ * Larger M runs the fused prefill (tcgen05/TMEM with shared-memory
+ * dequantization).  Results do not depend on the path beyond fp32 rounding.
+ * Errors: INVALID_ARGUMENT (NULL handle/pointers with M > 0, M < 0,
+ * misaligned x or out, handle made on another device), OUT_OF_MEMORY (growing
+ * a work buffer), CUDA_ERROR (launch failure). */
+int gptq_q4_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
+                   cudaStream_t stream);
+
+/* temp_dq[k][n] = fp16(scales[g][n] * (q[k][n] - (z[g][n] + 1))), rounded
+ * once to nearest-even, in the ORIGINAL row order (the permutation is undone
+ * on write).  The dequantized matrix of the Lorax page's "Description"
+ * (temp_dq), used for debugging and by the unfused prefill comparison.
+ *   temp_dq  device fp16 [K][N], 16-byte aligned, caller-owned: the handle
+ *            keeps no dense copy ("Runtime cache lifetime").
+ * Errors: INVALID_ARGUMENT, CUDA_ERROR. */
+int gptq_q4_dequant(gptq_q4_handle h, uint16_t *temp_dq, cudaStream_t stream);
+
+/* The unpacked codes, read back from the handle's private layout:
+ *   q  device uint8 [K][N], q[k][n] in 0..15, ORIGINAL row order
+ *   z  device uint8 [G][N], stored zero points (without the +1)
+ * Either pointer may be NULL to skip it.  For checking the repack bit-exactly.
+ * Errors: INVALID_ARGUMENT, CUDA_ERROR. */
+int gptq_q4_debug_unpack(gptq_q4_handle h, uint8_t *q, uint8_t *z, cudaStream_t stream);
+
+/* The unfused comparison route ("What the fallback actually does", with the
+ * matmul on the tensor cores): gptq_q4_dequant into the caller's temp_dq, then
+ * out = x . temp_dq + bias by the tcgen05 GEMM below.  Same arguments as
+ * gptq_q4_matmul plus temp_dq (device fp16 [K][N], caller-owned scratch).
+ * Errors: as gptq_q4_matmul and gptq_q4_dequant. */
+int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M,
+                           uint16_t *temp_dq, uint16_t *out, cudaStream_t stream);
+
+/* Dense fp16 GEMM on the 5th-generation tensor cores (tcgen05, accumulators
+ * in tensor memory, operands staged by TMA): out = a . b + bias with fp32
+ * accumulation and one rounding to fp16.  The matmul the Lorax page runs on
+ * temp_dq "during prefill".
+ *   a     device fp16 [M][K] row-major, b device fp16 [K][N] row-major,
+ *   bias  device fp16 [N] or NULL, out device fp16 [M][N];
+ *   all 16-byte aligned; K % 64 == 0, N % 64 == 0, M >= 0.
+ * Errors: INVALID_ARGUMENT, UNSUPPORTED (sizes), CUDA_ERROR. */
+int gptq_q4_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias,
+                     int M, int K, int N, uint16_t *out, cudaStream_t stream);
+
+/* Force a path for gptq_q4_matmul (tests, benchmarks): GPTQ_Q4_PATH_*. */
+int gptq_q4_set_path(gptq_q4_handle h, int path);
+
+/* Rows at and above which GPTQ_Q4_PATH_AUTO takes the prefill kernel (the
+ * decode/prefill switch of the Lorax page's set_tuning_params).  Default
+ * chosen by measurement; results never depend on it. */
+int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m);
+
+/* Facts about a handle (host outputs; any pointer may be NULL). */
+int gptq_q4_info(gptq_q4_handle h, int *K, int *N, int *groupsize, int *G,
+                 int *act_order, size_t *device_bytes);
+
+/* Synchronize the handle's device and return GPTQ_Q4_DEVICE_FAULT if any
+ * kernel of this handle has set its status word (a bounded wait that ran out,
+ * a failed internal check), else GPTQ_Q4_OK.  Clears the word. */
+int gptq_q4_device_error(gptq_q4_handle h);
+
+/* Release everything the handle owns (synchronizes its device).  NULL is a
+ * no-op. */
+void gptq_q4_free(gptq_q4_handle h);
+
+/* Status and message of the last call made on this host thread. */
+int gptq_q4_last_status(void);
+const char *gptq_q4_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t gptq_q4_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPTQ_Q4_H */

@@ -1,0 +1,223 @@
+"""GPU parity of the C-ABI path against the CPU oracle.
+
+Codes and dequantized weights must match bit for bit; y must be within
+1e-2 sqrt(K) max|x| max|w| / 64 + 2e-3 |y_ref| per element.  Every call goes
+through the C ABI (via the ctypes binding); inputs are seeded and synthetic.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gptq_bit_weight_gb300 as q4mod
+    return q4mod
+
+
+DEV = "cuda:0"
+
+
+def to_dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def make(q4, layer, bias=True):
+    return q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                       to_dev(layer.bias) if bias else None, layer.groupsize)
+
+
+def oracle_dq(layer):
+    return oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, layer.K, layer.N,
+                                   layer.groupsize)
+
+
+def check_y(y_gpu, x, dq, bias, K, what=""):
+    y_ref = oracle.reference_output(x, dq, bias)
+    tol = oracle.tolerance(x, dq.w16, y_ref, K)
+    y = y_gpu.float().cpu().numpy().astype(np.float64)
+    err = np.abs(y - y_ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside tolerance; worst err/tol "
+                           f"{float(np.max(err / np.maximum(tol, 1e-300))):.3f}")
+    return float(np.max(err / np.maximum(tol, 1e-300)))
+
+
+SMALL = [  # (K, N, groupsize, act_order)
+    (64, 64, 32, False),
+    (256, 128, 64, False),
+    (256, 192, -1, False),
+    (512, 320, 128, True),
+    (1024, 448, 32, True),
+    (1088, 576, 64, False),     # K not a multiple of the split slices -> ragged chunks
+    (2048, 960, 128, False),
+    (1024, 256, -1, True),      # one group: act-order reduces to the identity
+]
+
+
+@pytest.mark.parametrize("K,N,gs,act", SMALL)
+def test_unpack_and_dequant_bit_exact(q4, K, N, gs, act):
+    layer = synthetic.make_layer(K, N, gs, act_order=act, key=(21, K, N, gs & 0xFFFF, act))
+    dq = oracle_dq(layer)
+    mat = make(q4, layer, bias=False)
+    q, z = mat.debug_unpack()
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), dq.q)
+    assert np.array_equal(z.cpu().numpy(), dq.z)
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    mat.device_error()
+
+
+@pytest.mark.parametrize("K,N,gs,act", SMALL)
+def test_decode_matches_oracle(q4, K, N, gs, act):
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(22, K, N, gs & 0xFFFF, act))
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    mat.set_path(q4.GPTQ_Q4_PATH_DECODE)
+    for M in (1, 2, 3, 7, 8, 9, 16, 17, 33, 40):
+        x = synthetic.activations(M, K, key=(22, K, N, M))
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, layer.bias, K, f"K={K} N={N} g={gs} act={act} M={M}")
+    mat.device_error()
+
+
+def test_trivial_gidx_same_as_none(q4):
+    K, N, gs = 512, 256, 64
+    layer = synthetic.make_layer(K, N, gs, key=(23,))
+    x = to_dev(synthetic.activations(5, K, key=(23, 5)))
+    a = make(q4, layer, bias=False)
+    gi = to_dev((np.arange(K) // gs).astype(np.int32))
+    b = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), gi, None, gs)
+    assert b.info()["act_order"] is False
+    ya, yb = a(x), b(x)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yb)
+
+
+def test_deterministic_repeat(q4):
+    K, N, gs = 4096, 1024, 128
+    layer = synthetic.make_layer(K, N, gs, act_order=True, bias=True, key=(24,))
+    mat = make(q4, layer)
+    x = to_dev(synthetic.activations(4, K, key=(24, 4)))
+    y1 = mat(x).clone()
+    y2 = mat(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_zero_rows_is_noop(q4):
+    layer = synthetic.make_layer(256, 128, 64, key=(25,))
+    mat = make(q4, layer, bias=False)
+    x = torch.empty((0, 256), dtype=torch.float16, device=DEV)
+    y = mat(x)
+    assert y.shape == (0, 128)
+
+
+def test_no_dense_weight_cache(q4):
+    """The handle keeps the packed bytes plus O(G N + K) metadata, never K*N*2."""
+    K, N, gs = 4096, 4096, 128
+    layer = synthetic.make_layer(K, N, gs, act_order=True, key=(26,))
+    mat = make(q4, layer, bias=False)
+    info = mat.info()
+    packed = K * N // 2
+    meta = layer.G * N * 4 + layer.G * N // 2 + K * 4
+    split_k = 16 * N * 4 * 8   # split-K partials for up to 16 rows, at most 8 slices
+    assert info["device_bytes"] <= packed + meta + split_k + 4096
+    assert info["device_bytes"] < K * N * 2 // 2
+
+
+# ----------------------------------------------------------- workloads
+
+def test_single_layer_workload(q4):
+    layer, x = synthetic.single_layer()
+    dq = oracle_dq(layer)
+    mat = make(q4, layer, bias=False)
+    y = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check_y(y, x, dq, None, layer.K, "single_layer")
+
+
+@pytest.mark.parametrize("K,N", synthetic.DECODE_7B_SHAPES)
+def test_decode_7b_workload(q4, K, N):
+    layer = synthetic.workload_layer("decode_7b", K, N, 128, False)
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    q, z = mat.debug_unpack()
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), dq.q)
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    for M in synthetic.DECODE_7B_M:
+        x = synthetic.workload_x("decode_7b", K, N, 128, False, M)
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, layer.bias, K, f"decode_7b {K}x{N} M={M}")
+
+
+@pytest.mark.parametrize("K,N", synthetic.ACTORDER_7B_SHAPES)
+def test_actorder_7b_workload(q4, K, N):
+    layer = synthetic.workload_layer("actorder_7b", K, N, 128, True)
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    assert mat.info()["act_order"]
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    for M in synthetic.ACTORDER_7B_M:
+        x = synthetic.workload_x("actorder_7b", K, N, 128, True, M)
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, None, K, f"actorder_7b {K}x{N} M={M}")
+
+
+# --------------------------------------------------------- error codes
+
+def test_error_codes(q4):
+    from gptq_bit_weight_gb300 import GPTQ4Error
+    qw = torch.zeros((32, 256), dtype=torch.int32, device=DEV)
+    qz = torch.zeros((2, 32), dtype=torch.int32, device=DEV)
+    sc = torch.ones((2, 256), dtype=torch.float16, device=DEV)
+    with pytest.raises(GPTQ4Error) as e:
+        q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), None, 256, 256, 100)
+    assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
+    with pytest.raises(GPTQ4Error) as e:
+        q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), None, 256, 250, 128)
+    assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
+    with pytest.raises(GPTQ4Error) as e:       # valid GPTQ, but the GPU layout needs N % 64
+        q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), None, 256, 200, 128)
+    assert e.value.status in (q4.GPTQ_Q4_UNSUPPORTED, q4.GPTQ_Q4_INVALID_ARGUMENT)
+    gi = torch.zeros(256, dtype=torch.int32, device=DEV)
+    gi[3] = 2                                   # outside [0, G)
+    with pytest.raises(GPTQ4Error) as e:
+        q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), gi.data_ptr(), 256, 256, 128)
+    assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
+    gi = (torch.arange(256, device=DEV, dtype=torch.int32) % 3 == 0).to(torch.int32)   # uneven groups
+    with pytest.raises(GPTQ4Error) as e:
+        q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), gi.data_ptr(), 256, 256, 128)
+    assert e.value.status == q4.GPTQ_Q4_UNSUPPORTED
+    host = np.zeros((32, 256), np.int32)
+    with pytest.raises(GPTQ4Error) as e:       # host pointer
+        q4.gptq_q4_make(host.ctypes.data, qz.data_ptr(), sc.data_ptr(), None, 256, 256, 128)
+    assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
+    h = q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), None, 256, 256, 128)
+    try:
+        x = torch.zeros((4, 256), dtype=torch.float16, device=DEV)
+        out = torch.empty((4, 256), dtype=torch.float16, device=DEV)
+        with pytest.raises(GPTQ4Error) as e:   # misaligned x
+            q4.gptq_q4_matmul(h, x.data_ptr() + 2, 3, out.data_ptr(), 0)
+        assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
+        with pytest.raises(GPTQ4Error) as e:
+            q4.gptq_q4_matmul(h, x.data_ptr(), -1, out.data_ptr(), 0)
+        assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
+        assert q4.gptq_q4_matmul(h, 0, 0, 0, 0) == 0
+    finally:
+        q4.gptq_q4_free(h)
