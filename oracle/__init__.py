@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 from dataclasses import dataclass
@@ -33,7 +34,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gptq_oracle.c")
-_BUILD_DIR = os.path.join(_HERE, "_build")
+_BUILD_DIR = os.path.join(_HERE, "_build", platform.machine())
 _LIB_PATH = os.path.join(_BUILD_DIR, "libgptq_oracle.so")
 _lib = None
 _lock = threading.Lock()

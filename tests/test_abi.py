@@ -20,10 +20,11 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib_path():
-    from gptq_bit_weight_gb300 import build
-    if not os.path.exists(build.LIB):
-        build.build()
-    return build.LIB
+    import __graft_entry__
+    b = __graft_entry__._cuda_build_module()
+    if not os.path.exists(b.LIB):
+        b.build()
+    return b.LIB
 
 
 def test_header_declares_the_contract():
