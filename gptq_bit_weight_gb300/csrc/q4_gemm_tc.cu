@@ -1,15 +1,470 @@
-// Tensor-core (tcgen05) GEMM and fused prefill: not built yet.
+// Tensor-core (tcgen05 / TMEM / TMA) GEMMs for the prefill side of the GPTQ
+// W4A16 linear layer, on sm_103a.
+//
+//   dense:  out = a . b + bias, a [M][K] fp16, b [K][N] fp16 (the matmul on
+//           the dequantized matrix temp_dq "during prefill" of
+//           "Implementation: Predibase Lorax GPTQ Exllama V1", "Description")
+//   fused:  out = x . W + bias with W read packed (4-bit) and dequantized in
+//           shared memory inside the main loop, never written to HBM (the
+//           fused principle of "GPTQ's 'Exllama Kernel Not Installed'
+//           Warning", "What the fallback actually does").
+//
+// One CTA computes a 128 x 256 output tile with fp32 accumulators in tensor
+// memory (256 TMEM columns).  Warp roles:
+//   warp 0       one thread issues TMA loads into a ring of shared-memory
+//                stages (activations; dense: weight tiles; fused: packed
+//                words plus the stage's scales and zero points)
+//   warp 1       allocates TMEM; one thread issues tcgen05.mma (M=128,
+//                N=256, K=16) and commits each stage back to the producer
+//   warps 2..    fused: dequantize the packed words of a stage straight into
+//                the K-major, 128-byte-swizzled B operand layout; then all of
+//                them read TMEM (tcgen05.ld), add bias in fp32, round once to
+//                fp16 and store.
+// Every wait on an mbarrier is bounded (about two seconds of global time);
+// a wait that runs out records an error bit in the caller's status word,
+// stops its role, and the CTA still frees its TMEM before returning.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
 #include <climits>
+#include <cstdint>
+#include <mutex>
 
 #include "q4_internal.cuh"
 
 namespace q4 {
-cudaError_t launch_gemm_f16(const uint16_t *, const uint16_t *, const uint16_t *, int, int, int, uint16_t *, int *,
-                            cudaStream_t) {
-    return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kABytes = BM * BK * 2;         // 16 KB activation tile
+constexpr int kBBytes = BN * BK * 2;         // 32 KB weight tile (fp16)
+constexpr int kPBytes = BN * BK / 2;         // 8 KB packed weight tile
+constexpr int kSzBytes = 2 * 16 * 8 * 4 + 2 * 32 * 4;   // scales + zeros for up to two groups
+constexpr uint32_t kTmemCols = 256;
+
+template <bool FUSED>
+struct Cfg {
+    static constexpr int kStages = FUSED ? 3 : 4;
+    static constexpr int kAOff = 0;
+    static constexpr int kBOff = kABytes;
+    static constexpr int kPOff = kABytes + kBBytes;
+    static constexpr int kSzOff = kPOff + kPBytes;
+    static constexpr int kStageBytes = FUSED ? ((kSzOff + kSzBytes + 1023) / 1024) * 1024 : kABytes + kBBytes;
+    static constexpr int kWorkerWarps = FUSED ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kWorkerWarps;
+    static constexpr int kBarBytes = 8 * (3 * kStages + 1) + 16;
+    static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-cudaError_t launch_prefill(const HandleView &, const uint16_t *, int, uint16_t *, cudaStream_t) {
-    return cudaErrorNotSupported;
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-int prefill_default_min_m() { return INT_MAX; }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of the given parity to complete, for at most ~2 s.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > 2000000000ull) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (16-byte units), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, A K-major,
+// B K-major (fused: rows are output columns) or N-major (dense b [K][N]).
+__host__ __device__ constexpr uint32_t make_idesc(bool b_n_major) {
+    return (1u << 4) | ((b_n_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+           (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+struct TcArgs {
+    int M, N, K;
+    const uint16_t *bias;
+    uint16_t *out;
+    int *status;
+    const uint32_t *s2;      // fused: scale pairs [G][N/16][8]
+    const uint32_t *zeros;   // fused: zero words [G][N/8]
+    int bpg;                 // fused: 32-row blocks per group
+};
+
+__device__ __forceinline__ void record_error(int *status, int bit, int *abort_flag) {
+    if (status) atomicOr(status, bit);
+    atomicExch(abort_flag, 1);
+}
+
+template <bool FUSED>
+__global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+    using C = Cfg<FUSED>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + S * C::kStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto ready_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    const uint32_t done_bar = bar0 + 8u * (3 * S);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + S * C::kStageBytes + 8 * (3 * S + 1));
+    int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int KB = a.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(ready_bar(s), C::kWorkerWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+                if (!mbar_wait(empty_bar(s), ph ^ 1)) {
+                    record_error(a.status, 0x1, abort_flag);
+                    break;
+                }
+                const uint32_t st = base + s * C::kStageBytes;
+                if constexpr (FUSED) {
+                    const int nt0 = n0 >> 4;
+                    const int NT16 = a.N >> 4;
+                    const int tiles = min(16, NT16 - nt0);
+                    const int g_first = (2 * kb) / a.bpg, g_last = (2 * kb + 1) / a.bpg;
+                    const int ng = g_last - g_first + 1;
+                    const uint32_t sbytes = tiles * 32u, zbytes = tiles * 8u;
+                    mbar_arrive_expect_tx(full_bar(s), kABytes + kPBytes + ng * (sbytes + zbytes));
+                    tma_load_2d(st + C::kAOff, &tmA, full_bar(s), kb * BK, m0);
+                    tma_load_2d(st + C::kPOff, &tmB, full_bar(s), kb * 128, nt0);
+                    for (int gi = 0; gi < ng; ++gi) {
+                        const size_t gr = static_cast<size_t>(g_first + gi);
+                        bulk_load(st + C::kSzOff + gi * 512, a.s2 + (gr * NT16 + nt0) * 8, sbytes, full_bar(s));
+                        bulk_load(st + C::kSzOff + 1024 + gi * 128, a.zeros + gr * (a.N >> 3) + nt0 * 2, zbytes,
+                                  full_bar(s));
+                    }
+                } else {
+                    const int nb = min(4, (a.N - n0) / 64);
+                    mbar_arrive_expect_tx(full_bar(s), kABytes + nb * (BK * 64 * 2));
+                    tma_load_2d(st + C::kAOff, &tmA, full_bar(s), kb * BK, m0);
+                    for (int j = 0; j < nb; ++j)
+                        tma_load_2d(st + C::kBOff + j * (BK * 64 * 2), &tmB, full_bar(s), n0 + 64 * j, kb * BK);
+                }
+                ++issued;
+            }
+            if (*reinterpret_cast<volatile int *>(abort_flag)) {
+                // Let copies already in flight land before the CTA can exit.
+                for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb)
+                    mbar_wait(full_bar(kb % S), (kb / S) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(!FUSED);
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (*reinterpret_cast<volatile int *>(abort_flag) ||
+                    !mbar_wait(FUSED ? ready_bar(s) : full_bar(s), ph)) {
+                    record_error(a.status, 0x2, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = base + s * C::kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(st + C::kAOff + kk * 32, 16, 1024);
+                    const uint64_t bd = FUSED ? smem_desc_sw128(st + C::kBOff + kk * 32, 16, 1024)
+                                              : smem_desc_sw128(st + C::kBOff + kk * 2048, BK * 64 * 2, 1024);
+                    umma_f16(tmem, ad, bd, idesc, (kb | kk) != 0);
+                }
+                umma_commit(empty_bar(s));
+            }
+            if (ok) umma_commit(done_bar);
+        }
+    } else {
+        const int wi = warp - 2;
+        if constexpr (FUSED) {
+            // -------------------------------------------- dequantize into B
+            const int t = threadIdx.x - 64;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (kb / S) & 1;
+                if (*reinterpret_cast<volatile int *>(abort_flag)) break;
+                if (!mbar_wait(full_bar(s), ph)) {
+                    record_error(a.status, 0x4, abort_flag);
+                    break;
+                }
+                uint8_t *st = sbase + s * C::kStageBytes;
+                const uint4 *P = reinterpret_cast<const uint4 *>(st + C::kPOff);
+                const uint32_t *S2s = reinterpret_cast<const uint32_t *>(st + C::kSzOff);
+                const uint32_t *Zs = S2s + 256;
+                uint8_t *B = st + C::kBOff;
+                const int g0 = (2 * kb) / a.bpg;
+                const int gl1 = (2 * kb + 1) / a.bpg - g0;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int u = t + 256 * i;
+                    const int ntl = u >> 5, ls = u & 31, gq = ls >> 2, tq = ls & 3;
+                    const uint4 w4 = P[u];
+                    const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int n = 16 * ntl + gq + 8 * (j & 1);
+                        const int kch = 4 * (j >> 1) + tq;
+                        const int gl = (j >> 1) ? gl1 : 0;
+                        const uint32_t sp = S2s[gl * 128 + ntl * 8 + gq];
+                        const uint32_t sb = (j & 1) ? (sp >> 16) : (sp & 0xFFFFu);
+                        const uint32_t sv = sb | (sb << 16);
+                        const uint32_t zw = Zs[gl * 32 + ntl * 2 + (j & 1)];
+                        const uint32_t z = (zw >> (4 * gq)) & 0xFu;
+                        uint32_t q[4];
+                        unpack_qz(words[j], neg_zlo(z), neg_zhi(z), q);
+                        uint4 o;
+                        o.x = hmul2(q[0], sv);
+                        o.y = hmul2(q[1], sv);
+                        o.z = hmul2(q[2], sv);
+                        o.w = hmul2(q[3], sv);
+                        *reinterpret_cast<uint4 *>(B + (n >> 3) * 1024 + (n & 7) * 128 + ((kch ^ (n & 7)) << 4)) = o;
+                    }
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ready_bar(s));
+            }
+        }
+        // ------------------------------------------------ epilogue
+        const bool have = !*reinterpret_cast<volatile int *>(abort_flag);
+        bool ok = have && mbar_wait(done_bar, 0);
+        if (have && !ok) record_error(a.status, 0x8, abort_flag);
+        __syncwarp();
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            const int quad = warp & 3;
+            constexpr int kColsPerWarp = BN * 4 / C::kWorkerWarps;
+            const int c_beg = (wi >> 2) * kColsPerWarp;
+            const int row = m0 + 32 * quad + lane;
+#pragma unroll 1
+            for (int c0 = c_beg; c0 < c_beg + kColsPerWarp; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_x32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + c0, r);
+                if (row < a.M) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int n = n0 + c0 + 8 * v;
+                        if (n < a.N) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float lo = __uint_as_float(r[8 * v + 2 * e]);
+                                float hi = __uint_as_float(r[8 * v + 2 * e + 1]);
+                                if (a.bias) {
+                                    lo += __half2float(__ushort_as_half(a.bias[n + 2 * e]));
+                                    hi += __half2float(__ushort_as_half(a.bias[n + 2 * e + 1]));
+                                }
+                                pk[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+                                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+                            }
+                            *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool FUSED>
+cudaError_t ensure_smem_attr() {
+    static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg<FUSED>::kSmem);
+    return st;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
+                            uint16_t *out, int *status, cudaStream_t s) {
+    CUtensorMap tmA, tmB;
+    cudaError_t e;
+    if ((e = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a, K, M, static_cast<uint64_t>(K) * 2, BK, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if ((e = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, N, K, static_cast<uint64_t>(N) * 2, 64, BK,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if ((e = ensure_smem_attr<false>()) != cudaSuccess) return e;
+    TcArgs args{M, N, K, bias, out, status, nullptr, nullptr, 1};
+    dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+    tc_gemm_kernel<false><<<grid, Cfg<false>::kThreads, Cfg<false>::kSmem, s>>>(tmA, tmB, args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+    CUtensorMap tmA, tmW;
+    cudaError_t e;
+    const int KC = h.K / 64;
+    if ((e = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, h.K, M, static_cast<uint64_t>(h.K) * 2, BK, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
+                       static_cast<uint64_t>(KC) * 512, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+        return e;
+    if ((e = ensure_smem_attr<true>()) != cudaSuccess) return e;
+    TcArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32};
+    dim3 grid((h.N + BN - 1) / BN, (M + BM - 1) / BM);
+    tc_gemm_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmem, s>>>(tmA, tmW, args);
+    return cudaGetLastError();
+}
+
+int prefill_default_min_m() { return 64; }
+
 }  // namespace q4

@@ -1,0 +1,104 @@
+"""GPU parity of the tensor-core (tcgen05) paths: the dense fp16 GEMM on a
+dequantized matrix, the unfused prefill (dequantize to temp_dq + GEMM) and
+the fused prefill (shared-memory dequantization inside the GEMM main loop),
+each against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def q4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gptq_bit_weight_gb300 as q4mod
+    return q4mod
+
+
+def to_dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def check(y_gpu, y_ref, tol, what):
+    y = y_gpu.float().cpu().numpy().astype(np.float64)
+    err = np.abs(y - y_ref)
+    bad = err > tol
+    ratio = float(np.max(err / np.maximum(tol, 1e-300)))
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, worst err/tol {ratio:.3f}"
+    return ratio
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 64, 64), (64, 128, 256), (128, 256, 320), (200, 1024, 512),
+                                   (300, 576, 768), (513, 2048, 1024)])
+def test_gemm_f16_matches_oracle(q4, M, K, N):
+    g = np.random.default_rng(31 + M + K + N)
+    a = g.standard_normal((M, K)).astype(np.float16)
+    b = (g.standard_normal((K, N)) * 0.05).astype(np.float16)
+    bias = (g.standard_normal(N) * 0.1).astype(np.float16)
+    y = q4.gemm_f16(to_dev(a), to_dev(b), to_dev(bias))
+    torch.cuda.synchronize()
+    a64 = a.astype(np.float64)
+    b64 = b.astype(np.float64)
+    y_ref = oracle.linear_f64(a64, b64, bias.astype(np.float64))
+    tol = oracle.tolerance(a, b, y_ref, K)
+    check(y, y_ref, tol, f"gemm M={M} K={K} N={N}")
+
+
+LAYERS = [  # (K, N, groupsize, act_order)
+    (64, 64, 32, False),
+    (256, 320, 64, False),
+    (512, 256, 128, True),
+    (1024, 448, 32, True),
+    (1088, 576, 96, False),     # group of three 32-row blocks: some stages span two groups
+    (2048, 512, -1, False),
+]
+
+
+@pytest.mark.parametrize("K,N,gs,act", LAYERS)
+def test_prefill_fused_and_unfused_match_oracle(q4, K, N, gs, act):
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(32, K, N, gs & 0xFFFF, act))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs)
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                      to_dev(layer.bias), gs)
+    mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
+    for M in (1, 5, 127, 128, 129, 300):
+        x = synthetic.activations(M, K, key=(32, K, N, M))
+        y_ref = oracle.reference_output(x, dq, layer.bias)
+        tol = oracle.tolerance(x, dq.w16, y_ref, K)
+        y = mat(to_dev(x))
+        yu = mat.matmul_unfused(to_dev(x))
+        torch.cuda.synchronize()
+        check(y, y_ref, tol, f"fused K={K} N={N} g={gs} act={act} M={M}")
+        check(yu, y_ref, tol, f"unfused K={K} N={N} g={gs} act={act} M={M}")
+    mat.device_error()
+
+
+@pytest.mark.parametrize("K,N,act", [(4096, 4096, False), (4096, 11008, True), (11008, 4096, False)])
+def test_prefill_7b_workload_sampled(q4, K, N, act):
+    """prefill_7b shapes at M=512: full output, oracle on a row sample (all
+    N columns of 24 seeded rows, plus the first and last row)."""
+    M = 512
+    layer = synthetic.workload_layer("prefill_7b", K, N, 128, act)
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, 128)
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                      None, 128)
+    x = synthetic.workload_x("prefill_7b", K, N, 128, act, M)
+    rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(33).choice(M, 24, replace=False)]))
+    y_ref = oracle.reference_output(x[rows], dq)
+    tol = oracle.tolerance(x, dq.w16, y_ref, K)
+    mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
+    y = mat(to_dev(x))
+    yu = mat.matmul_unfused(to_dev(x))
+    mat.set_path(q4.GPTQ_Q4_PATH_DECODE)
+    yd = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check(y[rows], y_ref, tol, f"fused {K}x{N}")
+    check(yu[rows], y_ref, tol, f"unfused {K}x{N}")
+    check(yd[rows], y_ref, tol, f"decode path {K}x{N}")
+    mat.device_error()
