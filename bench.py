@@ -353,9 +353,73 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src):
-    """prefill_7b: M in {512, 2048} on the three 7B shapes, fused tensor-core path."""
-    return None
+def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
+    """prefill_7b: M in {512, 2048} x the three 7B shapes x {trivial, act-order}.
+
+    Fused (shared-memory dequantization inside the tcgen05 GEMM) against the
+    unfused route (dequantize to temp_dq, then the tcgen05 GEMM on it).  Each
+    case is timed with CUDA events over `reps` back-to-back calls after a
+    warm-up; the work is compute-bound, so the 129 MB L2 does not flatter it."""
+    sptr = stream.cuda_stream
+    cases, tot_flops, tot_fused, tot_unf = {}, 0.0, 0.0, 0.0
+    per_launch = []
+    for act in (False, True):
+        for (K, N) in synthetic.PREFILL_7B_SHAPES:
+            L = synthetic.workload_layer("prefill_7b", K, N, 128, act)
+            mat = q4.Q4Matrix(torch.from_numpy(L.qweight).to(dev), torch.from_numpy(L.qzeros).to(dev),
+                              torch.from_numpy(L.scales).to(dev),
+                              None if L.g_idx is None else torch.from_numpy(L.g_idx).to(dev), None, 128)
+            mat.reserve(max(synthetic.PREFILL_7B_M))
+            temp_dq = torch.empty((K, N), dtype=torch.float16, device=dev)
+            for M in synthetic.PREFILL_7B_M:
+                x = torch.from_numpy(synthetic.workload_x("prefill_7b", K, N, 128, act, M)).to(dev)
+                out = torch.empty((M, N), dtype=torch.float16, device=dev)
+
+                def fused():
+                    q4.gptq_q4_matmul(mat.handle, x.data_ptr(), M, out.data_ptr(), sptr)
+
+                def unfused():
+                    q4.gptq_q4_matmul_unfused(mat.handle, x.data_ptr(), M, temp_dq.data_ptr(), out.data_ptr(), sptr)
+
+                mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
+                times = {}
+                for name, fn in (("fused", fused), ("unfused", unfused)):
+                    for _ in range(3):
+                        fn()
+                    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                           for _ in range(reps)]
+                    for a, b in evs:
+                        a.record(stream)
+                        fn()
+                        b.record(stream)
+                    torch.cuda.synchronize()
+                    times[name] = float(np.median([a.elapsed_time(b) for a, b in evs]))
+                flops = 2.0 * M * K * N
+                tot_flops += flops
+                tot_fused += times["fused"]
+                tot_unf += times["unfused"]
+                if not act:
+                    per_launch.append((flops, times["fused"]))
+                cases[f"{K}x{N} M={M}{' act' if act else ''}"] = {
+                    "fused_us": round(times["fused"] * 1e3, 1),
+                    "fused_TFLOPS": round(flops / (times["fused"] * 1e-3) / 1e12, 1),
+                    "unfused_us": round(times["unfused"] * 1e3, 1),
+                    "unfused_TFLOPS": round(flops / (times["unfused"] * 1e-3) / 1e12, 1)}
+            mat.close()
+            del temp_dq
+    fused_tf = tot_flops / (tot_fused * 1e-3) / 1e12
+    kern_flops = sum(f for f, _ in per_launch)
+    kern_ms = sum(t for _, t in per_launch)
+    achieved = kern_flops / (kern_ms * 1e-3) / 1e12
+    return {
+        "workload": "prefill_7b", "metric": "prefill TFLOPS (2*M*K*N / time)", "value": fused_tf,
+        "unit": "TFLOP/s", "unfused_value": tot_flops / (tot_unf * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_tf, "traffic": None, "kernel": "tc_gemm_kernel<true> (fused prefill)",
+                     "peak_source": f"{peak_src} bf16 burst x 1 (fp16 and bf16 dense rates are equal)",
+                     "how": "trivial-g_idx cases: 2*M*K*N summed / per-call CUDA-event time summed"},
+        "cases": cases,
+    }
 
 
 def main():

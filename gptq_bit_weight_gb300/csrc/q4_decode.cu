@@ -33,6 +33,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "q4_internal.cuh"
 
@@ -54,13 +55,14 @@ struct DecodeArgs {
     int M;
     int splits;
     int slice_chunks;
+    int xrows;          // rows of x staged per CTA: min(8*MT, M)
 };
 
 __host__ __device__ inline int x_row_stride(int slice_chunks) { return slice_chunks * 64 + 32; }
 
 template <int MT>
-__host__ __device__ inline size_t smem_bytes(int slice_chunks, int max_groups) {
-    return static_cast<size_t>(8 * MT) * x_row_stride(slice_chunks) * 2     // x slice
+__host__ __device__ inline size_t smem_bytes(int xrows, int slice_chunks, int max_groups) {
+    return static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2      // x slice
            + static_cast<size_t>(kWarps) * kNTW * MT * 128 * 4              // warp partials
            + static_cast<size_t>(max_groups) * kNTW * 10 * 4;              // scale pairs + zero words
 }
@@ -70,7 +72,7 @@ __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : (MT == 2 ? 2 : 1)) decode_kernel(HandleView h, DecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gq = lane >> 2, tq = lane & 3;
@@ -87,20 +89,36 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeAr
     const int bpg = geff >> 5;                          // 32-row blocks per group
 
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + static_cast<size_t>(8 * MT) * XS * 2);
+    float *red = reinterpret_cast<float *>(smem + static_cast<size_t>(a.xrows) * XS * 2);
     uint32_t *gsz = reinterpret_cast<uint32_t *>(red + kWarps * kNTW * MT * 128);
 
-    // ---- stage x[m0 : m0 + 8MT][slice] (zero rows past M) and the slice's
-    //      scale pairs / zero words for this CTA's two column tiles.
+    // Let the next kernel in the stream start its own prologue as soon as
+    // every CTA of this grid is resident (programmatic dependent launch).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int wc_beg = c_beg + (nch * warp) / kWarps;
+    const int wc_end = c_beg + (nch * (warp + 1)) / kWarps;
+    const int wn = wc_end - wc_beg;
+    const int g_base = (c_beg * 64) / geff;
+
+    // ---- first kDepth chunks of packed weights: handle-owned constant data,
+    //      so the loads may be issued before the preceding grid has finished.
+    const uint4 *wbase[kNTW];
+#pragma unroll
+    for (int nt = 0; nt < kNTW; ++nt)
+        wbase[nt] = h.wp + (static_cast<size_t>(nt0 + nt) * KC + wc_beg) * 32 + lane;
+    uint4 buf[kDepth][kNTW];
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+        if (i < wn)
+#pragma unroll
+            for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(i) * 32);
+
+    // ---- stage the slice's scale pairs / zero words for this CTA's two
+    //      column tiles (constant), then, once the preceding grid is done,
+    //      x[m0 : m0 + xrows][slice].  Lanes whose x row is past M use zeros
+    //      without reading shared memory.
     {
-        const int vpr = nch * 8;                        // 16-byte vectors per row
-        for (int i = threadIdx.x; i < 8 * MT * vpr; i += kThreads) {
-            const int r = i / vpr, c = i - r * vpr;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < mrows)
-                v = __ldg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64 + c * 8));
-            *reinterpret_cast<uint4 *>(xs + r * XS + c * 8) = v;
-        }
         const int g_beg = (c_beg * 64) / geff;
         const int g_end = (c_end * 64 - 1) / geff + 1;
         const int ng = g_end - g_beg;
@@ -113,13 +131,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeAr
             else v = __ldg(h.zeros + gr * (N >> 3) + (nt0 + nt) * 2 + (w - 8));
             gsz[i] = v;
         }
+        // x, the workspace, the tickets and out may belong to the preceding
+        // grid: wait for it (a no-op without programmatic dependent launch).
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int vpr = nch * 8;                        // 16-byte vectors per row
+        for (int i = threadIdx.x; i < a.xrows * vpr; i += kThreads) {
+            const int r = i / vpr, c = i - r * vpr;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < mrows)
+                v = __ldg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64 + c * 8));
+            *reinterpret_cast<uint4 *>(xs + r * XS + c * 8) = v;
+        }
     }
     __syncthreads();
-
-    const int wc_beg = c_beg + (nch * warp) / kWarps;
-    const int wc_end = c_beg + (nch * (warp + 1)) / kWarps;
-    const int wn = wc_end - wc_beg;
-    const int g_base = (c_beg * 64) / geff;
 
     float acc[kNTW][MT][4], accg[kNTW][MT][4];
 #pragma unroll
@@ -164,18 +188,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeAr
         };
         load_group(grp);
 
-        const uint4 *wbase[kNTW];
-#pragma unroll
-        for (int nt = 0; nt < kNTW; ++nt)
-            wbase[nt] = h.wp + (static_cast<size_t>(nt0 + nt) * KC + wc_beg) * 32 + lane;
-
-        uint4 buf[kDepth][kNTW];
-#pragma unroll
-        for (int i = 0; i < kDepth; ++i)
-            if (i < wn)
-#pragma unroll
-                for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(i) * 32);
-
         for (int base = 0; base < wn; base += kDepth) {
 #pragma unroll
             for (int i = 0; i < kDepth; ++i) {
@@ -192,8 +204,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeAr
                         const int kk = (2 * (wc_beg + c - c_beg) + hh) * 32 + 8 * tq;
                         uint4 xb[MT];
 #pragma unroll
-                        for (int mt = 0; mt < MT; ++mt)
-                            xb[mt] = *reinterpret_cast<const uint4 *>(xs + (mt * 8 + gq) * XS + kk);
+                        for (int mt = 0; mt < MT; ++mt) {
+                            xb[mt] = make_uint4(0u, 0u, 0u, 0u);
+                            if (mt * 8 + gq < mrows)
+                                xb[mt] = *reinterpret_cast<const uint4 *>(xs + (mt * 8 + gq) * XS + kk);
+                        }
 #pragma unroll
                         for (int nt = 0; nt < kNTW; ++nt) {
                             const uint32_t lo = hh ? buf[i][nt].z : buf[i][nt].x;
@@ -285,20 +300,38 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(HandleView h, DecodeAr
     if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
 }
 
+// Programmatic dependent launch is on unless GPTQ_Q4_PDL=0.
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("GPTQ_Q4_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 template <int MT>
 cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                       uint16_t *out, cudaStream_t s) {
-    const size_t smem = smem_bytes<MT>(p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
+    const int xrows = M < 8 * MT ? M : 8 * MT;
+    const size_t smem = smem_bytes<MT>(xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
     static bool configured = false;   // per template instance; attribute is per-function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks};
-    dim3 grid(p.ctas_n, p.splits, p.zdim);
-    decode_kernel<MT><<<grid, kThreads, smem, s>>>(h, a);
-    return cudaGetLastError();
+    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.ctas_n, p.splits, p.zdim);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<MT>, h, a);
 }
 
 }  // namespace
