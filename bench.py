@@ -67,6 +67,32 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+# --------------------------------------------------------- replicas (N > 1)
+# Every rank runs the same workload on its own GPU (weak scaling); there is no
+# data-path collective.  The only cross-rank traffic is the barrier around the
+# timed region and the max of the per-rank times.
+
+def rank_barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks_value(v: float, world: int, device) -> float:
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job rate in TB/s: the units all ranks processed over the slowest rank's time."""
+    return bytes_per_rank_per_step * steps * world / seconds / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -233,18 +259,11 @@ def run_native(args):
             q4.gptq_q4_matmul(mats[s][r].handle, xs[(s, M)].data_ptr(), M, outs[(s, M)].data_ptr(), sptr)
 
     def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        rank_barrier(world)
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        import torch.distributed as dist
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_value(v, world, dev)
 
     with ClockSampler(local) as clk:
         t_end = time.perf_counter() + args.soak_s
@@ -277,7 +296,7 @@ def run_native(args):
             per_call.append([a.elapsed_time(b) for (a, b) in evs])
     clocks = clk.summary()
 
-    value = step_bytes * args.steps * world / (ms * 1e-3) / 1e12
+    value = job_throughput(step_bytes, args.steps, world, ms * 1e-3)
     kern_ms = float(np.sum(np.median(np.array(per_call), axis=0)))
     achieved_gbs = step_bytes / (kern_ms * 1e-3) / 1e9
     launches_per_step = len(calls)
@@ -312,7 +331,7 @@ def run_native(args):
         e2e_step()
     barrier()
     e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e_value = step_bytes * args.steps * world / e2e_s / 1e12
+    e2e_value = job_throughput(step_bytes, args.steps, world, e2e_s)
 
     prefill = None
     if not args.no_prefill:
