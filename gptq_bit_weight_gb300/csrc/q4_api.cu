@@ -356,7 +356,7 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(cuda_fail(e, "repack"));
     cudaStreamDestroy(s);
     s = nullptr;
-    const q4::DecodePlan p = q4::plan_decode(decode_max_ws_rows(), K, N);
+    const q4::DecodePlan p = q4::plan_decode(decode_max_ws_rows(), K, N, geff);
     if (ensure_decode_work(h, p.ws_floats, p.n_tickets, nullptr, true)) return fail(0);
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail(cuda_fail(e, "make"));
     ok();
@@ -387,12 +387,12 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
     size_t ws = 0;
     int nt = 0;
     for (int m = 1; m <= std::min(max_m, 64); ++m) {
-        const q4::DecodePlan p = q4::plan_decode(m, h->K, h->N);
+        const q4::DecodePlan p = q4::plan_decode(m, h->K, h->N, h->geff);
         ws = std::max(ws, p.ws_floats);
         nt = std::max(nt, p.n_tickets);
     }
     if (max_m > 64) {
-        const q4::DecodePlan p = q4::plan_decode(max_m, h->K, h->N);
+        const q4::DecodePlan p = q4::plan_decode(max_m, h->K, h->N, h->geff);
         ws = std::max(ws, p.ws_floats);
         nt = std::max(nt, p.n_tickets);
     }
@@ -417,7 +417,7 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N);
+    const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N, h->geff);
     if (int r = ensure_decode_work(h, p.ws_floats, p.n_tickets, stream, false)) return r;
     q4::DecodeWork w{h->ws, h->ws_floats, h->tickets, h->n_tickets};
     Q4_CUDA(q4::launch_decode(v, p, w, xin, M, out, stream), "decode launch");

@@ -67,6 +67,11 @@ __host__ __device__ inline size_t smem_bytes(int xrows, int slice_chunks, int ma
            + static_cast<size_t>(max_groups) * kNTW * 10 * 4;              // scale pairs + zero words
 }
 
+__host__ __device__ inline size_t smem_bytes_for(int mt, int xrows, int slice_chunks, int max_groups) {
+    return static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2 +
+           static_cast<size_t>(kWarps) * kNTW * mt * 128 * 4 + static_cast<size_t>(max_groups) * kNTW * 10 * 4;
+}
+
 __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
     return (slice_chunks * 64 + geff - 1) / geff + 1;
 }
@@ -336,28 +341,67 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
 
 }  // namespace
 
-DecodePlan plan_decode(int M, int K, int N) {
+// Resident CTAs per SM for a variant: registers (the launch bounds) and
+// shared memory, whichever is tighter.
+int resident_ctas(int mt, size_t smem) {
+    const int by_regs = mt == 1 ? 3 : (mt == 2 ? 2 : 1);
+    const size_t per_sm = 228 * 1024;                   // shared memory per SM
+    const int by_smem = static_cast<int>(per_sm / (smem + 1024));
+    return std::max(1, std::min(by_regs, by_smem));
+}
+
+// Split count.  Every slice fits the 64 KB x staging.  When the grid fits in
+// one wave of resident CTAs, take the most splits that still fit (the most
+// bytes in flight while the whole grid is one DRAM round trip deep); when it
+// does not, fill whole waves as closely as possible (fewer splits on a tie).
+DecodePlan plan_decode(int M, int K, int N, int geff) {
     DecodePlan p{};
     p.mt = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
     p.zdim = (M + 8 * p.mt - 1) / (8 * p.mt);
     p.ctas_n = N / kNB;
     const int KC = K / 64;
-    const int max_slice = 64 / p.mt;                    // x slice <= 64 KB of shared memory
-    const int min_slice = std::min(KC, 16);             // at least two chunks per warp
+    const int xrows = std::min(M, 8 * p.mt);
+    // x staging: xrows * slice * 64 fp16 <= 64 KB
+    const int max_slice = std::min(KC, std::max(8, std::min(64, 512 / xrows)));
     const int base = p.ctas_n * p.zdim;
-    const int target = 4 * kSMs;
-    int splits = (target + base - 1) / base;
-    splits = std::min(splits, std::max(1, KC / min_slice));
-    splits = std::max(splits, (KC + max_slice - 1) / max_slice);
-    splits = std::max(1, std::min(splits, KC));
-    p.slice_chunks = (KC + splits - 1) / splits;
+    const int min_splits = (KC + max_slice - 1) / max_slice;
+    const int max_splits = std::max(min_splits, KC / 16);   // at least two chunks per warp
+    auto slots_for = [&](int sp) {
+        const int slice = (KC + sp - 1) / sp;
+        const size_t smem = smem_bytes_for(p.mt, xrows, slice, max_groups_in_slice(slice, geff));
+        return static_cast<long long>(kSMs) * resident_ctas(p.mt, smem);
+    };
+    auto valid = [&](int sp) {
+        const int slice = (KC + sp - 1) / sp;
+        return (KC + slice - 1) / slice == sp;             // no empty slices
+    };
+    int best = min_splits;
+    if (static_cast<long long>(base) * min_splits <= slots_for(min_splits)) {
+        for (int sp = min_splits; sp <= max_splits; ++sp)
+            if (valid(sp) && static_cast<long long>(base) * sp <= slots_for(sp)) best = sp;
+    } else {
+        double best_eff = -1.0;
+        for (int sp = min_splits; sp <= max_splits; ++sp) {
+            if (!valid(sp)) continue;
+            const long long slots = slots_for(sp);
+            const long long ctas = static_cast<long long>(base) * sp;
+            const long long waves = (ctas + slots - 1) / slots;
+            const double eff = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+            if (eff > best_eff + 1e-9) {
+                best_eff = eff;
+                best = sp;
+            }
+            if (waves > 4) break;
+        }
+    }
+    p.slice_chunks = (KC + best - 1) / best;
     p.splits = (KC + p.slice_chunks - 1) / p.slice_chunks;
     p.n_tickets = base;
     p.ws_floats = p.splits > 1 ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
     return p;
 }
 
-size_t decode_ws_floats_for(int M, int K, int N) { return plan_decode(M, K, N).ws_floats; }
+size_t decode_ws_floats_for(int M, int K, int N, int geff) { return plan_decode(M, K, N, geff).ws_floats; }
 
 cudaError_t launch_decode(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                           uint16_t *out, cudaStream_t s) {

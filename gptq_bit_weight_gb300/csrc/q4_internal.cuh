@@ -136,8 +136,8 @@ struct DecodePlan {
     size_t ws_floats;  // workspace needed
     int n_tickets;
 };
-DecodePlan plan_decode(int M, int K, int N);
-size_t decode_ws_floats_for(int M, int K, int N);
+DecodePlan plan_decode(int M, int K, int N, int geff);
+size_t decode_ws_floats_for(int M, int K, int N, int geff);
 cudaError_t launch_decode(const HandleView &h, const DecodePlan &plan, const DecodeWork &w,
                           const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
 
