@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--soak-s", type=float, default=1.0)
+    p.add_argument("--only", choices=["decode", "prefill"], default=None,
+                   help="run one leg only (for profiling); the JSON line is then partial")
     return p.parse_args()
 
 
@@ -222,6 +224,14 @@ def run_native(args):
 
     import gptq_bit_weight_gb300 as q4
 
+    if args.only == "prefill":
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        _, bf16_tf, _, peak_src = peaks()
+        print(json.dumps({"prefill": run_prefill(q4, torch, dev, torch.cuda.current_stream(), bf16_tf, peak_src)}),
+              flush=True)
+        return
+
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -334,11 +344,11 @@ def run_native(args):
     e2e_value = job_throughput(step_bytes, args.steps, world, e2e_s)
 
     prefill = None
-    if not args.no_prefill:
+    if not args.no_prefill and args.only != "decode":
         prefill = run_prefill(q4, torch, dev, stream, bf16_tf, peak_src)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only is None:
         cpu = cpu_baseline_sample()
 
     if rank == 0:

@@ -319,12 +319,22 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
                       uint16_t *out, cudaStream_t s) {
     const int xrows = M < 8 * MT ? M : 8 * MT;
     const size_t smem = smem_bytes<MT>(xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
-    static bool configured = false;   // per template instance; attribute is per-function
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    // Opt in once to the largest dynamic shared memory the device allows
+    // next to the kernel's static shared memory.
+    static int max_dyn = -1;
+    if (max_dyn < 0) {
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT>);
+        const int want = optin - static_cast<int>(fa.sharedSizeBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess) return e;
-        configured = true;
+        max_dyn = want;
     }
+    if (smem > static_cast<size_t>(max_dyn)) return cudaErrorInvalidConfiguration;
     DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas_n, p.splits, p.zdim);

@@ -57,6 +57,7 @@ SMALL = [  # (K, N, groupsize, act_order)
     (512, 320, 128, True),
     (1024, 448, 32, True),
     (1088, 576, 64, False),     # K not a multiple of the split slices -> ragged chunks
+    (1152, 320, 96, True),      # group of three 32-row blocks
     (2048, 960, 128, False),
     (1024, 256, -1, True),      # one group: act-order reduces to the identity
 ]

@@ -55,7 +55,7 @@ LAYERS = [  # (K, N, groupsize, act_order)
     (256, 320, 64, False),
     (512, 256, 128, True),
     (1024, 448, 32, True),
-    (1088, 576, 96, False),     # group of three 32-row blocks: some stages span two groups
+    (1152, 576, 96, False),     # group of three 32-row blocks: some stages span two groups
     (2048, 512, -1, False),
 ]
 
