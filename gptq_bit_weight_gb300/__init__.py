@@ -37,7 +37,7 @@ EXPORTED = [
     "gptq_q4_make", "gptq_q4_set_bias", "gptq_q4_reserve", "gptq_q4_matmul", "gptq_q4_dequant",
     "gptq_q4_debug_unpack", "gptq_q4_matmul_unfused", "gptq_q4_gemm_f16", "gptq_q4_set_path",
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
-    "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count",
+    "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
 ]
 
 _P = ctypes.c_void_p
@@ -67,6 +67,9 @@ _sig("gptq_q4_free", None, _P)
 _sig("gptq_q4_last_status", _I)
 _sig("gptq_q4_last_error", ctypes.c_char_p)
 _sig("gptq_q4_launch_count", ctypes.c_uint64)
+_sig("gptq_q4_matmul_noalloc", _I, _P, _P, _I, _P, _P)
+
+GPTQ_Q4_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class GPTQ4Error(RuntimeError):
@@ -158,6 +161,12 @@ def gptq_q4_last_error() -> str:
 
 def gptq_q4_launch_count() -> int:
     return int(_lib.gptq_q4_launch_count())
+
+
+def gptq_q4_matmul_noalloc(h: int, x: int, M: int, out: int, stream: int) -> int:
+    """gptq_q4_matmul's decode path with its scratch in the library's fixed
+    device array: allocates nothing (see include/gptq_q4.h)."""
+    return _check(_lib.gptq_q4_matmul_noalloc(h, x or None, M, out or None, stream or None))
 
 
 # --------------------------------------------------------- torch marshalling

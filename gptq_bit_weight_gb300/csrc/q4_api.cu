@@ -26,26 +26,7 @@ cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16
 int prefill_default_min_m();
 }  // namespace q4
 
-struct gptq_q4_s {
-    int device = -1;
-    int K = 0, N = 0, groupsize = 0, geff = 0, G = 0;
-    int act_order = 0;
-    uint32_t *wp = nullptr;
-    uint32_t *s2 = nullptr;
-    uint32_t *zeros = nullptr;
-    int32_t *perm = nullptr;
-    uint16_t *bias = nullptr;
-    int *status = nullptr;
-    float *ws = nullptr;
-    size_t ws_floats = 0;
-    int *tickets = nullptr;
-    int n_tickets = 0;
-    uint16_t *temp_state = nullptr;
-    size_t temp_state_elems = 0;
-    int path = GPTQ_Q4_PATH_AUTO;
-    int prefill_min_m = 0;
-    size_t device_bytes = 0;
-};
+#include "q4_handle.h"
 
 namespace {
 
@@ -535,3 +516,13 @@ const char *gptq_q4_last_error(void) { return t_msg; }
 uint64_t gptq_q4_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+namespace q4 {
+int api_set_status(int code, const char *msg) { return set_status(code, msg ? "%s" : nullptr, msg); }
+int api_cuda_fail(cudaError_t e, const char *what) { return cuda_fail(e, what); }
+int api_check_matmul_args(gptq_q4_handle h, const void *x, int M, const void *out) {
+    return check_matmul_args(h, x, M, out);
+}
+HandleView api_view(const gptq_q4_s *h) { return view(h); }
+void api_count_launches(int n) { g_launches += static_cast<uint64_t>(n); }
+}  // namespace q4

@@ -181,6 +181,37 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M,
 int gptq_q4_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias,
                      int M, int K, int N, uint16_t *out, cudaStream_t stream);
 
+/* Bytes of the fixed device scratch used by gptq_q4_matmul_noalloc (16 MiB). */
+#define GPTQ_Q4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* out = x . W + bias through the decode kernel, allocating nothing.
+ *
+ * The web pages this library follows have no counterpart for this call.  It
+ * is for callers that cannot allocate device memory while they run a layer:
+ * a plugin inside a framework that owns all device memory, a service whose
+ * device memory is budgeted in full up front, a loop that must never hit
+ * cudaMalloc/cudaFree (which can synchronize the device).  gptq_q4_matmul may
+ * grow the handle's work buffers; this call never allocates or frees.
+ *
+ * It runs the decode kernel (any M) with its scratch -- split-K partial sums,
+ * per-tile tickets and, for act-order, temp_state -- taken from one static
+ * device array of GPTQ_Q4_NOALLOC_SCRATCH_BYTES bytes that every GPU loading
+ * the library holds until the process exits.  Arguments, layouts and results
+ * are those of gptq_q4_matmul (x, out: device fp16, 16-byte aligned).
+ *
+ *   - The first call on each device does a one-time set-up (it looks up the
+ *     array's device address with cudaGetSymbolAddress, with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     the call clears what must start at zero (the tickets) on its stream.
+ *     Calls that overlap on the GPU (other streams, other handles, other
+ *     threads) race on the array: order them, e.g. use one stream.
+ *   - Errors: as gptq_q4_matmul, plus INVALID_ARGUMENT when M (with this
+ *     layer's K and N) would need more scratch than the array holds; the
+ *     message gives both sizes. */
+int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
+                           cudaStream_t stream);
+
 /* Force a path for gptq_q4_matmul (tests, benchmarks): GPTQ_Q4_PATH_*. */
 int gptq_q4_set_path(gptq_q4_handle h, int path);
 
