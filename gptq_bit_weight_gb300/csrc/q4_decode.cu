@@ -41,11 +41,22 @@ namespace q4 {
 
 namespace {
 
-constexpr int kWarps = 8;
+// Tuning parameters (compile-time; the defaults are the measured choice).
+#ifndef Q4_DECODE_WARPS
+#define Q4_DECODE_WARPS 8
+#endif
+#ifndef Q4_DECODE_NTW
+#define Q4_DECODE_NTW 2
+#endif
+#ifndef Q4_DECODE_DEPTH
+#define Q4_DECODE_DEPTH 4
+#endif
+constexpr int kWarps = Q4_DECODE_WARPS;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kNTW = 2;             // 16-column tiles per CTA
+constexpr int kNTW = Q4_DECODE_NTW;             // 16-column tiles per CTA
 constexpr int kNB = 16 * kNTW;      // columns per CTA
-constexpr int kDepth = 4;           // chunks in the load ring
+constexpr int kDepth = Q4_DECODE_DEPTH;         // chunks in the load ring
+constexpr int kMaxCluster = 8;      // portable thread-block cluster size
 
 struct DecodeArgs {
     const uint16_t *x;
@@ -56,6 +67,7 @@ struct DecodeArgs {
     int splits;
     int slice_chunks;
     int xrows;          // rows of x staged per CTA: min(8*MT, M)
+    int cluster;        // slices reduce through distributed shared memory
 };
 
 __host__ __device__ inline int x_row_stride(int slice_chunks) { return slice_chunks * 64 + 32; }
@@ -76,8 +88,11 @@ __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
     return (slice_chunks * 64 + geff - 1) / geff + 1;
 }
 
+// Resident-CTA target per SM for the register budget: 24, 16 and 8 warps.
+constexpr int min_blocks(int mt) { return (mt == 1 ? 24 : (mt == 2 ? 16 : 8)) / kWarps > 0 ? (mt == 1 ? 24 : (mt == 2 ? 16 : 8)) / kWarps : 1; }
+
 template <int MT>
-__global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : (MT == 2 ? 2 : 1)) decode_kernel(HandleView h, DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(HandleView h, DecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gq = lane >> 2, tq = lane & 3;
@@ -119,10 +134,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : (MT == 2 ? 2 : 1)) dec
 #pragma unroll
             for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(i) * 32);
 
-    // ---- stage the slice's scale pairs / zero words for this CTA's two
-    //      column tiles (constant), then, once the preceding grid is done,
-    //      x[m0 : m0 + xrows][slice].  Lanes whose x row is past M use zeros
-    //      without reading shared memory.
+    // ---- stage the slice's scale pairs / zero words (constant) and, once
+    //      the preceding grid is done, x[m0 : m0 + mrows][slice], with
+    //      asynchronous global->shared copies: together with the weight loads
+    //      above they form a single round trip to memory.  Lanes whose x row
+    //      is past M use zeros without reading shared memory.
     {
         const int g_beg = (c_beg * 64) / geff;
         const int g_end = (c_end * 64 - 1) / geff + 1;
@@ -131,22 +147,19 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : (MT == 2 ? 2 : 1)) dec
             const int gl = i / (kNTW * 10), rest = i - gl * (kNTW * 10);
             const int nt = rest / 10, w = rest - nt * 10;
             const size_t gr = static_cast<size_t>(g_beg + gl);
-            uint32_t v;
-            if (w < 8) v = __ldg(h.s2 + (gr * NT16 + nt0 + nt) * 8 + w);
-            else v = __ldg(h.zeros + gr * (N >> 3) + (nt0 + nt) * 2 + (w - 8));
-            gsz[i] = v;
+            const uint32_t *src = (w < 8) ? h.s2 + (gr * NT16 + nt0 + nt) * 8 + w
+                                          : h.zeros + gr * (N >> 3) + (nt0 + nt) * 2 + (w - 8);
+            cp_async_4(gsz + i, src);
         }
         // x, the workspace, the tickets and out may belong to the preceding
         // grid: wait for it (a no-op without programmatic dependent launch).
         asm volatile("griddepcontrol.wait;" ::: "memory");
         const int vpr = nch * 8;                        // 16-byte vectors per row
-        for (int i = threadIdx.x; i < a.xrows * vpr; i += kThreads) {
+        for (int i = threadIdx.x; i < mrows * vpr; i += kThreads) {
             const int r = i / vpr, c = i - r * vpr;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < mrows)
-                v = __ldg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64 + c * 8));
-            *reinterpret_cast<uint4 *>(xs + r * XS + c * 8) = v;
+            cp_async_16(xs + r * XS + c * 8, a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64 + c * 8);
         }
+        cp_async_wait_all();
     }
     __syncthreads();
 
@@ -257,30 +270,49 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : (MT == 2 ? 2 : 1)) dec
         n = 16 * (nt0 + nt) + (l >> 2) + 8 * (i >> 1);
         m = m0 + mt * 8 + 2 * (l & 3) + (i & 1);
     };
-
-    const int tile_id = blockIdx.z * gridDim.x + blockIdx.x;
-    if (a.splits == 1) {
-        for (int e = threadIdx.x; e < E; e += kThreads) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += red[w * E + e];
-            int m, n;
-            element_mn(e, m, n);
-            if (m < a.M) {
-                if (h.bias) v += __half2float(__ushort_as_half(h.bias[n]));
-                a.out[static_cast<size_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
-            }
+    auto store_out = [&](int e, float v) {
+        int m, n;
+        element_mn(e, m, n);
+        if (m < a.M) {
+            if (h.bias) v += __half2float(__ushort_as_half(h.bias[n]));
+            a.out[static_cast<size_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
         }
-        return;
-    }
+    };
 
-    float *my_ws = a.ws + (static_cast<size_t>(tile_id) * a.splits + split) * E;
+    // CTA partial: the warps' partials summed in warp order, kept in red[0, E)
+    // (each thread reads its own elements of every warp before writing one).
     for (int e = threadIdx.x; e < E; e += kThreads) {
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) v += red[w * E + e];
-        __stcg(my_ws + e, v);
+        if (a.splits == 1) store_out(e, v);
+        else red[e] = v;
     }
+    if (a.splits == 1) return;
+
+    if (a.cluster) {
+        // The K slices of a column tile form one thread-block cluster: sum the
+        // slices' partials in slice order straight out of each other's shared
+        // memory.  Cluster rank r finishes elements [r E / S, (r + 1) E / S).
+        cluster_sync();
+        const int S = a.splits;
+        const int e0 = (split * E) / S, e1 = ((split + 1) * E) / S;
+        for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += kThreads) {
+            const uint32_t local = shared_addr(red + e);
+            float v = 0.f;
+            for (int r = 0; r < S; ++r) v += ld_dsmem_f32(local, r);
+            store_out(e, v);
+        }
+        cluster_sync();                                 // partials stay alive until all are read
+        return;
+    }
+
+    // Too many slices for one cluster: the partial goes to the workspace and
+    // the last CTA of the column tile to arrive (an atomic ticket; nobody
+    // waits) adds the slices in slice order.
+    const int tile_id = blockIdx.z * gridDim.x + blockIdx.x;
+    float *my_ws = a.ws + (static_cast<size_t>(tile_id) * a.splits + split) * E;
+    for (int e = threadIdx.x; e < E; e += kThreads) __stcg(my_ws + e, red[e]);
     __threadfence();
     __syncthreads();
     __shared__ int s_last;
@@ -293,14 +325,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : (MT == 2 ? 2 : 1)) dec
     __threadfence();
     const float *tile_ws = a.ws + static_cast<size_t>(tile_id) * a.splits * E;
     for (int e = threadIdx.x; e < E; e += kThreads) {
-        int m, n;
-        element_mn(e, m, n);
         float v = 0.f;
-        for (int s = 0; s < a.splits; ++s) v += __ldcg(tile_ws + static_cast<size_t>(s) * E + e);
-        if (m < a.M) {
-            if (h.bias) v += __half2float(__ushort_as_half(h.bias[n]));
-            a.out[static_cast<size_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
-        }
+        for (int sl = 0; sl < a.splits; ++sl) v += __ldcg(tile_ws + static_cast<size_t>(sl) * E + e);
+        store_out(e, v);
     }
     if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
 }
@@ -335,17 +362,28 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
         max_dyn = want;
     }
     if (smem > static_cast<size_t>(max_dyn)) return cudaErrorInvalidConfiguration;
-    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows};
+    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows, p.cluster};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas_n, p.splits, p.zdim);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.cluster) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = static_cast<unsigned>(p.splits);
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl_enabled()) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, decode_kernel<MT>, h, a);
 }
 
@@ -354,7 +392,7 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
 // Resident CTAs per SM for a variant: registers (the launch bounds) and
 // shared memory, whichever is tighter.
 int resident_ctas(int mt, size_t smem) {
-    const int by_regs = mt == 1 ? 3 : (mt == 2 ? 2 : 1);
+    const int by_regs = min_blocks(mt);
     const size_t per_sm = 228 * 1024;                   // shared memory per SM
     const int by_smem = static_cast<int>(per_sm / (smem + 1024));
     return std::max(1, std::min(by_regs, by_smem));
@@ -406,8 +444,9 @@ DecodePlan plan_decode(int M, int K, int N, int geff) {
     }
     p.slice_chunks = (KC + best - 1) / best;
     p.splits = (KC + p.slice_chunks - 1) / p.slice_chunks;
+    p.cluster = (p.splits > 1 && p.splits <= kMaxCluster) ? 1 : 0;
     p.n_tickets = base;
-    p.ws_floats = p.splits > 1 ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
+    p.ws_floats = (p.splits > 1 && !p.cluster) ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
     return p;
 }
 

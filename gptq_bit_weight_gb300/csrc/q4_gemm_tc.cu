@@ -292,7 +292,40 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
         const int wi = warp - 2;
         if constexpr (FUSED) {
             // -------------------------------------------- dequantize into B
-            const int t = threadIdx.x - 64;
+            // Lane -> packed-word assignment: in every 8-lane phase (p = lane
+            // >> 3) the lanes take columns gq in {p, p ^ 5} and all four tq.
+            // Then the eight 16-byte loads of packed words and the eight
+            // 16-byte stores into the 128-byte-swizzled B tile of a phase both
+            // hit eight distinct bank groups (no shared-memory conflicts).
+            const int wl = warp - 2;                       // worker warp 0..7
+            const int pq = lane >> 3;
+            const int gq = ((lane >> 2) & 1) ? (pq ^ 5) : pq;
+            const int tq = lane & 3;
+            const int ls = 4 * gq + tq;
+            // B-tile byte offset of word j of column tile ntl: row n = 16 ntl + gq + 8 (j & 1)
+            // (n & 7 == gq), 16-byte chunk kch = 4 (j >> 1) + tq, swizzled by n & 7.
+            const uint32_t sw0 = static_cast<uint32_t>((tq ^ gq) << 4);
+            const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
+            uint32_t s_sp[2][2][2], s_nzl[2][2][2], s_nzh[2][2][2];   // [half J][i][j & 1]
+            int cached_g0 = -1;
+            auto load_consts = [&](uint32_t sz_base, int gl, int J) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int ntl = wl + 8 * i;
+                    uint32_t sp, z0w, z1w;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sp) : "r"(sz_base + (gl * 128 + ntl * 8 + gq) * 4));
+                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                                 : "=r"(z0w), "=r"(z1w)
+                                 : "r"(sz_base + 1024 + (gl * 32 + ntl * 2) * 4));
+                    s_sp[J][i][0] = __byte_perm(sp, sp, 0x1010);
+                    s_sp[J][i][1] = __byte_perm(sp, sp, 0x3232);
+                    const uint32_t z0 = (z0w >> (4 * gq)) & 0xFu, z1 = (z1w >> (4 * gq)) & 0xFu;
+                    s_nzl[J][i][0] = neg_zlo(z0);
+                    s_nzh[J][i][0] = neg_zhi(z0);
+                    s_nzl[J][i][1] = neg_zlo(z1);
+                    s_nzh[J][i][1] = neg_zhi(z1);
+                }
+            };
             for (int kb = 0; kb < KB; ++kb) {
                 const int s = kb % S;
                 const uint32_t ph = (kb / S) & 1;
@@ -301,37 +334,35 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
                     record_error(a.status, 0x4, abort_flag);
                     break;
                 }
-                uint8_t *st = sbase + s * C::kStageBytes;
-                const uint4 *P = reinterpret_cast<const uint4 *>(st + C::kPOff);
-                const uint32_t *S2s = reinterpret_cast<const uint32_t *>(st + C::kSzOff);
-                const uint32_t *Zs = S2s + 256;
-                uint8_t *B = st + C::kBOff;
+                const uint32_t st = base + s * C::kStageBytes;
+                const uint32_t sz_base = st + C::kSzOff;
                 const int g0 = (2 * kb) / a.bpg;
                 const int gl1 = (2 * kb + 1) / a.bpg - g0;
+                if (g0 != cached_g0) {
+                    load_consts(sz_base, 0, 0);
+                    cached_g0 = g0;
+                }
+                if (gl1) load_consts(sz_base, 1, 1);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const int u = t + 256 * i;
-                    const int ntl = u >> 5, ls = u & 31, gq = ls >> 2, tq = ls & 3;
-                    const uint4 w4 = P[u];
-                    const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+                    const int ntl = wl + 8 * i;
+                    uint32_t w[4];
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                 : "r"(st + C::kPOff + (ntl * 32 + ls) * 16));
+                    const uint32_t brow = st + C::kBOff + static_cast<uint32_t>(2 * ntl * 1024 + gq * 128);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int n = 16 * ntl + gq + 8 * (j & 1);
-                        const int kch = 4 * (j >> 1) + tq;
-                        const int gl = (j >> 1) ? gl1 : 0;
-                        const uint32_t sp = S2s[gl * 128 + ntl * 8 + gq];
-                        const uint32_t sb = (j & 1) ? (sp >> 16) : (sp & 0xFFFFu);
-                        const uint32_t sv = sb | (sb << 16);
-                        const uint32_t zw = Zs[gl * 32 + ntl * 2 + (j & 1)];
-                        const uint32_t z = (zw >> (4 * gq)) & 0xFu;
+                        const int J = j >> 1, jj = j & 1;
+                        const uint32_t sp = (J && gl1) ? s_sp[1][i][jj] : s_sp[0][i][jj];
+                        const uint32_t nl = (J && gl1) ? s_nzl[1][i][jj] : s_nzl[0][i][jj];
+                        const uint32_t nh = (J && gl1) ? s_nzh[1][i][jj] : s_nzh[0][i][jj];
                         uint32_t q[4];
-                        unpack_qz(words[j], neg_zlo(z), neg_zhi(z), q);
-                        uint4 o;
-                        o.x = hmul2(q[0], sv);
-                        o.y = hmul2(q[1], sv);
-                        o.z = hmul2(q[2], sv);
-                        o.w = hmul2(q[3], sv);
-                        *reinterpret_cast<uint4 *>(B + (n >> 3) * 1024 + (n & 7) * 128 + ((kch ^ (n & 7)) << 4)) = o;
+                        unpack_qz(w[j], nl, nh, q);
+                        const uint32_t addr = brow + jj * 1024 + (J ? sw1 : sw0);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hmul2(q[0], sp)),
+                                     "r"(hmul2(q[1], sp)), "r"(hmul2(q[2], sp)), "r"(hmul2(q[3], sp))
+                                     : "memory");
                     }
                 }
                 fence_proxy_async();

@@ -99,6 +99,36 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Shared-memory (CTA window) address of a generic pointer.
+__device__ __forceinline__ uint32_t shared_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Asynchronous global -> shared copies (no register round trip).
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Hardware barrier over every thread of every CTA of the cluster, with
+// release/acquire ordering of shared-memory writes across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA's shared memory.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local, int rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------ launchers
 struct HandleView {
     int K, N, G, geff, groupsize;
@@ -133,7 +163,8 @@ struct DecodePlan {
     int ctas_n;        // column tiles of 32
     int splits;        // K slices
     int slice_chunks;  // 64-row chunks per slice
-    size_t ws_floats;  // workspace needed
+    int cluster;       // 1: the slices of a column tile form a cluster and reduce through DSMEM
+    size_t ws_floats;  // workspace needed (slices reduced through global memory)
     int n_tickets;
 };
 DecodePlan plan_decode(int M, int K, int N, int geff);

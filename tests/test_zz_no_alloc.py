@@ -32,8 +32,9 @@ def to_dev(a):
 
 
 @pytest.mark.parametrize("K,N,gs,act,M", [
-    (4096, 4096, 128, False, 1),      # split-K: partial sums and tickets in the scratch
-    (4096, 11008, 128, True, 4),      # act-order: temp_state in the scratch too
+    (4096, 4096, 128, False, 1),      # K slices reduced inside a thread-block cluster
+    (28672, 1024, 128, False, 16),    # 14 K slices: partial sums and tickets in the scratch
+    (4096, 11008, 128, True, 4),      # act-order: temp_state in the scratch
     (11008, 4096, 128, False, 8),
     (1024, 448, 32, True, 17),        # two m-tiles, ragged rows
 ])
@@ -83,7 +84,7 @@ def test_noalloc_rejects_sizes_beyond_the_scratch(q4):
     layer = synthetic.make_layer(K, N, gs, act_order=True, key=(43,))
     mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
                       None, gs)
-    M = 512                                  # needs far more than the fixed scratch
+    M = 2048                                 # act-order temp_state alone: 2048 x 8192 x 2 B = 32 MiB
     x = torch.zeros((M, K), dtype=torch.float16, device=DEV)
     out = torch.empty((M, N), dtype=torch.float16, device=DEV)
     with pytest.raises(q4.GPTQ4Error) as e:
