@@ -51,6 +51,11 @@ namespace {
 #ifndef Q4_DECODE_DEPTH
 #define Q4_DECODE_DEPTH 4
 #endif
+// 0: each warp streams one contiguous run of 64-row chunks; 1: the warps of a
+// CTA take consecutive chunk pairs, so a CTA reads one contiguous span per step.
+#ifndef Q4_DECODE_INTERLEAVE
+#define Q4_DECODE_INTERLEAVE 0
+#endif
 constexpr int kWarps = Q4_DECODE_WARPS;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kNTW = Q4_DECODE_NTW;             // 16-column tiles per CTA
@@ -68,6 +73,7 @@ struct DecodeArgs {
     int slice_chunks;
     int xrows;          // rows of x staged per CTA: min(8*MT, M)
     int cluster;        // slices reduce through distributed shared memory
+    uint64_t inv_bpg;   // ceil(2^32 / blocks-per-group): group of 32-row block b = (b * inv_bpg) >> 32
 };
 
 __host__ __device__ inline int x_row_stride(int slice_chunks) { return slice_chunks * 64 + 32; }
@@ -106,7 +112,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     const int nch = c_end - c_beg;
     const int XS = x_row_stride(a.slice_chunks);
     const int geff = h.geff;
-    const int bpg = geff >> 5;                          // 32-row blocks per group
 
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
     float *red = reinterpret_cast<float *>(smem + static_cast<size_t>(a.xrows) * XS * 2);
@@ -116,23 +121,31 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     // every CTA of this grid is resident (programmatic dependent launch).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // This warp's sequence of 64-row chunks within the CTA's slice.
+#if Q4_DECODE_INTERLEAVE
+    const int full_steps = nch / (2 * kWarps);
+    const int rem = nch - full_steps * 2 * kWarps;
+    const int extra = min(2, max(0, rem - 2 * warp));
+    const int wn = 2 * full_steps + extra;
+    auto chunk_of = [&](int c) { return c_beg + 2 * kWarps * (c >> 1) + 2 * warp + (c & 1); };
+#else
     const int wc_beg = c_beg + (nch * warp) / kWarps;
-    const int wc_end = c_beg + (nch * (warp + 1)) / kWarps;
-    const int wn = wc_end - wc_beg;
+    const int wn = c_beg + (nch * (warp + 1)) / kWarps - wc_beg;
+    auto chunk_of = [&](int c) { return wc_beg + c; };
+#endif
     const int g_base = (c_beg * 64) / geff;
 
     // ---- first kDepth chunks of packed weights: handle-owned constant data,
     //      so the loads may be issued before the preceding grid has finished.
     const uint4 *wbase[kNTW];
 #pragma unroll
-    for (int nt = 0; nt < kNTW; ++nt)
-        wbase[nt] = h.wp + (static_cast<size_t>(nt0 + nt) * KC + wc_beg) * 32 + lane;
+    for (int nt = 0; nt < kNTW; ++nt) wbase[nt] = h.wp + static_cast<size_t>(nt0 + nt) * KC * 32 + lane;
     uint4 buf[kDepth][kNTW];
 #pragma unroll
     for (int i = 0; i < kDepth; ++i)
         if (i < wn)
 #pragma unroll
-            for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(i) * 32);
+            for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(chunk_of(i)) * 32);
 
     // ---- stage the slice's scale pairs / zero words (constant) and, once
     //      the preceding grid is done, x[m0 : m0 + mrows][slice], with
@@ -142,22 +155,24 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     {
         const int g_beg = (c_beg * 64) / geff;
         const int g_end = (c_end * 64 - 1) / geff + 1;
-        const int ng = g_end - g_beg;
-        for (int i = threadIdx.x; i < ng * kNTW * 10; i += kThreads) {
-            const int gl = i / (kNTW * 10), rest = i - gl * (kNTW * 10);
-            const int nt = rest / 10, w = rest - nt * 10;
+        // per group: kNTW*8 scale-pair words, then kNTW*2 zero words
+        for (int gl = threadIdx.x; gl < g_end - g_beg; gl += kThreads) {
             const size_t gr = static_cast<size_t>(g_beg + gl);
-            const uint32_t *src = (w < 8) ? h.s2 + (gr * NT16 + nt0 + nt) * 8 + w
-                                          : h.zeros + gr * (N >> 3) + (nt0 + nt) * 2 + (w - 8);
-            cp_async_4(gsz + i, src);
+            uint32_t *dst = gsz + gl * (kNTW * 10);
+            const uint32_t *s2src = h.s2 + (gr * NT16 + nt0) * 8;
+#pragma unroll
+            for (int v = 0; v < kNTW * 2; ++v) cp_async_16(dst + 4 * v, s2src + 4 * v);
+            const uint32_t *zsrc = h.zeros + gr * (N >> 3) + nt0 * 2;
+            if (kNTW == 2) cp_async_16(dst + 16, zsrc);
+            else cp_async_8(dst + kNTW * 8, zsrc);
         }
         // x, the workspace, the tickets and out may belong to the preceding
         // grid: wait for it (a no-op without programmatic dependent launch).
         asm volatile("griddepcontrol.wait;" ::: "memory");
         const int vpr = nch * 8;                        // 16-byte vectors per row
-        for (int i = threadIdx.x; i < mrows * vpr; i += kThreads) {
-            const int r = i / vpr, c = i - r * vpr;
-            cp_async_16(xs + r * XS + c * 8, a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64 + c * 8);
+        for (int r = 0; r < mrows; ++r) {
+            const uint16_t *src = a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64;
+            for (int c = threadIdx.x; c < vpr; c += kThreads) cp_async_16(xs + r * XS + c * 8, src + c * 8);
         }
         cp_async_wait_all();
     }
@@ -174,16 +189,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     if (wn > 0) {
         uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
         float sc[kNTW][2];
-        int blk = 2 * wc_beg;
-        int grp = blk / bpg;
-        int left = bpg - (blk - grp * bpg);
+        int grp = -1;
 
         auto load_group = [&](int g) {
-            const uint32_t *base = gsz + (g - g_base) * kNTW * 10;
+            const uint32_t *base = gsz + (g - g_base) * (kNTW * 10);
 #pragma unroll
             for (int nt = 0; nt < kNTW; ++nt) {
-                const uint32_t sp = base[nt * 10 + gq];
-                const uint32_t zw0 = base[nt * 10 + 8], zw1 = base[nt * 10 + 9];
+                const uint32_t sp = base[nt * 8 + gq];
+                const uint32_t zw0 = base[kNTW * 8 + nt * 2], zw1 = base[kNTW * 8 + nt * 2 + 1];
                 sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
                 const uint32_t z0 = (zw0 >> (4 * gq)) & 0xFu, z1 = (zw1 >> (4 * gq)) & 0xFu;
@@ -204,22 +217,22 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
                         accg[nt][mt][i] = 0.f;
                     }
         };
-        load_group(grp);
 
         for (int base = 0; base < wn; base += kDepth) {
 #pragma unroll
             for (int i = 0; i < kDepth; ++i) {
                 const int c = base + i;
                 if (c < wn) {
+                    const int chunk = chunk_of(c);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        if (left == 0) {
-                            flush();
-                            ++grp;
-                            load_group(grp);
-                            left = bpg;
+                        const int g = static_cast<int>((static_cast<uint64_t>(2 * chunk + hh) * a.inv_bpg) >> 32);
+                        if (g != grp) {
+                            if (grp >= 0) flush();
+                            load_group(g);
+                            grp = g;
                         }
-                        const int kk = (2 * (wc_beg + c - c_beg) + hh) * 32 + 8 * tq;
+                        const int kk = (2 * (chunk - c_beg) + hh) * 32 + 8 * tq;
                         uint4 xb[MT];
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
@@ -242,12 +255,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
                                 mma_16816(accg[nt][mt], A1, xb[mt].z, xb[mt].w);
                             }
                         }
-                        --left;
                     }
                     if (c + kDepth < wn)
 #pragma unroll
                         for (int nt = 0; nt < kNTW; ++nt)
-                            buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(c + kDepth) * 32);
+                            buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(chunk_of(c + kDepth)) * 32);
                 }
             }
         }
@@ -362,7 +374,10 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
         max_dyn = want;
     }
     if (smem > static_cast<size_t>(max_dyn)) return cudaErrorInvalidConfiguration;
-    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows, p.cluster};
+    // exact floor(b / bpg) for b * bpg < 2^32 (b <= K / 32)
+    const uint64_t bpg = static_cast<uint64_t>(h.geff / 32);
+    const uint64_t inv_bpg = (0x100000000ull + bpg - 1) / bpg;
+    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows, p.cluster, inv_bpg};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas_n, p.splits, p.zdim);
     cfg.blockDim = dim3(kThreads);
