@@ -323,6 +323,15 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
     }
 }
 
+template <bool FUSED>
+cudaError_t ensure_smem_attr() {
+    static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg<FUSED>::kSmem);
+    return st;
+}
+
+}  // namespace
+
 // ----------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -355,15 +364,6 @@ cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool FUSED>
-cudaError_t ensure_smem_attr() {
-    static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Cfg<FUSED>::kSmem);
-    return st;
-}
-
-}  // namespace
-
 cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
                             uint16_t *out, int *status, cudaStream_t s) {
     CUtensorMap tmA, tmB;
@@ -381,23 +381,5 @@ cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
-    CUtensorMap tmA, tmW;
-    cudaError_t e;
-    const int KC = h.K / 64;
-    if ((e = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, h.K, M, static_cast<uint64_t>(h.K) * 2, BK, BM,
-                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-        return e;
-    if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
-                       static_cast<uint64_t>(KC) * 512, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
-        return e;
-    if ((e = ensure_smem_attr<true>()) != cudaSuccess) return e;
-    TcArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32};
-    dim3 grid((h.N + BN - 1) / BN, (M + BM - 1) / BM);
-    tc_gemm_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmem, s>>>(tmA, tmW, args);
-    return cudaGetLastError();
-}
-
-int prefill_default_min_m() { return 64; }
 
 }  // namespace q4

@@ -363,4 +363,6 @@ cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16
     return cudaGetLastError();
 }
 
+int prefill_default_min_m() { return 64; }
+
 }  // namespace q4
