@@ -62,6 +62,9 @@ constexpr int kNTW = Q4_DECODE_NTW;             // 16-column tiles per CTA
 constexpr int kNB = 16 * kNTW;      // columns per CTA
 constexpr int kDepth = Q4_DECODE_DEPTH;         // chunks in the load ring
 constexpr int kMaxCluster = 8;      // portable thread-block cluster size
+// Shared words staged per group: kNTW*8 scale pairs, then kNTW*2 zero words,
+// padded to a multiple of 4 so every group's copies start 16-byte aligned.
+constexpr int kGszStride = ((kNTW * 10 + 3) / 4) * 4;
 
 struct DecodeArgs {
     const uint16_t *x;
@@ -82,12 +85,12 @@ template <int MT>
 __host__ __device__ inline size_t smem_bytes(int xrows, int slice_chunks, int max_groups) {
     return static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2      // x slice
            + static_cast<size_t>(kWarps) * kNTW * MT * 128 * 4              // warp partials
-           + static_cast<size_t>(max_groups) * kNTW * 10 * 4;              // scale pairs + zero words
+           + static_cast<size_t>(max_groups) * kGszStride * 4;             // scale pairs + zero words
 }
 
 __host__ __device__ inline size_t smem_bytes_for(int mt, int xrows, int slice_chunks, int max_groups) {
     return static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2 +
-           static_cast<size_t>(kWarps) * kNTW * mt * 128 * 4 + static_cast<size_t>(max_groups) * kNTW * 10 * 4;
+           static_cast<size_t>(kWarps) * kNTW * mt * 128 * 4 + static_cast<size_t>(max_groups) * kGszStride * 4;
 }
 
 __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
@@ -158,13 +161,16 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
         // per group: kNTW*8 scale-pair words, then kNTW*2 zero words
         for (int gl = threadIdx.x; gl < g_end - g_beg; gl += kThreads) {
             const size_t gr = static_cast<size_t>(g_beg + gl);
-            uint32_t *dst = gsz + gl * (kNTW * 10);
+            uint32_t *dst = gsz + gl * kGszStride;      // 16-byte aligned (stride % 4 == 0)
             const uint32_t *s2src = h.s2 + (gr * NT16 + nt0) * 8;
 #pragma unroll
             for (int v = 0; v < kNTW * 2; ++v) cp_async_16(dst + 4 * v, s2src + 4 * v);
+            // zero words: 8 * kNTW bytes at a source offset that is a multiple
+            // of 8 * kNTW bytes; 16-byte copies while they fit, then one of 8.
             const uint32_t *zsrc = h.zeros + gr * (N >> 3) + nt0 * 2;
-            if (kNTW == 2) cp_async_16(dst + 16, zsrc);
-            else cp_async_8(dst + kNTW * 8, zsrc);
+#pragma unroll
+            for (int v = 0; v < kNTW / 2; ++v) cp_async_16(dst + kNTW * 8 + 4 * v, zsrc + 4 * v);
+            if (kNTW & 1) cp_async_8(dst + kNTW * 8 + 4 * (kNTW / 2), zsrc + 4 * (kNTW / 2));
         }
         // x, the workspace, the tickets and out may belong to the preceding
         // grid: wait for it (a no-op without programmatic dependent launch).
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
         int grp = -1;
 
         auto load_group = [&](int g) {
-            const uint32_t *base = gsz + (g - g_base) * (kNTW * 10);
+            const uint32_t *base = gsz + (g - g_base) * kGszStride;
 #pragma unroll
             for (int nt = 0; nt < kNTW; ++nt) {
                 const uint32_t sp = base[nt * 8 + gq];

@@ -1,25 +1,18 @@
-// Tensor-core (tcgen05 / TMEM / TMA) GEMMs for the prefill side of the GPTQ
-// W4A16 linear layer, on sm_103a.
-//
-//   dense:  out = a . b + bias, a [M][K] fp16, b [K][N] fp16 (the matmul on
-//           the dequantized matrix temp_dq "during prefill" of
-//           "Implementation: Predibase Lorax GPTQ Exllama V1", "Description")
-//   fused:  out = x . W + bias with W read packed (4-bit) and dequantized in
-//           shared memory inside the main loop, never written to HBM (the
-//           fused principle of "GPTQ's 'Exllama Kernel Not Installed'
-//           Warning", "What the fallback actually does").
+// Dense fp16 GEMM on the 5th-generation tensor cores (tcgen05 / TMEM / TMA),
+// sm_103a:  out = a . b + bias,  a [M][K] fp16 (K-major), b [K][N] fp16
+// (N-major), fp32 accumulation, one rounding to fp16.  The matmul on the
+// dequantized matrix temp_dq "during prefill" ("Implementation: Predibase
+// Lorax GPTQ Exllama V1", "Description"): the unfused comparison route.  The
+// fused route is in q4_prefill.cu.
 //
 // One CTA computes a 128 x 256 output tile with fp32 accumulators in tensor
 // memory (256 TMEM columns).  Warp roles:
-//   warp 0       one thread issues TMA loads into a ring of shared-memory
-//                stages (activations; dense: weight tiles; fused: packed
-//                words plus the stage's scales and zero points)
+//   warp 0       one thread issues TMA loads (128-byte swizzle) of the a and b
+//                tiles into a 4-stage ring of shared-memory stages
 //   warp 1       allocates TMEM; one thread issues tcgen05.mma (M=128,
 //                N=256, K=16) and commits each stage back to the producer
-//   warps 2..    fused: dequantize the packed words of a stage straight into
-//                the K-major, 128-byte-swizzled B operand layout; then all of
-//                them read TMEM (tcgen05.ld), add bias in fp32, round once to
-//                fp16 and store.
+//   warps 2..5   read TMEM (tcgen05.ld), add bias in fp32, round once to fp16
+//                and store.
 // Every wait on an mbarrier is bounded (about two seconds of global time);
 // a wait that runs out records an error bit in the caller's status word,
 // stops its role, and the CTA still frees its TMEM before returning.
@@ -42,30 +35,19 @@ using namespace tc;
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kABytes = BM * BK * 2;         // 16 KB activation tile
 constexpr int kBBytes = BN * BK * 2;         // 32 KB weight tile (fp16)
-constexpr int kPBytes = BN * BK / 2;         // 8 KB packed weight tile
-constexpr int kSzBytes = 2 * 16 * 8 * 4 + 2 * 32 * 4;   // scales + zeros for up to two groups
 constexpr uint32_t kTmemCols = 256;
 
-template <bool FUSED>
 struct Cfg {
-    static constexpr int kStages = FUSED ? 3 : 4;
+    static constexpr int kStages = 4;
     static constexpr int kAOff = 0;
     static constexpr int kBOff = kABytes;
-    static constexpr int kPOff = kABytes + kBBytes;
-    static constexpr int kSzOff = kPOff + kPBytes;
-    static constexpr int kStageBytes = FUSED ? ((kSzOff + kSzBytes + 1023) / 1024) * 1024 : kABytes + kBBytes;
-    static constexpr int kWorkerWarps = FUSED ? 8 : 4;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kWorkerWarps = 4;
     static constexpr int kThreads = 64 + 32 * kWorkerWarps;
-    static constexpr int kBarBytes = 8 * (3 * kStages + 1) + 16;
+    static constexpr int kBarBytes = 8 * (2 * kStages + 1) + 16;
     static constexpr int kSmem = kStages * kStageBytes + kBarBytes + 1024;
 };
 
-// Instruction descriptor, kind::f16: D fp32, A and B fp16, A K-major,
-// B K-major (fused: rows are output columns) or N-major (dense b [K][N]).
-__host__ __device__ constexpr uint32_t make_idesc(bool b_n_major) {
-    return (1u << 4) | ((b_n_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
-           (static_cast<uint32_t>(BM >> 4) << 24);
-}
 
 struct TcArgs {
     int M, N, K;
@@ -82,10 +64,9 @@ __device__ __forceinline__ void record_error(int *status, int bit, int *abort_fl
     atomicExch(abort_flag, 1);
 }
 
-template <bool FUSED>
-__global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
-    using C = Cfg<FUSED>;
+    using C = Cfg;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -94,9 +75,8 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
     const uint32_t bar0 = base + S * C::kStageBytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-    auto ready_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    const uint32_t done_bar = bar0 + 8u * (3 * S);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + S * C::kStageBytes + 8 * (3 * S + 1));
+    const uint32_t done_bar = bar0 + 8u * (2 * S);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + S * C::kStageBytes + 8 * (2 * S + 1));
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,7 +87,6 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(ready_bar(s), C::kWorkerWarps);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -132,29 +111,11 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
                     break;
                 }
                 const uint32_t st = base + s * C::kStageBytes;
-                if constexpr (FUSED) {
-                    const int nt0 = n0 >> 4;
-                    const int NT16 = a.N >> 4;
-                    const int tiles = min(16, NT16 - nt0);
-                    const int g_first = (2 * kb) / a.bpg, g_last = (2 * kb + 1) / a.bpg;
-                    const int ng = g_last - g_first + 1;
-                    const uint32_t sbytes = tiles * 32u, zbytes = tiles * 8u;
-                    mbar_arrive_expect_tx(full_bar(s), kABytes + kPBytes + ng * (sbytes + zbytes));
-                    tma_load_2d(st + C::kAOff, &tmA, full_bar(s), kb * BK, m0);
-                    tma_load_2d(st + C::kPOff, &tmB, full_bar(s), kb * 128, nt0);
-                    for (int gi = 0; gi < ng; ++gi) {
-                        const size_t gr = static_cast<size_t>(g_first + gi);
-                        bulk_load(st + C::kSzOff + gi * 512, a.s2 + (gr * NT16 + nt0) * 8, sbytes, full_bar(s));
-                        bulk_load(st + C::kSzOff + 1024 + gi * 128, a.zeros + gr * (a.N >> 3) + nt0 * 2, zbytes,
-                                  full_bar(s));
-                    }
-                } else {
-                    const int nb = min(4, (a.N - n0) / 64);
-                    mbar_arrive_expect_tx(full_bar(s), kABytes + nb * (BK * 64 * 2));
-                    tma_load_2d(st + C::kAOff, &tmA, full_bar(s), kb * BK, m0);
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_2d(st + C::kBOff + j * (BK * 64 * 2), &tmB, full_bar(s), n0 + 64 * j, kb * BK);
-                }
+                const int nb = min(4, (a.N - n0) / 64);
+                mbar_arrive_expect_tx(full_bar(s), kABytes + nb * (BK * 64 * 2));
+                tma_load_2d(st + C::kAOff, &tmA, full_bar(s), kb * BK, m0);
+                for (int j = 0; j < nb; ++j)
+                    tma_load_2d(st + C::kBOff + j * (BK * 64 * 2), &tmB, full_bar(s), n0 + 64 * j, kb * BK);
                 ++issued;
             }
             if (*reinterpret_cast<volatile int *>(abort_flag)) {
@@ -166,13 +127,13 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(!FUSED);
+            constexpr uint32_t idesc = idesc_f16(BM, BN, true);
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 const int s = kb % S;
                 const uint32_t ph = (kb / S) & 1;
                 if (*reinterpret_cast<volatile int *>(abort_flag) ||
-                    !mbar_wait(FUSED ? ready_bar(s) : full_bar(s), ph)) {
+                    !mbar_wait(full_bar(s), ph)) {
                     record_error(a.status, 0x2, abort_flag);
                     ok = false;
                     break;
@@ -182,8 +143,7 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint64_t ad = smem_desc_sw128(st + C::kAOff + kk * 32, 16, 1024);
-                    const uint64_t bd = FUSED ? smem_desc_sw128(st + C::kBOff + kk * 32, 16, 1024)
-                                              : smem_desc_sw128(st + C::kBOff + kk * 2048, BK * 64 * 2, 1024);
+                    const uint64_t bd = smem_desc_sw128(st + C::kBOff + kk * 2048, BK * 64 * 2, 1024);
                     umma_f16(tmem, ad, bd, idesc, (kb | kk) != 0);
                 }
                 umma_commit(empty_bar(s));
@@ -192,86 +152,6 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
         }
     } else {
         const int wi = warp - 2;
-        if constexpr (FUSED) {
-            // -------------------------------------------- dequantize into B
-            // Lane -> packed-word assignment: in every 8-lane phase (p = lane
-            // >> 3) the lanes take columns gq in {p, p ^ 5} and all four tq.
-            // Then the eight 16-byte loads of packed words and the eight
-            // 16-byte stores into the 128-byte-swizzled B tile of a phase both
-            // hit eight distinct bank groups (no shared-memory conflicts).
-            const int wl = warp - 2;                       // worker warp 0..7
-            const int pq = lane >> 3;
-            const int gq = ((lane >> 2) & 1) ? (pq ^ 5) : pq;
-            const int tq = lane & 3;
-            const int ls = 4 * gq + tq;
-            // B-tile byte offset of word j of column tile ntl: row n = 16 ntl + gq + 8 (j & 1)
-            // (n & 7 == gq), 16-byte chunk kch = 4 (j >> 1) + tq, swizzled by n & 7.
-            const uint32_t sw0 = static_cast<uint32_t>((tq ^ gq) << 4);
-            const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
-            uint32_t s_sp[2][2][2], s_nzl[2][2][2], s_nzh[2][2][2];   // [half J][i][j & 1]
-            int cached_g0 = -1;
-            auto load_consts = [&](uint32_t sz_base, int gl, int J) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int ntl = wl + 8 * i;
-                    uint32_t sp, z0w, z1w;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sp) : "r"(sz_base + (gl * 128 + ntl * 8 + gq) * 4));
-                    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                                 : "=r"(z0w), "=r"(z1w)
-                                 : "r"(sz_base + 1024 + (gl * 32 + ntl * 2) * 4));
-                    s_sp[J][i][0] = __byte_perm(sp, sp, 0x1010);
-                    s_sp[J][i][1] = __byte_perm(sp, sp, 0x3232);
-                    const uint32_t z0 = (z0w >> (4 * gq)) & 0xFu, z1 = (z1w >> (4 * gq)) & 0xFu;
-                    s_nzl[J][i][0] = neg_zlo(z0);
-                    s_nzh[J][i][0] = neg_zhi(z0);
-                    s_nzl[J][i][1] = neg_zlo(z1);
-                    s_nzh[J][i][1] = neg_zhi(z1);
-                }
-            };
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % S;
-                const uint32_t ph = (kb / S) & 1;
-                if (*reinterpret_cast<volatile int *>(abort_flag)) break;
-                if (!mbar_wait(full_bar(s), ph)) {
-                    record_error(a.status, 0x4, abort_flag);
-                    break;
-                }
-                const uint32_t st = base + s * C::kStageBytes;
-                const uint32_t sz_base = st + C::kSzOff;
-                const int g0 = (2 * kb) / a.bpg;
-                const int gl1 = (2 * kb + 1) / a.bpg - g0;
-                if (g0 != cached_g0) {
-                    load_consts(sz_base, 0, 0);
-                    cached_g0 = g0;
-                }
-                if (gl1) load_consts(sz_base, 1, 1);
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int ntl = wl + 8 * i;
-                    uint32_t w[4];
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                                 : "r"(st + C::kPOff + (ntl * 32 + ls) * 16));
-                    const uint32_t brow = st + C::kBOff + static_cast<uint32_t>(2 * ntl * 1024 + gq * 128);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int J = j >> 1, jj = j & 1;
-                        const uint32_t sp = (J && gl1) ? s_sp[1][i][jj] : s_sp[0][i][jj];
-                        const uint32_t nl = (J && gl1) ? s_nzl[1][i][jj] : s_nzl[0][i][jj];
-                        const uint32_t nh = (J && gl1) ? s_nzh[1][i][jj] : s_nzh[0][i][jj];
-                        uint32_t q[4];
-                        unpack_qz(w[j], nl, nh, q);
-                        const uint32_t addr = brow + jj * 1024 + (J ? sw1 : sw0);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hmul2(q[0], sp)),
-                                     "r"(hmul2(q[1], sp)), "r"(hmul2(q[2], sp)), "r"(hmul2(q[3], sp))
-                                     : "memory");
-                    }
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ready_bar(s));
-            }
-        }
         // ------------------------------------------------ epilogue
         const bool have = !*reinterpret_cast<volatile int *>(abort_flag);
         bool ok = have && mbar_wait(done_bar, 0);
@@ -323,10 +203,9 @@ __global__ void __launch_bounds__(Cfg<FUSED>::kThreads, 1)
     }
 }
 
-template <bool FUSED>
 cudaError_t ensure_smem_attr() {
-    static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Cfg<FUSED>::kSmem);
+    static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg::kSmem);
     return st;
 }
 
@@ -374,10 +253,10 @@ cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t
     if ((e = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, N, K, static_cast<uint64_t>(N) * 2, 64, BK,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
         return e;
-    if ((e = ensure_smem_attr<false>()) != cudaSuccess) return e;
+    if ((e = ensure_smem_attr()) != cudaSuccess) return e;
     TcArgs args{M, N, K, bias, out, status, nullptr, nullptr, 1};
     dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-    tc_gemm_kernel<false><<<grid, Cfg<false>::kThreads, Cfg<false>::kSmem, s>>>(tmA, tmB, args);
+    tc_gemm_kernel<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tmA, tmB, args);
     return cudaGetLastError();
 }
 
