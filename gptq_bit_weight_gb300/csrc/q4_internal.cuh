@@ -175,4 +175,16 @@ size_t decode_ws_floats_for(int M, int K, int N, int geff);
 cudaError_t launch_decode(const HandleView &h, const DecodePlan &plan, const DecodeWork &w,
                           const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
 
+// decode on the tcgen05 tensor cores (q4_decode_tc.cu), M <= 16
+struct DecodeTcPlan {
+    int ok;            // 0: shape not supported by this kernel
+    int splits;        // K slices (one cluster per column tile)
+    int slice_kb;      // 64-row blocks per slice
+    int tiles;         // 128-column tiles
+    int zdim;          // 16-row blocks of x
+};
+DecodeTcPlan plan_decode_tc(int M, int K, int N, int geff, int sms);
+bool decode_tc_supported(int M, int K, int N, int geff);
+cudaError_t launch_decode_tc(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
+
 }  // namespace q4

@@ -77,17 +77,20 @@ def test_unpack_and_dequant_bit_exact(q4, K, N, gs, act):
     mat.device_error()
 
 
+@pytest.mark.parametrize("path", ["DECODE", "DECODE_MMA"])
 @pytest.mark.parametrize("K,N,gs,act", SMALL)
-def test_decode_matches_oracle(q4, K, N, gs, act):
+def test_decode_matches_oracle(q4, K, N, gs, act, path):
+    """Both decode kernels: tcgen05 with per-group accumulators (M <= 16 under
+    DECODE) and the mma.sync kernel (DECODE_MMA, and DECODE above 16 rows)."""
     layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(22, K, N, gs & 0xFFFF, act))
     dq = oracle_dq(layer)
     mat = make(q4, layer)
-    mat.set_path(q4.GPTQ_Q4_PATH_DECODE)
+    mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
     for M in (1, 2, 3, 7, 8, 9, 16, 17, 33, 40):
         x = synthetic.activations(M, K, key=(22, K, N, M))
         y = mat(to_dev(x))
         torch.cuda.synchronize()
-        check_y(y, x, dq, layer.bias, K, f"K={K} N={N} g={gs} act={act} M={M}")
+        check_y(y, x, dq, layer.bias, K, f"{path} K={K} N={N} g={gs} act={act} M={M}")
     mat.device_error()
 
 
