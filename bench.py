@@ -365,6 +365,10 @@ def run_native(args):
     e2e_s = max_over_ranks(time.perf_counter() - t0)
     e2e_value = job_throughput(step_bytes, args.steps, world, e2e_s)
 
+    decode_70b = None
+    if args.only is None:
+        decode_70b = run_decode_70b(q4, torch, dev, stream, hbm_gbs)
+
     prefill = None
     if not args.no_prefill and args.only != "decode":
         prefill = run_prefill(q4, torch, dev, stream, bf16_tf, peak_src)
@@ -397,6 +401,8 @@ def run_native(args):
             "gpu_launches": launches,
             "clocks": clocks,
         }
+        if decode_70b:
+            line["decode_70b"] = decode_70b
         if prefill:
             line["prefill"] = prefill
         if cpu:
@@ -405,6 +411,46 @@ def run_native(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_decode_70b(q4, torch, dev, stream, hbm_gbs, reps=10):
+    """M=1 decode on the Llama-70B projection shapes (sweep_70b, g=128,
+    trivial g_idx): per shape, enough weight replicas to exceed L2, captured
+    in one CUDA graph and replayed; eff. TB/s on the stored weight bytes."""
+    out = {}
+    tot_bytes, tot_s = 0.0, 0.0
+    for (K, N) in synthetic.SWEEP_70B_SHAPES:
+        L = synthetic.workload_layer("sweep_70b", K, N, 128, False)
+        qw, qz, sc = (torch.from_numpy(a).to(dev) for a in (L.qweight, L.qzeros, L.scales))
+        R = max(2, int(np.ceil(3 * L2_BYTES / L.weight_bytes)))
+        mats = [q4.Q4Matrix(qw, qz, sc, None, None, 128) for _ in range(R)]
+        del qw, qz, sc
+        x = torch.from_numpy(synthetic.workload_x("sweep_70b", K, N, 128, False, 1)).to(dev)
+        o = torch.empty((1, N), dtype=torch.float16, device=dev)
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), stream.cuda_stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for m in mats:
+                q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        for _ in range(3):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * R)
+        tbs = L.weight_bytes / (us * 1e-6) / 1e12
+        out[f"{K}x{N} M=1"] = {"us": round(us, 2), "TB/s": round(tbs, 3), "frac": round(tbs * 1e3 / hbm_gbs, 3)}
+        tot_bytes += L.weight_bytes
+        tot_s += us * 1e-6
+        del g, mats
+    return {"workload": "sweep_70b M=1, g=128, trivial g_idx", "value": tot_bytes / tot_s / 1e12, "unit": "TB/s",
+            "frac_of_hbm_peak": tot_bytes / tot_s / 1e9 / hbm_gbs, "cases": out,
+            "how": "weight bytes / per-call time from CUDA-graph replays of >= 3x L2 of weight replicas"}
 
 
 def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
