@@ -255,7 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                              "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
                              : "memory");
             }
-            if (g1 != g0) cached_g = g1;
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
