@@ -398,7 +398,7 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    if (path == GPTQ_Q4_PATH_DECODE && q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
+    if (path == GPTQ_Q4_PATH_DECODE_TC && q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
         Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
         ++g_launches;
         return ok();
@@ -475,7 +475,7 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 
 int gptq_q4_set_path(gptq_q4_handle h, int path) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
-    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_MMA)
+    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_TC)
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "unknown path %d", path);
     h->path = path;
     return ok();

@@ -20,12 +20,12 @@
 //
 // CTA = one 128-column tile x one K slice (the slices of a tile form a
 // thread-block cluster and are summed through distributed shared memory).
-//   warp 0       one thread: TMA loads into a 16-stage ring of {x tile 16x64
+//   warp 0       one thread: TMA loads into an 8-stage ring of {x tile 16x64
 //                fp16 (128-byte swizzle), packed-word tile 128x64 (4 KB)};
 //                the slice's scales and zero words once, up front
 //   warp 1       allocates 512 TMEM columns; one thread issues
 //                tcgen05.mma M=128 N=16 K=16 into the group's columns
-//   warps 2-9    dequantize into a 3-stage ring of fp16 A tiles (K-major,
+//   warps 2-9    dequantize into an 8-stage ring of fp16 A tiles (K-major,
 //                128-byte swizzle); afterwards warps 2-5 run the epilogue
 // Every mbarrier wait is bounded (~2 s); a wait that runs out records an
 // error bit in the handle's status word, the CTA lets its copies land, frees
@@ -51,8 +51,8 @@ using namespace tc;
 constexpr int BN = 128;                              // output columns per CTA (UMMA M)
 constexpr int MP = 16;                               // x rows per CTA (UMMA N)
 constexpr int BK = 64;                               // rows of W per stage
-constexpr int kSP = 16;                              // TMA ring stages
-constexpr int kSA = 3;                               // fp16 A ring stages
+constexpr int kSP = 8;                               // TMA ring stages
+constexpr int kSA = 8;                               // fp16 A ring stages
 constexpr int kXOff = 0, kPOff = 2048;               // within a TMA stage
 constexpr int kPStage = 6144;                        // 2 KB x + 4 KB packed
 constexpr int kAStage = BN * BK * 2;                 // 16 KB
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % kSP, sa = i % kSA;
-                if (aborted(abort_flag) || !mbar_wait(fullP(s), (i / kSP) & 1) || !mbar_wait(fullA(sa), (i / kSA) & 1)) {
+                if (aborted(abort_flag) || !mbar_poll(fullP(s), (i / kSP) & 1) || !mbar_poll(fullA(sa), (i / kSA) & 1)) {
                     fail(a.status, 0x200, abort_flag);
                     ok = false;
                     break;

@@ -15,10 +15,11 @@
 //   warp 1       allocates 512 TMEM columns (two 128x256 fp32 accumulators);
 //                one thread issues tcgen05.mma M=128 N=256 K=16 and commits
 //                stages back to the producer and the dequantizers
-//   warps 2-9    dequantize each stage's packed words into a 2-stage ring of
+//   warps 2-17   dequantize each stage's packed words into a 2-stage ring of
 //                fp16 B tiles (K-major, 128-byte swizzle: the UMMA operand
-//                layout), w16 = fp16(s * (q - z - 1)) rounded once
-//   warps 10-13  epilogue: tcgen05.ld an accumulator, add bias, round to fp16,
+//                layout), w16 = fp16(s * (q - z - 1)) rounded once; each
+//                thread one 16-byte vector (four words) per stage
+//   warps 18-21  epilogue: tcgen05.ld an accumulator, add bias, round to fp16,
 //                store; then hand the accumulator back, so the epilogue of
 //                one tile overlaps the main loop of the next.
 //
@@ -55,7 +56,7 @@ constexpr int kRingB = kSA * kAStage;                // byte offset of the B rin
 constexpr int kBarOff = kRingB + kSB * kBStage;
 constexpr int kNumBars = 2 * kSA + 2 * kSB + 4;
 constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
-constexpr int kDqWarps = 8, kEpiWarps = 4;
+constexpr int kDqWarps = 16, kEpiWarps = 4;
 constexpr int kThreads = 32 * (2 + kDqWarps + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 
@@ -167,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kSA, sb = it % kSB;
-                    if (aborted(abort_flag) || !mbar_wait(fullA(s), (it / kSA) & 1) ||
-                        !mbar_wait(fullB(sb), (it / kSB) & 1)) {
+                    if (aborted(abort_flag) || !mbar_poll(fullA(s), (it / kSA) & 1) ||
+                        !mbar_poll(fullB(sb), (it / kSB) & 1)) {
                         fail(a.status, 0x20, abort_flag);
                         ok = false;
                         break;
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the lanes take columns gq in {p, p ^ 5} and all four tq, so the
         // 16-byte loads of packed words and the 16-byte stores into the
         // swizzled B tile both hit eight distinct bank groups per phase.
+        // Warp wl owns n16 tile wl of the 256-column tile.
         const int wl = warp - 2;
         const int pq = lane >> 3;
         const int gq = ((lane >> 2) & 1) ? (pq ^ 5) : pq;
@@ -199,24 +201,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ls = 4 * gq + tq;
         const uint32_t sw0 = static_cast<uint32_t>((tq ^ gq) << 4);
         const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
-        uint32_t c_s[2][2][2], c_nl[2][2][2], c_nh[2][2][2];   // [half J][i][j & 1]
-        auto load_consts = [&](uint32_t sz_base, int gl, int J) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int ntl = wl + 8 * i;
-                uint32_t sp, z0w, z1w;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sp) : "r"(sz_base + (gl * 128 + ntl * 8 + gq) * 4));
-                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                             : "=r"(z0w), "=r"(z1w)
-                             : "r"(sz_base + 1024 + (gl * 32 + ntl * 2) * 4));
-                c_s[J][i][0] = __byte_perm(sp, sp, 0x1010);
-                c_s[J][i][1] = __byte_perm(sp, sp, 0x3232);
-                const uint32_t z0 = (z0w >> (4 * gq)) & 0xFu, z1 = (z1w >> (4 * gq)) & 0xFu;
-                c_nl[J][i][0] = neg_zlo(z0);
-                c_nh[J][i][0] = neg_zhi(z0);
-                c_nl[J][i][1] = neg_zlo(z1);
-                c_nh[J][i][1] = neg_zhi(z1);
-            }
+        uint32_t c_s[2][2], c_nl[2][2], c_nh[2][2];   // [half J][column gq / gq+8]
+        auto load_consts = [&](const uint8_t *sz, int gl, int J) {
+            const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + (gl * 128 + wl * 8 + gq) * 4);
+            const uint2 zw = *reinterpret_cast<const uint2 *>(sz + 1024 + (gl * 32 + wl * 2) * 4);
+            c_s[J][0] = __byte_perm(sp, sp, 0x1010);
+            c_s[J][1] = __byte_perm(sp, sp, 0x3232);
+            const uint32_t z0 = (zw.x >> (4 * gq)) & 0xFu, z1 = (zw.y >> (4 * gq)) & 0xFu;
+            c_nl[J][0] = neg_zlo(z0);
+            c_nh[J][0] = neg_zhi(z0);
+            c_nl[J][1] = neg_zlo(z1);
+            c_nh[J][1] = neg_zhi(z1);
         };
         int it = 0;
         bool ok = true;
@@ -230,37 +225,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t st = base + s * kAStage;
-                const uint32_t sz_base = st + kSzOff;
+                const uint8_t *st = sbase + s * kAStage;
+                const uint8_t *sz = st + kSzOff;
                 const int g0 = (2 * kb) / a.bpg;
                 const int gl1 = (2 * kb + 1) / a.bpg - g0;
                 if (g0 != cached_g0) {
-                    load_consts(sz_base, 0, 0);
+                    load_consts(sz, 0, 0);
                     cached_g0 = g0;
                 }
-                if (gl1) load_consts(sz_base, 1, 1);
-                const uint32_t bst = base + kRingB + sb * kBStage;
+                if (gl1) load_consts(sz, 1, 1);
+                const uint4 wv = *reinterpret_cast<const uint4 *>(st + kPOff + (wl * 32 + ls) * 16);
+                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                uint8_t *brow = sbase + kRingB + sb * kBStage + 2 * wl * 1024 + gq * 128;
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int ntl = wl + 8 * i;
-                    uint32_t w[4];
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                                 : "r"(st + kPOff + (ntl * 32 + ls) * 16));
-                    const uint32_t brow = bst + static_cast<uint32_t>(2 * ntl * 1024 + gq * 128);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int J = j >> 1, jj = j & 1;
-                        const uint32_t sp = (J && gl1) ? c_s[1][i][jj] : c_s[0][i][jj];
-                        const uint32_t nl = (J && gl1) ? c_nl[1][i][jj] : c_nl[0][i][jj];
-                        const uint32_t nh = (J && gl1) ? c_nh[1][i][jj] : c_nh[0][i][jj];
-                        uint32_t q[4];
-                        unpack_qz(w[j], nl, nh, q);
-                        const uint32_t addr = brow + jj * 1024 + (J ? sw1 : sw0);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hmul2(q[0], sp)),
-                                     "r"(hmul2(q[1], sp)), "r"(hmul2(q[2], sp)), "r"(hmul2(q[3], sp))
-                                     : "memory");
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    const int J = j >> 1, jj = j & 1;
+                    const uint32_t sp = (J && gl1) ? c_s[1][jj] : c_s[0][jj];
+                    const uint32_t nl = (J && gl1) ? c_nl[1][jj] : c_nl[0][jj];
+                    const uint32_t nh = (J && gl1) ? c_nh[1][jj] : c_nh[0][jj];
+                    uint32_t q[4];
+                    unpack_qz(w[j], nl, nh, q);
+                    *reinterpret_cast<uint4 *>(brow + jj * 1024 + (J ? sw1 : sw0)) =
+                        make_uint4(hmul2(q[0], sp), hmul2(q[1], sp), hmul2(q[2], sp), hmul2(q[3], sp));
                 }
                 fence_proxy_async();
                 __syncwarp();

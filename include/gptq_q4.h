@@ -74,10 +74,11 @@ extern "C" {
 
 /* Paths gptq_q4_matmul can take (see gptq_q4_set_path). */
 #define GPTQ_Q4_PATH_AUTO      0  /* decode below the prefill threshold, fused prefill above */
-#define GPTQ_Q4_PATH_DECODE    1  /* decode kernels: tcgen05 with per-group TMEM accumulators for
-                                     M <= 16, the mma.sync kernel above that */
+#define GPTQ_Q4_PATH_DECODE    1  /* always the decode kernel (register dequant, mma.sync, split-K) */
 #define GPTQ_Q4_PATH_PREFILL   2  /* always the fused shared-memory-dequant tensor-core kernel */
-#define GPTQ_Q4_PATH_DECODE_MMA 3 /* always the register-dequant split-K kernel on mma.sync */
+#define GPTQ_Q4_PATH_DECODE_MMA 3 /* same kernel as GPTQ_Q4_PATH_DECODE */
+#define GPTQ_Q4_PATH_DECODE_TC 4  /* decode on tcgen05 with one tensor-memory accumulator per
+                                     quantization group (M <= 16, else as DECODE) */
 
 typedef struct gptq_q4_s *gptq_q4_handle;   /* opaque; owns device memory */
 
@@ -136,14 +137,15 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m);
  *   M    rows; 0 is a valid no-op
  *
  * With act-order, x is first gathered into temp_state (temp_state[m][j] =
- * x[m][P[j]]).  Rows below the prefill threshold run a decode kernel.  For
- * M <= 16: packed weights streamed by TMA, dequantized in shared memory to the
- * exact integers (q - z - 1), multiplied on the tcgen05 tensor cores with one
- * tensor-memory accumulator per quantization group, the scales applied once
- * per group in an fp32 epilogue, the K slices of a column tile summed inside
- * a thread-block cluster.  Larger M below the threshold: packed weights
- * streamed with 128-bit loads, dequantized in registers, fp32 accumulation on
- * mma.sync, split-K with a fixed-order fp32 reduction.
+ * x[m][P[j]]).  Rows below the prefill threshold run the decode kernel:
+ * packed weights streamed with 128-bit loads, dequantized in registers, fp32
+ * accumulation on mma.sync, split-K whose slices are summed in a fixed order
+ * inside a thread-block cluster (distributed shared memory) or, past eight
+ * slices, by the last CTA to finish.  GPTQ_Q4_PATH_DECODE_TC selects the
+ * tcgen05 decode instead (M <= 16): packed weights streamed by TMA,
+ * dequantized in shared memory to the exact integers (q - z - 1), one
+ * tensor-memory accumulator per quantization group, scales applied once per
+ * group in an fp32 epilogue.
  * Larger M runs the fused prefill (tcgen05/TMEM with shared-memory
  * dequantization).  Results do not depend on the path beyond fp32 rounding.
  * Errors: INVALID_ARGUMENT (NULL handle/pointers with M > 0, M < 0,
