@@ -403,6 +403,14 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
+    if (path == GPTQ_Q4_PATH_DECODE) {
+        const q4::DecodeRingPlan rp = q4::plan_decode_ring(M, h->K, h->N, h->geff, q4::device_sm_count());
+        if (rp.ok) {
+            Q4_CUDA(q4::launch_decode_ring(v, rp, xin, M, out, stream), "decode launch");
+            ++g_launches;
+            return ok();
+        }
+    }
     const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N, h->geff);
     if (int r = ensure_decode_work(h, p.ws_floats, p.n_tickets, stream, false)) return r;
     q4::DecodeWork w{h->ws, h->ws_floats, h->tickets, h->n_tickets};

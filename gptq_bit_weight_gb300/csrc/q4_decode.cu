@@ -350,15 +350,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
 }
 
-// Programmatic dependent launch is on unless GPTQ_Q4_PDL=0.
-bool pdl_enabled() {
-    static const bool on = [] {
-        const char *e = getenv("GPTQ_Q4_PDL");
-        return !(e && e[0] == '0');
-    }();
-    return on;
-}
-
 template <int MT>
 cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                       uint16_t *out, cudaStream_t s) {
@@ -409,6 +400,15 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
 }
 
 }  // namespace
+
+// Programmatic dependent launch is on unless GPTQ_Q4_PDL=0.
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("GPTQ_Q4_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
 
 // Resident CTAs per SM for a variant: registers (the launch bounds) and
 // shared memory, whichever is tighter.

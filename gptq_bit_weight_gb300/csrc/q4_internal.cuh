@@ -186,5 +186,20 @@ struct DecodeTcPlan {
 DecodeTcPlan plan_decode_tc(int M, int K, int N, int geff, int sms);
 bool decode_tc_supported(int M, int K, int N, int geff);
 cudaError_t launch_decode_tc(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
+// decode fed by a TMA ring, register dequantization, mma.sync (q4_decode_ring.cu), M <= 16
+struct DecodeRingPlan {
+    int ok;            // 0: shape not supported by this kernel
+    int mt;            // 8-row m tiles (1 or 2)
+    int splits;        // K slices (one cluster per column tile)
+    int slice_kb;      // 64-row stages per slice
+    int tiles;         // 128-column tiles
+};
+DecodeRingPlan plan_decode_ring(int M, int K, int N, int geff, int sms);
+cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &plan, const uint16_t *x, int M,
+                               uint16_t *out, cudaStream_t s);
+// SMs of the current device (queried once)
+int device_sm_count();
+// programmatic dependent launch switch (GPTQ_Q4_PDL=0 turns it off)
+bool pdl_enabled();
 
 }  // namespace q4

@@ -77,11 +77,12 @@ def test_unpack_and_dequant_bit_exact(q4, K, N, gs, act):
     mat.device_error()
 
 
-@pytest.mark.parametrize("path", ["DECODE", "DECODE_TC"])
+@pytest.mark.parametrize("path", ["DECODE", "DECODE_MMA", "DECODE_TC"])
 @pytest.mark.parametrize("K,N,gs,act", SMALL)
 def test_decode_matches_oracle(q4, K, N, gs, act, path):
-    """Both decode kernels: the mma.sync kernel (DECODE) and the tcgen05 one
-    with per-group accumulators (DECODE_TC for M <= 16, mma.sync above)."""
+    """Every decode kernel: DECODE runs the TMA-ring kernel for M <= 16 and the
+    register-streaming one above; DECODE_MMA always the register-streaming
+    one; DECODE_TC the tcgen05 one with per-group accumulators for M <= 16."""
     layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(22, K, N, gs & 0xFFFF, act))
     dq = oracle_dq(layer)
     mat = make(q4, layer)
