@@ -34,6 +34,7 @@ GPTQ_Q4_PATH_DECODE = 1
 GPTQ_Q4_PATH_PREFILL = 2
 GPTQ_Q4_PATH_DECODE_MMA = 3
 GPTQ_Q4_PATH_DECODE_TC = 4
+GPTQ_Q4_PATH_DECODE_RING = 5
 
 EXPORTED = [
     "gptq_q4_make", "gptq_q4_set_bias", "gptq_q4_reserve", "gptq_q4_matmul", "gptq_q4_dequant",

@@ -403,7 +403,14 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    if (path == GPTQ_Q4_PATH_DECODE) {
+    // Which decode kernel: measured on GB300 (CUDA-graph replays over more
+    // weights than L2), the register-streaming kernel is ahead on layers
+    // below 24 Mi weights, and at M <= 4 on layers below 64 Mi weights,
+    // where its smaller fixed cost per call outweighs the ring's faster
+    // streaming; the TMA-ring kernel is ahead everywhere else it applies.
+    const size_t weights = static_cast<size_t>(h->K) * h->N;
+    const bool small_layer = weights < (size_t{24} << 20) || (M <= 4 && weights < (size_t{64} << 20));
+    if ((path == GPTQ_Q4_PATH_DECODE && !small_layer) || path == GPTQ_Q4_PATH_DECODE_RING) {
         const q4::DecodeRingPlan rp = q4::plan_decode_ring(M, h->K, h->N, h->geff, q4::device_sm_count());
         if (rp.ok) {
             Q4_CUDA(q4::launch_decode_ring(v, rp, xin, M, out, stream), "decode launch");
@@ -483,7 +490,7 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 
 int gptq_q4_set_path(gptq_q4_handle h, int path) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
-    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_TC)
+    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_RING)
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "unknown path %d", path);
     h->path = path;
     return ok();

@@ -403,38 +403,62 @@ cudaError_t ensure_attr() {
 
 }  // namespace
 
+// Co-resident clusters of `sp` CTAs (one K slice each) the device can hold
+// for the MT variant, from the occupancy calculator; queried once per MT on
+// the first device that asks.
+template <int MT>
+int max_active_clusters(int sp) {
+    static int table[kMaxCluster + 1] = {};
+    static bool done = false;
+    if (!done) {
+        done = true;
+        if (ensure_attr<MT>() == cudaSuccess) {
+            for (int c = 1; c <= kMaxCluster; ++c) {
+                cudaLaunchConfig_t cfg{};
+                cfg.gridDim = dim3(1, c, 1);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = RingCfg<MT>::kSmem;
+                cudaLaunchAttribute attr;
+                attr.id = cudaLaunchAttributeClusterDimension;
+                attr.val.clusterDim.x = 1;
+                attr.val.clusterDim.y = static_cast<unsigned>(c);
+                attr.val.clusterDim.z = 1;
+                cfg.attrs = &attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, decode_ring_kernel<MT>, &cfg) != cudaSuccess) n = 0;
+                table[c] = n;
+            }
+        }
+        cudaGetLastError();                          // a failed query leaves no sticky error
+    }
+    return table[sp];
+}
+
 // Slices: whole stages, at most kMaxGroups groups and at most 8 per tile
-// (portable cluster size).  Cost of a split count: the rounds of resident
-// CTAs (three per SM) an SM runs times the slice length, plus a fixed
-// prologue and epilogue of a few stages.
+// (portable cluster size).  The split count is the largest one whose
+// clusters (one per 128-column tile) can all be resident at once, so the
+// grid is a single wave; when even one slice per tile needs more than one
+// wave, one slice per tile.
 DecodeRingPlan plan_decode_ring(int M, int K, int N, int geff, int sms) {
     DecodeRingPlan p{};
     if (M < 1 || M > 16 || K % BK != 0 || N % 64 != 0 || geff % 32 != 0) return p;
+    const int mt = M > 8 ? 2 : 1;
     const int KB = K / BK;
     const int bpg = geff / 32;
     const int tiles = (N + BN - 1) / BN;
-#ifndef Q4_RING_FIXED
-#define Q4_RING_FIXED 6.0
-#endif
-    constexpr double kFixed = Q4_RING_FIXED;         // prologue + epilogue, in stages
-    constexpr int kResident = 3;
     int best = -1;
-    double best_cost = 0.0;
     for (int sp = 1; sp <= std::min(kMaxCluster, KB); ++sp) {
         const int slice = (KB + sp - 1) / sp;
         if ((KB + slice - 1) / slice != sp) continue;  // no empty slice
         if ((slice * 2 + bpg - 1) / bpg + 1 > kMaxGroups) continue;
-        const long long ctas = static_cast<long long>(tiles) * sp;
-        const long long rounds = (ctas + static_cast<long long>(kResident) * sms - 1) / (static_cast<long long>(kResident) * sms);
-        const double cost = static_cast<double>(rounds) * slice + kFixed;
-        if (best < 0 || cost < best_cost - 1e-9) {
-            best = sp;
-            best_cost = cost;
-        }
+        int fit = mt == 1 ? max_active_clusters<1>(sp) : max_active_clusters<2>(sp);
+        if (fit <= 0) fit = (3 * sms) / sp;            // occupancy query unavailable: three CTAs per SM
+        if (best < 0 || tiles <= fit) best = sp;       // first feasible, then the largest that fits one wave
     }
     if (best < 0) return p;
     p.ok = 1;
-    p.mt = M > 8 ? 2 : 1;
+    p.mt = mt;
     p.splits = best;
     p.slice_kb = (KB + best - 1) / best;
     p.tiles = tiles;

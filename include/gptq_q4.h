@@ -74,12 +74,16 @@ extern "C" {
 
 /* Paths gptq_q4_matmul can take (see gptq_q4_set_path). */
 #define GPTQ_Q4_PATH_AUTO      0  /* decode below the prefill threshold, fused prefill above */
-#define GPTQ_Q4_PATH_DECODE    1  /* always decode: the TMA-ring kernel for M <= 16 when the shape
+#define GPTQ_Q4_PATH_DECODE    1  /* always decode: the TMA-ring kernel for M <= 16 on layers of at
+                                     least 24 Mi weights (64 Mi when M <= 4) where the shape
                                      allows it, the register-streaming kernel otherwise */
 #define GPTQ_Q4_PATH_PREFILL   2  /* always the fused shared-memory-dequant tensor-core kernel */
 #define GPTQ_Q4_PATH_DECODE_MMA 3 /* always the register-streaming decode kernel */
 #define GPTQ_Q4_PATH_DECODE_TC 4  /* decode on tcgen05 with one tensor-memory accumulator per
-                                     quantization group (M <= 16, else as DECODE) */
+                                     quantization group (M <= 16, else register-streaming) */
+#define GPTQ_Q4_PATH_DECODE_RING 5 /* the TMA-ring decode kernel whenever the shape allows it
+                                      (M <= 16, a K slice within 48 groups), else
+                                      register-streaming */
 
 typedef struct gptq_q4_s *gptq_q4_handle;   /* opaque; owns device memory */
 
@@ -138,15 +142,17 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m);
  *   M    rows; 0 is a valid no-op
  *
  * With act-order, x is first gathered into temp_state (temp_state[m][j] =
- * x[m][P[j]]).  Rows below the prefill threshold run a decode kernel.  For
- * M <= 16: packed-word tiles and x tiles stream through a ring of shared
- * memory stages by TMA; each warp owns 16 columns for a whole K slice,
- * dequantizes in registers and accumulates in fp32 on mma.sync; the K
+ * x[m][P[j]]).  Rows below the prefill threshold run one of two decode
+ * kernels (GPTQ_Q4_PATH_DECODE says which).  The TMA-ring kernel (M <= 16):
+ * packed-word tiles and x tiles stream through a ring of shared-memory
+ * stages by TMA; each warp owns 32 columns for a whole K slice, turns code
+ * pairs into fp16 with one LOP3 each and accumulates on mma.sync in fp32,
+ * the zero point removed per group from MMA-accumulated sums of x; the K
  * slices of a 128-column tile (at most 8) are summed in slice order inside a
- * thread-block cluster.  Otherwise (or where a slice would span more than 64
- * groups): packed weights streamed with 128-bit loads straight into
- * registers, the same arithmetic, split-K summed in a fixed order inside a
- * cluster or, past eight slices, by the last CTA to finish.
+ * thread-block cluster.  The register-streaming kernel: packed weights
+ * streamed with 128-bit loads straight into registers, exact (q - z - 1) in
+ * fp16, fp32 accumulation on mma.sync, split-K summed in a fixed order
+ * inside a cluster or, past eight slices, by the last CTA to finish.
  * GPTQ_Q4_PATH_DECODE_TC selects the
  * tcgen05 decode instead (M <= 16): packed weights streamed by TMA,
  * dequantized in shared memory to the exact integers (q - z - 1), one

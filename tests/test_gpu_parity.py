@@ -77,12 +77,13 @@ def test_unpack_and_dequant_bit_exact(q4, K, N, gs, act):
     mat.device_error()
 
 
-@pytest.mark.parametrize("path", ["DECODE", "DECODE_MMA", "DECODE_TC"])
+@pytest.mark.parametrize("path", ["DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC"])
 @pytest.mark.parametrize("K,N,gs,act", SMALL)
 def test_decode_matches_oracle(q4, K, N, gs, act, path):
-    """Every decode kernel: DECODE runs the TMA-ring kernel for M <= 16 and the
-    register-streaming one above; DECODE_MMA always the register-streaming
-    one; DECODE_TC the tcgen05 one with per-group accumulators for M <= 16."""
+    """Every decode kernel: DECODE_RING runs the TMA-ring kernel for M <= 16
+    (register-streaming above); DECODE_MMA always the register-streaming one;
+    DECODE_TC the tcgen05 one with per-group accumulators for M <= 16; DECODE
+    chooses by layer size and M (on these small layers: register-streaming)."""
     layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(22, K, N, gs & 0xFFFF, act))
     dq = oracle_dq(layer)
     mat = make(q4, layer)
