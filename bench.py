@@ -52,7 +52,33 @@ def parse():
     p.add_argument("--soak-s", type=float, default=1.0)
     p.add_argument("--only", choices=["decode", "prefill"], default=None,
                    help="run one leg only (for profiling); the JSON line is then partial")
+    p.add_argument("--single", default=None, metavar="K,N,M[,PATH]",
+                   help="profiling target instead of the bench: one synthetic g=128 layer, a 256 MB L2 "
+                        "flush before each of four calls on PATH (a GPTQ_Q4_PATH_* suffix, default DECODE)")
     return p.parse_args()
+
+
+def run_single(spec: str) -> None:
+    """Four calls of one layer, each after an L2 flush: a short, fixed launch
+    sequence for ncu captures (-s 3 -c 1 takes the fourth call)."""
+    import torch
+    import gptq_bit_weight_gb300 as q4
+    parts = spec.split(",")
+    K, N, M = int(parts[0]), int(parts[1]), int(parts[2])
+    path = getattr(q4, "GPTQ_Q4_PATH_" + (parts[3].upper() if len(parts) > 3 else "DECODE"))
+    layer = synthetic.make_layer(K, N, 128, bias=True, key=(77, K, N))
+    dev = torch.device("cuda", 0)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    mat = q4.Q4Matrix(t(layer.qweight), t(layer.qzeros), t(layer.scales), None, t(layer.bias), 128)
+    mat.set_path(path)
+    x = t(synthetic.activations(M, K, key=(77, K, N, M)))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(4):
+        flush.zero_()
+        y = mat(x)
+    torch.cuda.synchronize()
+    mat.device_error()
+    print(json.dumps({"single": spec, "max_abs_y": float(y.float().abs().max())}))
 
 
 def peaks():
@@ -392,7 +418,9 @@ def run_native(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved_gbs / hbm_gbs, "traffic": None,
-                         "kernel": "decode_kernel", "peak_source": peak_src,
+                         "kernel": ("decode_kernel (register-streaming; M <= 4 on these layers) and "
+                                    "decode_ring_kernel (TMA ring; M = 8 on all but 4096x4096)"),
+                         "peak_source": peak_src,
                          "how": "algorithmic bytes of the timed region / its CUDA-event time (only decode kernels run in it)"},
             "eager": {"value": eager_value, "unit": "TB/s",
                       "how": "the same steps launched call by call from Python through the C ABI"},
@@ -515,7 +543,7 @@ def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
         "workload": "prefill_7b", "metric": "prefill TFLOPS (2*M*K*N / time)", "value": fused_tf,
         "unit": "TFLOP/s", "unfused_value": tot_flops / (tot_unf * 1e-3) / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
-                     "frac": achieved / bf16_tf, "traffic": None, "kernel": "tc_gemm_kernel<true> (fused prefill)",
+                     "frac": achieved / bf16_tf, "traffic": None, "kernel": "prefill_kernel (fused prefill)",
                      "peak_source": f"{peak_src} bf16 burst x 1 (fp16 and bf16 dense rates are equal)",
                      "how": "trivial-g_idx cases: 2*M*K*N summed / per-call CUDA-event time summed"},
         "cases": cases,
@@ -524,7 +552,9 @@ def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.single:
+        run_single(args.single)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

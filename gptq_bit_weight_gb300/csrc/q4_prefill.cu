@@ -47,8 +47,14 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kSA = 6;                               // TMA ring stages
-constexpr int kSB = 2;                               // fp16 B ring stages
+#ifndef Q4_PREFILL_SA
+#define Q4_PREFILL_SA 6
+#endif
+#ifndef Q4_PREFILL_SB
+#define Q4_PREFILL_SB 2
+#endif
+constexpr int kSA = Q4_PREFILL_SA;                   // TMA ring stages
+constexpr int kSB = Q4_PREFILL_SB;                   // fp16 B ring stages
 constexpr int kAOff = 0, kPOff = 16384, kSzOff = 24576;
 constexpr int kAStage = 26624;                       // 16 KB x + 8 KB packed + 1.25 KB scales/zeros
 constexpr int kBStage = BN * BK * 2;                 // 32 KB
@@ -123,20 +129,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            int it = 0;
+            int it = 0, s = 0;
+            uint32_t ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
                 const int m0 = (t % a.tiles_m) * BM;
                 const int nt0 = (t / a.tiles_m) * (BN / 16);
                 const int tiles16 = min(16, NT16 - nt0);
                 const uint32_t sbytes = tiles16 * 32u, zbytes = tiles16 * 8u;
+                int gcur = -1, left = 0;                 // group of the next 32-row block, blocks left in it
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kSA;
-                    const uint32_t ph = (it / kSA) & 1;
                     if (aborted(abort_flag)) { ok = false; break; }
                     if (!mbar_wait(emptyA(s), ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
-                    const int g_first = (2 * kb) / a.bpg, g_last = (2 * kb + 1) / a.bpg;
-                    const int ng = g_last - g_first + 1;
+                    if (left == 0) { ++gcur; left = a.bpg; }
+                    const int g_first = gcur;
+                    --left;
+                    if (left == 0) { ++gcur; left = a.bpg; }
+                    --left;
+                    const int ng = gcur - g_first + 1;
                     const uint32_t st = base + s * kAStage;
                     mbar_arrive_expect_tx(fullA(s), 16384u + 8192u + ng * (sbytes + zbytes));
                     tma_load_2d(st + kAOff, &tmA, fullA(s), kb * BK, m0);
@@ -146,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_load(st + kSzOff + gi * 512, a.s2 + (gr * NT16 + nt0) * 8, sbytes, fullA(s));
                         bulk_load(st + kSzOff + 1024 + gi * 128, a.zeros + gr * (a.N >> 3) + nt0 * 2, zbytes, fullA(s));
                     }
+                    if (++s == kSA) { s = 0; ph ^= 1; }
                 }
             }
             if (aborted(abort_flag))
@@ -213,27 +224,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             c_nl[J][1] = neg_zlo(z1);
             c_nh[J][1] = neg_zhi(z1);
         };
-        int it = 0;
+        int s = 0, sb = 0;
+        uint32_t ph = 0, phb = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-            int cached_g0 = -1;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int s = it % kSA, sb = it % kSB;
+            int left = 0;                             // 32-row blocks left in the current group
+            for (int kb = 0; kb < KB; ++kb) {
                 if (aborted(abort_flag)) { ok = false; break; }
-                if (!mbar_wait(fullA(s), (it / kSA) & 1) || !mbar_wait(emptyB(sb), ((it / kSB) & 1) ^ 1)) {
+                if (!mbar_wait(fullA(s), ph) || !mbar_wait(emptyB(sb), phb ^ 1)) {
                     fail(a.status, 0x40, abort_flag);
                     ok = false;
                     break;
                 }
                 const uint8_t *st = sbase + s * kAStage;
                 const uint8_t *sz = st + kSzOff;
-                const int g0 = (2 * kb) / a.bpg;
-                const int gl1 = (2 * kb + 1) / a.bpg - g0;
-                if (g0 != cached_g0) {
-                    load_consts(sz, 0, 0);
-                    cached_g0 = g0;
-                }
-                if (gl1) load_consts(sz, 1, 1);
+                // first block: a new group starts here (slot 0) or continues from the
+                // previous stage's second block, whose constants are already in slot 0
+                if (left == 0) { load_consts(sz, 0, 0); left = a.bpg; }
+                --left;
+                const bool gl1 = left == 0;           // the second block starts a new group (slot 1)
+                if (gl1) { load_consts(sz, 1, 1); left = a.bpg; }
+                --left;
                 const uint4 wv = *reinterpret_cast<const uint4 *>(st + kPOff + (wl * 32 + ls) * 16);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
                 uint8_t *brow = sbase + kRingB + sb * kBStage + 2 * wl * 1024 + gq * 128;
@@ -254,6 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(fullB(sb));
                     mbar_arrive(emptyA(s));
                 }
+                if (gl1) {                            // that group continues into the next stage
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        c_s[0][c] = c_s[1][c];
+                        c_nl[0][c] = c_nl[1][c];
+                        c_nh[0][c] = c_nh[1][c];
+                    }
+                }
+                if (++s == kSA) { s = 0; ph ^= 1; }
+                if (++sb == kSB) { sb = 0; phb ^= 1; }
             }
         }
     } else {
