@@ -6,8 +6,10 @@
 // to the fp32 sum before the single rounding to fp16 ("Inference Backends",
 // "Numeric epilogues and input gradients").
 //
-// Persistent kernel, one CTA per SM, 128 x 256 output tiles taken round-robin
-// (m fastest, so the CTAs working at the same time share weight tiles in L2).
+// Persistent kernel, one CTA per SM, 128 x BN output tiles taken round-robin
+// (m fastest, so the CTAs working at the same time share weight tiles in L2);
+// BN = 256, or 128 when 256-wide tiles would leave SMs idle (small M).  The
+// roles below are for BN = 256 (BN = 128: 8 dequant warps, 256 TMEM columns).
 //
 //   warp 0       one thread: TMA loads into a 6-stage ring of {x tile 128x64
 //                fp16 (128-byte swizzle), packed-word tile 256x64 (8 KB), the
@@ -46,7 +48,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
 #ifndef Q4_PREFILL_SA
 #define Q4_PREFILL_SA 6
 #endif
@@ -55,16 +57,30 @@ constexpr int BM = 128, BN = 256, BK = 64;
 #endif
 constexpr int kSA = Q4_PREFILL_SA;                   // TMA ring stages
 constexpr int kSB = Q4_PREFILL_SB;                   // fp16 B ring stages
-constexpr int kAOff = 0, kPOff = 16384, kSzOff = 24576;
-constexpr int kAStage = 26624;                       // 16 KB x + 8 KB packed + 1.25 KB scales/zeros
-constexpr int kBStage = BN * BK * 2;                 // 32 KB
-constexpr int kRingB = kSA * kAStage;                // byte offset of the B ring
-constexpr int kBarOff = kRingB + kSB * kBStage;
-constexpr int kNumBars = 2 * kSA + 2 * kSB + 4;
-constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
-constexpr int kDqWarps = 16, kEpiWarps = 4;
-constexpr int kThreads = 32 * (2 + kDqWarps + kEpiWarps);
-constexpr uint32_t kTmemCols = 512;
+constexpr int kEpiWarps = 4;
+
+// Per tile width BN (256, or 128 where 256-wide tiles leave SMs idle): one
+// dequant warp per 16 columns; a stage holds {x 16 KB, packed words BN*32 B,
+// scale pairs of up to two groups (BN*2 B each), their zero words (BN/2 B
+// each)}, padded to 1 KB so every x tile keeps the 128-byte swizzle atom.
+template <int BN_>
+struct PfCfg {
+    static constexpr int BN = BN_;
+    static constexpr int kAOff = 0, kPOff = 16384;
+    static constexpr int kSGroup = BN * 2, kZGroup = BN / 2;
+    static constexpr int kSzOff = kPOff + BN * 32;
+    static constexpr int kZOff = 2 * kSGroup;           // zero words after both groups' scales
+    static constexpr int kAStage = ((kSzOff + 2 * kSGroup + 2 * kZGroup) + 1023) / 1024 * 1024;
+    static constexpr int kBStage = BN * BK * 2;
+    static constexpr int kRingB = kSA * kAStage;
+    static constexpr int kBarOff = kRingB + kSB * kBStage;
+    static constexpr int kNumBars = 2 * kSA + 2 * kSB + 4;
+    static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+    static constexpr int kDqWarps = BN / 16;
+    static constexpr int kThreads = 32 * (2 + kDqWarps + kEpiWarps);
+    static constexpr uint32_t kTmemCols = 2 * BN;
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 
 struct PfArgs {
     int M, N, K;
@@ -83,8 +99,14 @@ __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
 }
 __device__ __forceinline__ bool aborted(int *abort_flag) { return *reinterpret_cast<volatile int *>(abort_flag) != 0; }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BNT>
+__global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, PfArgs a) {
+    using P = PfCfg<BNT>;
+    constexpr int BN = P::BN, kAOff = P::kAOff, kPOff = P::kPOff, kSzOff = P::kSzOff, kZOff = P::kZOff;
+    constexpr int kAStage = P::kAStage, kBStage = P::kBStage, kRingB = P::kRingB, kBarOff = P::kBarOff;
+    constexpr int kNumBars = P::kNumBars, kDqWarps = P::kDqWarps;
+    constexpr uint32_t kTmemCols = P::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -135,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
                 const int m0 = (t % a.tiles_m) * BM;
                 const int nt0 = (t / a.tiles_m) * (BN / 16);
-                const int tiles16 = min(16, NT16 - nt0);
+                const int tiles16 = min(BN / 16, NT16 - nt0);
                 const uint32_t sbytes = tiles16 * 32u, zbytes = tiles16 * 8u;
                 int gcur = -1, left = 0;                 // group of the next 32-row block, blocks left in it
                 for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -148,13 +170,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     --left;
                     const int ng = gcur - g_first + 1;
                     const uint32_t st = base + s * kAStage;
-                    mbar_arrive_expect_tx(fullA(s), 16384u + 8192u + ng * (sbytes + zbytes));
+                    mbar_arrive_expect_tx(fullA(s), 16384u + BN * 32u + ng * (sbytes + zbytes));
                     tma_load_2d(st + kAOff, &tmA, fullA(s), kb * BK, m0);
                     tma_load_2d(st + kPOff, &tmW, fullA(s), kb * 128, nt0);
                     for (int gi = 0; gi < ng; ++gi) {
                         const size_t gr = static_cast<size_t>(g_first + gi);
-                        bulk_load(st + kSzOff + gi * 512, a.s2 + (gr * NT16 + nt0) * 8, sbytes, fullA(s));
-                        bulk_load(st + kSzOff + 1024 + gi * 128, a.zeros + gr * (a.N >> 3) + nt0 * 2, zbytes, fullA(s));
+                        bulk_load(st + kSzOff + gi * P::kSGroup, a.s2 + (gr * NT16 + nt0) * 8, sbytes, fullA(s));
+                        bulk_load(st + kSzOff + kZOff + gi * P::kZGroup, a.zeros + gr * (a.N >> 3) + nt0 * 2, zbytes,
+                                  fullA(s));
                     }
                     if (++s == kSA) { s = 0; ph ^= 1; }
                 }
@@ -214,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
         uint32_t c_s[2][2], c_nl[2][2], c_nh[2][2];   // [half J][column gq / gq+8]
         auto load_consts = [&](const uint8_t *sz, int gl, int J) {
-            const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + (gl * 128 + wl * 8 + gq) * 4);
-            const uint2 zw = *reinterpret_cast<const uint2 *>(sz + 1024 + (gl * 32 + wl * 2) * 4);
+            const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + gl * P::kSGroup + (wl * 8 + gq) * 4);
+            const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + gl * P::kZGroup + wl * 8);
             c_s[J][0] = __byte_perm(sp, sp, 0x1010);
             c_s[J][1] = __byte_perm(sp, sp, 0x3232);
             const uint32_t z0 = (zw.x >> (4 * gq)) & 0xFu, z1 = (zw.y >> (4 * gq)) & 0xFu;
@@ -349,9 +372,10 @@ int sm_count() {
     return n;
 }
 
-}  // namespace
 
-cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+template <int BN>
+cudaError_t launch_prefill_bn(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+    using P = PfCfg<BN>;
     CUtensorMap tmA, tmW;
     cudaError_t e;
     const int KC = h.K / 64;
@@ -359,15 +383,27 @@ cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16
                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
         return e;
     if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
-                       static_cast<uint64_t>(KC) * 512, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+                       static_cast<uint64_t>(KC) * 512, 128, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
-    static cudaError_t attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    static cudaError_t attr =
+        cudaFuncSetAttribute(prefill_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
     if (attr != cudaSuccess) return attr;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM, (h.N + BN - 1) / BN};
     const int ntiles = args.tiles_m * args.tiles_n;
     const int grid = ntiles < sm_count() ? ntiles : sm_count();
-    prefill_kernel<<<grid, kThreads, kSmem, s>>>(tmA, tmW, args);
+    prefill_kernel<BN><<<grid, P::kThreads, P::kSmem, s>>>(tmA, tmW, args);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+// 256-column tiles unless they leave more than a quarter of the SMs without a
+// tile (small M): then 128-column tiles, at the same cost per flop, twice as
+// many of them.
+cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+    const long long tiles256 = static_cast<long long>((M + BM - 1) / BM) * ((h.N + 255) / 256);
+    if (4 * tiles256 < 3LL * sm_count()) return launch_prefill_bn<128>(h, x, M, out, s);
+    return launch_prefill_bn<256>(h, x, M, out, s);
 }
 
 int prefill_default_min_m() { return 64; }

@@ -102,3 +102,23 @@ def test_prefill_7b_workload_sampled(q4, K, N, act):
     check(yu[rows], y_ref, tol, f"unfused {K}x{N}")
     check(yd[rows], y_ref, tol, f"decode path {K}x{N}")
     mat.device_error()
+
+
+@pytest.mark.parametrize("K,N,gs,act,M", [(1152, 576, 96, False, 4900), (1024, 448, 32, True, 7300)])
+def test_prefill_wide_tiles_sampled(q4, K, N, gs, act, M):
+    """Enough rows that the fused prefill takes 256-column tiles on a narrow
+    layer (ragged last column tile and ragged last row tile); oracle on a row
+    sample."""
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(34, K, N, gs & 0xFFFF, act))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs)
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                      to_dev(layer.bias), gs)
+    x = synthetic.activations(M, K, key=(34, K, N, M))
+    rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(35).choice(M, 48, replace=False)]))
+    y_ref = oracle.reference_output(x[rows], dq, layer.bias)
+    tol = oracle.tolerance(x, dq.w16, y_ref, K)
+    mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
+    y = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check(y[rows], y_ref, tol, f"fused wide tiles K={K} N={N} g={gs} act={act} M={M}")
+    mat.device_error()
