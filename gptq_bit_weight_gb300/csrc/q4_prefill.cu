@@ -48,38 +48,41 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BK = 64;
-#ifndef Q4_PREFILL_SA
-#define Q4_PREFILL_SA 6
-#endif
-#ifndef Q4_PREFILL_SB
-#define Q4_PREFILL_SB 2
-#endif
-constexpr int kSA = Q4_PREFILL_SA;                   // TMA ring stages
-constexpr int kSB = Q4_PREFILL_SB;                   // fp16 B ring stages
+constexpr int BK = 64;
 constexpr int kEpiWarps = 4;
 
-// Per tile width BN (256, or 128 where 256-wide tiles leave SMs idle): one
-// dequant warp per 16 columns; a stage holds {x 16 KB, packed words BN*32 B,
-// scale pairs of up to two groups (BN*2 B each), their zero words (BN/2 B
-// each)}, padded to 1 KB so every x tile keeps the 128-byte swizzle atom.
-template <int BN_>
+// Per tile BM x BN: BN = 256, or 128 where 256-wide tiles leave SMs idle (one
+// dequant warp per 16 columns); BM = 128, or 256 (two M = 128 MMAs per k step
+// on the same fp16 B tile, halving the dequantization per flop, with the one
+// accumulator pair filling tensor memory) when there are tiles enough.
+// Three rings: x tiles (BM x 64 fp16, 128-byte swizzle), packed-word stages
+// {packed words BN*32 B, scale pairs of up to two groups (BN*2 B each), their
+// zero words (BN/2 B each)}, and fp16 B tiles (K-major, 128-byte swizzle).
+template <int BM_, int BN_>
 struct PfCfg {
-    static constexpr int BN = BN_;
-    static constexpr int kAOff = 0, kPOff = 16384;
+    static constexpr int BM = BM_, BN = BN_;
+    static constexpr int kHalves = BM / 128;           // M = 128 MMAs per k step
+    static constexpr int kAccBufs = BM == 128 ? 2 : 1; // accumulator sets (double-buffered when they fit)
+    static constexpr int kSX = BM == 128 ? 5 : 3;      // x-tile ring (released by the MMAs)
+    static constexpr int kSP = 4;                      // packed-word ring (released by the dequantizers)
+    static constexpr int kSB = BM == 128 ? 3 : 2;      // fp16 B ring
+    static constexpr int kXStage = BM * BK * 2;
     static constexpr int kSGroup = BN * 2, kZGroup = BN / 2;
-    static constexpr int kSzOff = kPOff + BN * 32;
-    static constexpr int kZOff = 2 * kSGroup;           // zero words after both groups' scales
-    static constexpr int kAStage = ((kSzOff + 2 * kSGroup + 2 * kZGroup) + 1023) / 1024 * 1024;
+    static constexpr int kSzOff = BN * 32;             // within a packed stage
+    static constexpr int kZOff = 2 * kSGroup;          // zero words after both groups' scales
+    static constexpr int kPStage = (kSzOff + 2 * kSGroup + 2 * kZGroup + 127) / 128 * 128;
     static constexpr int kBStage = BN * BK * 2;
-    static constexpr int kRingB = kSA * kAStage;
+    static constexpr int kRingP = kSX * kXStage;
+    static constexpr int kRingB = (kRingP + kSP * kPStage + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kRingB + kSB * kBStage;
-    static constexpr int kNumBars = 2 * kSA + 2 * kSB + 4;
+    static constexpr int kNumBars = 2 * kSX + 2 * kSP + 2 * kSB + 4;
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr int kDqWarps = BN / 16;
-    static constexpr int kThreads = 32 * (2 + kDqWarps + kEpiWarps);
-    static constexpr uint32_t kTmemCols = 2 * BN;
+    static constexpr int kDq0 = 3;                     // first dequant warp
+    static constexpr int kThreads = 32 * (kDq0 + kDqWarps + kEpiWarps);
+    static constexpr uint32_t kTmemCols = kAccBufs * kHalves * BN;
     static_assert(kSmem <= 227 * 1024, "shared memory");
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "tensor memory");
 };
 
 struct PfArgs {
@@ -99,25 +102,41 @@ __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
 }
 __device__ __forceinline__ bool aborted(int *abort_flag) { return *reinterpret_cast<volatile int *>(abort_flag) != 0; }
 
-template <int BNT>
-__global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
+// Ring position: slot and the parity of its current phase.
+struct RingPos {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+};
+
+template <int BMT, int BNT>
+__global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, PfArgs a) {
-    using P = PfCfg<BNT>;
-    constexpr int BN = P::BN, kAOff = P::kAOff, kPOff = P::kPOff, kSzOff = P::kSzOff, kZOff = P::kZOff;
-    constexpr int kAStage = P::kAStage, kBStage = P::kBStage, kRingB = P::kRingB, kBarOff = P::kBarOff;
-    constexpr int kNumBars = P::kNumBars, kDqWarps = P::kDqWarps;
+    using P = PfCfg<BMT, BNT>;
+    constexpr int BM = P::BM, BN = P::BN, kSzOff = P::kSzOff, kZOff = P::kZOff;
+    constexpr int kSX = P::kSX, kSP = P::kSP, kSB = P::kSB, kHalves = P::kHalves, kAccBufs = P::kAccBufs;
+    constexpr int kXStage = P::kXStage, kPStage = P::kPStage, kBStage = P::kBStage;
+    constexpr int kRingP = P::kRingP, kRingB = P::kRingB, kBarOff = P::kBarOff;
+    constexpr int kNumBars = P::kNumBars, kDqWarps = P::kDqWarps, kDq0 = P::kDq0;
     constexpr uint32_t kTmemCols = P::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sbase = smem_raw + (base - raw);
     const uint32_t bar0 = base + kBarOff;
-    auto fullA = [&](int s) { return bar0 + 8u * s; };
-    auto emptyA = [&](int s) { return bar0 + 8u * (kSA + s); };
-    auto fullB = [&](int s) { return bar0 + 8u * (2 * kSA + s); };
-    auto emptyB = [&](int s) { return bar0 + 8u * (2 * kSA + kSB + s); };
-    auto accF = [&](int i) { return bar0 + 8u * (2 * kSA + 2 * kSB + i); };
-    auto accE = [&](int i) { return bar0 + 8u * (2 * kSA + 2 * kSB + 2 + i); };
+    auto fullX = [&](int s) { return bar0 + 8u * s; };
+    auto emptyX = [&](int s) { return bar0 + 8u * (kSX + s); };
+    auto fullP = [&](int s) { return bar0 + 8u * (2 * kSX + s); };
+    auto emptyP = [&](int s) { return bar0 + 8u * (2 * kSX + kSP + s); };
+    auto fullB = [&](int s) { return bar0 + 8u * (2 * kSX + 2 * kSP + s); };
+    auto emptyB = [&](int s) { return bar0 + 8u * (2 * kSX + 2 * kSP + kSB + s); };
+    auto accF = [&](int i) { return bar0 + 8u * (2 * kSX + 2 * kSP + 2 * kSB + i); };
+    auto accE = [&](int i) { return bar0 + 8u * (2 * kSX + 2 * kSP + 2 * kSB + 2 + i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + kBarOff + kNumBars * 8);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -127,9 +146,13 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
     const int ntiles = a.tiles_m * a.tiles_n;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSA; ++s) {
-            mbar_init(fullA(s), 1);
-            mbar_init(emptyA(s), 1 + kDqWarps);
+        for (int s = 0; s < kSX; ++s) {
+            mbar_init(fullX(s), 1);
+            mbar_init(emptyX(s), 1);                 // the MMAs that read it
+        }
+        for (int s = 0; s < kSP; ++s) {
+            mbar_init(fullP(s), 1);
+            mbar_init(emptyP(s), kDqWarps);          // every dequant warp has read it
         }
         for (int s = 0; s < kSB; ++s) {
             mbar_init(fullB(s), kDqWarps);
@@ -149,86 +172,108 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------ producer
+        // ------------------------------------------ producer: packed words, scales, zeros
         if (lane == 0) {
-            int it = 0, s = 0;
-            uint32_t ph = 0;
+            RingPos r;
+            int issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-                const int m0 = (t % a.tiles_m) * BM;
                 const int nt0 = (t / a.tiles_m) * (BN / 16);
                 const int tiles16 = min(BN / 16, NT16 - nt0);
                 const uint32_t sbytes = tiles16 * 32u, zbytes = tiles16 * 8u;
                 int gcur = -1, left = 0;                 // group of the next 32-row block, blocks left in it
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int kb = 0; kb < KB; ++kb) {
                     if (aborted(abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(emptyA(s), ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
+                    if (!mbar_wait(emptyP(r.s), r.ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
                     if (left == 0) { ++gcur; left = a.bpg; }
                     const int g_first = gcur;
                     --left;
                     if (left == 0) { ++gcur; left = a.bpg; }
                     --left;
                     const int ng = gcur - g_first + 1;
-                    const uint32_t st = base + s * kAStage;
-                    mbar_arrive_expect_tx(fullA(s), 16384u + BN * 32u + ng * (sbytes + zbytes));
-                    tma_load_2d(st + kAOff, &tmA, fullA(s), kb * BK, m0);
-                    tma_load_2d(st + kPOff, &tmW, fullA(s), kb * 128, nt0);
+                    const uint32_t st = base + kRingP + r.s * kPStage;
+                    mbar_arrive_expect_tx(fullP(r.s), BN * 32u + ng * (sbytes + zbytes));
+                    tma_load_2d(st, &tmW, fullP(r.s), kb * 128, nt0);
                     for (int gi = 0; gi < ng; ++gi) {
                         const size_t gr = static_cast<size_t>(g_first + gi);
-                        bulk_load(st + kSzOff + gi * P::kSGroup, a.s2 + (gr * NT16 + nt0) * 8, sbytes, fullA(s));
+                        bulk_load(st + kSzOff + gi * P::kSGroup, a.s2 + (gr * NT16 + nt0) * 8, sbytes, fullP(r.s));
                         bulk_load(st + kSzOff + kZOff + gi * P::kZGroup, a.zeros + gr * (a.N >> 3) + nt0 * 2, zbytes,
-                                  fullA(s));
+                                  fullP(r.s));
                     }
-                    if (++s == kSA) { s = 0; ph ^= 1; }
+                    ++issued;
+                    r.next(kSP);
                 }
             }
             if (aborted(abort_flag))
-                for (int j = it > kSA ? it - kSA : 0; j < it; ++j) mbar_wait(fullA(j % kSA), (j / kSA) & 1);
+                for (int j = issued > kSP ? issued - kSP : 0; j < issued; ++j) mbar_wait(fullP(j % kSP), (j / kSP) & 1);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------ producer: x tiles
+        if (lane == 0) {
+            RingPos r;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const int m0 = (t % a.tiles_m) * BM;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (aborted(abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(emptyX(r.s), r.ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
+                    mbar_arrive_expect_tx(fullX(r.s), static_cast<uint32_t>(kXStage));
+                    tma_load_2d(base + r.s * kXStage, &tmA, fullX(r.s), kb * BK, m0);
+                    ++issued;
+                    r.next(kSX);
+                }
+            }
+            if (aborted(abort_flag))
+                for (int j = issued > kSX ? issued - kSX : 0; j < issued; ++j) mbar_wait(fullX(j % kSX), (j / kSX) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN, false);
-            int it = 0, lt = 0;
+            constexpr uint32_t idesc = idesc_f16(128, BN, false);
+            RingPos rx, rb;
+            int lt = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++lt) {
-                const int acc = lt & 1;
-                const uint32_t aph = (lt >> 1) & 1;
+                const int acc = lt % kAccBufs;
+                const uint32_t aph = (lt / kAccBufs) & 1;
                 if (aborted(abort_flag) || !mbar_wait(accE(acc), aph ^ 1)) {
                     fail(a.status, 0x20, abort_flag);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kSA, sb = it % kSB;
-                    if (aborted(abort_flag) || !mbar_poll(fullA(s), (it / kSA) & 1) ||
-                        !mbar_poll(fullB(sb), (it / kSB) & 1)) {
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kHalves * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (aborted(abort_flag) || !mbar_poll(fullX(rx.s), rx.ph) || !mbar_poll(fullB(rb.s), rb.ph)) {
                         fail(a.status, 0x20, abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * kAStage + kAOff;
-                    const uint32_t sbb = base + kRingB + sb * kBStage;
+                    const uint32_t sa = base + rx.s * kXStage;
+                    const uint32_t sbb = base + kRingB + rb.s * kBStage;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_f16(d, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(sbb + kk * 32, 16, 1024),
-                                 idesc, (kb | kk) != 0);
-                    umma_commit(emptyA(s));
-                    umma_commit(emptyB(sb));
+#pragma unroll
+                        for (int hm = 0; hm < kHalves; ++hm)    // rows 128*hm.. of the x tile, same B tile
+                            umma_f16(d + hm * BN, smem_desc_sw128(sa + hm * 16384 + kk * 32, 16, 1024),
+                                     smem_desc_sw128(sbb + kk * 32, 16, 1024), idesc, (kb | kk) != 0);
+                    umma_commit(emptyX(rx.s));
+                    umma_commit(emptyB(rb.s));
+                    rx.next(kSX);
+                    rb.next(kSB);
                 }
                 if (ok) umma_commit(accF(acc));
             }
         }
-    } else if (warp < 2 + kDqWarps) {
+    } else if (warp < kDq0 + kDqWarps) {
         // ------------------------------------------------------ dequantizers
         // Lane -> packed-word assignment: in every 8-lane phase (p = lane >> 3)
         // the lanes take columns gq in {p, p ^ 5} and all four tq, so the
         // 16-byte loads of packed words and the 16-byte stores into the
         // swizzled B tile both hit eight distinct bank groups per phase.
-        // Warp wl owns n16 tile wl of the 256-column tile.
-        const int wl = warp - 2;
+        // Warp wl owns n16 tile wl of the tile.
+        const int wl = warp - kDq0;
         const int pq = lane >> 3;
         const int gq = ((lane >> 2) & 1) ? (pq ^ 5) : pq;
         const int tq = lane & 3;
@@ -247,19 +292,18 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
             c_nl[J][1] = neg_zlo(z1);
             c_nh[J][1] = neg_zhi(z1);
         };
-        int s = 0, sb = 0;
-        uint32_t ph = 0, phb = 0;
+        RingPos rp, rb;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
             int left = 0;                             // 32-row blocks left in the current group
             for (int kb = 0; kb < KB; ++kb) {
                 if (aborted(abort_flag)) { ok = false; break; }
-                if (!mbar_wait(fullA(s), ph) || !mbar_wait(emptyB(sb), phb ^ 1)) {
+                if (!mbar_wait(fullP(rp.s), rp.ph) || !mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
                     fail(a.status, 0x40, abort_flag);
                     ok = false;
                     break;
                 }
-                const uint8_t *st = sbase + s * kAStage;
+                const uint8_t *st = sbase + kRingP + rp.s * kPStage;
                 const uint8_t *sz = st + kSzOff;
                 // first block: a new group starts here (slot 0) or continues from the
                 // previous stage's second block, whose constants are already in slot 0
@@ -268,9 +312,9 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
                 const bool gl1 = left == 0;           // the second block starts a new group (slot 1)
                 if (gl1) { load_consts(sz, 1, 1); left = a.bpg; }
                 --left;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(st + kPOff + (wl * 32 + ls) * 16);
+                const uint4 wv = *reinterpret_cast<const uint4 *>(st + (wl * 32 + ls) * 16);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                uint8_t *brow = sbase + kRingB + sb * kBStage + 2 * wl * 1024 + gq * 128;
+                uint8_t *brow = sbase + kRingB + rb.s * kBStage + 2 * wl * 1024 + gq * 128;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int J = j >> 1, jj = j & 1;
@@ -285,8 +329,8 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(fullB(sb));
-                    mbar_arrive(emptyA(s));
+                    mbar_arrive(fullB(rb.s));
+                    mbar_arrive(emptyP(rp.s));        // every register loaded from it is consumed
                 }
                 if (gl1) {                            // that group continues into the next stage
 #pragma unroll
@@ -296,8 +340,8 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
                         c_nh[0][c] = c_nh[1][c];
                     }
                 }
-                if (++s == kSA) { s = 0; ph ^= 1; }
-                if (++sb == kSB) { sb = 0; phb ^= 1; }
+                rp.next(kSP);
+                rb.next(kSB);
             }
         }
     } else {
@@ -305,8 +349,8 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. +31
         int lt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
-            const int acc = lt & 1;
-            const uint32_t aph = (lt >> 1) & 1;
+            const int acc = lt % kAccBufs;
+            const uint32_t aph = (lt / kAccBufs) & 1;
             bool ok = !aborted(abort_flag) && mbar_wait(accF(acc), aph);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -316,11 +360,13 @@ __global__ void __launch_bounds__(PfCfg<BNT>::kThreads, 1)
             tc_fence_after();
             const int m0 = (t % a.tiles_m) * BM;
             const int n0 = (t / a.tiles_m) * BN;
-            const int row = m0 + 32 * quad + lane;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int hc = 0; hc < kHalves * BN; hc += 32) {
+                const int hm = hc / BN, c0 = hc % BN;
+                const int row = m0 + 128 * hm + 32 * quad + lane;
                 uint32_t r[32];
-                tmem_ld_x32(tmem + static_cast<uint32_t>(acc * BN + c0) + (static_cast<uint32_t>(32 * quad) << 16), r);
+                tmem_ld_x32(tmem + static_cast<uint32_t>(acc * kHalves * BN + hc) + (static_cast<uint32_t>(32 * quad) << 16),
+                            r);
                 if (row < a.M) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -373,9 +419,9 @@ int sm_count() {
 }
 
 
-template <int BN>
-cudaError_t launch_prefill_bn(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
-    using P = PfCfg<BN>;
+template <int BM, int BN>
+cudaError_t launch_prefill_tile(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+    using P = PfCfg<BM, BN>;
     CUtensorMap tmA, tmW;
     cudaError_t e;
     const int KC = h.K / 64;
@@ -386,24 +432,28 @@ cudaError_t launch_prefill_bn(const HandleView &h, const uint16_t *x, int M, uin
                        static_cast<uint64_t>(KC) * 512, 128, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
     static cudaError_t attr =
-        cudaFuncSetAttribute(prefill_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
+        cudaFuncSetAttribute(prefill_kernel<BM, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
     if (attr != cudaSuccess) return attr;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM, (h.N + BN - 1) / BN};
     const int ntiles = args.tiles_m * args.tiles_n;
     const int grid = ntiles < sm_count() ? ntiles : sm_count();
-    prefill_kernel<BN><<<grid, P::kThreads, P::kSmem, s>>>(tmA, tmW, args);
+    prefill_kernel<BM, BN><<<grid, P::kThreads, P::kSmem, s>>>(tmA, tmW, args);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// 256-column tiles unless they leave more than a quarter of the SMs without a
-// tile (small M): then 128-column tiles, at the same cost per flop, twice as
-// many of them.
+// Tile shape by tile count (c = SMs): 256 x 256 when those tiles still give
+// every SM at least three quarters of a tile's work; else 128 x 256; else
+// 128 x 128 (small M), at the same cost per flop as 128 x 256.
 cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
-    const long long tiles256 = static_cast<long long>((M + BM - 1) / BM) * ((h.N + 255) / 256);
-    if (4 * tiles256 < 3LL * sm_count()) return launch_prefill_bn<128>(h, x, M, out, s);
-    return launch_prefill_bn<256>(h, x, M, out, s);
+    const long long c = sm_count();
+    const long long n256 = (h.N + 255) / 256;
+    const long long t256x256 = static_cast<long long>((M + 255) / 256) * n256;
+    const long long t128x256 = static_cast<long long>((M + 127) / 128) * n256;
+    if (4 * t256x256 >= 3 * c) return launch_prefill_tile<256, 256>(h, x, M, out, s);
+    if (4 * t128x256 >= 3 * c) return launch_prefill_tile<128, 256>(h, x, M, out, s);
+    return launch_prefill_tile<128, 128>(h, x, M, out, s);
 }
 
 int prefill_default_min_m() { return 64; }
