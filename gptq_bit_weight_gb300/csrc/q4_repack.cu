@@ -9,6 +9,8 @@
 // and temp_dq receives dequantized weights.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "q4_internal.cuh"
 
 namespace q4 {
@@ -204,8 +206,50 @@ __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *_
     }
 }
 
+// Many rows: the permutation is staged once per CTA and each row of x is
+// staged in shared memory with 16-byte loads, so that both the reads and the
+// gathered 16-byte writes are coalesced (the gather itself hits shared
+// memory).  Rows are taken round-robin by the CTAs.
+__global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__restrict__ x,
+                                                             const int32_t *__restrict__ perm, int M, int K,
+                                                             uint16_t *__restrict__ ts) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    int32_t *sp = reinterpret_cast<int32_t *>(sm);
+    uint16_t *sx = reinterpret_cast<uint16_t *>(sm + static_cast<size_t>(K) * 4);
+    const int nv = K / 8;                                  // 16-byte vectors per row
+    for (int i = threadIdx.x; i < K / 4; i += blockDim.x)
+        reinterpret_cast<int4 *>(sp)[i] = reinterpret_cast<const int4 *>(perm)[i];
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K);
+        __syncthreads();                                   // the previous row's gathers are done
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) reinterpret_cast<uint4 *>(sx)[i] = xr[i];
+        __syncthreads();
+        uint4 *out = reinterpret_cast<uint4 *>(ts + static_cast<size_t>(m) * K);
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            const int4 p0 = reinterpret_cast<const int4 *>(sp)[2 * i];
+            const int4 p1 = reinterpret_cast<const int4 *>(sp)[2 * i + 1];
+            uint4 v;
+            v.x = static_cast<uint32_t>(sx[p0.x]) | (static_cast<uint32_t>(sx[p0.y]) << 16);
+            v.y = static_cast<uint32_t>(sx[p0.z]) | (static_cast<uint32_t>(sx[p0.w]) << 16);
+            v.z = static_cast<uint32_t>(sx[p1.x]) | (static_cast<uint32_t>(sx[p1.y]) << 16);
+            v.w = static_cast<uint32_t>(sx[p1.z]) | (static_cast<uint32_t>(sx[p1.w]) << 16);
+            out[i] = v;
+        }
+    }
+}
+
 cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K, uint16_t *temp_state,
                             cudaStream_t s) {
+    const size_t rows_smem = static_cast<size_t>(K) * 6;   // permutation + one row
+    if (M >= 32 && rows_smem <= 200 * 1024) {
+        static cudaError_t attr =
+            cudaFuncSetAttribute(xreorder_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (attr != cudaSuccess) return attr;
+        const int per_sm = static_cast<int>((228 * 1024) / (rows_smem + 1024));
+        const int ctas = std::min(M, kSMs * std::max(1, std::min(per_sm, 8)));
+        xreorder_rows_kernel<<<ctas, 256, rows_smem, s>>>(x, perm, M, K, temp_state);
+        return cudaGetLastError();
+    }
     const size_t total = static_cast<size_t>(M) * (K / 8);
     const int threads = 256;
     const size_t want = (total + threads - 1) / threads;
