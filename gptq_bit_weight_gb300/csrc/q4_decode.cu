@@ -97,11 +97,18 @@ __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
     return (slice_chunks * 64 + geff - 1) / geff + 1;
 }
 
-// Resident-CTA target per SM for the register budget: 24, 16 and 8 warps.
-constexpr int min_blocks(int mt) { return (mt == 1 ? 24 : (mt == 2 ? 16 : 8)) / kWarps > 0 ? (mt == 1 ? 24 : (mt == 2 ? 16 : 8)) / kWarps : 1; }
+// Resident-CTA target per SM for the register budget: 24, 16 and 8 warps
+// (16 for the raw-pair arithmetic at MT = 1, whose partial sums take more
+// registers).
+constexpr int min_warps(int mt, bool raw) { return mt == 1 ? (raw ? 16 : 24) : (mt == 2 ? 16 : 8); }
+constexpr int min_blocks(int mt, bool raw) { return min_warps(mt, raw) / kWarps > 0 ? min_warps(mt, raw) / kWarps : 1; }
 
-template <int MT>
-__global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(HandleView h, DecodeArgs a) {
+// RAW: code pairs enter the MMAs as raw 1024 + q / 1024 + 16 q (one LOP3 per
+// pair) and the zero point is removed per group from MMA-accumulated sums of
+// x; otherwise each pair is turned into the exact fp16 (q - z - 1) first (one
+// LOP3 and one HFMA2).  Same result up to fp32 rounding.
+template <int MT, bool RAW>
+__global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(HandleView h, DecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gq = lane >> 2, tq = lane & 3;
@@ -184,17 +191,33 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     }
     __syncthreads();
 
-    float acc[kNTW][MT][4], accg[kNTW][MT][4];
+    float acc[kNTW][MT][4];
 #pragma unroll
     for (int nt = 0; nt < kNTW; ++nt)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][mt][i] = 0.f, accg[nt][mt][i] = 0.f;
+            for (int i = 0; i < 4; ++i) acc[nt][mt][i] = 0.f;
 
     if (wn > 0) {
+        // per group: products of x with the raw pairs (dlo: 1024 + q rows,
+        // dhi: 1024 + 16 q rows) and the sums of x that met them (slo, shi);
+        // exact arithmetic: dlo alone holds sum x (q - z - 1)
+        float dlo[kNTW][MT][4], dhi[kNTW][MT][4], slo[MT][4], shi[MT][4];
         uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
-        float sc[kNTW][2];
+        auto clear_partials = [&]() {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    slo[mt][i] = 0.f;
+                    shi[mt][i] = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < kNTW; ++nt) dlo[nt][mt][i] = dhi[nt][mt][i] = 0.f;
+                }
+        };
+        clear_partials();
+        float sc[kNTW][2], czl[kNTW][2], czh[kNTW][2];   // scale, -(1025 + z), -(65 + z)
         int grp = -1;
 
         auto load_group = [&](int g) {
@@ -205,13 +228,22 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
                 const uint32_t zw0 = base[kNTW * 8 + nt * 2], zw1 = base[kNTW * 8 + nt * 2 + 1];
                 sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                const uint32_t z0 = (zw0 >> (4 * gq)) & 0xFu, z1 = (zw1 >> (4 * gq)) & 0xFu;
-                nzlo[nt][0] = neg_zlo(z0);
-                nzhi[nt][0] = neg_zhi(z0);
-                nzlo[nt][1] = neg_zlo(z1);
-                nzhi[nt][1] = neg_zhi(z1);
+                const float z0 = static_cast<float>((zw0 >> (4 * gq)) & 0xFu);
+                const float z1 = static_cast<float>((zw1 >> (4 * gq)) & 0xFu);
+                czl[nt][0] = -(1025.f + z0);
+                czl[nt][1] = -(1025.f + z1);
+                czh[nt][0] = -(65.f + z0);
+                czh[nt][1] = -(65.f + z1);
+                if (!RAW) {
+                    const uint32_t zi0 = (zw0 >> (4 * gq)) & 0xFu, zi1 = (zw1 >> (4 * gq)) & 0xFu;
+                    nzlo[nt][0] = neg_zlo(zi0);
+                    nzhi[nt][0] = neg_zhi(zi0);
+                    nzlo[nt][1] = neg_zlo(zi1);
+                    nzhi[nt][1] = neg_zhi(zi1);
+                }
             }
         };
+        // sum_k x (q - z - 1) = dlo - (1025 + z) slo + (dhi - (1040 + 16 z) shi) / 16
         auto flush = [&]() {
 #pragma unroll
             for (int nt = 0; nt < kNTW; ++nt)
@@ -219,10 +251,19 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        acc[nt][mt][i] = fmaf(sc[nt][i >> 1], accg[nt][mt][i], acc[nt][mt][i]);
-                        accg[nt][mt][i] = 0.f;
+                        const int c = i >> 1;
+                        float p = dlo[nt][mt][i];
+                        if (RAW) {
+                            p = fmaf(czl[nt][c], slo[mt][i], p);
+                            p = fmaf(0.0625f, dhi[nt][mt][i], p);
+                            p = fmaf(czh[nt][c], shi[mt][i], p);
+                        }
+                        acc[nt][mt][i] = fmaf(sc[nt][c], p, acc[nt][mt][i]);
                     }
+            clear_partials();
         };
+        constexpr uint32_t kOnes = 0x3C003C00u;
+        const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
 
         for (int base = 0; base < wn; base += kDepth) {
 #pragma unroll
@@ -246,19 +287,38 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
                             if (mt * 8 + gq < mrows)
                                 xb[mt] = *reinterpret_cast<const uint4 *>(xs + (mt * 8 + gq) * XS + kk);
                         }
-#pragma unroll
-                        for (int nt = 0; nt < kNTW; ++nt) {
-                            const uint32_t lo = hh ? buf[i][nt].z : buf[i][nt].x;
-                            const uint32_t hi = hh ? buf[i][nt].w : buf[i][nt].y;
-                            uint32_t al[4], ah[4];
-                            unpack_qz(lo, nzlo[nt][0], nzhi[nt][0], al);
-                            unpack_qz(hi, nzlo[nt][1], nzhi[nt][1], ah);
-                            const uint32_t A0[4] = {al[0], ah[0], al[1], ah[1]};
-                            const uint32_t A1[4] = {al[2], ah[2], al[3], ah[3]};
+                        if (RAW) {
 #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
-                                mma_16816(accg[nt][mt], A0, xb[mt].x, xb[mt].y);
-                                mma_16816(accg[nt][mt], A1, xb[mt].z, xb[mt].w);
+                                mma_16816(slo[mt], ones, xb[mt].x, xb[mt].z);
+                                mma_16816(shi[mt], ones, xb[mt].y, xb[mt].w);
+                            }
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < kNTW; ++nt) {
+                            const uint32_t lo = hh ? buf[i][nt].z : buf[i][nt].x;    // column 16nt + gq
+                            const uint32_t hi = hh ? buf[i][nt].w : buf[i][nt].y;    // column 16nt + gq + 8
+                            uint32_t al[4], ah[4];
+                            if (RAW) {
+                                unpack_raw(lo, al);
+                                unpack_raw(hi, ah);
+                                const uint32_t alo[4] = {al[0], ah[0], al[2], ah[2]};
+                                const uint32_t ahi[4] = {al[1], ah[1], al[3], ah[3]};
+#pragma unroll
+                                for (int mt = 0; mt < MT; ++mt) {
+                                    mma_16816(dlo[nt][mt], alo, xb[mt].x, xb[mt].z);
+                                    mma_16816(dhi[nt][mt], ahi, xb[mt].y, xb[mt].w);
+                                }
+                            } else {
+                                unpack_qz(lo, nzlo[nt][0], nzhi[nt][0], al);
+                                unpack_qz(hi, nzlo[nt][1], nzhi[nt][1], ah);
+                                const uint32_t A0[4] = {al[0], ah[0], al[1], ah[1]};
+                                const uint32_t A1[4] = {al[2], ah[2], al[3], ah[3]};
+#pragma unroll
+                                for (int mt = 0; mt < MT; ++mt) {
+                                    mma_16816(dlo[nt][mt], A0, xb[mt].x, xb[mt].y);
+                                    mma_16816(dlo[nt][mt], A1, xb[mt].z, xb[mt].w);
+                                }
                             }
                         }
                     }
@@ -350,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT)) decode_kernel(Handle
     if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
 }
 
-template <int MT>
+template <int MT, bool RAW>
 cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                       uint16_t *out, cudaStream_t s) {
     const int xrows = M < 8 * MT ? M : 8 * MT;
@@ -363,10 +423,10 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
         cudaFuncAttributes fa{};
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT, RAW>);
         const int want = optin - static_cast<int>(fa.sharedSizeBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+            e = cudaFuncSetAttribute(decode_kernel<MT, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess) return e;
         max_dyn = want;
     }
@@ -396,7 +456,7 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<MT>, h, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<MT, RAW>, h, a);
 }
 
 }  // namespace
@@ -412,8 +472,8 @@ bool pdl_enabled() {
 
 // Resident CTAs per SM for a variant: registers (the launch bounds) and
 // shared memory, whichever is tighter.
-int resident_ctas(int mt, size_t smem) {
-    const int by_regs = min_blocks(mt);
+int resident_ctas(int mt, bool raw, size_t smem) {
+    const int by_regs = min_blocks(mt, raw);
     const size_t per_sm = 228 * 1024;                   // shared memory per SM
     const int by_smem = static_cast<int>(per_sm / (smem + 1024));
     return std::max(1, std::min(by_regs, by_smem));
@@ -423,8 +483,9 @@ int resident_ctas(int mt, size_t smem) {
 // one wave of resident CTAs, take the most splits that still fit (the most
 // bytes in flight while the whole grid is one DRAM round trip deep); when it
 // does not, fill whole waves as closely as possible (fewer splits on a tie).
-DecodePlan plan_decode(int M, int K, int N, int geff) {
+static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw) {
     DecodePlan p{};
+    p.raw = raw ? 1 : 0;
     p.mt = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
     p.zdim = (M + 8 * p.mt - 1) / (8 * p.mt);
     p.ctas_n = N / kNB;
@@ -438,7 +499,7 @@ DecodePlan plan_decode(int M, int K, int N, int geff) {
     auto slots_for = [&](int sp) {
         const int slice = (KC + sp - 1) / sp;
         const size_t smem = smem_bytes_for(p.mt, xrows, slice, max_groups_in_slice(slice, geff));
-        return static_cast<long long>(kSMs) * resident_ctas(p.mt, smem);
+        return static_cast<long long>(kSMs) * resident_ctas(p.mt, raw, smem);
     };
     auto valid = [&](int sp) {
         const int slice = (KC + sp - 1) / sp;
@@ -468,7 +529,22 @@ DecodePlan plan_decode(int M, int K, int N, int geff) {
     p.cluster = (p.splits > 1 && p.splits <= kMaxCluster) ? 1 : 0;
     p.n_tickets = base;
     p.ws_floats = (p.splits > 1 && !p.cluster) ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
+    p.one_wave = static_cast<long long>(base) * p.splits <=
+                 static_cast<long long>(kSMs) *
+                     resident_ctas(p.mt, raw, smem_bytes_for(p.mt, std::min(M, 8 * p.mt), p.slice_chunks,
+                                                             max_groups_in_slice(p.slice_chunks, geff)));
     return p;
+}
+
+// M <= 8: the raw-pair arithmetic (fewer instructions, 2 CTAs per SM) when its
+// grid is a single wave, else the exact-pair arithmetic at 3 CTAs per SM,
+// which keeps mid-size layers in one wave.  Larger M: exact pairs.
+DecodePlan plan_decode(int M, int K, int N, int geff) {
+    if (M <= 8) {
+        const DecodePlan r = plan_decode_arith(M, K, N, geff, true);
+        if (r.one_wave) return r;
+    }
+    return plan_decode_arith(M, K, N, geff, false);
 }
 
 size_t decode_ws_floats_for(int M, int K, int N, int geff) { return plan_decode(M, K, N, geff).ws_floats; }
@@ -476,9 +552,9 @@ size_t decode_ws_floats_for(int M, int K, int N, int geff) { return plan_decode(
 cudaError_t launch_decode(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                           uint16_t *out, cudaStream_t s) {
     switch (p.mt) {
-        case 1: return launch_mt<1>(h, p, w, x, M, out, s);
-        case 2: return launch_mt<2>(h, p, w, x, M, out, s);
-        default: return launch_mt<4>(h, p, w, x, M, out, s);
+        case 1: return p.raw ? launch_mt<1, true>(h, p, w, x, M, out, s) : launch_mt<1, false>(h, p, w, x, M, out, s);
+        case 2: return launch_mt<2, false>(h, p, w, x, M, out, s);
+        default: return launch_mt<4, false>(h, p, w, x, M, out, s);
     }
 }
 

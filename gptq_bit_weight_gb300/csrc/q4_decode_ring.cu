@@ -53,7 +53,10 @@ using namespace tc;
 
 constexpr int BN = 128;                              // columns per CTA (8 n16 tiles)
 constexpr int BK = 64;                               // rows per stage
-constexpr int kTPW = 2;                              // n16 tiles per consumer warp
+#ifndef Q4_RING_TPW
+#define Q4_RING_TPW 2
+#endif
+constexpr int kTPW = Q4_RING_TPW;                    // n16 tiles per consumer warp
 constexpr int kCW = (BN / 16) / kTPW;                // consumer warps
 constexpr int kThreads = 32 * (kCW + 1);
 #ifndef Q4_RING_STAGES
@@ -108,18 +111,6 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
-// Code pairs of one packed word as fp16 pairs: rows (0,1) and (4,5) as
-// 1024 + q, rows (2,3) and (6,7) as 1024 + 16 q (nibble order of the packed
-// layout: nibbles 0..7 hold rows 0,2,4,6,1,3,5,7).
-__device__ __forceinline__ void unpack_raw(uint32_t w, uint32_t (&t)[4]) {
-    const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
-    const uint32_t w8 = w >> 8;
-    t[0] = lop3_and_or(w, kLo, kMagic);
-    t[1] = lop3_and_or(w, kHi, kMagic);
-    t[2] = lop3_and_or(w8, kLo, kMagic);
-    t[3] = lop3_and_or(w8, kHi, kMagic);
-}
-
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_ring_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, RingArgs a) {

@@ -86,6 +86,20 @@ __device__ __forceinline__ void unpack_qz(uint32_t w, uint32_t nzlo, uint32_t nz
     a[3] = hfma2(t3, kSixteenth, nzhi);
 }
 
+// Code pairs of one packed word as raw fp16 pairs, no zero point: rows
+// (0,1) and (4,5) as 1024 + q, rows (2,3) and (6,7) as 1024 + 16 q (nibble
+// order of the packed layout: nibbles 0..7 hold rows 0,2,4,6,1,3,5,7).  One
+// LOP3 per pair; the decode kernels remove 1024 + z + 1 (16 (64 + z + 1) for
+// the second kind) per group from MMA-accumulated sums of x.
+__device__ __forceinline__ void unpack_raw(uint32_t w, uint32_t (&t)[4]) {
+    const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
+    const uint32_t w8 = w >> 8;
+    t[0] = lop3_and_or(w, kLo, kMagic);
+    t[1] = lop3_and_or(w, kHi, kMagic);
+    t[2] = lop3_and_or(w8, kLo, kMagic);
+    t[3] = lop3_and_or(w8, kHi, kMagic);
+}
+
 // Zero-point constants for unpack_qz from a stored zero z (0..15).
 __device__ __forceinline__ uint32_t neg_zlo(uint32_t z) { return (0xE401u + z) * 0x00010001u; }
 __device__ __forceinline__ uint32_t neg_zhi(uint32_t z) { return (0xD410u + 16u * z) * 0x00010001u; }
@@ -169,6 +183,8 @@ struct DecodePlan {
     int cluster;       // 1: the slices of a column tile form a cluster and reduce through DSMEM
     size_t ws_floats;  // workspace needed (slices reduced through global memory)
     int n_tickets;
+    int raw;           // 1: raw code pairs + sums of x (M <= 8); 0: exact (q - z - 1) pairs
+    int one_wave;      // every CTA of the grid is resident at once
 };
 DecodePlan plan_decode(int M, int K, int N, int geff);
 size_t decode_ws_floats_for(int M, int K, int N, int geff);
