@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--soak-s", type=float, default=1.0)
     p.add_argument("--only", choices=["decode", "prefill"], default=None,
                    help="run one leg only (for profiling); the JSON line is then partial")
+    p.add_argument("--sweep70b", action="store_true",
+                   help="also time all 240 sweep_70b cases (several minutes); adds a sweep_70b key")
     p.add_argument("--single", default=None, metavar="K,N,M[,PATH]",
                    help="profiling target instead of the bench: one synthetic g=128 layer, a 256 MB L2 "
                         "flush before each of four calls on PATH (a GPTQ_Q4_PATH_* suffix, default DECODE)")
@@ -408,6 +410,8 @@ def run_native(args):
     decode_70b = None
     if args.only is None:
         decode_70b = run_decode_70b(q4, torch, dev, stream, hbm_gbs)
+        actorder = run_actorder_decode(q4, torch, dev, stream, hbm_gbs, bf16_tf)
+        sweep70 = run_sweep_70b(q4, torch, dev, stream, hbm_gbs, bf16_tf) if args.sweep70b else None
 
     prefill = None
     if not args.no_prefill and args.only != "decode":
@@ -445,6 +449,9 @@ def run_native(args):
         }
         if decode_70b:
             line["decode_70b"] = decode_70b
+            line["actorder_7b"] = actorder
+            if sweep70:
+                line["sweep_70b"] = sweep70
         if prefill:
             line["prefill"] = prefill
         if cpu:
@@ -493,6 +500,83 @@ def run_decode_70b(q4, torch, dev, stream, hbm_gbs, reps=10):
     return {"workload": "sweep_70b M=1, g=128, trivial g_idx", "value": tot_bytes / tot_s / 1e12, "unit": "TB/s",
             "frac_of_hbm_peak": tot_bytes / tot_s / 1e9 / hbm_gbs, "cases": out,
             "how": "weight bytes / per-call time from CUDA-graph replays of >= 3x L2 of weight replicas"}
+
+
+def time_layer_cases(q4, torch, dev, stream, workload, K, N, g, act, Ms, hbm_gbs, tf_peak, reps=10):
+    """One layer configuration of a workload at several M through the default
+    path (GPTQ_Q4_PATH_AUTO): enough weight replicas to exceed L2 three times,
+    each M captured in one CUDA graph over the replicas and replayed.  Per
+    case: time per call, eff. TB/s on the stored weight bytes, TFLOP/s, and the
+    fraction of the roofline that binds, max(bytes/HBM, flops/tensor)/time."""
+    L = synthetic.workload_layer(workload, K, N, g, act)
+    t = lambda a: None if a is None else torch.from_numpy(a).to(dev)
+    qw, qz, sc, gi = t(L.qweight), t(L.qzeros), t(L.scales), t(L.g_idx)
+    R = max(2, int(np.ceil(3 * L2_BYTES / L.weight_bytes)))
+    mats = [q4.Q4Matrix(qw, qz, sc, gi, None, g) for _ in range(R)]
+    del qw, qz, sc, gi
+    for m in mats:
+        m.reserve(max(Ms))
+    res = {}
+    for M in Ms:
+        x = t(synthetic.workload_x(workload, K, N, g, act, M))
+        o = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), stream.cuda_stream)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for m in mats:
+                q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        for _ in range(3):
+            gr.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        sec = a.elapsed_time(b) * 1e-3 / (reps * R)
+        flops = 2.0 * M * K * N
+        t_bw, t_tc = L.weight_bytes / (hbm_gbs * 1e9), flops / (tf_peak * 1e12)
+        res[M] = {"us": round(sec * 1e6, 2), "TB/s": round(L.weight_bytes / sec / 1e12, 3),
+                  "TFLOP/s": round(flops / sec / 1e12, 1), "bound": "hbm" if t_bw >= t_tc else "tensor",
+                  "frac": round(max(t_bw, t_tc) / sec, 3)}
+        del gr
+    del mats
+    torch.cuda.empty_cache()
+    return L.weight_bytes, res
+
+
+def run_actorder_decode(q4, torch, dev, stream, hbm_gbs, tf_peak):
+    """actorder_7b: decode with a scattered act-order g_idx, M in {1, 4, 16},
+    on (4096, 11008) and (11008, 4096); the x reorder runs inside each call."""
+    cases, tot_b, tot_s = {}, 0.0, 0.0
+    for (K, N) in synthetic.ACTORDER_7B_SHAPES:
+        wb, res = time_layer_cases(q4, torch, dev, stream, "actorder_7b", K, N, 128, True, synthetic.ACTORDER_7B_M,
+                                   hbm_gbs, tf_peak)
+        for M, r in res.items():
+            cases[f"{K}x{N} M={M}"] = r
+            tot_b += wb
+            tot_s += r["us"] * 1e-6
+    return {"workload": "actorder_7b", "value": tot_b / tot_s / 1e12, "unit": "TB/s",
+            "frac_of_hbm_peak": tot_b / tot_s / 1e9 / hbm_gbs, "cases": cases,
+            "how": "weight bytes / per-call time (x reorder included) from CUDA-graph replays of >= 3x L2 of replicas"}
+
+
+def run_sweep_70b(q4, torch, dev, stream, hbm_gbs, tf_peak):
+    """sweep_70b in full: 3 shapes x 4 group sizes x {trivial, act-order} x
+    10 values of M (240 cases), through the default path."""
+    cases = {}
+    for (K, N) in synthetic.SWEEP_70B_SHAPES:
+        for g in synthetic.SWEEP_70B_G:
+            for act in (False, True):
+                _, res = time_layer_cases(q4, torch, dev, stream, "sweep_70b", K, N, g, act, synthetic.SWEEP_70B_M,
+                                          hbm_gbs, tf_peak, reps=5)
+                for M, r in res.items():
+                    cases[f"{K}x{N} g={g} act={int(act)} M={M}"] = r
+    fr = [r["frac"] for r in cases.values()]
+    return {"workload": "sweep_70b (all 240 cases)", "cases": cases, "median_frac": float(np.median(fr)),
+            "min_frac": float(np.min(fr)), "max_frac": float(np.max(fr))}
 
 
 def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):

@@ -236,8 +236,9 @@ int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 int gptq_q4_set_path(gptq_q4_handle h, int path);
 
 /* Rows at and above which GPTQ_Q4_PATH_AUTO takes the prefill kernel (the
- * decode/prefill switch of the Lorax page's set_tuning_params).  Default
- * chosen by measurement; results never depend on it. */
+ * decode/prefill switch of the Lorax page's set_tuning_params).  Default 17:
+ * decode covers up to 16 rows; measured on GB300, the fused prefill is faster
+ * than the decode kernels beyond that.  Results never depend on it. */
 int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m);
 
 /* Facts about a handle (host outputs; any pointer may be NULL). */
