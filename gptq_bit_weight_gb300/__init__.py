@@ -35,12 +35,15 @@ GPTQ_Q4_PATH_PREFILL = 2
 GPTQ_Q4_PATH_DECODE_MMA = 3
 GPTQ_Q4_PATH_DECODE_TC = 4
 GPTQ_Q4_PATH_DECODE_RING = 5
+GPTQ_Q4_FORMAT_GPTQ = 0
+GPTQ_Q4_FORMAT_GPTQ_V2 = 1
 
 EXPORTED = [
     "gptq_q4_make", "gptq_q4_set_bias", "gptq_q4_reserve", "gptq_q4_matmul", "gptq_q4_dequant",
     "gptq_q4_debug_unpack", "gptq_q4_matmul_unfused", "gptq_q4_gemm_f16", "gptq_q4_set_path",
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
+    "gptq_q4_set_format",
 ]
 
 _P = ctypes.c_void_p
@@ -64,6 +67,7 @@ _sig("gptq_q4_matmul_unfused", _I, _P, _P, _I, _P, _P, _P)
 _sig("gptq_q4_gemm_f16", _I, _P, _P, _P, _I, _I, _I, _P, _P)
 _sig("gptq_q4_set_path", _I, _P, _I)
 _sig("gptq_q4_set_prefill_min_m", _I, _P, _I)
+_sig("gptq_q4_set_format", _I, _P, _I)
 _sig("gptq_q4_info", _I, _P, _P, _P, _P, _P, _P, _P)
 _sig("gptq_q4_device_error", _I, _P)
 _sig("gptq_q4_free", None, _P)
@@ -133,6 +137,10 @@ def gptq_q4_set_path(h: int, path: int) -> int:
 
 def gptq_q4_set_prefill_min_m(h: int, min_m: int) -> int:
     return _check(_lib.gptq_q4_set_prefill_min_m(h, min_m))
+
+
+def gptq_q4_set_format(h: int, fmt: int) -> int:
+    return _check(_lib.gptq_q4_set_format(h, fmt))
 
 
 def gptq_q4_info(h: int) -> dict:
@@ -207,6 +215,9 @@ class Q4Matrix:
 
     def set_prefill_min_m(self, m: int) -> None:
         gptq_q4_set_prefill_min_m(self.handle, m)
+
+    def set_format(self, fmt: int) -> None:
+        gptq_q4_set_format(self.handle, fmt)
 
     def matmul(self, x, out=None):
         import torch

@@ -137,6 +137,7 @@ q4::HandleView view(const gptq_q4_s *h) {
     v.wp = reinterpret_cast<const uint4 *>(h->wp);
     v.s2 = h->s2;
     v.zeros = h->zeros;
+    v.zero_offset = h->zero_offset;
     v.perm = h->act_order ? h->perm : nullptr;
     v.bias = h->bias;
     v.status = h->status;
@@ -500,6 +501,15 @@ int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
     if (min_m < 0) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "min_m=%d < 0", min_m);
     h->prefill_min_m = min_m;
+    return ok();
+}
+
+int gptq_q4_set_format(gptq_q4_handle h, int format) {
+    if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
+    if (format != GPTQ_Q4_FORMAT_GPTQ && format != GPTQ_Q4_FORMAT_GPTQ_V2)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "format=%d is neither GPTQ_Q4_FORMAT_GPTQ nor GPTQ_Q4_FORMAT_GPTQ_V2",
+                          format);
+    h->zero_offset = format == GPTQ_Q4_FORMAT_GPTQ ? 1 : 0;
     return ok();
 }
 

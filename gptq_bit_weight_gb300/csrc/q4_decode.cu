@@ -228,14 +228,16 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
                 const uint32_t zw0 = base[kNTW * 8 + nt * 2], zw1 = base[kNTW * 8 + nt * 2 + 1];
                 sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                const float z0 = static_cast<float>((zw0 >> (4 * gq)) & 0xFu);
-                const float z1 = static_cast<float>((zw1 >> (4 * gq)) & 0xFu);
-                czl[nt][0] = -(1025.f + z0);
-                czl[nt][1] = -(1025.f + z1);
-                czh[nt][0] = -(65.f + z0);
-                czh[nt][1] = -(65.f + z1);
+                // effective zero points (stored + zero_offset) of columns gq, gq + 8
+                const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + h.zero_offset);
+                const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + h.zero_offset);
+                czl[nt][0] = -(1024.f + z0);
+                czl[nt][1] = -(1024.f + z1);
+                czh[nt][0] = -(64.f + z0);
+                czh[nt][1] = -(64.f + z1);
                 if (!RAW) {
-                    const uint32_t zi0 = (zw0 >> (4 * gq)) & 0xFu, zi1 = (zw1 >> (4 * gq)) & 0xFu;
+                    const uint32_t zi0 = ((zw0 >> (4 * gq)) & 0xFu) + h.zero_offset - 1u;
+                    const uint32_t zi1 = ((zw1 >> (4 * gq)) & 0xFu) + h.zero_offset - 1u;
                     nzlo[nt][0] = neg_zlo(zi0);
                     nzhi[nt][0] = neg_zhi(zi0);
                     nzlo[nt][1] = neg_zlo(zi1);

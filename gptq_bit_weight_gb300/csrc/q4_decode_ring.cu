@@ -88,6 +88,7 @@ struct RingArgs {
     const uint32_t *s2;
     const uint32_t *zeros;
     int bpg;             // 32-row blocks per group
+    int zero_offset;     // effective zero = stored + zero_offset
     int slice_kb;        // stages per slice
     int splits;
 };
@@ -239,12 +240,13 @@ __global__ void __launch_bounds__(kThreads, 3)
                 const uint32_t zw1 = ld_shared_u32(gb + 256 + nt * 8 + 4);
                 sc[t][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[t][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                const float z0 = static_cast<float>((zw0 >> (4 * gq)) & 0xFu);
-                const float z1 = static_cast<float>((zw1 >> (4 * gq)) & 0xFu);
-                czl[t][0] = -(1025.f + z0);
-                czl[t][1] = -(1025.f + z1);
-                czh[t][0] = -(65.f + z0);
-                czh[t][1] = -(65.f + z1);
+                // effective zero points (stored + zero_offset) of columns gq, gq + 8
+                const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + a.zero_offset);
+                const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + a.zero_offset);
+                czl[t][0] = -(1024.f + z0);
+                czl[t][1] = -(1024.f + z1);
+                czh[t][0] = -(64.f + z0);
+                czh[t][1] = -(64.f + z1);
             }
         };
         auto flush = [&]() {
@@ -477,7 +479,7 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &p, con
     if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
                        static_cast<uint64_t>(KC) * 512, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
-    RingArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, p.slice_kb, p.splits};
+    RingArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, h.zero_offset, p.slice_kb, p.splits};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.tiles, p.splits, 1);
     cfg.blockDim = dim3(kThreads);

@@ -79,6 +79,7 @@ struct DtArgs {
     int geff;
     int slice_kb;        // k-blocks per slice
     int splits;
+    int zero_offset;     // effective zero = stored + zero_offset
 };
 
 __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
@@ -219,7 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
                          : "=r"(z0w), "=r"(z1w)
                          : "r"(szb + gl * kSzGroupBytes + 256 + wl * 8));
-            const uint32_t z0 = (z0w >> (4 * gq)) & 0xFu, z1 = (z1w >> (4 * gq)) & 0xFu;
+            // effective zero points minus one (stored + zero_offset - 1)
+            const uint32_t z0 = ((z0w >> (4 * gq)) & 0xFu) + a.zero_offset - 1u;
+            const uint32_t z1 = ((z1w >> (4 * gq)) & 0xFu) + a.zero_offset - 1u;
             nzl[J][0] = neg_zlo(z0);
             nzh[J][0] = neg_zhi(z0);
             nzl[J][1] = neg_zlo(z1);
@@ -396,7 +399,7 @@ cudaError_t launch_decode_tc(const HandleView &h, const uint16_t *x, int M, uint
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const DecodeTcPlan p = plan_decode_tc(M, h.K, h.N, h.geff, sms);
     if (!p.ok) return cudaErrorInvalidValue;
-    DtArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff, p.slice_kb, p.splits};
+    DtArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff, p.slice_kb, p.splits, h.zero_offset};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.tiles, p.splits, p.zdim);
     cfg.blockDim = dim3(kThreads);

@@ -24,6 +24,7 @@ struct gptq_q4_s {
     size_t temp_state_elems = 0;
     int path = GPTQ_Q4_PATH_AUTO;
     int prefill_min_m = 0;
+    int zero_offset = 1;    // GPTQ_Q4_FORMAT_GPTQ: effective zero = stored + 1
     size_t device_bytes = 0;
 };
 

@@ -100,7 +100,10 @@ __device__ __forceinline__ void unpack_raw(uint32_t w, uint32_t (&t)[4]) {
     t[3] = lop3_and_or(w8, kHi, kMagic);
 }
 
-// Zero-point constants for unpack_qz from a stored zero z (0..15).
+// Zero-point constants for unpack_qz from zm1 = (effective zero) - 1, i.e.
+// the stored zero for GPTQ (v1) checkpoints and the stored zero minus one
+// for GPTQ_V2 (zm1 = 0xFFFFFFFF for a stored 0: the 32-bit sums below then
+// wrap to -1024 and -64 exactly).
 __device__ __forceinline__ uint32_t neg_zlo(uint32_t z) { return (0xE401u + z) * 0x00010001u; }
 __device__ __forceinline__ uint32_t neg_zhi(uint32_t z) { return (0xD410u + 16u * z) * 0x00010001u; }
 
@@ -155,6 +158,7 @@ struct HandleView {
     const int32_t *perm;    // P (device) or nullptr
     const uint16_t *bias;   // device fp16 [N] or nullptr
     int *status;            // device status word
+    int zero_offset;        // effective zero = stored + zero_offset (1: GPTQ, 0: GPTQ_V2)
 };
 
 struct DecodeWork {

@@ -94,6 +94,7 @@ struct PfArgs {
     const uint32_t *zeros;   // zero words [G][N/8]
     int bpg;                 // 32-row blocks per group
     int tiles_m, tiles_n;
+    int zero_offset;         // effective zero = stored + zero_offset
 };
 
 __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
@@ -286,7 +287,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + gl * P::kZGroup + wl * 8);
             c_s[J][0] = __byte_perm(sp, sp, 0x1010);
             c_s[J][1] = __byte_perm(sp, sp, 0x3232);
-            const uint32_t z0 = (zw.x >> (4 * gq)) & 0xFu, z1 = (zw.y >> (4 * gq)) & 0xFu;
+            // effective zero points minus one (stored + zero_offset - 1)
+            const uint32_t z0 = ((zw.x >> (4 * gq)) & 0xFu) + a.zero_offset - 1u;
+            const uint32_t z1 = ((zw.y >> (4 * gq)) & 0xFu) + a.zero_offset - 1u;
             c_nl[J][0] = neg_zlo(z0);
             c_nh[J][0] = neg_zhi(z0);
             c_nl[J][1] = neg_zlo(z1);
@@ -434,7 +437,8 @@ cudaError_t launch_prefill_tile(const HandleView &h, const uint16_t *x, int M, u
     static cudaError_t attr =
         cudaFuncSetAttribute(prefill_kernel<BM, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
     if (attr != cudaSuccess) return attr;
-    PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM, (h.N + BN - 1) / BN};
+    PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
+                (h.N + BN - 1) / BN, h.zero_offset};
     const int ntiles = args.tiles_m * args.tiles_n;
     const int grid = ntiles < sm_count() ? ntiles : sm_count();
     prefill_kernel<BM, BN><<<grid, P::kThreads, P::kSmem, s>>>(tmA, tmW, args);

@@ -121,7 +121,7 @@ cudaError_t launch_debug_unpack(const HandleView &h, uint8_t *q, uint8_t *z, cud
 }
 
 // -------------------------------------------------------------- dequant
-// temp_dq[k][n] = fp16(s * (q - (z + 1))), original row order.
+// temp_dq[k][n] = fp16(s * (q - (z + zero_offset))), original row order.
 // A CTA takes 64 columns x 64 (permuted) rows at a time: 256 threads each
 // dequantize two private words (16 values) into a shared tile, then the tile
 // is written out one 128-byte row per 8 threads, each row to its original
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(HandleView h, uint16_t *__
             const int gr = (64 * kc + kl) / 32 / bpg;  // group of these eight rows
             const uint32_t w = wp[wp_index(nt, kc, lane, j, KC)];
             const uint32_t zw = h.zeros[static_cast<size_t>(gr) * (N / 8) + n / 8];
-            const int zeff = static_cast<int>((zw >> (4 * (n & 7))) & 0xFu) + 1;
+            const int zeff = static_cast<int>((zw >> (4 * (n & 7))) & 0xFu) + h.zero_offset;
             const uint32_t sp = h.s2[(static_cast<size_t>(gr) * (N / 16) + nt) * 8 + gq];
             const uint16_t sbits = static_cast<uint16_t>((j & 1) ? (sp >> 16) : (sp & 0xFFFFu));
             const float s = __half2float(__ushort_as_half(sbits));

@@ -235,6 +235,17 @@ int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 /* Force a path for gptq_q4_matmul (tests, benchmarks): GPTQ_Q4_PATH_*. */
 int gptq_q4_set_path(gptq_q4_handle h, int path);
 
+/* Checkpoint zero-point convention of a handle ("Inference Backends",
+ * "Concepts": GPTQ and GPTQ_V2 are distinct checkpoint formats).  The two
+ * store qweight, qzeros and scales in the same layout and differ in the
+ * zero point: GPTQ keeps z_eff - 1 in qzeros, so w = s * (q - (z + 1));
+ * GPTQ_V2 keeps z_eff itself, so w = s * (q - z).  Default GPTQ.  Changes
+ * what later matmul/dequant calls compute; the handle's other state is
+ * untouched.  Errors: INVALID_ARGUMENT (NULL handle, unknown format). */
+#define GPTQ_Q4_FORMAT_GPTQ    0
+#define GPTQ_Q4_FORMAT_GPTQ_V2 1
+int gptq_q4_set_format(gptq_q4_handle h, int format);
+
 /* Rows at and above which GPTQ_Q4_PATH_AUTO takes the prefill kernel (the
  * decode/prefill switch of the Lorax page's set_tuning_params).  Default 17:
  * decode covers up to 16 rows; measured on GB300, the fused prefill is faster

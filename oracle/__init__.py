@@ -72,7 +72,7 @@ def _load():
         lib.oracle_unpack_qzeros.argtypes = [P, I, I, P]
         lib.oracle_row_groups.argtypes = [P, I, I, P]
         lib.oracle_row_groups.restype = I
-        lib.oracle_dequant.argtypes = [P, P, P, P, I, I, P, P]
+        lib.oracle_dequant.argtypes = [P, P, P, P, I, I, P, P, I]
         lib.oracle_linear_f64.argtypes = [P, P, P, I, I, I, P, I]
         lib.oracle_linear_f64.restype = I
         _lib = lib
@@ -133,14 +133,15 @@ def row_groups(g_idx, K: int, groupsize: int):
     return gr, G
 
 
-def dequant(q, z, scales_bits, gr, K: int, N: int, want_f64: bool = True):
-    """w16 (fp16 bits) and, if asked, the exact fp64 weights."""
+def dequant(q, z, scales_bits, gr, K: int, N: int, want_f64: bool = True, zero_offset: int = 1):
+    """w16 (fp16 bits) and, if asked, the exact fp64 weights.  zero_offset:
+    1 for GPTQ checkpoints (effective zero = stored + 1), 0 for GPTQ_V2."""
     qa, za = _c(q, np.uint8), _c(z, np.uint8)
     sb, ga = _c(scales_bits, np.uint16), _c(gr, np.int32)
     w16 = np.empty((K, N), np.uint16)
     w64 = np.empty((K, N), np.float64) if want_f64 else None
     _load().oracle_dequant(_ptr(qa), _ptr(za), _ptr(sb), _ptr(ga), K, N,
-                           _ptr(w16), _ptr(w64))
+                           _ptr(w16), _ptr(w64), int(zero_offset))
     return w16, w64
 
 
@@ -167,16 +168,18 @@ class Dequantized:
     gr: np.ndarray       # int32 [K]
     G: int
     w16: np.ndarray      # uint16 fp16 bits [K, N]
-    w64: np.ndarray      # float64 [K, N], exact s * (q - z - 1)
+    w64: np.ndarray      # float64 [K, N], exact s * (q - z - zero_offset)
 
 
-def dequantize_layer(qweight, qzeros, scales, g_idx, K: int, N: int, groupsize: int) -> Dequantized:
-    """Steps 1-3: unpack, group map, dequantize.  scales: fp16 array or its bits."""
+def dequantize_layer(qweight, qzeros, scales, g_idx, K: int, N: int, groupsize: int,
+                     zero_offset: int = 1) -> Dequantized:
+    """Steps 1-3: unpack, group map, dequantize.  scales: fp16 array or its
+    bits.  zero_offset 1: GPTQ (v1) checkpoints, 0: GPTQ_V2."""
     gr, G = row_groups(g_idx, K, groupsize)
     q = unpack_qweight(qweight, K, N)
     z = unpack_qzeros(qzeros, G, N)
     sb = np.ascontiguousarray(scales).view(np.uint16) if np.asarray(scales).dtype != np.uint16 else scales
-    w16, w64 = dequant(q, z, sb, gr, K, N)
+    w16, w64 = dequant(q, z, sb, gr, K, N, zero_offset=zero_offset)
     return Dequantized(q, z, gr, G, w16, w64)
 
 
@@ -201,9 +204,9 @@ def tolerance(x_fp16, w16_bits, y_ref: np.ndarray, K: int) -> np.ndarray:
     return 1e-2 * np.sqrt(K) * xmax * wmax / 64.0 + 2e-3 * np.abs(y_ref)
 
 
-def linear_layer(qweight, qzeros, scales, g_idx, bias, x, K, N, groupsize, nthreads=None):
+def linear_layer(qweight, qzeros, scales, g_idx, bias, x, K, N, groupsize, nthreads=None, zero_offset: int = 1):
     """The whole oracle: returns (Dequantized, y_ref, y_exact, tol)."""
-    dq = dequantize_layer(qweight, qzeros, scales, g_idx, K, N, groupsize)
+    dq = dequantize_layer(qweight, qzeros, scales, g_idx, K, N, groupsize, zero_offset)
     y_ref = reference_output(x, dq, bias, nthreads)
     y_exact = reference_output(x, dq, bias, nthreads, exact=True)
     tol = tolerance(x, dq.w16, y_ref, K)

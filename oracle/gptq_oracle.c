@@ -26,6 +26,10 @@
  *    word along N, lowest nibble first; scales [G][N] fp16; the effective
  *    zero point is the stored value plus one, so
  *        w[k][n] = scales[g][n] * (q[k][n] - (z[g][n] + 1)),  g = g_idx[k].
+ *    The same page names GPTQ_V2 as a distinct format; read here as the same
+ *    layout with the effective zero point stored as is, so
+ *        w[k][n] = scales[g][n] * (q[k][n] - z[g][n])
+ *    (oracle_dequant takes the offset, 1 or 0, as its last argument).
  *  - "Inference Backends", section "Numeric epilogues and input gradients":
  *    bias joins the wide accumulator before the single final cast.  Here
  *    everything is fp64, bias is added after the k-sum.
@@ -151,16 +155,17 @@ int oracle_row_groups(const int32_t *g_idx, int K, int groupsize, int32_t *gr)
     return G;
 }
 
-/* w64[k][n] = s * (q - (z + 1)) exactly; w16 = that value rounded once to
- * fp16, nearest-even.  w64 may be NULL. */
+/* w64[k][n] = s * (q - (z + zero_offset)) exactly (zero_offset 1: GPTQ,
+ * 0: GPTQ_V2); w16 = that value rounded once to fp16, nearest-even.  w64 may
+ * be NULL. */
 void oracle_dequant(const uint8_t *q, const uint8_t *z, const uint16_t *scales,
-                    const int32_t *gr, int K, int N, uint16_t *w16, double *w64)
+                    const int32_t *gr, int K, int N, uint16_t *w16, double *w64, int zero_offset)
 {
     for (int k = 0; k < K; ++k) {
         int g = gr[k];
         for (int n = 0; n < N; ++n) {
             double s = oracle_half_to_double(scales[(size_t)g * N + n]);
-            int iq = (int)q[(size_t)k * N + n] - ((int)z[(size_t)g * N + n] + 1);
+            int iq = (int)q[(size_t)k * N + n] - ((int)z[(size_t)g * N + n] + zero_offset);
             double v = s * (double)iq;
             if (w64) w64[(size_t)k * N + n] = v;
             w16[(size_t)k * N + n] = oracle_double_to_half(v);

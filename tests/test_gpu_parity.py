@@ -96,6 +96,50 @@ def test_decode_matches_oracle(q4, K, N, gs, act, path):
     mat.device_error()
 
 
+V2_CASES = [  # (K, N, groupsize, act_order)
+    (256, 128, 64, False),
+    (1024, 448, 32, True),
+    (1152, 320, 96, True),
+    (2048, 960, 128, False),
+]
+
+
+@pytest.mark.parametrize("K,N,gs,act", V2_CASES)
+def test_gptq_v2_format_matches_oracle(q4, K, N, gs, act):
+    """GPTQ_V2 checkpoints (effective zero = stored zero): dequant bit for bit,
+    every decode kernel and the fused prefill within tolerance, against the
+    oracle run with the same convention; stored zeros include 0, whose
+    effective zero lies below every GPTQ one."""
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(25, K, N, gs & 0xFFFF, act))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs, zero_offset=0)
+    assert np.any(dq.z == 0)
+    mat = make(q4, layer)
+    mat.set_format(q4.GPTQ_Q4_FORMAT_GPTQ_V2)
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    for path in ("DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "PREFILL"):
+        mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+        for M in (1, 3, 8, 16, 40):
+            x = synthetic.activations(M, K, key=(25, K, N, M))
+            y = mat(to_dev(x))
+            yu = mat.matmul_unfused(to_dev(x)) if path == "PREFILL" else None
+            torch.cuda.synchronize()
+            check_y(y, x, dq, layer.bias, K, f"v2 {path} K={K} N={N} g={gs} act={act} M={M}")
+            if yu is not None:
+                check_y(yu, x, dq, layer.bias, K, f"v2 unfused K={K} N={N} g={gs} act={act} M={M}")
+    mat.set_format(q4.GPTQ_Q4_FORMAT_GPTQ)
+    dq1 = oracle_dq(layer)
+    mat.set_path(q4.GPTQ_Q4_PATH_AUTO)
+    x = synthetic.activations(4, K, key=(25, K, N, 4))
+    y = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check_y(y, x, dq1, layer.bias, K, "back to GPTQ")
+    with pytest.raises(q4.GPTQ4Error):
+        mat.set_format(7)
+    mat.device_error()
+
+
 def test_trivial_gidx_same_as_none(q4):
     K, N, gs = 512, 256, 64
     layer = synthetic.make_layer(K, N, gs, key=(23,))

@@ -173,6 +173,43 @@ def test_dequant_power_of_two_scale_and_numpy_cast():
     assert np.array_equal(w16, exact.astype(np.float16).view(np.uint16))
 
 
+# ------------------------------------------------------- GPTQ_V2 zeros
+
+def test_v2_zero_convention_closed_forms():
+    """GPTQ_V2 ("Inference Backends", "Concepts": a checkpoint format distinct
+    from GPTQ), read as the same layout with the effective zero stored as is:
+    codes equal to the stored zero dequantize to exactly 0 (under GPTQ they
+    give -s), and with unit scales w is the integer q - z."""
+    g = np.random.default_rng(70)
+    K, N = 64, 24
+    z = g.integers(0, 16, (1, N)).astype(np.uint8)
+    q = np.repeat(z, K, axis=0)
+    s = g.uniform(1e-3, 2.0, (1, N)).astype(np.float16)
+    gr = np.zeros(K, np.int32)
+    w16, w64 = oracle.dequant(q, z, s.view(np.uint16), gr, K, N, zero_offset=0)
+    assert np.all(w64 == 0.0) and np.all(w16.view(np.float16) == 0)
+    w16, w64 = oracle.dequant(q, z, s.view(np.uint16), gr, K, N, zero_offset=1)
+    assert np.array_equal(w64, np.repeat(-s.astype(np.float64), K, axis=0))
+    q = g.integers(0, 16, (K, N)).astype(np.uint8)
+    one = np.ones((1, N), np.float16).view(np.uint16)
+    w16, w64 = oracle.dequant(q, z, one, gr, K, N, zero_offset=0)
+    assert np.array_equal(w64, (q.astype(np.int64) - z.astype(np.int64)).astype(np.float64))
+
+
+def test_v2_layer_equals_v1_layer_with_zeros_minus_one():
+    """Through the packed checkpoint: a GPTQ_V2 layer whose stored zeros are
+    z + 1 is the GPTQ layer with stored zeros z (z <= 14), bit for bit."""
+    g = np.random.default_rng(71)
+    K, N, gs = 256, 64, 64
+    G = K // gs
+    q = g.integers(0, 16, (K, N)).astype(np.uint8)
+    z = g.integers(0, 15, (G, N)).astype(np.uint8)
+    scales = g.uniform(0.002, 0.02, (G, N)).astype(np.float16)
+    v1 = oracle.dequantize_layer(pack_rows(q), pack_cols(z), scales, None, K, N, gs, zero_offset=1)
+    v2 = oracle.dequantize_layer(pack_rows(q), pack_cols(z + 1), scales, None, K, N, gs, zero_offset=0)
+    assert np.array_equal(v1.w16, v2.w16) and np.array_equal(v1.w64, v2.w64)
+
+
 # --------------------------------------------------------------- products
 
 def test_linear_matches_numpy_matmul():
