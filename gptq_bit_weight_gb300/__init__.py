@@ -43,7 +43,7 @@ EXPORTED = [
     "gptq_q4_debug_unpack", "gptq_q4_matmul_unfused", "gptq_q4_gemm_f16", "gptq_q4_set_path",
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
-    "gptq_q4_set_format",
+    "gptq_q4_set_format", "gptq_q4_debug_wait_probe",
 ]
 
 _P = ctypes.c_void_p
@@ -68,6 +68,7 @@ _sig("gptq_q4_gemm_f16", _I, _P, _P, _P, _I, _I, _I, _P, _P)
 _sig("gptq_q4_set_path", _I, _P, _I)
 _sig("gptq_q4_set_prefill_min_m", _I, _P, _I)
 _sig("gptq_q4_set_format", _I, _P, _I)
+_sig("gptq_q4_debug_wait_probe", _I, _P, ctypes.c_uint, _P)
 _sig("gptq_q4_info", _I, _P, _P, _P, _P, _P, _P, _P)
 _sig("gptq_q4_device_error", _I, _P)
 _sig("gptq_q4_free", None, _P)
@@ -141,6 +142,10 @@ def gptq_q4_set_prefill_min_m(h: int, min_m: int) -> int:
 
 def gptq_q4_set_format(h: int, fmt: int) -> int:
     return _check(_lib.gptq_q4_set_format(h, fmt))
+
+
+def gptq_q4_debug_wait_probe(status: int, limit_us: int, stream: int) -> int:
+    return _check(_lib.gptq_q4_debug_wait_probe(status, limit_us, stream or None))
 
 
 def gptq_q4_info(h: int) -> dict:

@@ -504,6 +504,15 @@ int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m) {
     return ok();
 }
 
+int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream) {
+    if (!status) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "status must not be NULL");
+    if (limit_us == 0 || limit_us > 2000000u)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "limit_us=%u outside [1, 2000000]", limit_us);
+    Q4_CUDA(q4::launch_wait_probe(status, static_cast<uint64_t>(limit_us) * 1000ull, stream), "wait probe launch");
+    ++g_launches;
+    return ok();
+}
+
 int gptq_q4_set_format(gptq_q4_handle h, int format) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
     if (format != GPTQ_Q4_FORMAT_GPTQ && format != GPTQ_Q4_FORMAT_GPTQ_V2)

@@ -221,5 +221,7 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &plan, 
 int device_sm_count();
 // programmatic dependent launch switch (GPTQ_Q4_PDL=0 turns it off)
 bool pdl_enabled();
+// test hook: a bounded mbarrier wait that runs out (q4_debug.cu)
+cudaError_t launch_wait_probe(int *status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace q4

@@ -42,13 +42,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of the given parity to complete, for at most ~2 s.
 // Inlined on purpose: an out-of-line call and return measured ~225 cycles on
 // sm_103a, several times a pipeline stage's hand-off budget.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > 2000000000ull) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {

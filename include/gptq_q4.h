@@ -235,6 +235,17 @@ int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 /* Force a path for gptq_q4_matmul (tests, benchmarks): GPTQ_Q4_PATH_*. */
 int gptq_q4_set_path(gptq_q4_handle h, int path);
 
+/* Test hook for failure detection (the pages have no counterpart).  The TMA
+ * and tcgen05 kernels bound every mbarrier wait: a wait that runs out sets
+ * a bit in the handle's status word (reported by gptq_q4_device_error) and
+ * the kernel returns instead of hanging.  This launches one CTA whose thread
+ * runs that same wait, limited to limit_us microseconds (1 .. 2,000,000), on
+ * an mbarrier that nothing arrives at; when the limit runs out it ORs 1 into
+ * *status (a device int the caller owns and zeroes).  Asynchronous on
+ * `stream`.  Errors: INVALID_ARGUMENT (NULL status, limit out of range),
+ * CUDA_ERROR (launch). */
+int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream);
+
 /* Checkpoint zero-point convention of a handle ("Inference Backends",
  * "Concepts": GPTQ and GPTQ_V2 are distinct checkpoint formats).  The two
  * store qweight, qzeros and scales in the same layout and differ in the

@@ -56,6 +56,7 @@ def test_null_handle_is_invalid_argument(lib_path):
     assert "NULL" in q4.gptq_q4_last_error()
     assert lib.gptq_q4_set_prefill_min_m(None, 4) == q4.GPTQ_Q4_INVALID_ARGUMENT
     assert lib.gptq_q4_set_format(None, q4.GPTQ_Q4_FORMAT_GPTQ_V2) == q4.GPTQ_Q4_INVALID_ARGUMENT
+    assert lib.gptq_q4_debug_wait_probe(None, 1000, None) == q4.GPTQ_Q4_INVALID_ARGUMENT
     assert lib.gptq_q4_info(None, None, None, None, None, None, None) == q4.GPTQ_Q4_INVALID_ARGUMENT
     assert q4.gptq_q4_last_status() == q4.GPTQ_Q4_INVALID_ARGUMENT
     q4.gptq_q4_free(None)
