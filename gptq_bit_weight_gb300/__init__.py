@@ -43,7 +43,7 @@ EXPORTED = [
     "gptq_q4_debug_unpack", "gptq_q4_matmul_unfused", "gptq_q4_gemm_f16", "gptq_q4_set_path",
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
-    "gptq_q4_set_format", "gptq_q4_debug_wait_probe",
+    "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_make_fused",
 ]
 
 _P = ctypes.c_void_p
@@ -68,6 +68,7 @@ _sig("gptq_q4_gemm_f16", _I, _P, _P, _P, _I, _I, _I, _P, _P)
 _sig("gptq_q4_set_path", _I, _P, _I)
 _sig("gptq_q4_set_prefill_min_m", _I, _P, _I)
 _sig("gptq_q4_set_format", _I, _P, _I)
+_sig("gptq_q4_make_fused", _P, _I, _P, _P, _P, _P, _I, _P, _I)
 _sig("gptq_q4_debug_wait_probe", _I, _P, ctypes.c_uint, _P)
 _sig("gptq_q4_info", _I, _P, _P, _P, _P, _P, _P, _P)
 _sig("gptq_q4_device_error", _I, _P)
@@ -99,6 +100,17 @@ def _check(rc: int) -> int:
 
 def gptq_q4_make(qweight: int, qzeros: int, scales: int, g_idx: int | None, K: int, N: int, groupsize: int) -> int:
     h = _lib.gptq_q4_make(qweight, qzeros, scales, g_idx or None, K, N, groupsize)
+    if not h:
+        raise GPTQ4Error(gptq_q4_last_status(), gptq_q4_last_error())
+    return h
+
+
+def gptq_q4_make_fused(qweights, qzeros, scales, g_idx: int | None, K: int, Ns, groupsize: int) -> int:
+    """Sequences of device pointers (one per part) and the parts' widths."""
+    n = len(Ns)
+    arr = lambda seq: (ctypes.c_void_p * n)(*seq)
+    widths = (ctypes.c_int * n)(*Ns)
+    h = _lib.gptq_q4_make_fused(n, arr(qweights), arr(qzeros), arr(scales), g_idx or None, K, widths, groupsize)
     if not h:
         raise GPTQ4Error(gptq_q4_last_status(), gptq_q4_last_error())
     return h
@@ -208,6 +220,30 @@ class Q4Matrix:
         if bias is not None:
             b = bias.to(torch.float16).contiguous()
             gptq_q4_set_bias(self.handle, b.data_ptr())
+
+    @classmethod
+    def fused(cls, parts, g_idx=None, biases=None, groupsize: int = 128):
+        """One handle over projections that read the same input (e.g. Q, K, V),
+        concatenated along N; parts = [(qweight, qzeros, scales), ...] torch
+        CUDA tensors.  matmul returns [.., sum N_i]; part i is the column range
+        [sum_{j<i} N_j, + N_i)."""
+        import torch
+        self = cls.__new__(cls)
+        parts = [(q.contiguous(), z.contiguous(), s.contiguous()) for q, z, s in parts]
+        K = parts[0][0].shape[0] * 8
+        Ns = [q.shape[1] for q, _, _ in parts]
+        g_idx = None if g_idx is None else g_idx.to(torch.int32).contiguous()
+        torch.cuda.current_stream().synchronize()
+        self.K, self.N, self.groupsize = K, sum(Ns), groupsize
+        self.device = parts[0][0].device
+        self.parts = Ns
+        self.handle = gptq_q4_make_fused([q.data_ptr() for q, _, _ in parts], [z.data_ptr() for _, z, _ in parts],
+                                         [s.data_ptr() for _, _, s in parts],
+                                         None if g_idx is None else g_idx.data_ptr(), K, Ns, groupsize)
+        if biases is not None:
+            b = torch.cat([bb.to(torch.float16) for bb in biases]).contiguous()
+            gptq_q4_set_bias(self.handle, b.data_ptr())
+        return self
 
     def info(self) -> dict:
         return gptq_q4_info(self.handle)

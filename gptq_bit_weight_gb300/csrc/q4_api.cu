@@ -345,6 +345,78 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
     return h;
 }
 
+gptq_q4_handle gptq_q4_make_fused(int parts, const int32_t *const *qweight, const int32_t *const *qzeros,
+                                  const uint16_t *const *scales, const int32_t *g_idx, int K, const int *N,
+                                  int groupsize) {
+    if (parts < 1 || parts > GPTQ_Q4_MAX_FUSED_PARTS || !qweight || !qzeros || !scales || !N) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "parts=%d must be in [1, %d] with non-NULL arrays", parts,
+                   GPTQ_Q4_MAX_FUSED_PARTS);
+        return nullptr;
+    }
+    if (K <= 0 || K % 8 || !(groupsize == -1 || (groupsize > 0 && K % groupsize == 0))) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "K=%d must be a positive multiple of 8 and groupsize=%d -1 or a divisor",
+                   K, groupsize);
+        return nullptr;
+    }
+    long long ntot = 0;
+    for (int i = 0; i < parts; ++i) {
+        if (!qweight[i] || !qzeros[i] || !scales[i] || N[i] <= 0 || N[i] % 8) {
+            set_status(GPTQ_Q4_INVALID_ARGUMENT, "part %d: NULL tensor or N=%d not a positive multiple of 8", i,
+                       N[i]);
+            return nullptr;
+        }
+        ntot += N[i];
+    }
+    if (ntot > INT_MAX / 8) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "total N=%lld too large", ntot);
+        return nullptr;
+    }
+    const int Nt = static_cast<int>(ntot);
+    const int G = groupsize == -1 ? 1 : K / groupsize;
+    int dev = -1;
+    if (check_device_sm103(&dev) != GPTQ_Q4_OK) return nullptr;
+    for (int i = 0; i < parts; ++i)
+        if (check_device_ptr(qweight[i], dev, "qweight part") || check_device_ptr(qzeros[i], dev, "qzeros part") ||
+            check_device_ptr(scales[i], dev, "scales part"))
+            return nullptr;
+    // Concatenate the parts along N into temporaries in the checkpoint layout,
+    // then make one handle from them (make copies what it keeps).
+    int32_t *qw = nullptr, *qz = nullptr;
+    uint16_t *sc = nullptr;
+    gptq_q4_handle h = nullptr;
+    if (dev_alloc(&qw, static_cast<size_t>(K / 8) * Nt, nullptr, "fused qweight") == GPTQ_Q4_OK &&
+        dev_alloc(&qz, static_cast<size_t>(G) * (Nt / 8), nullptr, "fused qzeros") == GPTQ_Q4_OK &&
+        dev_alloc(&sc, static_cast<size_t>(G) * Nt, nullptr, "fused scales") == GPTQ_Q4_OK) {
+        bool copied = true;
+        size_t off = 0;
+        for (int i = 0; i < parts && copied; ++i) {
+            const size_t n = static_cast<size_t>(N[i]);
+            cudaError_t e = cudaMemcpy2D(qw + off, Nt * 4, qweight[i], n * 4, n * 4, K / 8, cudaMemcpyDeviceToDevice);
+            if (e == cudaSuccess)
+                e = cudaMemcpy2D(qz + off / 8, (Nt / 8) * 4, qzeros[i], (n / 8) * 4, (n / 8) * 4, G,
+                                 cudaMemcpyDeviceToDevice);
+            if (e == cudaSuccess)
+                e = cudaMemcpy2D(sc + off, Nt * 2, scales[i], n * 2, n * 2, G, cudaMemcpyDeviceToDevice);
+            if (e != cudaSuccess) {
+                cuda_fail(e, "concatenating the fused parts");
+                copied = false;
+            }
+            off += n;
+        }
+        if (copied) h = gptq_q4_make(qw, qz, sc, g_idx, K, Nt, groupsize);
+    }
+    const int status = t_status;
+    char msg[sizeof(t_msg)];
+    memcpy(msg, t_msg, sizeof(t_msg));
+    cudaDeviceSynchronize();
+    cudaFree(qw);
+    cudaFree(qz);
+    cudaFree(sc);
+    t_status = status;                                 // keep make's status and message
+    memcpy(t_msg, msg, sizeof(t_msg));
+    return h;
+}
+
 int gptq_q4_set_bias(gptq_q4_handle h, const uint16_t *bias) {
     if (int r = check_handle(h)) return r;
     if (!bias) {

@@ -246,6 +246,23 @@ int gptq_q4_set_path(gptq_q4_handle h, int path);
  * CUDA_ERROR (launch). */
 int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream);
 
+/* Projection fusion ("Inference Backends", "How AUTO selection works":
+ * post-quantization QKV or gate/up projections that read the same input are
+ * combined into one call).  One handle over `parts` GPTQ layers that share
+ * K, groupsize and g_idx, concatenated along N in the given order:
+ *   qweight[i] dev [K/8][N[i]], qzeros[i] dev [G][N[i]/8], scales[i] dev
+ *   [G][N[i]] fp16, N[i] a positive multiple of 8, sum of N[i] a multiple of
+ *   64 (the handle's N); g_idx as for gptq_q4_make, shared by all parts.
+ * gptq_q4_matmul on the handle writes out [M][sum N[i]]: part i occupies
+ * columns [sum_{j<i} N[j], + N[i]) of each row (views of one buffer, no copy);
+ * a bias set with gptq_q4_set_bias is the parts' biases concatenated the same
+ * way.  The parts' tensors are copied; the caller may free them on return.
+ * Returns NULL on error (status and message as for gptq_q4_make). */
+#define GPTQ_Q4_MAX_FUSED_PARTS 16
+gptq_q4_handle gptq_q4_make_fused(int parts, const int32_t *const *qweight, const int32_t *const *qzeros,
+                                  const uint16_t *const *scales, const int32_t *g_idx, int K, const int *N,
+                                  int groupsize);
+
 /* Checkpoint zero-point convention of a handle ("Inference Backends",
  * "Concepts": GPTQ and GPTQ_V2 are distinct checkpoint formats).  The two
  * store qweight, qzeros and scales in the same layout and differ in the

@@ -271,3 +271,39 @@ def test_error_codes(q4):
         assert q4.gptq_q4_matmul(h, 0, 0, 0, 0) == 0
     finally:
         q4.gptq_q4_free(h)
+
+
+@pytest.mark.parametrize("act", [False, True])
+def test_fused_projections_match_oracle(q4, act):
+    """Three projections of one input (widths 256, 128, 320) in one handle:
+    dequant bit for bit and every path within tolerance against the oracle of
+    the N-concatenated checkpoint; each part's columns against that part's own
+    oracle."""
+    K, gs, Ns = 1024, 128, [256, 128, 320]
+    base = synthetic.make_layer(K, sum(Ns), gs, act_order=act, bias=True, key=(26, K, act))
+    parts, off = [], 0
+    for n in Ns:
+        parts.append((base.qweight[:, off:off + n], base.qzeros[:, off // 8:(off + n) // 8],
+                      base.scales[:, off:off + n], base.bias[off:off + n]))
+        off += n
+    mat = q4.Q4Matrix.fused([(to_dev(q), to_dev(z), to_dev(s)) for q, z, s, _ in parts], to_dev(base.g_idx),
+                            [to_dev(b) for _, _, _, b in parts], gs)
+    assert mat.info()["N"] == sum(Ns)
+    dq = oracle_dq(base)
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    for path in ("AUTO", "DECODE", "DECODE_RING", "PREFILL"):
+        mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+        for M in (1, 8, 33):
+            x = synthetic.activations(M, K, key=(26, K, M))
+            y = mat(to_dev(x))
+            torch.cuda.synchronize()
+            check_y(y, x, dq, base.bias, K, f"fused {path} act={act} M={M}")
+            off = 0
+            for (q, z, s, b), n in zip(parts, Ns):
+                dqi = oracle.dequantize_layer(q, z, s, base.g_idx, K, n, gs)
+                check_y(y[:, off:off + n], x, dqi, b, K, f"fused part {off} {path} M={M}")
+                off += n
+    mat.device_error()
+    mat.close()
