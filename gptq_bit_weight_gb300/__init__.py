@@ -43,7 +43,7 @@ EXPORTED = [
     "gptq_q4_debug_unpack", "gptq_q4_matmul_unfused", "gptq_q4_gemm_f16", "gptq_q4_set_path",
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
-    "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_make_fused",
+    "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_make_fused", "gptq_q4_pack",
 ]
 
 _P = ctypes.c_void_p
@@ -69,6 +69,7 @@ _sig("gptq_q4_set_path", _I, _P, _I)
 _sig("gptq_q4_set_prefill_min_m", _I, _P, _I)
 _sig("gptq_q4_set_format", _I, _P, _I)
 _sig("gptq_q4_make_fused", _P, _I, _P, _P, _P, _P, _I, _P, _I)
+_sig("gptq_q4_pack", _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P)
 _sig("gptq_q4_debug_wait_probe", _I, _P, ctypes.c_uint, _P)
 _sig("gptq_q4_info", _I, _P, _P, _P, _P, _P, _P, _P)
 _sig("gptq_q4_device_error", _I, _P)
@@ -114,6 +115,31 @@ def gptq_q4_make_fused(qweights, qzeros, scales, g_idx: int | None, K: int, Ns, 
     if not h:
         raise GPTQ4Error(gptq_q4_last_status(), gptq_q4_last_error())
     return h
+
+
+def gptq_q4_pack(w: int, scales: int, zeros: int | None, g_idx: int | None, K: int, N: int, groupsize: int,
+                 fmt: int, qweight: int, qzeros: int, stream: int) -> int:
+    return _check(_lib.gptq_q4_pack(w, scales, zeros or None, g_idx or None, K, N, groupsize, fmt, qweight, qzeros,
+                                    stream or None))
+
+
+def pack(w, scales, zeros=None, g_idx=None, groupsize: int = 128, fmt: int = 0):
+    """Torch CUDA tensors in: w [K, N] fp16, scales [G, N] fp16, zeros [G, N]
+    int (effective zero points) or None, g_idx [K] or None.  Returns
+    (qweight [K/8, N], qzeros [G, N/8]) int32 checkpoint tensors."""
+    import torch
+    K, N = w.shape
+    G = 1 if groupsize == -1 else K // groupsize
+    w = w.to(torch.float16).contiguous()
+    scales = scales.to(torch.float16).contiguous()
+    zeros = None if zeros is None else zeros.to(torch.int32).contiguous()
+    g_idx = None if g_idx is None else g_idx.to(torch.int32).contiguous()
+    qweight = torch.empty((K // 8, N), dtype=torch.int32, device=w.device)
+    qzeros = torch.empty((G, N // 8), dtype=torch.int32, device=w.device)
+    gptq_q4_pack(w.data_ptr(), scales.data_ptr(), None if zeros is None else zeros.data_ptr(),
+                 None if g_idx is None else g_idx.data_ptr(), K, N, groupsize, fmt, qweight.data_ptr(),
+                 qzeros.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    return qweight, qzeros
 
 
 def gptq_q4_set_bias(h: int, bias: int | None) -> int:

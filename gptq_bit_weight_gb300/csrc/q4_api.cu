@@ -576,6 +576,43 @@ int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m) {
     return ok();
 }
 
+int gptq_q4_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros, const int32_t *g_idx, int K,
+                 int N, int groupsize, int format, int32_t *qweight, int32_t *qzeros, cudaStream_t stream) {
+    if (!w || !scales || !qweight || !qzeros)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "w, scales, qweight and qzeros must not be NULL");
+    if (K <= 0 || N <= 0 || K % 8 || N % 8)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "K=%d and N=%d must be positive multiples of 8", K, N);
+    if (!(groupsize == -1 || (groupsize > 0 && K % groupsize == 0)))
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "groupsize=%d must be -1 or a positive divisor of K=%d",
+                          groupsize, K);
+    if (format != GPTQ_Q4_FORMAT_GPTQ && format != GPTQ_Q4_FORMAT_GPTQ_V2)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "format=%d is neither GPTQ nor GPTQ_V2", format);
+    const int geff = groupsize == -1 ? K : groupsize;
+    const int G = K / geff;
+    int dev = -1;
+    Q4_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    if (int r = check_device_ptr(w, dev, "w")) return r;
+    if (int r = check_device_ptr(scales, dev, "scales")) return r;
+    if (zeros)
+        if (int r = check_device_ptr(zeros, dev, "zeros")) return r;
+    if (g_idx)
+        if (int r = check_device_ptr(g_idx, dev, "g_idx")) return r;
+    if (int r = check_device_ptr(qweight, dev, "qweight")) return r;
+    if (int r = check_device_ptr(qzeros, dev, "qzeros")) return r;
+    if (g_idx) {   // every row's group must exist: checked on the host before any kernel reads it
+        std::vector<int32_t> gi(K);
+        Q4_CUDA(cudaMemcpy(gi.data(), g_idx, sizeof(int32_t) * K, cudaMemcpyDeviceToHost), "copying g_idx");
+        for (int k = 0; k < K; ++k)
+            if (gi[k] < 0 || gi[k] >= G)
+                return set_status(GPTQ_Q4_INVALID_ARGUMENT, "g_idx[%d]=%d outside [0, %d)", k, gi[k], G);
+    }
+    Q4_CUDA(q4::launch_pack(w, scales, zeros, g_idx, K, N, geff, G, format == GPTQ_Q4_FORMAT_GPTQ ? 1 : 0, qweight,
+                            qzeros, stream),
+            "pack launch");
+    g_launches += 2;
+    return ok();
+}
+
 int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream) {
     if (!status) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "status must not be NULL");
     if (limit_us == 0 || limit_us > 2000000u)

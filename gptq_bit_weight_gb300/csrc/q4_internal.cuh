@@ -221,6 +221,10 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &plan, 
 int device_sm_count();
 // programmatic dependent launch switch (GPTQ_Q4_PDL=0 turns it off)
 bool pdl_enabled();
+// float weights + scales + zero points -> GPTQ checkpoint words (q4_pack.cu)
+cudaError_t launch_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros, const int32_t *g_idx,
+                        int K, int N, int geff, int G, int zero_offset, int32_t *qweight, int32_t *qzeros,
+                        cudaStream_t s);
 // test hook: a bounded mbarrier wait that runs out (q4_debug.cu)
 cudaError_t launch_wait_probe(int *status, uint64_t limit_ns, cudaStream_t s);
 

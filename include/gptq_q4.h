@@ -235,6 +235,25 @@ int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 /* Force a path for gptq_q4_matmul (tests, benchmarks): GPTQ_Q4_PATH_*. */
 int gptq_q4_set_path(gptq_q4_handle h, int path);
 
+/* GPU packer ("Inference Backends", "Packing, conversion, and runtime
+ * initialization": packing takes the original layer's weights with the
+ * quantizer's scales, zeros and optional act-order index; a GPU path does the
+ * packing math; symmetric modules without zeros use 2^(bits-1)).
+ *   w       dev [K][N] fp16, the float weights (row k = input feature k)
+ *   scales  dev [G][N] fp16
+ *   zeros   dev [G][N] int32 effective zero points (0..15), or NULL: all 8
+ *   g_idx   dev [K] int32 group of each row, or NULL: k / groupsize
+ *   format  GPTQ_Q4_FORMAT_GPTQ (stores z - 1) or GPTQ_Q4_FORMAT_GPTQ_V2 (z)
+ *   qweight dev [K/8][N] int32 out, qzeros dev [G][N/8] int32 out
+ * Code q = clamp(rint(w / s) + z, 0, 15) with w / s the IEEE binary32
+ * quotient, ties to even (0/0 gives z); qweight and qzeros in the
+ * checkpoint layout gptq_q4_make reads; stored zeros are taken mod 16.
+ * Asynchronous on `stream` once its arguments are checked (g_idx is copied to
+ * the host for the range check).  Errors: INVALID_ARGUMENT (NULL, sizes,
+ * groupsize, format, g_idx out of [0, G), non-device pointers), CUDA_ERROR. */
+int gptq_q4_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros, const int32_t *g_idx, int K,
+                 int N, int groupsize, int format, int32_t *qweight, int32_t *qzeros, cudaStream_t stream);
+
 /* Test hook for failure detection (the pages have no counterpart).  The TMA
  * and tcgen05 kernels bound every mbarrier wait: a wait that runs out sets
  * a bit in the handle's status word (reported by gptq_q4_device_error) and

@@ -74,6 +74,8 @@ def _load():
         lib.oracle_row_groups.restype = I
         lib.oracle_dequant.argtypes = [P, P, P, P, I, I, P, P, I]
         lib.oracle_linear_f64.argtypes = [P, P, P, I, I, I, P, I]
+        lib.oracle_pack.argtypes = [P, P, P, P, I, I, I, I, P, P]
+        lib.oracle_pack.restype = I
         lib.oracle_linear_f64.restype = I
         _lib = lib
         return lib
@@ -157,6 +159,24 @@ def linear_f64(x64: np.ndarray, w64: np.ndarray, bias64=None, nthreads: int | No
     nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
     _load().oracle_linear_f64(_ptr(x), _ptr(w), _ptr(b), M, K, N, _ptr(y), nt)
     return y
+
+
+def pack(w16, scales_bits, zeros, g_idx, K: int, N: int, groupsize: int, zero_offset: int = 1):
+    """Float weights w16 [K, N] (fp16 bits) with the quantizer's scales [G, N]
+    (fp16 bits) and effective zero points [G, N] (int; None: symmetric, 8)
+    -> (qweight [K/8, N], qzeros [G, N/8]) int32, GPTQ (zero_offset 1) or
+    GPTQ_V2 (0) storage."""
+    wa, sb = _c(w16, np.uint16), _c(scales_bits, np.uint16)
+    za = None if zeros is None else _c(zeros, np.int32)
+    gi = None if g_idx is None else _c(g_idx, np.int32)
+    G = 1 if groupsize == -1 else K // groupsize
+    qw = np.zeros((K // 8, N), np.int32)
+    qz = np.zeros((G, N // 8), np.int32)
+    r = _load().oracle_pack(_ptr(wa), _ptr(sb), _ptr(za), _ptr(gi), K, N, groupsize, int(zero_offset),
+                            _ptr(qw), _ptr(qz))
+    if r < 0:
+        raise ValueError("invalid groupsize or g_idx")
+    return qw, qz
 
 
 # ------------------------------------------------------------ composed

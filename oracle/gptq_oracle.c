@@ -173,6 +173,58 @@ void oracle_dequant(const uint8_t *q, const uint8_t *z, const uint16_t *scales,
     }
 }
 
+/* ------------------------------------------------------------- packing */
+
+/* Pack float weights into a GPTQ checkpoint ("Inference Backends",
+ * "Packing, conversion, and runtime initialization": packing takes the
+ * original linear layer's weights with the quantizer's scales, zeros and
+ * optional activation-order index; symmetric modules without zeros use
+ * 2^(bits-1)).  Reading: the code of w is the nearest integer to w / s
+ * (quotient of the fp16 values in IEEE binary32, ties to even) plus the
+ * effective zero point, clamped to [0, 15]:
+ *     q[k][n] = clamp(rint((float)w[k][n] / (float)s[g][n]) + z[g][n], 0, 15)
+ * with g = g_idx[k] (or k / groupsize).  qweight [K/8][N] holds q along K,
+ * lowest nibble first; qzeros [G][N/8] holds the stored zero along N,
+ * lowest nibble first: z - 1 for GPTQ (zero_offset 1; taken mod 16, so an
+ * effective zero of 0 is stored as 15), z for GPTQ_V2 (zero_offset 0).
+ * zeros may be NULL: every effective zero is then 8.
+ * Returns G, or -1 for an invalid groupsize / g_idx. */
+int oracle_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros, const int32_t *g_idx,
+                int K, int N, int groupsize, int zero_offset, int32_t *qweight, int32_t *qzeros)
+{
+    int32_t *gr = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
+    if (!gr) return -1;
+    int G = oracle_row_groups(g_idx, K, groupsize, gr);
+    if (G < 0) { free(gr); return -1; }
+    memset(qweight, 0, sizeof(int32_t) * (size_t)(K / 8) * N);
+    for (int k = 0; k < K; ++k) {
+        int g = gr[k];
+        for (int n = 0; n < N; ++n) {
+            float wf = (float)oracle_half_to_double(w[(size_t)k * N + n]);
+            float sf = (float)oracle_half_to_double(scales[(size_t)g * N + n]);
+            float qf = rintf(wf / sf);
+            int z = zeros ? zeros[(size_t)g * N + n] : 8;
+            /* clamp in float (an infinite quotient clamps too); 0/0 gives the zero point */
+            float v = (qf != qf) ? (float)z : qf + (float)z;
+            if (v < 0.0f) v = 0.0f;
+            if (v > 15.0f) v = 15.0f;
+            long q = (long)v;
+            uint32_t *word = (uint32_t *)&qweight[(size_t)(k / 8) * N + n];
+            *word |= (uint32_t)q << (4 * (k % 8));
+        }
+    }
+    memset(qzeros, 0, sizeof(int32_t) * (size_t)G * (N / 8));
+    for (int g = 0; g < G; ++g)
+        for (int n = 0; n < N; ++n) {
+            int z = zeros ? zeros[(size_t)g * N + n] : 8;
+            uint32_t stored = (uint32_t)(z - zero_offset) & 0xFu;
+            uint32_t *word = (uint32_t *)&qzeros[(size_t)g * (N / 8) + n / 8];
+            *word |= stored << (4 * (n % 8));
+        }
+    free(gr);
+    return G;
+}
+
 /* ------------------------------------------------------------- linear */
 
 struct linear_job {

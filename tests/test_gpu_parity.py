@@ -307,3 +307,45 @@ def test_fused_projections_match_oracle(q4, act):
                 off += n
     mat.device_error()
     mat.close()
+
+
+@pytest.mark.parametrize("K,N,gs,act,fmt,sym", [
+    (256, 128, 64, False, 0, False),
+    (1024, 448, 32, True, 0, False),
+    (1152, 320, 96, True, 1, False),
+    (512, 256, -1, False, 0, True),
+])
+def test_gpu_pack_matches_oracle(q4, K, N, gs, act, fmt, sym):
+    """GPU packer against the oracle's packer, bit for bit, on random weights
+    plus forced ties (quotients k + 1/2), far out-of-range weights and zero
+    points at both ends; then the packed checkpoint through make + matmul."""
+    g = np.random.default_rng((27, K, N, act, fmt))
+    G = 1 if gs == -1 else K // gs
+    geff = K if gs == -1 else gs
+    g_idx = (g.permutation(K) // geff).astype(np.int32) if act else None
+    scales = g.uniform(0.002, 0.02, (G, N)).astype(np.float16)
+    scales[0, :8] = np.float16(0.125)                    # exact quotients for the forced cases
+    zeros = None if sym else g.integers(0, 16, (G, N)).astype(np.int32)
+    if zeros is not None:
+        zeros[0, 0], zeros[0, 1] = 0, 15
+    w = g.normal(0, 0.05, (K, N)).astype(np.float16)
+    rows0 = np.nonzero((g_idx if act else np.arange(K) // geff) == 0)[0][:8]
+    for j, r in enumerate(rows0):
+        w[r, :8] = np.float16((j - 3.5) * 0.125)         # quotients -3.5 .. 3.5: ties to even
+    w[rows0[0], 8:16] = np.float16(60.0)                  # clamps to 15
+    w[rows0[1], 8:16] = np.float16(-60.0)                 # clamps to 0
+    qw_ref, qz_ref = oracle.pack(w.view(np.uint16), scales.view(np.uint16), zeros, g_idx, K, N, gs, 1 - fmt)
+    qw, qz = q4.pack(to_dev(w), to_dev(scales), None if zeros is None else to_dev(zeros),
+                     None if g_idx is None else to_dev(g_idx), gs, fmt)
+    torch.cuda.synchronize()
+    assert np.array_equal(qw.cpu().numpy(), qw_ref)
+    assert np.array_equal(qz.cpu().numpy(), qz_ref)
+    mat = q4.Q4Matrix(qw, qz, to_dev(scales), None if g_idx is None else to_dev(g_idx), None, gs)
+    mat.set_format(fmt)
+    dq = oracle.dequantize_layer(qw_ref, qz_ref, scales, g_idx, K, N, gs, zero_offset=1 - fmt)
+    for M in (1, 20):
+        x = synthetic.activations(M, K, key=(27, K, N, M))
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, None, K, f"packed K={K} N={N} g={gs} act={act} fmt={fmt} M={M}")
+    mat.device_error()

@@ -210,6 +210,60 @@ def test_v2_layer_equals_v1_layer_with_zeros_minus_one():
     assert np.array_equal(v1.w16, v2.w16) and np.array_equal(v1.w64, v2.w64)
 
 
+# ------------------------------------------------------------- packing
+
+def test_pack_round_trips_exact_weights():
+    """Weights that are exactly s * (q - z) (power-of-two scales) pack back to
+    q, with the GPTQ zero stored as z - 1 and the GPTQ_V2 zero as z; the
+    layout matches an independent packer; dequantizing gives the weights."""
+    g = np.random.default_rng(80)
+    K, N, gs = 128, 64, 32
+    G = K // gs
+    q = g.integers(0, 16, (K, N)).astype(np.int64)
+    z = g.integers(1, 16, (G, N)).astype(np.int64)
+    s = (2.0 ** g.integers(-12, -2, (G, N))).astype(np.float16)
+    gr = np.arange(K) // gs
+    w = (s.astype(np.float64)[gr] * (q - z[gr])).astype(np.float16)
+    assert np.array_equal(w.astype(np.float64), s.astype(np.float64)[gr] * (q - z[gr]))
+    for off in (1, 0):
+        qw, qz = oracle.pack(w.view(np.uint16), s.view(np.uint16), z.astype(np.int32), None, K, N, gs, off)
+        assert np.array_equal(qw, pack_rows(q.astype(np.uint8)))
+        assert np.array_equal(qz, pack_cols((z - off).astype(np.uint8)))
+        dq = oracle.dequantize_layer(qw, qz, s, None, K, N, gs, zero_offset=off)
+        assert np.array_equal(dq.w16, w.view(np.uint16))
+
+
+def test_pack_rounding_clamping_and_symmetric_zero():
+    """Hand-worked codes, unit scale: ties go to even (2.5 -> 2, 3.5 -> 4,
+    -0.5 -> 0), out-of-range quotients clamp to 0 and 15, no zeros means
+    the symmetric zero 8 (stored 7 for GPTQ)."""
+    K, N = 8, 8
+    vals = np.array([2.5, 3.5, -0.5, 0.49, -100.0, 100.0, 6.5, -7.5], np.float16)
+    w = np.tile(vals[:, None], (1, N))
+    one = np.ones((1, N), np.float16)
+    qw, qz = oracle.pack(w.view(np.uint16), one.view(np.uint16), None, None, K, N, -1, 1)
+    codes = [(int(qw[0, 0]) >> (4 * r)) & 0xF for r in range(8)]
+    assert codes == [8 + 2, 8 + 4, 8 + 0, 8 + 0, 0, 15, 8 + 6, 8 - 8]
+    assert all(((int(qz[0, 0]) & 0xFFFFFFFF) >> (4 * r)) & 0xF == 7 for r in range(8))
+
+
+def test_pack_follows_act_order_groups():
+    """With an act-order g_idx each row takes the scale and zero of its own
+    group: packing through g_idx equals packing each row against its group."""
+    g = np.random.default_rng(81)
+    K, N, gs = 64, 16, 16
+    G = K // gs
+    g_idx = (g.permutation(K) // gs).astype(np.int32)
+    s = g.uniform(0.01, 0.1, (G, N)).astype(np.float16)
+    z = g.integers(0, 16, (G, N)).astype(np.int32)
+    w = g.normal(0, 0.3, (K, N)).astype(np.float16)
+    qw, _ = oracle.pack(w.view(np.uint16), s.view(np.uint16), z, g_idx, K, N, gs, 0)
+    q = oracle.unpack_qweight(qw, K, N).astype(np.int64)
+    sf = s.astype(np.float32)[g_idx]
+    expect = np.clip(np.rint(w.astype(np.float32) / sf) + z[g_idx], 0, 15)
+    assert np.array_equal(q, expect.astype(np.int64))
+
+
 # --------------------------------------------------------------- products
 
 def test_linear_matches_numpy_matmul():
