@@ -411,6 +411,7 @@ def run_native(args):
     if args.only is None:
         decode_70b = run_decode_70b(q4, torch, dev, stream, hbm_gbs)
         actorder = run_actorder_decode(q4, torch, dev, stream, hbm_gbs, bf16_tf)
+        next_rows = run_next_rows(q4, torch, dev, stream, hbm_gbs)
         sweep70 = run_sweep_70b(q4, torch, dev, stream, hbm_gbs, bf16_tf) if args.sweep70b else None
 
     prefill = None
@@ -450,6 +451,7 @@ def run_native(args):
         if decode_70b:
             line["decode_70b"] = decode_70b
             line["actorder_7b"] = actorder
+            line["next_rows"] = next_rows
             if sweep70:
                 line["sweep_70b"] = sweep70
         if prefill:
@@ -577,6 +579,94 @@ def run_sweep_70b(q4, torch, dev, stream, hbm_gbs, tf_peak):
     fr = [r["frac"] for r in cases.values()]
     return {"workload": "sweep_70b (all 240 cases)", "cases": cases, "median_frac": float(np.median(fr)),
             "min_frac": float(np.min(fr)), "max_frac": float(np.max(fr))}
+
+
+def _graph_time(torch, stream, issue, reps=20):
+    """Per-replay seconds of a CUDA graph of issue(stream_ptr)."""
+    issue(stream.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        issue(torch.cuda.current_stream().cuda_stream)
+    for _ in range(3):
+        g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e-3 / reps
+
+
+def run_next_rows(q4, torch, dev, stream, hbm_gbs):
+    """Measurements of the rows added past the hot path, on Llama-7B shapes:
+    projection fusion (Q, K, V of one input as one handle vs three), the
+    GPTQ_V2 zero convention (same kernels; must cost the same), and the GPU
+    packer (float weights -> checkpoint words)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    res = {}
+    K, Nq = 4096, 4096
+    R = 6                                                   # 6 x 3 x 8.7 MB = 157 MB of weights > 129 MB L2
+    layers = [synthetic.workload_layer("decode_7b", K, Nq, 128, False) for _ in range(3)]
+    sep = [[q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for L in layers] for _ in range(R)]
+    fused = [q4.Q4Matrix.fused([(t(L.qweight), t(L.qzeros), t(L.scales)) for L in layers], None, None, 128)
+             for _ in range(R)]
+    wbytes = 3 * layers[0].weight_bytes
+    for M in (1, 8):
+        x = t(synthetic.workload_x("decode_7b", K, Nq, 128, False, M))
+        o1 = torch.empty((M, Nq), dtype=torch.float16, device=dev)
+        o3 = torch.empty((M, 3 * Nq), dtype=torch.float16, device=dev)
+
+        def issue_sep(sp):
+            for r in range(R):
+                for m in sep[r]:
+                    q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o1.data_ptr(), sp)
+
+        def issue_fused(sp):
+            for r in range(R):
+                q4.gptq_q4_matmul(fused[r].handle, x.data_ptr(), M, o3.data_ptr(), sp)
+
+        ts = _graph_time(torch, stream, issue_sep) / R
+        tf = _graph_time(torch, stream, issue_fused) / R
+        res[f"qkv_7b M={M}"] = {"separate_us": round(ts * 1e6, 2), "fused_us": round(tf * 1e6, 2),
+                                "separate_TB/s": round(wbytes / ts / 1e12, 3), "fused_TB/s": round(wbytes / tf / 1e12, 3)}
+    del sep, fused
+    # GPTQ_V2: the same layer read as a V2 checkpoint
+    L = synthetic.workload_layer("decode_7b", 4096, 11008, 128, False)
+    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
+    x = t(synthetic.workload_x("decode_7b", 4096, 11008, 128, False, 1))
+    o = torch.empty((1, 11008), dtype=torch.float16, device=dev)
+
+    def issue(sp):
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), sp)
+
+    t1 = _graph_time(torch, stream, issue) / len(mats)
+    for m in mats:
+        m.set_format(q4.GPTQ_Q4_FORMAT_GPTQ_V2)
+    t2 = _graph_time(torch, stream, issue) / len(mats)
+    res["gptq_v2 4096x11008 M=1"] = {"gptq_us": round(t1 * 1e6, 2), "gptq_v2_us": round(t2 * 1e6, 2),
+                                     "gptq_v2_TB/s": round(L.weight_bytes / t2 / 1e12, 3)}
+    del mats
+    # GPU packer: float weights (fp16) + scales + zeros -> qweight/qzeros
+    K, N, gs = 4096, 11008, 128
+    g = np.random.default_rng(5)
+    w = torch.from_numpy(g.normal(0, 0.05, (K, N)).astype(np.float16)).to(dev)
+    sc = torch.from_numpy(g.uniform(0.002, 0.02, (K // gs, N)).astype(np.float16)).to(dev)
+    zs = torch.from_numpy(g.integers(0, 16, (K // gs, N)).astype(np.int32)).to(dev)
+    qw = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
+    qz = torch.empty((K // gs, N // 8), dtype=torch.int32, device=dev)
+
+    def issue_pack(sp):
+        q4.gptq_q4_pack(w.data_ptr(), sc.data_ptr(), zs.data_ptr(), None, K, N, gs, 0, qw.data_ptr(), qz.data_ptr(), sp)
+
+    tp = _graph_time(torch, stream, issue_pack, reps=10)
+    moved = K * N * 2 + K * N // 2 + (K // gs) * N * 6 + (K // gs) * N // 2
+    res["pack 4096x11008"] = {"us": round(tp * 1e6, 2), "TB/s": round(moved / tp / 1e12, 3),
+                              "frac_of_hbm_peak": round(moved / tp / 1e9 / hbm_gbs, 3),
+                              "bytes": "w fp16 read + qweight written + scales/zeros read + qzeros written"}
+    return res
 
 
 def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):

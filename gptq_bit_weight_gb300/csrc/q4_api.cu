@@ -587,6 +587,7 @@ int gptq_q4_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros
                           groupsize, K);
     if (format != GPTQ_Q4_FORMAT_GPTQ && format != GPTQ_Q4_FORMAT_GPTQ_V2)
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "format=%d is neither GPTQ nor GPTQ_V2", format);
+    if (K / 8 > 65535) return set_status(GPTQ_Q4_UNSUPPORTED, "K=%d: the packer takes K <= 524280", K);
     const int geff = groupsize == -1 ? K : groupsize;
     const int G = K / geff;
     int dev = -1;

@@ -21,29 +21,29 @@
 namespace q4 {
 namespace {
 
+// One thread per checkpoint word: column n = blockIdx.x * blockDim.x + tid,
+// word row kw = blockIdx.y (eight rows of w, coalesced across the warp).
 __global__ void pack_qweight_kernel(const uint16_t *__restrict__ w, const uint16_t *__restrict__ scales,
                                     const int32_t *__restrict__ zeros, const int32_t *__restrict__ g_idx, int K,
                                     int N, int geff, int32_t *__restrict__ qweight) {
-    const size_t total = static_cast<size_t>(K / 8) * N;
-    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int kw = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
-        uint32_t word = 0;
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    const int kw = blockIdx.y;
+    if (n >= N) return;
+    uint32_t word = 0;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int k = 8 * kw + r;
-            const int g = g_idx ? g_idx[k] : k / geff;
-            const size_t gi = static_cast<size_t>(g) * N + n;
-            const float wf = __half2float(__ushort_as_half(w[static_cast<size_t>(k) * N + n]));
-            const float sf = __half2float(__ushort_as_half(scales[gi]));
-            const float qf = rintf(__fdiv_rn(wf, sf));
-            const int z = zeros ? zeros[gi] : 8;
-            float v = (qf != qf) ? static_cast<float>(z) : qf + static_cast<float>(z);
-            v = fminf(fmaxf(v, 0.0f), 15.0f);
-            word |= static_cast<uint32_t>(v) << (4 * r);
-        }
-        qweight[idx] = static_cast<int32_t>(word);
+    for (int r = 0; r < 8; ++r) {
+        const int k = 8 * kw + r;
+        const int g = g_idx ? g_idx[k] : k / geff;
+        const size_t gi = static_cast<size_t>(g) * N + n;
+        const float wf = __half2float(__ushort_as_half(w[static_cast<size_t>(k) * N + n]));
+        const float sf = __half2float(__ushort_as_half(scales[gi]));
+        const float qf = rintf(__fdiv_rn(wf, sf));
+        const int z = zeros ? zeros[gi] : 8;
+        float v = (qf != qf) ? static_cast<float>(z) : qf + static_cast<float>(z);
+        v = fminf(fmaxf(v, 0.0f), 15.0f);
+        word |= static_cast<uint32_t>(v) << (4 * r);
     }
+    qweight[static_cast<size_t>(kw) * N + n] = static_cast<int32_t>(word);
 }
 
 __global__ void pack_qzeros_kernel(const int32_t *__restrict__ zeros, int G, int N, int zero_offset,
@@ -68,10 +68,10 @@ cudaError_t launch_pack(const uint16_t *w, const uint16_t *scales, const int32_t
                         int K, int N, int geff, int G, int zero_offset, int32_t *qweight, int32_t *qzeros,
                         cudaStream_t s) {
     const int threads = 256;
-    const size_t nw = static_cast<size_t>(K / 8) * N, nz = static_cast<size_t>(G) * (N / 8);
-    const int bw = static_cast<int>(std::min<size_t>((nw + threads - 1) / threads, static_cast<size_t>(kSMs) * 32));
+    const size_t nz = static_cast<size_t>(G) * (N / 8);
     const int bz = static_cast<int>(std::min<size_t>((nz + threads - 1) / threads, static_cast<size_t>(kSMs) * 32));
-    pack_qweight_kernel<<<bw > 0 ? bw : 1, threads, 0, s>>>(w, scales, zeros, g_idx, K, N, geff, qweight);
+    pack_qweight_kernel<<<dim3((N + threads - 1) / threads, K / 8), threads, 0, s>>>(w, scales, zeros, g_idx, K, N,
+                                                                                  geff, qweight);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     pack_qzeros_kernel<<<bz > 0 ? bz : 1, threads, 0, s>>>(zeros, G, N, zero_offset, qzeros);
