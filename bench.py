@@ -674,8 +674,9 @@ def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
 
     Fused (shared-memory dequantization inside the tcgen05 GEMM) against the
     unfused route (dequantize to temp_dq, then the tcgen05 GEMM on it).  Each
-    case is timed with CUDA events over `reps` back-to-back calls after a
-    warm-up; the work is compute-bound, so the 129 MB L2 does not flatter it."""
+    case is one call captured in a CUDA graph, replayed `reps` times back to
+    back after a warm-up and timed with CUDA events around the replays; the
+    work is compute-bound, so the 129 MB L2 does not flatter it."""
     sptr = stream.cuda_stream
     cases, tot_flops, tot_fused, tot_unf = {}, 0.0, 0.0, 0.0
     per_launch = []
@@ -691,25 +692,32 @@ def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
                 x = torch.from_numpy(synthetic.workload_x("prefill_7b", K, N, 128, act, M)).to(dev)
                 out = torch.empty((M, N), dtype=torch.float16, device=dev)
 
-                def fused():
-                    q4.gptq_q4_matmul(mat.handle, x.data_ptr(), M, out.data_ptr(), sptr)
+                def fused(sp):
+                    q4.gptq_q4_matmul(mat.handle, x.data_ptr(), M, out.data_ptr(), sp)
 
-                def unfused():
-                    q4.gptq_q4_matmul_unfused(mat.handle, x.data_ptr(), M, temp_dq.data_ptr(), out.data_ptr(), sptr)
+                def unfused(sp):
+                    q4.gptq_q4_matmul_unfused(mat.handle, x.data_ptr(), M, temp_dq.data_ptr(), out.data_ptr(), sp)
 
                 mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
                 times = {}
                 for name, fn in (("fused", fused), ("unfused", unfused)):
+                    # one call captured in a CUDA graph and replayed back to back, so that the
+                    # host's launch cost does not show as device time on the short cases
                     for _ in range(3):
-                        fn()
-                    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                           for _ in range(reps)]
-                    for a, b in evs:
-                        a.record(stream)
-                        fn()
-                        b.record(stream)
+                        fn(sptr)
                     torch.cuda.synchronize()
-                    times[name] = float(np.median([a.elapsed_time(b) for a, b in evs]))
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        fn(torch.cuda.current_stream().cuda_stream)
+                    g.replay()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    times[name] = a.elapsed_time(b) / reps
+                    del g
                 flops = 2.0 * M * K * N
                 tot_flops += flops
                 tot_fused += times["fused"]
@@ -733,7 +741,7 @@ def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
                      "frac": achieved / bf16_tf, "traffic": None, "kernel": "prefill_kernel (fused prefill)",
                      "peak_source": f"{peak_src} bf16 burst x 1 (fp16 and bf16 dense rates are equal)",
-                     "how": "trivial-g_idx cases: 2*M*K*N summed / per-call CUDA-event time summed"},
+                     "how": "trivial-g_idx cases: 2*M*K*N summed / per-call time (CUDA-graph replays) summed"},
         "cases": cases,
     }
 

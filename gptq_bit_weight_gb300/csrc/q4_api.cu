@@ -22,7 +22,6 @@
 namespace q4 {
 cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
                             uint16_t *out, int *status, cudaStream_t s);
-cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s);
 int prefill_default_min_m();
 }  // namespace q4
 
@@ -467,7 +466,9 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
     }
     const q4::HandleView v = view(h);
     if (path == GPTQ_Q4_PATH_PREFILL) {
-        Q4_CUDA(q4::launch_prefill(v, xin, M, out, stream), "prefill launch");
+        const q4::PrefillPlan pp = q4::plan_prefill(M, h->K, h->N);
+        if (int r = ensure_decode_work(h, pp.ws_floats, pp.n_tickets, stream, false)) return r;
+        Q4_CUDA(q4::launch_prefill(v, pp, h->ws, h->tickets, xin, M, out, stream), "prefill launch");
         ++g_launches;
         return ok();
     }

@@ -221,6 +221,16 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &plan, 
 int device_sm_count();
 // programmatic dependent launch switch (GPTQ_Q4_PDL=0 turns it off)
 bool pdl_enabled();
+// fused prefill (q4_prefill.cu): tile shape, K split and split workspace
+struct PrefillPlan {
+    int bm, bn;        // tile
+    int splits;        // K slices per tile (1: none)
+    size_t ws_floats;  // fp32 partial tiles when splits > 1
+    int n_tickets;     // one per tile when splits > 1
+};
+PrefillPlan plan_prefill(int M, int K, int N);
+cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets, const uint16_t *x,
+                           int M, uint16_t *out, cudaStream_t s);
 // float weights + scales + zero points -> GPTQ checkpoint words (q4_pack.cu)
 cudaError_t launch_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros, const int32_t *g_idx,
                         int K, int N, int geff, int G, int zero_offset, int32_t *qweight, int32_t *qzeros,

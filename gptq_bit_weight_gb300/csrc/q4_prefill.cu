@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "q4_internal.cuh"
@@ -95,6 +96,9 @@ struct PfArgs {
     int bpg;                 // 32-row blocks per group
     int tiles_m, tiles_n;
     int zero_offset;         // effective zero = stored + zero_offset
+    int splits;              // K slices per tile (> 1: one unit per CTA, cooperative launch)
+    float *ws;               // fp32 partial tiles [tile][slice][BM][BN] when splits > 1
+    int *tickets;            // one per tile, zero between calls
 };
 
 __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
@@ -145,6 +149,12 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
     const int KB = a.K / BK;
     const int NT16 = a.N >> 4;
     const int ntiles = a.tiles_m * a.tiles_n;
+    const int nunits = ntiles * a.splits;                 // (tile, K slice) work units
+    auto kb_range = [&](int u, int &kb0, int &kb1) {
+        const int ks = u % a.splits;
+        kb0 = (KB * ks) / a.splits;
+        kb1 = (KB * (ks + 1)) / a.splits;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSX; ++s) {
@@ -178,12 +188,16 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             RingPos r;
             int issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+                const int t = u / a.splits;
+                int kbeg, kend;
+                kb_range(u, kbeg, kend);
                 const int nt0 = (t / a.tiles_m) * (BN / 16);
                 const int tiles16 = min(BN / 16, NT16 - nt0);
                 const uint32_t sbytes = tiles16 * 32u, zbytes = tiles16 * 8u;
-                int gcur = -1, left = 0;                 // group of the next 32-row block, blocks left in it
-                for (int kb = 0; kb < KB; ++kb) {
+                // group of the first 32-row block and the blocks left in it (itself included)
+                int gcur = (2 * kbeg) / a.bpg, left = a.bpg - (2 * kbeg - gcur * a.bpg);
+                for (int kb = kbeg; kb < kend; ++kb) {
                     if (aborted(abort_flag)) { ok = false; break; }
                     if (!mbar_wait(emptyP(r.s), r.ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
                     if (left == 0) { ++gcur; left = a.bpg; }
@@ -214,9 +228,12 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             RingPos r;
             int issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+                const int t = u / a.splits;
+                int kbeg, kend;
+                kb_range(u, kbeg, kend);
                 const int m0 = (t % a.tiles_m) * BM;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kbeg; kb < kend; ++kb) {
                     if (aborted(abort_flag)) { ok = false; break; }
                     if (!mbar_wait(emptyX(r.s), r.ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
                     mbar_arrive_expect_tx(fullX(r.s), static_cast<uint32_t>(kXStage));
@@ -235,7 +252,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             RingPos rx, rb;
             int lt = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++lt) {
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x, ++lt) {
+                int kbeg, kend;
+                kb_range(u, kbeg, kend);
                 const int acc = lt % kAccBufs;
                 const uint32_t aph = (lt / kAccBufs) & 1;
                 if (aborted(abort_flag) || !mbar_wait(accE(acc), aph ^ 1)) {
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * kHalves * BN);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kbeg; kb < kend; ++kb) {
                     if (aborted(abort_flag) || !mbar_poll(fullX(rx.s), rx.ph) || !mbar_poll(fullB(rb.s), rb.ph)) {
                         fail(a.status, 0x20, abort_flag);
                         ok = false;
@@ -258,7 +277,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
 #pragma unroll
                         for (int hm = 0; hm < kHalves; ++hm)    // rows 128*hm.. of the x tile, same B tile
                             umma_f16(d + hm * BN, smem_desc_sw128(sa + hm * 16384 + kk * 32, 16, 1024),
-                                     smem_desc_sw128(sbb + kk * 32, 16, 1024), idesc, (kb | kk) != 0);
+                                     smem_desc_sw128(sbb + kk * 32, 16, 1024), idesc, (kb != kbeg) || (kk != 0));
                     umma_commit(emptyX(rx.s));
                     umma_commit(emptyB(rb.s));
                     rx.next(kSX);
@@ -297,9 +316,11 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         };
         RingPos rp, rb;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+            int kbeg, kend;
+            kb_range(u, kbeg, kend);
             int left = 0;                             // 32-row blocks left in the current group
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = kbeg; kb < kend; ++kb) {
                 if (aborted(abort_flag)) { ok = false; break; }
                 if (!mbar_wait(fullP(rp.s), rp.ph) || !mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
                     fail(a.status, 0x40, abort_flag);
@@ -310,7 +331,10 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 const uint8_t *sz = st + kSzOff;
                 // first block: a new group starts here (slot 0) or continues from the
                 // previous stage's second block, whose constants are already in slot 0
-                if (left == 0) { load_consts(sz, 0, 0); left = a.bpg; }
+                if (left == 0 || kb == kbeg) {      // a slice may start inside a group
+                    load_consts(sz, 0, 0);
+                    left = kb == kbeg ? a.bpg - (2 * kbeg) % a.bpg : a.bpg;
+                }
                 --left;
                 const bool gl1 = left == 0;           // the second block starts a new group (slot 1)
                 if (gl1) { load_consts(sz, 1, 1); left = a.bpg; }
@@ -351,7 +375,8 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         // ------------------------------------------------------ epilogue
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. +31
         int lt = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lt) {
+            const int t = u / a.splits;
             const int acc = lt % kAccBufs;
             const uint32_t aph = (lt / kAccBufs) & 1;
             bool ok = !aborted(abort_flag) && mbar_wait(accF(acc), aph);
@@ -370,7 +395,17 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 uint32_t r[32];
                 tmem_ld_x32(tmem + static_cast<uint32_t>(acc * kHalves * BN + hc) + (static_cast<uint32_t>(32 * quad) << 16),
                             r);
-                if (row < a.M) {
+                if (a.splits > 1) {
+                    // the fp32 partial of this K slice, whole tile, lane-major so that
+                    // each warp store is 512 contiguous bytes:
+                    // float4 index (((u * (kHalves*BN/32) + hc/32) * 4 + quad) * 8 + v) * 32 + lane
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws) +
+                                  ((static_cast<size_t>(u) * (kHalves * BN / 32) + hc / 32) * 4 + quad) * 8 * 32 + lane;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                } else if (row < a.M) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int n = n0 + c0 + 8 * v;
@@ -406,6 +441,71 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+
+    if (a.splits > 1 && blockIdx.x < nunits) {
+        // K slices of one tile: every unit has written its partial tile; once
+        // all have (a bounded wait: the cooperative launch keeps every unit
+        // resident), each unit finishes rows [ks*BM/S, (ks+1)*BM/S) of the
+        // tile, summing the partials in slice order, adding bias, rounding once.
+        const int u = blockIdx.x, t = u / a.splits, ks = u % a.splits, S = a.splits;
+        __shared__ int s_ready;
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(a.tickets + t, 1);
+            bool ready = true;
+            const uint64_t t0 = globaltimer();
+            while (atomicAdd(a.tickets + t, 0) < S) {
+                if (aborted(abort_flag) || globaltimer() - t0 > 2000000000ull) {
+                    ready = false;
+                    break;
+                }
+                __nanosleep(256);
+            }
+            __threadfence();
+            s_ready = ready;
+            if (!ready) fail(a.status, 0x100, abort_flag);
+        }
+        __syncthreads();
+        if (s_ready) {
+            const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
+            const int r0 = (BM * ks) / S, r1 = (BM * (ks + 1)) / S, rows = r1 - r0;
+            const float4 *ws4 = reinterpret_cast<const float4 *>(a.ws);
+            // consecutive threads take consecutive rows of one 8-column group: their
+            // loads of the lane-major partials are contiguous
+            for (int i = threadIdx.x; i < rows * (BN / 8); i += blockDim.x) {
+                const int rl = r0 + i % rows, c = 8 * (i / rows);
+                const int row = m0 + rl, n = n0 + c;
+                if (row >= a.M || n >= a.N) continue;
+                const int hm = rl / 128, q = (rl % 128) / 32, ln = rl % 32;
+                const int hc = hm * BN + c;
+                float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int j = 0; j < S; ++j) {
+                    const float4 *src =
+                        ws4 + ((static_cast<size_t>(t * S + j) * (kHalves * BN / 32) + hc / 32) * 4 + q) * 8 * 32 +
+                        ((hc % 32) / 4) * 32 + ln;
+                    const float4 p0 = __ldcg(src), p1 = __ldcg(src + 32);
+                    v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+                    v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+                }
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float lo = v[2 * e], hi = v[2 * e + 1];
+                    if (a.bias) {
+                        lo += __half2float(__ushort_as_half(a.bias[n + 2 * e]));
+                        hi += __half2float(__ushort_as_half(a.bias[n + 2 * e + 1]));
+                    }
+                    pk[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+                            (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+                }
+                *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        __syncthreads();
+        // second arrival: the last of the 2S resets the ticket for the next call
+        if (threadIdx.x == 0 && atomicAdd(a.tickets + t, 1) == 2 * S - 1) atomicExch(a.tickets + t, 0);
+    }
 }
 
 int sm_count() {
@@ -423,7 +523,8 @@ int sm_count() {
 
 
 template <int BM, int BN>
-cudaError_t launch_prefill_tile(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets,
+                                const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
     using P = PfCfg<BM, BN>;
     CUtensorMap tmA, tmW;
     cudaError_t e;
@@ -438,31 +539,60 @@ cudaError_t launch_prefill_tile(const HandleView &h, const uint16_t *x, int M, u
         cudaFuncSetAttribute(prefill_kernel<BM, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
     if (attr != cudaSuccess) return attr;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
-                (h.N + BN - 1) / BN, h.zero_offset};
-    const int ntiles = args.tiles_m * args.tiles_n;
-    const int grid = ntiles < sm_count() ? ntiles : sm_count();
-    prefill_kernel<BM, BN><<<grid, P::kThreads, P::kSmem, s>>>(tmA, tmW, args);
-    return cudaGetLastError();
+                (h.N + BN - 1) / BN, h.zero_offset, p.splits, ws, tickets};
+    const int nunits = args.tiles_m * args.tiles_n * p.splits;
+    const int grid = nunits < sm_count() ? nunits : sm_count();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(P::kThreads);
+    cfg.dynamicSmemBytes = P::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeCooperative;         // split units wait on each other: all resident
+    at.val.cooperative = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = p.splits > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<BM, BN>, tmA, tmW, args);
 }
 
 }  // namespace
 
-// Tile shape by tile count (c = SMs): 256 x 256 when those tiles still give
-// every SM at least three quarters of a tile's work; else 128 x 256; else
-// 128 x 128 (small M), at the same cost per flop as 128 x 256.
-cudaError_t launch_prefill(const HandleView &h, const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
+// Tile shape and K split by tile count (c = SMs): 256 x 256 when those tiles
+// give every SM at least three quarters of a tile's work; else 256 x 256 with
+// the K range split S ways (S = floor(c / tiles) <= 8, every unit resident at
+// once, at least 8 stages each) when that makes at least two slices; else
+// 128 x 256; else 128 x 128 (small M), at the same cost per flop as 128 x 256.
+PrefillPlan plan_prefill(int M, int K, int N) {
+    PrefillPlan p{};
     const long long c = sm_count();
-    const long long n256 = (h.N + 255) / 256;
+    const long long n256 = (N + 255) / 256;
     const long long t256x256 = static_cast<long long>((M + 255) / 256) * n256;
     const long long t128x256 = static_cast<long long>((M + 127) / 128) * n256;
-    if (4 * t256x256 >= 3 * c) return launch_prefill_tile<256, 256>(h, x, M, out, s);
-    if (4 * t128x256 >= 3 * c) return launch_prefill_tile<128, 256>(h, x, M, out, s);
-    return launch_prefill_tile<128, 128>(h, x, M, out, s);
+    const int KB = K / BK;
+    p.splits = 1;
+    if (4 * t256x256 >= 3 * c) {
+        p.bm = 256, p.bn = 256;
+    } else if (c / t256x256 >= 2 && KB / 2 >= 8) {
+        p.bm = 256, p.bn = 256;
+        p.splits = static_cast<int>(std::min<long long>(8, c / t256x256));
+        while (p.splits > 2 && KB / p.splits < 8) --p.splits;
+        p.ws_floats = static_cast<size_t>(t256x256) * p.splits * 256 * 256;
+        p.n_tickets = static_cast<int>(t256x256);
+    } else if (4 * t128x256 >= 3 * c) {
+        p.bm = 128, p.bn = 256;
+    } else {
+        p.bm = 128, p.bn = 128;
+    }
+    return p;
 }
 
-// Above 16 rows the decode kernels fall back to the register-streaming one
-// with four m tiles per CTA (8 warps, heavy on registers); the fused prefill
-// is 3-4x faster there on the 70B shapes (M = 32), so it starts at 17 rows.
+cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets, const uint16_t *x,
+                           int M, uint16_t *out, cudaStream_t s) {
+    if (p.bm == 256) return launch_prefill_tile<256, 256>(h, p, ws, tickets, x, M, out, s);
+    if (p.bn == 256) return launch_prefill_tile<128, 256>(h, p, ws, tickets, x, M, out, s);
+    return launch_prefill_tile<128, 128>(h, p, ws, tickets, x, M, out, s);
+}
+
 int prefill_default_min_m() { return 17; }
 
 }  // namespace q4

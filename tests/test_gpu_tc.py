@@ -57,6 +57,7 @@ LAYERS = [  # (K, N, groupsize, act_order)
     (1024, 448, 32, True),
     (1152, 576, 96, False),     # group of three 32-row blocks: some stages span two groups
     (2048, 512, -1, False),
+    (1344, 320, 96, True),      # K split in two at stage 10: the second slice starts inside a group
 ]
 
 
