@@ -11,9 +11,18 @@
 //
 // Work split.  A CTA (8 warps) owns 32 output columns (two 16-column tiles),
 // up to 8*MT rows of x, and one K slice.  Its warps split the slice into
-// contiguous runs of 64-row chunks.  For each chunk a lane issues one 16-byte
-// streaming load per column tile; a ring of DEPTH chunks keeps loads in
-// flight while earlier chunks are computed.
+// contiguous runs of 64-row chunks; for each chunk a lane needs one 16-byte
+// vector per column tile.  Two ways to keep those in flight:
+//   shared ring (SR, M <= 4): each warp owns a ring of kDepth chunk slots in
+//     shared memory, filled by asynchronous copies (one commit group per
+//     chunk); a lane reads back exactly the vectors it copied, so no barrier
+//     is needed.  The first kDepth - 1 chunks are requested before the
+//     preceding grid has finished (they are handle constants), and x comes in
+//     with plain loads so that waiting for x does not wait for the weights.
+//   register ring (larger M, whose x slice takes the shared memory): each
+//     warp keeps kRegDepth chunks of loads in flight in registers.
+// Groups are tracked with counters along the warp's run (no division in
+// the loop).
 //
 // Arithmetic.  Each packed word gives, with one LOP3 and one HFMA2 per pair,
 // the exact integers (q - z - 1) of eight consecutive rows of one column as
@@ -51,16 +60,13 @@ namespace {
 #ifndef Q4_DECODE_DEPTH
 #define Q4_DECODE_DEPTH 4
 #endif
-// 0: each warp streams one contiguous run of 64-row chunks; 1: the warps of a
-// CTA take consecutive chunk pairs, so a CTA reads one contiguous span per step.
-#ifndef Q4_DECODE_INTERLEAVE
-#define Q4_DECODE_INTERLEAVE 0
-#endif
 constexpr int kWarps = Q4_DECODE_WARPS;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kNTW = Q4_DECODE_NTW;             // 16-column tiles per CTA
 constexpr int kNB = 16 * kNTW;      // columns per CTA
-constexpr int kDepth = Q4_DECODE_DEPTH;         // chunks in the load ring
+constexpr int kDepth = Q4_DECODE_DEPTH;         // shared ring: slots per warp (kDepth - 1 chunks in flight)
+constexpr int kRingWarpBytes = kDepth * kNTW * 512;   // one warp's ring (16 bytes per lane and tile)
+constexpr int kRegDepth = 4;                    // register ring: chunks in flight per warp
 constexpr int kMaxCluster = 8;      // portable thread-block cluster size
 // Shared words staged per group: kNTW*8 scale pairs, then kNTW*2 zero words,
 // padded to a multiple of 4 so every group's copies start 16-byte aligned.
@@ -76,21 +82,21 @@ struct DecodeArgs {
     int slice_chunks;
     int xrows;          // rows of x staged per CTA: min(8*MT, M)
     int cluster;        // slices reduce through distributed shared memory
-    uint64_t inv_bpg;   // ceil(2^32 / blocks-per-group): group of 32-row block b = (b * inv_bpg) >> 32
 };
 
 __host__ __device__ inline int x_row_stride(int slice_chunks) { return slice_chunks * 64 + 32; }
 
-template <int MT>
-__host__ __device__ inline size_t smem_bytes(int xrows, int slice_chunks, int max_groups) {
-    return static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2      // x slice
-           + static_cast<size_t>(kWarps) * kNTW * MT * 128 * 4              // warp partials
-           + static_cast<size_t>(max_groups) * kGszStride * 4;             // scale pairs + zero words
+// Bytes per warp of the first shared region: the weight ring (shared ring)
+// or the warp partials alone (register ring); the ring holds the partials
+// at the end.
+__host__ __device__ constexpr int warp_region_bytes(int mt, bool sr) {
+    return sr ? kRingWarpBytes : kNTW * mt * 512;
 }
-
-__host__ __device__ inline size_t smem_bytes_for(int mt, int xrows, int slice_chunks, int max_groups) {
-    return static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2 +
-           static_cast<size_t>(kWarps) * kNTW * mt * 128 * 4 + static_cast<size_t>(max_groups) * kGszStride * 4;
+// Shared memory: the warps' regions, the x slice, the slice's scale pairs
+// and zero words.
+__host__ __device__ inline size_t smem_bytes_for(int mt, bool sr, int xrows, int slice_chunks, int max_groups) {
+    return static_cast<size_t>(kWarps) * warp_region_bytes(mt, sr) +
+           static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2 + static_cast<size_t>(max_groups) * kGszStride * 4;
 }
 
 __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
@@ -107,8 +113,10 @@ constexpr int min_blocks(int mt, bool raw) { return min_warps(mt, raw) / kWarps 
 // pair) and the zero point is removed per group from MMA-accumulated sums of
 // x; otherwise each pair is turned into the exact fp16 (q - z - 1) first (one
 // LOP3 and one HFMA2).  Same result up to fp32 rounding.
-template <int MT, bool RAW>
+template <int MT, bool RAW, bool SR>
 __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(HandleView h, DecodeArgs a) {
+    static_assert(!RAW || MT == 1, "raw pairs: one m tile");
+    constexpr int kRegion = warp_region_bytes(MT, SR);
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gq = lane >> 2, tq = lane & 3;
@@ -123,45 +131,27 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     const int XS = x_row_stride(a.slice_chunks);
     const int geff = h.geff;
 
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + static_cast<size_t>(a.xrows) * XS * 2);
-    uint32_t *gsz = reinterpret_cast<uint32_t *>(red + kWarps * kNTW * MT * 128);
+    static_assert(kDepth >= 2 && kRegion >= kNTW * MT * 128 * 4, "a warp's region holds its partials at the end");
+    unsigned char *wring = smem;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + kWarps * kRegion);
+    uint32_t *gsz = reinterpret_cast<uint32_t *>(smem + kWarps * kRegion + static_cast<size_t>(a.xrows) * XS * 2);
 
     // Let the next kernel in the stream start its own prologue as soon as
     // every CTA of this grid is resident (programmatic dependent launch).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // This warp's sequence of 64-row chunks within the CTA's slice.
-#if Q4_DECODE_INTERLEAVE
-    const int full_steps = nch / (2 * kWarps);
-    const int rem = nch - full_steps * 2 * kWarps;
-    const int extra = min(2, max(0, rem - 2 * warp));
-    const int wn = 2 * full_steps + extra;
-    auto chunk_of = [&](int c) { return c_beg + 2 * kWarps * (c >> 1) + 2 * warp + (c & 1); };
-#else
+    // This warp's run of 64-row chunks within the CTA's slice.
     const int wc_beg = c_beg + (nch * warp) / kWarps;
     const int wn = c_beg + (nch * (warp + 1)) / kWarps - wc_beg;
     auto chunk_of = [&](int c) { return wc_beg + c; };
-#endif
     const int g_base = (c_beg * 64) / geff;
 
-    // ---- first kDepth chunks of packed weights: handle-owned constant data,
-    //      so the loads may be issued before the preceding grid has finished.
-    const uint4 *wbase[kNTW];
-#pragma unroll
-    for (int nt = 0; nt < kNTW; ++nt) wbase[nt] = h.wp + static_cast<size_t>(nt0 + nt) * KC * 32 + lane;
-    uint4 buf[kDepth][kNTW];
-#pragma unroll
-    for (int i = 0; i < kDepth; ++i)
-        if (i < wn)
-#pragma unroll
-            for (int nt = 0; nt < kNTW; ++nt) buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(chunk_of(i)) * 32);
-
-    // ---- stage the slice's scale pairs / zero words (constant) and, once
-    //      the preceding grid is done, x[m0 : m0 + mrows][slice], with
-    //      asynchronous global->shared copies: together with the weight loads
-    //      above they form a single round trip to memory.  Lanes whose x row
-    //      is past M use zeros without reading shared memory.
+    // ---- the slice's scale pairs / zero words (constant), then the first
+    //      kDepth - 1 chunks of this warp's packed weights into its ring
+    //      (handle-owned constant data, so both go out before the preceding
+    //      grid has finished), then x[m0 : m0 + mrows][slice] once it has.
+    //      Each is a group of asynchronous global->shared copies; a lane
+    //      later reads back exactly the 16-byte ring entries it copied.
     {
         const int g_beg = (c_beg * 64) / geff;
         const int g_end = (c_end * 64 - 1) / geff + 1;
@@ -179,15 +169,67 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
             for (int v = 0; v < kNTW / 2; ++v) cp_async_16(dst + kNTW * 8 + 4 * v, zsrc + 4 * v);
             if (kNTW & 1) cp_async_8(dst + kNTW * 8 + 4 * (kNTW / 2), zsrc + 4 * (kNTW / 2));
         }
+        cp_async_commit();
+    }
+    unsigned char *myring = wring + warp * kRingWarpBytes + lane * 16;   // + (slot * kNTW + nt) * 512
+    const uint4 *wsrc[kNTW];
+#pragma unroll
+    for (int nt = 0; nt < kNTW; ++nt) wsrc[nt] = h.wp + static_cast<size_t>(nt0 + nt) * KC * 32 + lane;
+    uint4 buf[SR ? 1 : kRegDepth][kNTW];               // register ring
+    if (SR) {
+#pragma unroll
+        for (int i = 0; i < kDepth - 1; ++i) {
+            if (i < wn)
+#pragma unroll
+                for (int nt = 0; nt < kNTW; ++nt)
+                    cp_async_16(myring + (i * kNTW + nt) * 512, wsrc[nt] + static_cast<size_t>(chunk_of(i)) * 32);
+            cp_async_commit();
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRegDepth; ++i)
+            if (i < wn)
+#pragma unroll
+                for (int nt = 0; nt < kNTW; ++nt)
+                    buf[SR ? 0 : i][nt] = ldg_stream(wsrc[nt] + static_cast<size_t>(chunk_of(i)) * 32);
+    }
+    {
         // x, the workspace, the tickets and out may belong to the preceding
         // grid: wait for it (a no-op without programmatic dependent launch).
         asm volatile("griddepcontrol.wait;" ::: "memory");
         const int vpr = nch * 8;                        // 16-byte vectors per row
-        for (int r = 0; r < mrows; ++r) {
-            const uint16_t *src = a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64;
-            for (int c = threadIdx.x; c < vpr; c += kThreads) cp_async_16(xs + r * XS + c * 8, src + c * 8);
+        if (SR) {
+            // plain L2 loads, eight per thread in flight, so that waiting for
+            // x does not wait for the weight copies
+            const int total = mrows * vpr;
+            for (int v0 = threadIdx.x; v0 < total; v0 += 8 * kThreads) {
+                uint4 xv8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + u * kThreads;
+                    if (v < total) {
+                        const int r = v / vpr, cv = v - r * vpr;
+                        xv8[u] = __ldcg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64) + cv);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + u * kThreads;
+                    if (v < total) {
+                        const int r = v / vpr, cv = v - r * vpr;
+                        *reinterpret_cast<uint4 *>(xs + r * XS + cv * 8) = xv8[u];
+                    }
+                }
+            }
+            cp_async_wait<kDepth - 1>();                // the scale/zero copies: the oldest group
+        } else {
+            for (int r = 0; r < mrows; ++r) {
+                const uint16_t *src = a.x + static_cast<size_t>(m0 + r) * K + c_beg * 64;
+                for (int c = threadIdx.x; c < vpr; c += kThreads) cp_async_16(xs + r * XS + c * 8, src + c * 8);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
         }
-        cp_async_wait_all();
     }
     __syncthreads();
 
@@ -204,7 +246,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         // dhi: 1024 + 16 q rows) and the sums of x that met them (slo, shi);
         // exact arithmetic: dlo alone holds sum x (q - z - 1)
         float dlo[kNTW][MT][4], dhi[kNTW][MT][4], slo[MT][4], shi[MT][4];
-        uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
         auto clear_partials = [&]() {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
@@ -217,31 +258,32 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
                 }
         };
         clear_partials();
-        float sc[kNTW][2], czl[kNTW][2], czh[kNTW][2];   // scale, -(1025 + z), -(65 + z)
-        int grp = -1;
 
-        auto load_group = [&](int g) {
-            const uint32_t *base = gsz + (g - g_base) * kGszStride;
+        // The current group's scales, and per pair kind either the unpack_qz
+        // constants (exact pairs) or -(1024 + z), -(64 + z) (raw pairs), z
+        // the effective zero point of columns gq, gq + 8.
+        float sc[kNTW][2], czl[kNTW][2], czh[kNTW][2];
+        uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
+        auto load_group = [&](int gl) {
+            const uint32_t *base = gsz + gl * kGszStride;
 #pragma unroll
             for (int nt = 0; nt < kNTW; ++nt) {
                 const uint32_t sp = base[nt * 8 + gq];
                 const uint32_t zw0 = base[kNTW * 8 + nt * 2], zw1 = base[kNTW * 8 + nt * 2 + 1];
                 sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                // effective zero points (stored + zero_offset) of columns gq, gq + 8
-                const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + h.zero_offset);
-                const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + h.zero_offset);
-                czl[nt][0] = -(1024.f + z0);
-                czl[nt][1] = -(1024.f + z1);
-                czh[nt][0] = -(64.f + z0);
-                czh[nt][1] = -(64.f + z1);
-                if (!RAW) {
-                    const uint32_t zi0 = ((zw0 >> (4 * gq)) & 0xFu) + h.zero_offset - 1u;
-                    const uint32_t zi1 = ((zw1 >> (4 * gq)) & 0xFu) + h.zero_offset - 1u;
-                    nzlo[nt][0] = neg_zlo(zi0);
-                    nzhi[nt][0] = neg_zhi(zi0);
-                    nzlo[nt][1] = neg_zlo(zi1);
-                    nzhi[nt][1] = neg_zhi(zi1);
+                const uint32_t z0 = ((zw0 >> (4 * gq)) & 0xFu) + h.zero_offset;
+                const uint32_t z1 = ((zw1 >> (4 * gq)) & 0xFu) + h.zero_offset;
+                if (RAW) {
+                    czl[nt][0] = -(1024.f + static_cast<float>(z0));
+                    czl[nt][1] = -(1024.f + static_cast<float>(z1));
+                    czh[nt][0] = -(64.f + static_cast<float>(z0));
+                    czh[nt][1] = -(64.f + static_cast<float>(z1));
+                } else {
+                    nzlo[nt][0] = neg_zlo(z0 - 1u);
+                    nzhi[nt][0] = neg_zhi(z0 - 1u);
+                    nzlo[nt][1] = neg_zlo(z1 - 1u);
+                    nzhi[nt][1] = neg_zhi(z1 - 1u);
                 }
             }
         };
@@ -267,80 +309,122 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         constexpr uint32_t kOnes = 0x3C003C00u;
         const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
 
-        for (int base = 0; base < wn; base += kDepth) {
+        // Group of the warp's first 32-row block and the blocks left in it;
+        // the run's blocks are consecutive, so counters track the rest.
+        const int bpg = geff >> 5;
+        const int blk0 = 2 * wc_beg;
+        int gl = blk0 / bpg - g_base;
+        int left = bpg - (blk0 - (gl + g_base) * bpg);
+        load_group(gl);
+
+        // This lane's x row in each m tile and its 16-byte piece of the first
+        // 32-row block of the run.
+        const uint16_t *xp[MT];
+        bool xv[MT];
 #pragma unroll
-            for (int i = 0; i < kDepth; ++i) {
-                const int c = base + i;
-                if (c < wn) {
-                    const int chunk = chunk_of(c);
+        for (int mt = 0; mt < MT; ++mt) {
+            const int r = mt * 8 + gq;
+            xv[mt] = r < mrows;
+            xp[mt] = xs + (xv[mt] ? r : 0) * XS + 2 * (wc_beg - c_beg) * 32 + 8 * tq;
+        }
+
+        auto run_chunk = [&](int c, const uint4 (&w)[kNTW]) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int g = static_cast<int>((static_cast<uint64_t>(2 * chunk + hh) * a.inv_bpg) >> 32);
-                        if (g != grp) {
-                            if (grp >= 0) flush();
-                            load_group(g);
-                            grp = g;
-                        }
-                        const int kk = (2 * (chunk - c_beg) + hh) * 32 + 8 * tq;
-                        uint4 xb[MT];
+            for (int hh = 0; hh < 2; ++hh) {
+                if (left == 0) {
+                    flush();
+                    load_group(++gl);
+                    left = bpg;
+                }
+                --left;
+                uint4 xb[MT];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+                    xb[mt] = xv[mt] ? *reinterpret_cast<const uint4 *>(xp[mt] + (2 * c + hh) * 32)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                if (RAW) {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        mma_16816(slo[mt], ones, xb[mt].x, xb[mt].z);
+                        mma_16816(shi[mt], ones, xb[mt].y, xb[mt].w);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < kNTW; ++nt) {
+                    const uint32_t lo = hh ? w[nt].z : w[nt].x;    // column 16nt + gq
+                    const uint32_t hi = hh ? w[nt].w : w[nt].y;    // column 16nt + gq + 8
+                    uint32_t al[4], ah[4];
+                    if (RAW) {
+                        unpack_raw(lo, al);
+                        unpack_raw(hi, ah);
+                        const uint32_t alo[4] = {al[0], ah[0], al[2], ah[2]};
+                        const uint32_t ahi[4] = {al[1], ah[1], al[3], ah[3]};
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
-                            xb[mt] = make_uint4(0u, 0u, 0u, 0u);
-                            if (mt * 8 + gq < mrows)
-                                xb[mt] = *reinterpret_cast<const uint4 *>(xs + (mt * 8 + gq) * XS + kk);
+                            mma_16816(dlo[nt][mt], alo, xb[mt].x, xb[mt].z);
+                            mma_16816(dhi[nt][mt], ahi, xb[mt].y, xb[mt].w);
                         }
-                        if (RAW) {
+                    } else {
+                        unpack_qz(lo, nzlo[nt][0], nzhi[nt][0], al);
+                        unpack_qz(hi, nzlo[nt][1], nzhi[nt][1], ah);
+                        const uint32_t A0[4] = {al[0], ah[0], al[1], ah[1]};
+                        const uint32_t A1[4] = {al[2], ah[2], al[3], ah[3]};
 #pragma unroll
-                            for (int mt = 0; mt < MT; ++mt) {
-                                mma_16816(slo[mt], ones, xb[mt].x, xb[mt].z);
-                                mma_16816(shi[mt], ones, xb[mt].y, xb[mt].w);
-                            }
-                        }
-#pragma unroll
-                        for (int nt = 0; nt < kNTW; ++nt) {
-                            const uint32_t lo = hh ? buf[i][nt].z : buf[i][nt].x;    // column 16nt + gq
-                            const uint32_t hi = hh ? buf[i][nt].w : buf[i][nt].y;    // column 16nt + gq + 8
-                            uint32_t al[4], ah[4];
-                            if (RAW) {
-                                unpack_raw(lo, al);
-                                unpack_raw(hi, ah);
-                                const uint32_t alo[4] = {al[0], ah[0], al[2], ah[2]};
-                                const uint32_t ahi[4] = {al[1], ah[1], al[3], ah[3]};
-#pragma unroll
-                                for (int mt = 0; mt < MT; ++mt) {
-                                    mma_16816(dlo[nt][mt], alo, xb[mt].x, xb[mt].z);
-                                    mma_16816(dhi[nt][mt], ahi, xb[mt].y, xb[mt].w);
-                                }
-                            } else {
-                                unpack_qz(lo, nzlo[nt][0], nzhi[nt][0], al);
-                                unpack_qz(hi, nzlo[nt][1], nzhi[nt][1], ah);
-                                const uint32_t A0[4] = {al[0], ah[0], al[1], ah[1]};
-                                const uint32_t A1[4] = {al[2], ah[2], al[3], ah[3]};
-#pragma unroll
-                                for (int mt = 0; mt < MT; ++mt) {
-                                    mma_16816(dlo[nt][mt], A0, xb[mt].x, xb[mt].y);
-                                    mma_16816(dlo[nt][mt], A1, xb[mt].z, xb[mt].w);
-                                }
-                            }
+                        for (int mt = 0; mt < MT; ++mt) {
+                            mma_16816(dlo[nt][mt], A0, xb[mt].x, xb[mt].y);
+                            mma_16816(dlo[nt][mt], A1, xb[mt].z, xb[mt].w);
                         }
                     }
-                    if (c + kDepth < wn)
+                }
+            }
+        };
+        if (SR) {
+            int rs = 0;                                 // ring slot of chunk c
+            for (int c = 0; c < wn; ++c) {
+                cp_async_wait<kDepth - 2>();            // chunk c has landed
+                uint4 w[kNTW];
 #pragma unroll
-                        for (int nt = 0; nt < kNTW; ++nt)
-                            buf[i][nt] = ldg_stream(wbase[nt] + static_cast<size_t>(chunk_of(c + kDepth)) * 32);
+                for (int nt = 0; nt < kNTW; ++nt) w[nt] = *reinterpret_cast<const uint4 *>(myring + (rs * kNTW + nt) * 512);
+                // refill the slot of chunk c - 1 (consumed) with chunk c + kDepth - 1
+                const int fs = rs == 0 ? kDepth - 1 : rs - 1;
+                if (c + kDepth - 1 < wn)
+#pragma unroll
+                    for (int nt = 0; nt < kNTW; ++nt)
+                        cp_async_16(myring + (fs * kNTW + nt) * 512,
+                                    wsrc[nt] + static_cast<size_t>(chunk_of(c + kDepth - 1)) * 32);
+                cp_async_commit();
+                rs = rs + 1 == kDepth ? 0 : rs + 1;
+                run_chunk(c, w);
+            }
+        } else {
+            for (int base = 0; base < wn; base += kRegDepth) {
+#pragma unroll
+                for (int i = 0; i < kRegDepth; ++i) {
+                    const int c = base + i;
+                    if (c < wn) {
+                        run_chunk(c, buf[SR ? 0 : i]);
+                        if (c + kRegDepth < wn)
+#pragma unroll
+                            for (int nt = 0; nt < kNTW; ++nt)
+                                buf[SR ? 0 : i][nt] = ldg_stream(wsrc[nt] + static_cast<size_t>(chunk_of(c + kRegDepth)) * 32);
+                    }
                 }
             }
         }
         flush();
     }
 
-    // ---- fixed-order reduction over the CTA's warps
+    // ---- fixed-order reduction over the CTA's warps; warp w's partials go to
+    //      its own (drained) ring, so no warp waits before writing them
     constexpr int E = kNTW * MT * 128;                 // partial elements per CTA
+    constexpr int RW = kRegion / 4;                     // floats between two warps' partials
+    float *red = reinterpret_cast<float *>(wring);
+    cp_async_wait<0>();
 #pragma unroll
     for (int nt = 0; nt < kNTW; ++nt)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
-            *reinterpret_cast<float4 *>(red + warp * E + (nt * MT + mt) * 128 + lane * 4) =
+            *reinterpret_cast<float4 *>(red + warp * RW + (nt * MT + mt) * 128 + lane * 4) =
                 make_float4(acc[nt][mt][0], acc[nt][mt][1], acc[nt][mt][2], acc[nt][mt][3]);
     __syncthreads();
 
@@ -364,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     for (int e = threadIdx.x; e < E; e += kThreads) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += red[w * E + e];
+        for (int w = 0; w < kWarps; ++w) v += red[w * RW + e];
         if (a.splits == 1) store_out(e, v);
         else red[e] = v;
     }
@@ -412,11 +496,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
 }
 
-template <int MT, bool RAW>
+template <int MT, bool RAW, bool SR>
 cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                       uint16_t *out, cudaStream_t s) {
     const int xrows = M < 8 * MT ? M : 8 * MT;
-    const size_t smem = smem_bytes<MT>(xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
+    const size_t smem = smem_bytes_for(MT, SR, xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
     // Opt in once to the largest dynamic shared memory the device allows
     // next to the kernel's static shared memory.
     static int max_dyn = -1;
@@ -425,18 +509,15 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
         cudaFuncAttributes fa{};
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT, RAW>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT, RAW, SR>);
         const int want = optin - static_cast<int>(fa.sharedSizeBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_kernel<MT, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+            e = cudaFuncSetAttribute(decode_kernel<MT, RAW, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess) return e;
         max_dyn = want;
     }
     if (smem > static_cast<size_t>(max_dyn)) return cudaErrorInvalidConfiguration;
-    // exact floor(b / bpg) for b * bpg < 2^32 (b <= K / 32)
-    const uint64_t bpg = static_cast<uint64_t>(h.geff / 32);
-    const uint64_t inv_bpg = (0x100000000ull + bpg - 1) / bpg;
-    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows, p.cluster, inv_bpg};
+    DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows, p.cluster};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas_n, p.splits, p.zdim);
     cfg.blockDim = dim3(kThreads);
@@ -458,7 +539,7 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<MT, RAW>, h, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<MT, RAW, SR>, h, a);
 }
 
 }  // namespace
@@ -485,9 +566,10 @@ int resident_ctas(int mt, bool raw, size_t smem) {
 // one wave of resident CTAs, take the most splits that still fit (the most
 // bytes in flight while the whole grid is one DRAM round trip deep); when it
 // does not, fill whole waves as closely as possible (fewer splits on a tie).
-static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw) {
+static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw, bool sr) {
     DecodePlan p{};
     p.raw = raw ? 1 : 0;
+    p.sr = sr ? 1 : 0;
     p.mt = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
     p.zdim = (M + 8 * p.mt - 1) / (8 * p.mt);
     p.ctas_n = N / kNB;
@@ -500,7 +582,7 @@ static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw) {
     const int max_splits = std::max(min_splits, KC / 16);   // at least two chunks per warp
     auto slots_for = [&](int sp) {
         const int slice = (KC + sp - 1) / sp;
-        const size_t smem = smem_bytes_for(p.mt, xrows, slice, max_groups_in_slice(slice, geff));
+        const size_t smem = smem_bytes_for(p.mt, sr, xrows, slice, max_groups_in_slice(slice, geff));
         return static_cast<long long>(kSMs) * resident_ctas(p.mt, raw, smem);
     };
     auto valid = [&](int sp) {
@@ -533,20 +615,26 @@ static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw) {
     p.ws_floats = (p.splits > 1 && !p.cluster) ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
     p.one_wave = static_cast<long long>(base) * p.splits <=
                  static_cast<long long>(kSMs) *
-                     resident_ctas(p.mt, raw, smem_bytes_for(p.mt, std::min(M, 8 * p.mt), p.slice_chunks,
+                     resident_ctas(p.mt, raw, smem_bytes_for(p.mt, sr, std::min(M, 8 * p.mt), p.slice_chunks,
                                                              max_groups_in_slice(p.slice_chunks, geff)));
     return p;
 }
 
+// Weight ring in shared memory for M <= Q4_DECODE_SR_MAX_M rows (a short x
+// slice leaves room for it), in registers otherwise.
+#ifndef Q4_DECODE_SR_MAX_M
+#define Q4_DECODE_SR_MAX_M 4
+#endif
 // M <= 8: the raw-pair arithmetic (fewer instructions, 2 CTAs per SM) when its
 // grid is a single wave, else the exact-pair arithmetic at 3 CTAs per SM,
 // which keeps mid-size layers in one wave.  Larger M: exact pairs.
 DecodePlan plan_decode(int M, int K, int N, int geff) {
+    const bool sr = M <= Q4_DECODE_SR_MAX_M;
     if (M <= 8) {
-        const DecodePlan r = plan_decode_arith(M, K, N, geff, true);
+        const DecodePlan r = plan_decode_arith(M, K, N, geff, true, sr);
         if (r.one_wave) return r;
     }
-    return plan_decode_arith(M, K, N, geff, false);
+    return plan_decode_arith(M, K, N, geff, false, sr);
 }
 
 size_t decode_ws_floats_for(int M, int K, int N, int geff) { return plan_decode(M, K, N, geff).ws_floats; }
@@ -554,9 +642,11 @@ size_t decode_ws_floats_for(int M, int K, int N, int geff) { return plan_decode(
 cudaError_t launch_decode(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                           uint16_t *out, cudaStream_t s) {
     switch (p.mt) {
-        case 1: return p.raw ? launch_mt<1, true>(h, p, w, x, M, out, s) : launch_mt<1, false>(h, p, w, x, M, out, s);
-        case 2: return launch_mt<2, false>(h, p, w, x, M, out, s);
-        default: return launch_mt<4, false>(h, p, w, x, M, out, s);
+        case 1:
+            if (p.raw) return p.sr ? launch_mt<1, true, true>(h, p, w, x, M, out, s) : launch_mt<1, true, false>(h, p, w, x, M, out, s);
+            return p.sr ? launch_mt<1, false, true>(h, p, w, x, M, out, s) : launch_mt<1, false, false>(h, p, w, x, M, out, s);
+        case 2: return launch_mt<2, false, false>(h, p, w, x, M, out, s);
+        default: return launch_mt<4, false, false>(h, p, w, x, M, out, s);
     }
 }
 

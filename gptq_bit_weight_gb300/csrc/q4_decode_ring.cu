@@ -27,7 +27,14 @@
 // At the end of a quantization group, per column (zero point z, scale s):
 //     sum_k x (q - z - 1) = Dlo - (1025 + z) Slo + (Dhi - (1040 + 16 z) Shi) / 16
 // and acc += s * that, in fp32.  Products on the tensor cores are exact; the
-// only rounding is fp32 accumulation.  The stage is released once the MMAs
+// only rounding is fp32 accumulation.
+// Group slots (M <= 4): an m16n8k16 MMA has 8 B columns and M rows of x use
+// only MP of them (MP = M rounded up to a power of two).  The other columns
+// then carry the next groups: B column c holds x row c % MP while the
+// slice is in its (c / MP)-th group of the current batch of 8 / MP groups,
+// and zeros otherwise.  So D, Slo and Shi keep each group of a batch apart,
+// and the per-group step above runs once per batch instead of once per
+// group.  At the end the slots of each row are summed across the lanes.  The stage is released once the MMAs
 // have consumed every register loaded from it, so no load of it can still
 // be outstanding when the producer refills it.
 // Every mbarrier wait is bounded (~2 s); a wait that runs out records an
@@ -37,6 +44,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstdint>
 
 #include "q4_internal.cuh"
@@ -112,9 +120,11 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
-template <int MT>
+template <int MT, int MP>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_ring_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, RingArgs a) {
+    static_assert(MP == 8 || (MT == 1 && (MP == 1 || MP == 2 || MP == 4)), "group slots need one m tile");
+    constexpr int kSlots = 8 / MP;                   // groups per batch
     using C = RingCfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -228,58 +238,69 @@ __global__ void __launch_bounds__(kThreads, 3)
                 }
         };
         clear_partials();
-        // per tile and column (gq / gq+8): scale, -(1025 + z), -(65 + z)
-        float sc[kTPW][2], czl[kTPW][2], czh[kTPW][2];
-        auto load_group = [&](int gl) {
-            const uint32_t gb = szb + gl * kSzGroupBytes;
+        // The batch's groups start at slice group gb0.  Accumulator element
+        // i of a lane sits in B column 2 tq + (i & 1), i.e. slot
+        // (2 tq + (i & 1)) / MP; with MP >= 2 both elements of a lane share
+        // one slot, with MP = 1 they are two.  Per slot and column (gq,
+        // gq + 8): scale s, -(1024 + z), -(64 + z).  A slot past the slice's
+        // last group has all-zero partials; it reads the last group's
+        // constants (finite), so it adds exactly zero.
+        int gb0 = 0;
+        auto flush = [&]() {
+            constexpr int kLaneSlots = MP == 1 ? 2 : 1;
 #pragma unroll
             for (int t = 0; t < kTPW; ++t) {
                 const int nt = kTPW * warp + t;
-                const uint32_t sp = ld_shared_u32(gb + (nt * 8 + gq) * 4);
-                const uint32_t zw0 = ld_shared_u32(gb + 256 + nt * 8);
-                const uint32_t zw1 = ld_shared_u32(gb + 256 + nt * 8 + 4);
-                sc[t][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
-                sc[t][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                // effective zero points (stored + zero_offset) of columns gq, gq + 8
-                const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + a.zero_offset);
-                const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + a.zero_offset);
-                czl[t][0] = -(1024.f + z0);
-                czl[t][1] = -(1024.f + z1);
-                czh[t][0] = -(64.f + z0);
-                czh[t][1] = -(64.f + z1);
+#pragma unroll
+                for (int j = 0; j < kLaneSlots; ++j) {
+                    const int gle = min(gb0 + (2 * tq + j) / MP, ng - 1);
+                    const uint32_t gb = szb + gle * kSzGroupBytes;
+                    const uint32_t sp = ld_shared_u32(gb + (nt * 8 + gq) * 4);
+                    const uint32_t zw0 = ld_shared_u32(gb + 256 + nt * 8);
+                    const uint32_t zw1 = ld_shared_u32(gb + 256 + nt * 8 + 4);
+                    float sc[2], czl[2], czh[2];
+                    sc[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
+                    sc[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
+                    // effective zero points (stored + zero_offset) of columns gq, gq + 8
+                    const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + a.zero_offset);
+                    const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + a.zero_offset);
+                    czl[0] = -(1024.f + z0);
+                    czl[1] = -(1024.f + z1);
+                    czh[0] = -(64.f + z0);
+                    czh[1] = -(64.f + z1);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if (kLaneSlots == 2 && (i & 1) != j) continue;
+                            const int c = i >> 1;
+                            float p = fmaf(czl[c], slo[mt][i], dlo[t][mt][i]);
+                            p = fmaf(0.0625f, dhi[t][mt][i], p);
+                            p = fmaf(czh[c], shi[mt][i], p);
+                            acc[t][mt][i] = fmaf(sc[c], p, acc[t][mt][i]);
+                        }
+                }
             }
-        };
-        auto flush = [&]() {
-#pragma unroll
-            for (int t = 0; t < kTPW; ++t)
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int c = i >> 1;
-                        float p = fmaf(czl[t][c], slo[mt][i], dlo[t][mt][i]);
-                        p = fmaf(0.0625f, dhi[t][mt][i], p);
-                        p = fmaf(czh[t][c], shi[mt][i], p);
-                        acc[t][mt][i] = fmaf(sc[t][c], p, acc[t][mt][i]);
-                    }
             clear_partials();
         };
         // this lane's x row in each m tile and its 16-byte chunk of each
-        // 32-row block inside the 128-byte swizzled row (0xFFFFFFFF: row >= M)
+        // 32-row block inside the 128-byte swizzled row (0xFFFFFFFF: row >= M);
+        // with group slots, lane gq serves row gq % MP in slot gq / MP
         uint32_t xoff[2][MT];
+        const int my_slot = gq / MP;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                const int r = mt * 8 + gq;
+                const int r = mt * 8 + (MP == 8 ? gq : gq % MP);
                 xoff[hh][mt] = r < mrows ? static_cast<uint32_t>(r * 128 + ((((hh << 2) | tq) ^ (r & 7)) << 4))
                                          : 0xFFFFFFFFu;
             }
         constexpr uint32_t kOnes = 0x3C003C00u;
         const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
         int gl = 0;
+        int slot = 0;                                       // slot of group gl in its batch
         int left = a.bpg - (2 * kb_beg - g_beg * a.bpg);   // 32-row blocks left in the current group
-        if (wactive) load_group(0);
         int s = 0;
         uint32_t ph = 0;
         for (int i = 0; ok && i < nkb; ++i) {
@@ -295,15 +316,21 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     if (left == 0) {
-                        flush();
-                        load_group(++gl);
+                        ++gl;
+                        if (++slot == kSlots) {
+                            flush();
+                            gb0 = gl;
+                            slot = 0;
+                        }
                         left = a.bpg;
                     }
                     --left;
                     uint4 xb[MT];
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
-                        xb[mt] = xoff[hh][mt] != 0xFFFFFFFFu ? ld_shared_v4(st + xoff[hh][mt]) : make_uint4(0u, 0u, 0u, 0u);
+                        xb[mt] = xoff[hh][mt] != 0xFFFFFFFFu && (MP == 8 || my_slot == slot)
+                                     ? ld_shared_v4(st + xoff[hh][mt])
+                                     : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
                         mma_16816(slo[mt], ones, xb[mt].x, xb[mt].z);
@@ -332,7 +359,25 @@ __global__ void __launch_bounds__(kThreads, 3)
                 ph ^= 1;
             }
         }
-        if (wactive) flush();
+        if (wactive) {
+            flush();
+            if (MP < 8) {
+                // sum each row's slots: element i of lane tq is column
+                // 2 tq + (i & 1) = slot * MP + row
+#pragma unroll
+                for (int t = 0; t < kTPW; ++t) {
+                    float v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = acc[t][0][i] + (MP == 1 ? acc[t][0][i ^ 1] : 0.f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (MP <= 2) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
+                        v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], 2);
+                        acc[t][0][i] = v[i];            // valid where 2 tq + (i & 1) < MP
+                    }
+                }
+            }
+        }
     }
 
     // ------------------------------------------------------------ epilogue
@@ -387,11 +432,30 @@ __global__ void __launch_bounds__(kThreads, 3)
     cluster_sync();                                   // partials stay alive until all are read
 }
 
-template <int MT>
+template <int MT, int MP>
 cudaError_t ensure_attr() {
-    static cudaError_t e =
-        cudaFuncSetAttribute(decode_ring_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, RingCfg<MT>::kSmem);
+    static cudaError_t e = cudaFuncSetAttribute(decode_ring_kernel<MT, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                RingCfg<MT>::kSmem);
     return e;
+}
+
+// Rows of x per group slot for M rows (8: no slots)
+int slot_rows(int M, int mt) {
+    static const bool on = [] {
+        const char *v = getenv("GPTQ_Q4_RING_SLOTS");
+        return !(v && v[0] == '0');
+    }();
+    if (!on || mt != 1 || M > 4) return 8;
+    return M == 1 ? 1 : (M == 2 ? 2 : 4);
+}
+
+template <int MT, int MP>
+cudaError_t launch_variant(cudaLaunchConfig_t &cfg, const CUtensorMap &tmX, const CUtensorMap &tmW,
+                           const RingArgs &args) {
+    cudaError_t e;
+    if ((e = ensure_attr<MT, MP>()) != cudaSuccess) return e;
+    cfg.dynamicSmemBytes = RingCfg<MT>::kSmem;
+    return cudaLaunchKernelEx(&cfg, decode_ring_kernel<MT, MP>, tmX, tmW, args);
 }
 
 }  // namespace
@@ -405,7 +469,7 @@ int max_active_clusters(int sp) {
     static bool done = false;
     if (!done) {
         done = true;
-        if (ensure_attr<MT>() == cudaSuccess) {
+        if (ensure_attr<MT, 8>() == cudaSuccess) {
             for (int c = 1; c <= kMaxCluster; ++c) {
                 cudaLaunchConfig_t cfg{};
                 cfg.gridDim = dim3(1, c, 1);
@@ -419,7 +483,7 @@ int max_active_clusters(int sp) {
                 cfg.attrs = &attr;
                 cfg.numAttrs = 1;
                 int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, decode_ring_kernel<MT>, &cfg) != cudaSuccess) n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, decode_ring_kernel<MT, 8>, &cfg) != cudaSuccess) n = 0;
                 table[c] = n;
             }
         }
@@ -500,14 +564,13 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &p, con
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    if (p.mt == 1) {
-        if ((e = ensure_attr<1>()) != cudaSuccess) return e;
-        cfg.dynamicSmemBytes = RingCfg<1>::kSmem;
-        return cudaLaunchKernelEx(&cfg, decode_ring_kernel<1>, tmX, tmW, args);
+    if (p.mt == 2) return launch_variant<2, 8>(cfg, tmX, tmW, args);
+    switch (slot_rows(M, p.mt)) {
+        case 1: return launch_variant<1, 1>(cfg, tmX, tmW, args);
+        case 2: return launch_variant<1, 2>(cfg, tmX, tmW, args);
+        case 4: return launch_variant<1, 4>(cfg, tmX, tmW, args);
+        default: return launch_variant<1, 8>(cfg, tmX, tmW, args);
     }
-    if ((e = ensure_attr<2>()) != cudaSuccess) return e;
-    cfg.dynamicSmemBytes = RingCfg<2>::kSmem;
-    return cudaLaunchKernelEx(&cfg, decode_ring_kernel<2>, tmX, tmW, args);
 }
 
 }  // namespace q4

@@ -132,6 +132,10 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(shared_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's most recent copy groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Hardware barrier over every thread of every CTA of the cluster, with
 // release/acquire ordering of shared-memory writes across the cluster.
@@ -188,6 +192,7 @@ struct DecodePlan {
     size_t ws_floats;  // workspace needed (slices reduced through global memory)
     int n_tickets;
     int raw;           // 1: raw code pairs + sums of x (M <= 8); 0: exact (q - z - 1) pairs
+    int sr;            // 1: weight ring in shared memory; 0: in registers
     int one_wave;      // every CTA of the grid is resident at once
 };
 DecodePlan plan_decode(int M, int K, int N, int geff);

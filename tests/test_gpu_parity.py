@@ -88,11 +88,37 @@ def test_decode_matches_oracle(q4, K, N, gs, act, path):
     dq = oracle_dq(layer)
     mat = make(q4, layer)
     mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
-    for M in (1, 2, 3, 7, 8, 9, 16, 17, 33, 40):
+    for M in (1, 2, 3, 4, 7, 8, 9, 16, 17, 33, 40):
         x = synthetic.activations(M, K, key=(22, K, N, M))
         y = mat(to_dev(x))
         torch.cuda.synchronize()
         check_y(y, x, dq, layer.bias, K, f"{path} K={K} N={N} g={gs} act={act} M={M}")
+    mat.device_error()
+
+
+RING_SLOT_CASES = [  # (K, N, groupsize, act_order)
+    (4096, 256, 32, False),     # 16 groups per slice: two full batches of 8 group slots at M = 1
+    (2304, 192, 96, True),      # 320-row slices start inside groups; a 64-column last tile idles two warps
+    (1024, 128, -1, False),     # one group for the whole K
+    (6144, 128, 64, True),      # many groups, few tiles: the widest K split
+]
+
+
+@pytest.mark.parametrize("K,N,gs,act", RING_SLOT_CASES)
+def test_ring_group_slots_match_oracle(q4, K, N, gs, act):
+    """TMA-ring decode with M <= 4: spare MMA columns carry consecutive
+    quantization groups (a batch of 8 / MP groups per flush, MP = M rounded up
+    to a power of two), summed across lanes at the end; M = 5 and 8 run
+    without slots."""
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(27, K, N, gs & 0xFFFF, act))
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    mat.set_path(q4.GPTQ_Q4_PATH_DECODE_RING)
+    for M in (1, 2, 3, 4, 5, 8):
+        x = synthetic.activations(M, K, key=(27, K, N, M))
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, layer.bias, K, f"ring slots K={K} N={N} g={gs} act={act} M={M}")
     mat.device_error()
 
 
