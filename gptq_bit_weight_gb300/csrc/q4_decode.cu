@@ -58,7 +58,7 @@ namespace {
 #define Q4_DECODE_NTW 2
 #endif
 #ifndef Q4_DECODE_DEPTH
-#define Q4_DECODE_DEPTH 4
+#define Q4_DECODE_DEPTH 3
 #endif
 constexpr int kWarps = Q4_DECODE_WARPS;
 constexpr int kThreads = 32 * kWarps;
