@@ -437,8 +437,8 @@ def run_native(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved_gbs / hbm_gbs, "traffic": None,
-                         "kernel": ("decode_kernel<1,0|1> (register-streaming; M <= 4, and M = 8 on 4096x4096) and "
-                                    "decode_ring_kernel<1> (TMA ring; M = 8 on the other layers)"),
+                         "kernel": ("decode_kernel<1,*> (register-streaming with a shared-memory weight ring; "
+                                    "every decode_7b case)"),
                          "peak_source": peak_src,
                          "how": "algorithmic bytes of the timed region / its CUDA-event time (only decode kernels run in it)"},
             "eager": {"value": eager_value, "unit": "TB/s",

@@ -478,12 +478,13 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         return ok();
     }
     // Which decode kernel: measured on GB300 (CUDA-graph replays over more
-    // weights than L2), the register-streaming kernel is ahead on layers
-    // below 24 Mi weights, and at M <= 4 on layers below 64 Mi weights,
-    // where its smaller fixed cost per call outweighs the ring's faster
-    // streaming; the TMA-ring kernel is ahead everywhere else it applies.
+    // weights than L2), the register-streaming kernel (with its shared
+    // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
+    // layers below 64 Mi weights and at any M on layers below 24 Mi weights;
+    // the TMA-ring kernel is ahead everywhere else it applies.
     const size_t weights = static_cast<size_t>(h->K) * h->N;
-    const bool small_layer = weights < (size_t{24} << 20) || (M <= 4 && weights < (size_t{64} << 20));
+    const bool small_layer =
+        M <= 4 || weights < (size_t{24} << 20) || (M <= 8 && weights < (size_t{64} << 20));
     if ((path == GPTQ_Q4_PATH_DECODE && !small_layer) || path == GPTQ_Q4_PATH_DECODE_RING) {
         const q4::DecodeRingPlan rp = q4::plan_decode_ring(M, h->K, h->N, h->geff, q4::device_sm_count());
         if (rp.ok) {

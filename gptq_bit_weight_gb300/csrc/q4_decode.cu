@@ -65,8 +65,15 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kNTW = Q4_DECODE_NTW;             // 16-column tiles per CTA
 constexpr int kNB = 16 * kNTW;      // columns per CTA
 constexpr int kDepth = Q4_DECODE_DEPTH;         // shared ring: slots per warp (kDepth - 1 chunks in flight)
-constexpr int kRingWarpBytes = kDepth * kNTW * 512;   // one warp's ring (16 bytes per lane and tile)
+// A shared-ring slot: the chunk's packed words (16 bytes per lane and tile)
+// and its x fragments (8 rows x 64 fp16, 128 bytes per row).
+constexpr int kSlotBytes = kNTW * 512 + 8 * 128;
+constexpr int kRingWarpBytes = kDepth * kSlotBytes;
 constexpr int kRegDepth = 4;                    // register ring: chunks in flight per warp
+#ifndef Q4_DECODE_XSTAGE_BYTES
+#define Q4_DECODE_XSTAGE_BYTES 16384
+#endif
+constexpr long long kXStageBytes = Q4_DECODE_XSTAGE_BYTES;   // largest staged x slice with the shared ring
 constexpr int kMaxCluster = 8;      // portable thread-block cluster size
 // Shared words staged per group: kNTW*8 scale pairs, then kNTW*2 zero words,
 // padded to a multiple of 4 so every group's copies start 16-byte aligned.
@@ -92,11 +99,12 @@ __host__ __device__ inline int x_row_stride(int slice_chunks) { return slice_chu
 __host__ __device__ constexpr int warp_region_bytes(int mt, bool sr) {
     return sr ? kRingWarpBytes : kNTW * mt * 512;
 }
-// Shared memory: the warps' regions, the x slice, the slice's scale pairs
-// and zero words.
-__host__ __device__ inline size_t smem_bytes_for(int mt, bool sr, int xrows, int slice_chunks, int max_groups) {
+// Shared memory: the warps' regions, the staged x slice (none when the
+// shared ring carries x per chunk), the slice's scale pairs and zero words.
+__host__ __device__ inline size_t smem_bytes_for(int mt, bool sr, bool xr, int xrows, int slice_chunks, int max_groups) {
     return static_cast<size_t>(kWarps) * warp_region_bytes(mt, sr) +
-           static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2 + static_cast<size_t>(max_groups) * kGszStride * 4;
+           (xr ? 0 : static_cast<size_t>(xrows) * x_row_stride(slice_chunks) * 2) +
+           static_cast<size_t>(max_groups) * kGszStride * 4;
 }
 
 __host__ __device__ inline int max_groups_in_slice(int slice_chunks, int geff) {
@@ -113,8 +121,9 @@ constexpr int min_blocks(int mt, bool raw) { return min_warps(mt, raw) / kWarps 
 // pair) and the zero point is removed per group from MMA-accumulated sums of
 // x; otherwise each pair is turned into the exact fp16 (q - z - 1) first (one
 // LOP3 and one HFMA2).  Same result up to fp32 rounding.
-template <int MT, bool RAW, bool SR>
+template <int MT, bool RAW, bool SR, bool XR>
 __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(HandleView h, DecodeArgs a) {
+    static_assert(!XR || SR, "x rides in the shared ring only");
     static_assert(!RAW || MT == 1, "raw pairs: one m tile");
     constexpr int kRegion = warp_region_bytes(MT, SR);
     extern __shared__ __align__(16) unsigned char smem[];
@@ -132,9 +141,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     const int geff = h.geff;
 
     static_assert(kDepth >= 2 && kRegion >= kNTW * MT * 128 * 4, "a warp's region holds its partials at the end");
+    static_assert(!SR || MT == 1, "the shared ring serves one m tile");
     unsigned char *wring = smem;
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + kWarps * kRegion);
-    uint32_t *gsz = reinterpret_cast<uint32_t *>(smem + kWarps * kRegion + static_cast<size_t>(a.xrows) * XS * 2);
+    uint32_t *gsz = reinterpret_cast<uint32_t *>(smem + kWarps * kRegion + (XR ? 0 : static_cast<size_t>(a.xrows) * XS * 2));
 
     // Let the next kernel in the stream start its own prologue as soon as
     // every CTA of this grid is resident (programmatic dependent launch).
@@ -147,11 +157,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     const int g_base = (c_beg * 64) / geff;
 
     // ---- the slice's scale pairs / zero words (constant), then the first
-    //      kDepth - 1 chunks of this warp's packed weights into its ring
-    //      (handle-owned constant data, so both go out before the preceding
-    //      grid has finished), then x[m0 : m0 + mrows][slice] once it has.
-    //      Each is a group of asynchronous global->shared copies; a lane
-    //      later reads back exactly the 16-byte ring entries it copied.
+    //      chunks of this warp's packed weights (handle-owned constant data,
+    //      so both go out before the preceding grid has finished), then x
+    //      once it has.
     {
         const int g_beg = (c_beg * 64) / geff;
         const int g_end = (c_end * 64 - 1) / geff + 1;
@@ -171,7 +179,26 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         }
         cp_async_commit();
     }
-    unsigned char *myring = wring + warp * kRingWarpBytes + lane * 16;   // + (slot * kNTW + nt) * 512
+    // Shared ring: slot s of this warp holds at  s * kSlotBytes
+    //   + nt * 512 + lane * 16                      the lane's packed words of tile nt
+    //   + kNTW * 512 + gq * 128 + hh * 64 + tq * 16 its x fragment of row gq, half hh
+    //                                               (XR: x carried per chunk)
+    // Every lane copies exactly the pieces it later reads, so the ring needs
+    // no barrier; each chunk is one commit group.  Without XR the CTA stages
+    // its whole x slice once instead: better when that slice is short, since
+    // with XR every CTA asks for the same x line of a chunk at about the same
+    // time.
+    unsigned char *myring = wring + warp * kRingWarpBytes;
+    unsigned char *myw = myring + lane * 16;
+    unsigned char *myx = myring + kNTW * 512 + gq * 128 + tq * 16;
+    const bool xrow = gq < mrows;                       // this lane's x row exists
+    const uint16_t *xsrc = a.x + static_cast<size_t>(m0 + (xrow ? gq : 0)) * K + 8 * tq;
+    auto copy_x = [&](int slot, int chunk) {
+        if (xrow) {
+            cp_async_16(myx + slot * kSlotBytes, xsrc + chunk * 64);
+            cp_async_16(myx + slot * kSlotBytes + 64, xsrc + chunk * 64 + 32);
+        }
+    };
     const uint4 *wsrc[kNTW];
 #pragma unroll
     for (int nt = 0; nt < kNTW; ++nt) wsrc[nt] = h.wp + static_cast<size_t>(nt0 + nt) * KC * 32 + lane;
@@ -182,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
             if (i < wn)
 #pragma unroll
                 for (int nt = 0; nt < kNTW; ++nt)
-                    cp_async_16(myring + (i * kNTW + nt) * 512, wsrc[nt] + static_cast<size_t>(chunk_of(i)) * 32);
+                    cp_async_16(myw + i * kSlotBytes + nt * 512, wsrc[nt] + static_cast<size_t>(chunk_of(i)) * 32);
             cp_async_commit();
         }
     } else {
@@ -198,7 +225,14 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         // grid: wait for it (a no-op without programmatic dependent launch).
         asm volatile("griddepcontrol.wait;" ::: "memory");
         const int vpr = nch * 8;                        // 16-byte vectors per row
-        if (SR) {
+        if (XR) {
+            // x of the first kDepth - 1 chunks: one more group
+#pragma unroll
+            for (int i = 0; i < kDepth - 1; ++i)
+                if (i < wn) copy_x(i, chunk_of(i));
+            cp_async_commit();
+            cp_async_wait<kDepth>();                    // the scale/zero copies: the oldest group
+        } else if (SR) {
             // plain L2 loads, eight per thread in flight, so that waiting for
             // x does not wait for the weight copies
             const int total = mrows * vpr;
@@ -328,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
             xp[mt] = xs + (xv[mt] ? r : 0) * XS + 2 * (wc_beg - c_beg) * 32 + 8 * tq;
         }
 
+        const unsigned char *xcur = myx;               // shared ring: x fragments of the current chunk
         auto run_chunk = [&](int c, const uint4 (&w)[kNTW]) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -339,9 +374,13 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
                 --left;
                 uint4 xb[MT];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-                    xb[mt] = xv[mt] ? *reinterpret_cast<const uint4 *>(xp[mt] + (2 * c + hh) * 32)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+                for (int mt = 0; mt < MT; ++mt) {
+                    if (XR)
+                        xb[mt] = xrow ? *reinterpret_cast<const uint4 *>(xcur + hh * 64) : make_uint4(0u, 0u, 0u, 0u);
+                    else
+                        xb[mt] = xv[mt] ? *reinterpret_cast<const uint4 *>(xp[mt] + (2 * c + hh) * 32)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                }
                 if (RAW) {
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
@@ -381,17 +420,23 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         if (SR) {
             int rs = 0;                                 // ring slot of chunk c
             for (int c = 0; c < wn; ++c) {
-                cp_async_wait<kDepth - 2>();            // chunk c has landed
+                // chunk c has landed: the first waits for the prologue's x
+                // group as well (the most recent one)
+                if (XR && c == 0) cp_async_wait<0>();
+                else cp_async_wait<kDepth - 2>();
                 uint4 w[kNTW];
 #pragma unroll
-                for (int nt = 0; nt < kNTW; ++nt) w[nt] = *reinterpret_cast<const uint4 *>(myring + (rs * kNTW + nt) * 512);
+                for (int nt = 0; nt < kNTW; ++nt) w[nt] = *reinterpret_cast<const uint4 *>(myw + rs * kSlotBytes + nt * 512);
+                if (XR) xcur = myx + rs * kSlotBytes;
                 // refill the slot of chunk c - 1 (consumed) with chunk c + kDepth - 1
                 const int fs = rs == 0 ? kDepth - 1 : rs - 1;
-                if (c + kDepth - 1 < wn)
+                if (c + kDepth - 1 < wn) {
 #pragma unroll
                     for (int nt = 0; nt < kNTW; ++nt)
-                        cp_async_16(myring + (fs * kNTW + nt) * 512,
+                        cp_async_16(myw + fs * kSlotBytes + nt * 512,
                                     wsrc[nt] + static_cast<size_t>(chunk_of(c + kDepth - 1)) * 32);
+                    if (XR) copy_x(fs, chunk_of(c + kDepth - 1));
+                }
                 cp_async_commit();
                 rs = rs + 1 == kDepth ? 0 : rs + 1;
                 run_chunk(c, w);
@@ -496,11 +541,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     if (threadIdx.x == 0) a.tickets[tile_id] = 0;     // ready for the next call on this stream
 }
 
-template <int MT, bool RAW, bool SR>
+template <int MT, bool RAW, bool SR, bool XR>
 cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork &w, const uint16_t *x, int M,
                       uint16_t *out, cudaStream_t s) {
     const int xrows = M < 8 * MT ? M : 8 * MT;
-    const size_t smem = smem_bytes_for(MT, SR, xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
+    const size_t smem = smem_bytes_for(MT, SR, XR, xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
     // Opt in once to the largest dynamic shared memory the device allows
     // next to the kernel's static shared memory.
     static int max_dyn = -1;
@@ -509,10 +554,10 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
         cudaFuncAttributes fa{};
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT, RAW, SR>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT, RAW, SR, XR>);
         const int want = optin - static_cast<int>(fa.sharedSizeBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_kernel<MT, RAW, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+            e = cudaFuncSetAttribute(decode_kernel<MT, RAW, SR, XR>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
         if (e != cudaSuccess) return e;
         max_dyn = want;
     }
@@ -539,7 +584,7 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<MT, RAW, SR>, h, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<MT, RAW, SR, XR>, h, a);
 }
 
 }  // namespace
@@ -575,14 +620,22 @@ static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw, boo
     p.ctas_n = N / kNB;
     const int KC = K / 64;
     const int xrows = std::min(M, 8 * p.mt);
-    // x staging: xrows * slice * 64 fp16 <= 64 KB
-    const int max_slice = std::min(KC, std::max(8, std::min(64, 512 / xrows)));
+    // register ring: the x slice is staged, xrows * slice * 64 fp16 <= 64 KB.
+    // Shared ring: x is staged when its slice takes at most kXStageBytes
+    // (half that with at most one column tile per SM, where fewer CTAs share
+    // each x line and carrying x per chunk measured faster), else carried
+    // per chunk.
+    const int max_slice = sr ? KC : std::min(KC, std::max(8, std::min(64, 512 / xrows)));
+    auto xr_for = [&](int slice) {
+        const long long xb = static_cast<long long>(xrows) * slice * 128;
+        return sr && (xb > kXStageBytes || (p.ctas_n * p.zdim <= kSMs && xb > kXStageBytes / 2));
+    };
     const int base = p.ctas_n * p.zdim;
     const int min_splits = (KC + max_slice - 1) / max_slice;
     const int max_splits = std::max(min_splits, KC / 16);   // at least two chunks per warp
     auto slots_for = [&](int sp) {
         const int slice = (KC + sp - 1) / sp;
-        const size_t smem = smem_bytes_for(p.mt, sr, xrows, slice, max_groups_in_slice(slice, geff));
+        const size_t smem = smem_bytes_for(p.mt, sr, xr_for(slice), xrows, slice, max_groups_in_slice(slice, geff));
         return static_cast<long long>(kSMs) * resident_ctas(p.mt, raw, smem);
     };
     auto valid = [&](int sp) {
@@ -610,20 +663,21 @@ static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw, boo
     }
     p.slice_chunks = (KC + best - 1) / best;
     p.splits = (KC + p.slice_chunks - 1) / p.slice_chunks;
+    p.xr = xr_for(p.slice_chunks) ? 1 : 0;
     p.cluster = (p.splits > 1 && p.splits <= kMaxCluster) ? 1 : 0;
     p.n_tickets = base;
     p.ws_floats = (p.splits > 1 && !p.cluster) ? static_cast<size_t>(base) * p.splits * kNTW * p.mt * 128 : 0;
     p.one_wave = static_cast<long long>(base) * p.splits <=
                  static_cast<long long>(kSMs) *
-                     resident_ctas(p.mt, raw, smem_bytes_for(p.mt, sr, std::min(M, 8 * p.mt), p.slice_chunks,
+                     resident_ctas(p.mt, raw, smem_bytes_for(p.mt, sr, p.xr != 0, std::min(M, 8 * p.mt), p.slice_chunks,
                                                              max_groups_in_slice(p.slice_chunks, geff)));
     return p;
 }
 
-// Weight ring in shared memory for M <= Q4_DECODE_SR_MAX_M rows (a short x
-// slice leaves room for it), in registers otherwise.
+// Weight and x ring in shared memory for M <= Q4_DECODE_SR_MAX_M rows (one
+// m tile), in registers otherwise.
 #ifndef Q4_DECODE_SR_MAX_M
-#define Q4_DECODE_SR_MAX_M 4
+#define Q4_DECODE_SR_MAX_M 8
 #endif
 // M <= 8: the raw-pair arithmetic (fewer instructions, 2 CTAs per SM) when its
 // grid is a single wave, else the exact-pair arithmetic at 3 CTAs per SM,
@@ -643,10 +697,16 @@ cudaError_t launch_decode(const HandleView &h, const DecodePlan &p, const Decode
                           uint16_t *out, cudaStream_t s) {
     switch (p.mt) {
         case 1:
-            if (p.raw) return p.sr ? launch_mt<1, true, true>(h, p, w, x, M, out, s) : launch_mt<1, true, false>(h, p, w, x, M, out, s);
-            return p.sr ? launch_mt<1, false, true>(h, p, w, x, M, out, s) : launch_mt<1, false, false>(h, p, w, x, M, out, s);
-        case 2: return launch_mt<2, false, false>(h, p, w, x, M, out, s);
-        default: return launch_mt<4, false, false>(h, p, w, x, M, out, s);
+            if (p.raw) {
+                if (!p.sr) return launch_mt<1, true, false, false>(h, p, w, x, M, out, s);
+                return p.xr ? launch_mt<1, true, true, true>(h, p, w, x, M, out, s)
+                            : launch_mt<1, true, true, false>(h, p, w, x, M, out, s);
+            }
+            if (!p.sr) return launch_mt<1, false, false, false>(h, p, w, x, M, out, s);
+            return p.xr ? launch_mt<1, false, true, true>(h, p, w, x, M, out, s)
+                        : launch_mt<1, false, true, false>(h, p, w, x, M, out, s);
+        case 2: return launch_mt<2, false, false, false>(h, p, w, x, M, out, s);
+        default: return launch_mt<4, false, false, false>(h, p, w, x, M, out, s);
     }
 }
 

@@ -193,6 +193,7 @@ struct DecodePlan {
     int n_tickets;
     int raw;           // 1: raw code pairs + sums of x (M <= 8); 0: exact (q - z - 1) pairs
     int sr;            // 1: weight ring in shared memory; 0: in registers
+    int xr;            // shared ring: 1 x carried per chunk in the ring; 0 x slice staged once
     int one_wave;      // every CTA of the grid is resident at once
 };
 DecodePlan plan_decode(int M, int K, int N, int geff);

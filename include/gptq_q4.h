@@ -74,9 +74,10 @@ extern "C" {
 
 /* Paths gptq_q4_matmul can take (see gptq_q4_set_path). */
 #define GPTQ_Q4_PATH_AUTO      0  /* decode below the prefill threshold, fused prefill above */
-#define GPTQ_Q4_PATH_DECODE    1  /* always decode: the TMA-ring kernel for M <= 16 on layers of at
-                                     least 24 Mi weights (64 Mi when M <= 4) where the shape
-                                     allows it, the register-streaming kernel otherwise */
+#define GPTQ_Q4_PATH_DECODE    1  /* always decode: the register-streaming kernel at M <= 4, at
+                                     M <= 8 on layers below 64 Mi weights and on any layer below
+                                     24 Mi weights; the TMA-ring kernel (M <= 16) otherwise, where
+                                     the shape allows it */
 #define GPTQ_Q4_PATH_PREFILL   2  /* always the fused shared-memory-dequant tensor-core kernel */
 #define GPTQ_Q4_PATH_DECODE_MMA 3 /* always the register-streaming decode kernel */
 #define GPTQ_Q4_PATH_DECODE_TC 4  /* decode on tcgen05 with one tensor-memory accumulator per
@@ -150,9 +151,12 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m);
  * the zero point removed per group from MMA-accumulated sums of x; the K
  * slices of a 128-column tile (at most 8) are summed in slice order inside a
  * thread-block cluster.  The register-streaming kernel: packed weights
- * streamed with 128-bit loads straight into registers, exact (q - z - 1) in
- * fp16, fp32 accumulation on mma.sync, split-K summed in a fixed order
- * inside a cluster or, past eight slices, by the last CTA to finish.
+ * streamed with 128-bit loads, through a per-warp ring of asynchronous
+ * copies in shared memory at M <= 8 (x staged once per CTA, or carried with
+ * each chunk when the x slice is long) and straight into registers above,
+ * exact (q - z - 1) in fp16 (or raw code pairs with per-group sums of x),
+ * fp32 accumulation on mma.sync, split-K summed in a fixed order inside a
+ * cluster or, past eight slices, by the last CTA to finish.
  * GPTQ_Q4_PATH_DECODE_TC selects the
  * tcgen05 decode instead (M <= 16): packed weights streamed by TMA,
  * dequantized in shared memory to the exact integers (q - z - 1), one

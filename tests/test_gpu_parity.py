@@ -237,6 +237,16 @@ def test_decode_7b_workload(q4, K, N):
         y = mat(to_dev(x))
         torch.cuda.synchronize()
         check_y(y, x, dq, layer.bias, K, f"decode_7b {K}x{N} M={M}")
+    # the register-streaming kernel at every M <= 8 it serves: shared weight
+    # ring with the x slice staged (short x slices) or carried per chunk
+    # (long ones), and the raw-pair variant where its grid is one wave
+    mat.set_path(q4.GPTQ_Q4_PATH_DECODE_MMA)
+    for M in (1, 2, 3, 5, 8):
+        x = synthetic.activations(M, K, key=(28, K, N, M))
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, layer.bias, K, f"register decode {K}x{N} M={M}")
+    mat.device_error()
 
 
 @pytest.mark.parametrize("K,N", synthetic.ACTORDER_7B_SHAPES)
