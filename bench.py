@@ -83,6 +83,13 @@ def run_single(spec: str) -> None:
     print(json.dumps({"single": spec, "max_abs_y": float(y.float().abs().max())}))
 
 
+# DRAM bytes the decode kernels move per algorithmic byte, from an ncu launch
+# list of the decode_7b leg (dram__bytes_read.sum + dram__bytes_write.sum over
+# 1216 launches / their K*N/2 + G*N*2.5 bytes); the kernels read every packed
+# word, scale and zero once.
+DECODE_DRAM_PER_ALGORITHMIC_BYTE = 24946.7e6 / 24841.4e6
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -436,7 +443,11 @@ def run_native(args):
                        "bytes_per_step": step_bytes, "soak_s": args.soak_s,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": achieved_gbs / hbm_gbs, "traffic": None,
+                         "frac": achieved_gbs / hbm_gbs,
+                         # DRAM bytes (read + write) per step: the algorithmic bytes times the ratio
+                         # ncu measured over every decode_7b launch of the bench
+                         "traffic": round(step_bytes * DECODE_DRAM_PER_ALGORITHMIC_BYTE),
+                         "traffic_unit": "bytes per step",
                          "kernel": ("decode_kernel<1,*> (register-streaming with a shared-memory weight ring; "
                                     "every decode_7b case)"),
                          "peak_source": peak_src,
