@@ -298,6 +298,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         // the effective zero point of columns gq, gq + 8.
         float sc[kNTW][2], czl[kNTW][2], czh[kNTW][2];
         uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
+        // neg_zlo / neg_zhi of (stored zero + zero_offset - 1) = stored zero
+        // times the pair stride plus these (32-bit wrap-around included)
+        const uint32_t lo_base = neg_zlo(static_cast<uint32_t>(h.zero_offset) - 1u);
+        const uint32_t hi_base = neg_zhi(static_cast<uint32_t>(h.zero_offset) - 1u);
         auto load_group = [&](int gl) {
             const uint32_t *base = gsz + gl * kGszStride;
 #pragma unroll
@@ -306,18 +310,19 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
                 const uint32_t zw0 = base[kNTW * 8 + nt * 2], zw1 = base[kNTW * 8 + nt * 2 + 1];
                 sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                const uint32_t z0 = ((zw0 >> (4 * gq)) & 0xFu) + h.zero_offset;
-                const uint32_t z1 = ((zw1 >> (4 * gq)) & 0xFu) + h.zero_offset;
+                const uint32_t z0s = (zw0 >> (4 * gq)) & 0xFu, z1s = (zw1 >> (4 * gq)) & 0xFu;   // stored
+                const uint32_t z0 = z0s + h.zero_offset, z1 = z1s + h.zero_offset;
                 if (RAW) {
                     czl[nt][0] = -(1024.f + static_cast<float>(z0));
                     czl[nt][1] = -(1024.f + static_cast<float>(z1));
                     czh[nt][0] = -(64.f + static_cast<float>(z0));
                     czh[nt][1] = -(64.f + static_cast<float>(z1));
                 } else {
-                    nzlo[nt][0] = neg_zlo(z0 - 1u);
-                    nzhi[nt][0] = neg_zhi(z0 - 1u);
-                    nzlo[nt][1] = neg_zlo(z1 - 1u);
-                    nzhi[nt][1] = neg_zhi(z1 - 1u);
+                    // unpack_qz constants of (effective zero) - 1, one multiply-add each
+                    nzlo[nt][0] = z0s * 0x00010001u + lo_base;
+                    nzhi[nt][0] = z0s * 0x00100010u + hi_base;
+                    nzlo[nt][1] = z1s * 0x00010001u + lo_base;
+                    nzhi[nt][1] = z1s * 0x00100010u + hi_base;
                 }
             }
         };
@@ -418,28 +423,43 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
             }
         };
         if (SR) {
-            int rs = 0;                                 // ring slot of chunk c
-            for (int c = 0; c < wn; ++c) {
-                // chunk c has landed: the first waits for the prologue's x
-                // group as well (the most recent one)
-                if (XR && c == 0) cp_async_wait<0>();
-                else cp_async_wait<kDepth - 2>();
-                uint4 w[kNTW];
+            // sources of the next chunk to request, c + kDepth - 1
+            const uint4 *wnext[kNTW];
 #pragma unroll
-                for (int nt = 0; nt < kNTW; ++nt) w[nt] = *reinterpret_cast<const uint4 *>(myw + rs * kSlotBytes + nt * 512);
-                if (XR) xcur = myx + rs * kSlotBytes;
-                // refill the slot of chunk c - 1 (consumed) with chunk c + kDepth - 1
-                const int fs = rs == 0 ? kDepth - 1 : rs - 1;
-                if (c + kDepth - 1 < wn) {
+            for (int nt = 0; nt < kNTW; ++nt) wnext[nt] = wsrc[nt] + static_cast<size_t>(chunk_of(kDepth - 1)) * 32;
+            const uint16_t *xnext = xsrc + chunk_of(kDepth - 1) * 64;
+            for (int base = 0; base < wn; base += kDepth) {
 #pragma unroll
-                    for (int nt = 0; nt < kNTW; ++nt)
-                        cp_async_16(myw + fs * kSlotBytes + nt * 512,
-                                    wsrc[nt] + static_cast<size_t>(chunk_of(c + kDepth - 1)) * 32);
-                    if (XR) copy_x(fs, chunk_of(c + kDepth - 1));
+                for (int i = 0; i < kDepth; ++i) {       // chunk c sits in slot i = c % kDepth
+                    const int c = base + i;
+                    if (c < wn) {
+                        // chunk c has landed: the first waits for the prologue's
+                        // x group as well (the most recent one)
+                        if (XR && c == 0) cp_async_wait<0>();
+                        else cp_async_wait<kDepth - 2>();
+                        uint4 w[kNTW];
+#pragma unroll
+                        for (int nt = 0; nt < kNTW; ++nt)
+                            w[nt] = *reinterpret_cast<const uint4 *>(myw + i * kSlotBytes + nt * 512);
+                        if (XR) xcur = myx + i * kSlotBytes;
+                        // refill the slot of chunk c - 1 (consumed) with chunk c + kDepth - 1
+                        const int fs = (i + kDepth - 1) % kDepth;
+                        if (c + kDepth - 1 < wn) {
+#pragma unroll
+                            for (int nt = 0; nt < kNTW; ++nt) {
+                                cp_async_16(myw + fs * kSlotBytes + nt * 512, wnext[nt]);
+                                wnext[nt] += 32;
+                            }
+                            if (XR && xrow) {
+                                cp_async_16(myx + fs * kSlotBytes, xnext);
+                                cp_async_16(myx + fs * kSlotBytes + 64, xnext + 32);
+                            }
+                            xnext += 64;
+                        }
+                        cp_async_commit();
+                        run_chunk(c, w);
+                    }
                 }
-                cp_async_commit();
-                rs = rs + 1 == kDepth ? 0 : rs + 1;
-                run_chunk(c, w);
             }
         } else {
             for (int base = 0; base < wn; base += kRegDepth) {
