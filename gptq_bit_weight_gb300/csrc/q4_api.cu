@@ -246,14 +246,24 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
 
     // act-order: one stable argsort of g_idx (a counting sort by group keeps
     // the original order inside each group), identity -> no act-order.
+    // Groups of unequal size, or of a size that is not whole 32-row blocks,
+    // are each padded to gpad rows (the largest group rounded up to 32-row
+    // blocks): padding rows carry code 0 and perm = -1, and the x gather
+    // writes 0 there, so they add nothing.
     std::vector<int32_t> perm;
     bool act = false;
-    if (g_idx) {
+    int gpad = geff;           // rows per group in the private layout
+    int Kp = K;                // rows of the private layout
+    if (g_idx || geff % 32) {
         std::vector<int32_t> gi(K);
-        cudaError_t e = cudaMemcpy(gi.data(), g_idx, sizeof(int32_t) * K, cudaMemcpyDeviceToHost);
-        if (e != cudaSuccess) {
-            cuda_fail(e, "copying g_idx to the host");
-            return nullptr;
+        if (g_idx) {
+            cudaError_t e = cudaMemcpy(gi.data(), g_idx, sizeof(int32_t) * K, cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) {
+                cuda_fail(e, "copying g_idx to the host");
+                return nullptr;
+            }
+        } else {
+            for (int k = 0; k < K; ++k) gi[k] = k / geff;
         }
         std::vector<int> count(G + 1, 0);
         for (int k = 0; k < K; ++k) {
@@ -263,28 +273,37 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
             }
             ++count[gi[k] + 1];
         }
+        bool uniform = true;
+        int largest = 0;
         for (int g = 0; g < G; ++g) {
-            if (count[g + 1] != geff) {
+            uniform = uniform && count[g + 1] == geff;
+            largest = std::max(largest, count[g + 1]);
+        }
+        if (!uniform || geff % 32) {
+            gpad = (largest + 31) / 32 * 32;
+            if ((static_cast<long long>(G) * gpad) % 64) gpad += 32;     // whole 64-row chunks
+            if (static_cast<long long>(G) * gpad > 4LL * K) {
                 set_status(GPTQ_Q4_UNSUPPORTED,
-                           "group %d holds %d rows; the GPU layout needs every group to hold exactly %d", g,
-                           count[g + 1], geff);
+                           "groups of unequal size (largest %d rows of %d) padded to %d rows each would make the "
+                           "packed layout more than 4x the checkpoint",
+                           largest, K, gpad);
                 return nullptr;
             }
-            count[g + 1] += count[g];
+            Kp = G * gpad;
         }
-        perm.resize(K);
-        for (int k = 0; k < K; ++k) perm[count[gi[k]]++] = k;
-        for (int k = 0; k < K; ++k)
-            if (perm[k] != k) {
-                act = true;
-                break;
-            }
+        // first padded row of each group, then the rows of each group in order
+        std::vector<int> next(G);
+        for (int g = 0; g < G; ++g) next[g] = g * gpad;
+        perm.assign(Kp, -1);
+        for (int k = 0; k < K; ++k) perm[next[gi[k]]++] = k;
+        act = Kp != K;
+        for (int j = 0; j < K && !act; ++j) act = perm[j] != j;
     }
-    if (K % 64 || N % 64 || geff % 32) {
+    if (K % 64 || N % 64 || gpad % 32) {
         set_status(GPTQ_Q4_UNSUPPORTED,
                    "the GPU kernels need K %% 64 == 0, N %% 64 == 0 and a group size that is a multiple of 32 "
                    "(K=%d N=%d group=%d)",
-                   K, N, geff);
+                   K, N, gpad);
         return nullptr;
     }
 
@@ -294,10 +313,11 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
         return nullptr;
     }
     h->device = dev;
-    h->K = K;
+    h->K = Kp;
+    h->Kx = K;
     h->N = N;
     h->groupsize = groupsize;
-    h->geff = geff;
+    h->geff = gpad;
     h->G = G;
     h->act_order = act ? 1 : 0;
     h->prefill_min_m = q4::prefill_default_min_m();
@@ -313,23 +333,23 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
         std::memcpy(t_msg, msg, sizeof(msg));
         return nullptr;
     };
-    const size_t words = static_cast<size_t>(K / 8) * N;
+    const size_t words = static_cast<size_t>(Kp / 8) * N;
     if (dev_alloc(&h->wp, words, h, "allocating packed weights") ||
         dev_alloc(&h->s2, static_cast<size_t>(G) * (N / 16) * 8, h, "allocating scales") ||
         dev_alloc(&h->zeros, static_cast<size_t>(G) * (N / 8), h, "allocating zeros") ||
         dev_alloc(&h->status, 1, h, "allocating status word") ||
-        (act && dev_alloc(&h->perm, static_cast<size_t>(K), h, "allocating permutation")))
+        (act && dev_alloc(&h->perm, static_cast<size_t>(Kp), h, "allocating permutation")))
         return fail(0);
     cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
     if (e != cudaSuccess) return fail(cuda_fail(e, "cudaStreamCreate"));
     if ((e = cudaMemsetAsync(h->status, 0, sizeof(int), s)) != cudaSuccess) return fail(cuda_fail(e, "memset"));
-    if (act && (e = cudaMemcpyAsync(h->perm, perm.data(), sizeof(int32_t) * K, cudaMemcpyHostToDevice, s)) !=
+    if (act && (e = cudaMemcpyAsync(h->perm, perm.data(), sizeof(int32_t) * Kp, cudaMemcpyHostToDevice, s)) !=
                    cudaSuccess)
         return fail(cuda_fail(e, "copying the permutation"));
     if ((e = cudaMemcpyAsync(h->zeros, qzeros, sizeof(uint32_t) * G * (N / 8), cudaMemcpyDeviceToDevice, s)) !=
         cudaSuccess)
         return fail(cuda_fail(e, "copying qzeros"));
-    if ((e = q4::launch_repack_codes(qweight, act ? h->perm : nullptr, K, N, h->wp, s)) != cudaSuccess)
+    if ((e = q4::launch_repack_codes(qweight, act ? h->perm : nullptr, Kp, N, h->wp, s)) != cudaSuccess)
         return fail(cuda_fail(e, "repack launch"));
     if ((e = q4::launch_repack_scales(scales, G, N, h->s2, s)) != cudaSuccess)
         return fail(cuda_fail(e, "scale repack launch"));
@@ -337,7 +357,7 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(cuda_fail(e, "repack"));
     cudaStreamDestroy(s);
     s = nullptr;
-    const q4::DecodePlan p = q4::plan_decode(decode_max_ws_rows(), K, N, geff);
+    const q4::DecodePlan p = q4::plan_decode(decode_max_ws_rows(), Kp, N, gpad);
     if (ensure_decode_work(h, p.ws_floats, p.n_tickets, nullptr, true)) return fail(0);
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail(cuda_fail(e, "make"));
     ok();
@@ -460,7 +480,7 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
     const uint16_t *xin = x;
     if (h->act_order) {
         if (int r = ensure_temp_state(h, M, stream, false)) return r;
-        Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->K, h->temp_state, stream), "xreorder launch");
+        Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, h->temp_state, stream), "xreorder launch");
         ++g_launches;
         xin = h->temp_state;
     }
@@ -558,7 +578,7 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must be a 16-byte aligned device buffer");
     Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
     ++g_launches;
-    Q4_CUDA(q4::launch_gemm_f16(x, temp_dq, h->bias, M, h->K, h->N, out, h->status, stream), "gemm launch");
+    Q4_CUDA(q4::launch_gemm_f16(x, temp_dq, h->bias, M, h->Kx, h->N, out, h->status, stream), "gemm launch");
     ++g_launches;
     return ok();
 }
@@ -636,7 +656,7 @@ int gptq_q4_set_format(gptq_q4_handle h, int format) {
 
 int gptq_q4_info(gptq_q4_handle h, int *K, int *N, int *groupsize, int *G, int *act_order, size_t *device_bytes) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
-    if (K) *K = h->K;
+    if (K) *K = h->Kx;
     if (N) *N = h->N;
     if (groupsize) *groupsize = h->groupsize;
     if (G) *G = h->G;

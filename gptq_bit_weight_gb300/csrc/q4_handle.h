@@ -8,7 +8,8 @@
 
 struct gptq_q4_s {
     int device = -1;
-    int K = 0, N = 0, groupsize = 0, geff = 0, G = 0;
+    int K = 0, N = 0, groupsize = 0, geff = 0, G = 0;   // K, geff: rows and rows per group of the private layout
+    int Kx = 0;             // the caller's K (columns of x); K > Kx when groups are padded
     int act_order = 0;
     uint32_t *wp = nullptr;
     uint32_t *s2 = nullptr;

@@ -178,7 +178,9 @@ cudaError_t launch_repack_codes(const int32_t *qweight, const int32_t *perm, int
 cudaError_t launch_repack_scales(const uint16_t *scales, int G, int N, uint32_t *s2, cudaStream_t s);
 cudaError_t launch_debug_unpack(const HandleView &h, uint8_t *q, uint8_t *z, cudaStream_t s);
 cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t s);
-cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K,
+// temp_state[m][j] = x[m][perm[j]] (0 where perm[j] = -1); x rows hold Kx
+// values, temp_state rows K
+cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int Kx, int K,
                             uint16_t *temp_state, cudaStream_t s);
 
 // decode (q4_decode.cu)

@@ -19,7 +19,8 @@ namespace q4 {
 // One thread per private word.  Each of its eight rows (permuted order) is
 // looked up in the checkpoint through P, its nibble extracted and placed at
 // nib_pos(r).  Rows of one act-order word come from different checkpoint
-// words, so the codes are unpacked and repacked one by one.
+// words, so the codes are unpacked and repacked one by one.  P[j] = -1 marks
+// a padding row (groups of unequal size padded to a common length): code 0.
 __global__ void repack_codes_kernel(const int32_t *__restrict__ qweight, const int32_t *__restrict__ perm,
                                     int K, int N, uint32_t *__restrict__ wp) {
     const int KC = K / 64;
@@ -38,6 +39,7 @@ __global__ void repack_codes_kernel(const int32_t *__restrict__ qweight, const i
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
             const int k = perm ? perm[kb + r] : kb + r;
+            if (k < 0) continue;                        // a padding row: code 0 (x is 0 there)
             const uint32_t word = static_cast<uint32_t>(qweight[static_cast<size_t>(k >> 3) * N + n]);
             const uint32_t code = (word >> (4 * (k & 7))) & 0xFu;
             out |= code << (4 * nib_pos(r));
@@ -100,7 +102,7 @@ __global__ void debug_unpack_kernel(HandleView h, uint8_t *__restrict__ q, uint8
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int k = h.perm ? h.perm[kb + r] : kb + r;
-                q[static_cast<size_t>(k) * N + n] = static_cast<uint8_t>((w >> (4 * nib_pos(r))) & 0xFu);
+                if (k >= 0) q[static_cast<size_t>(k) * N + n] = static_cast<uint8_t>((w >> (4 * nib_pos(r))) & 0xFu);
             }
         }
     }
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(HandleView h, uint16_t *__
             const int jrow = 64 * kc + row;
             const int k = h.perm ? h.perm[jrow] : jrow;
             const uint4 v = *reinterpret_cast<const uint4 *>(&tile[row][8 * c8]);
-            *reinterpret_cast<uint4 *>(out + static_cast<size_t>(k) * N + 64 * n64 + 8 * c8) = v;
+            if (k >= 0) *reinterpret_cast<uint4 *>(out + static_cast<size_t>(k) * N + 64 * n64 + 8 * c8) = v;
         }
         __syncthreads();
     }
@@ -185,23 +187,30 @@ cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t 
 }
 
 // ------------------------------------------------------------- xreorder
-// temp_state[m][j] = x[m][P[j]]: eight consecutive j per thread, written as
-// one 16-byte store; the gathered reads come from the small x (L2-resident).
-__global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int K,
-                                uint16_t *__restrict__ ts) {
+// temp_state[m][j] = x[m][P[j]] (0 where P[j] = -1, a padding row): eight
+// consecutive j per thread, written as one 16-byte store; the gathered reads
+// come from the small x (L2-resident).  x rows hold Kx values, temp_state
+// rows K >= Kx.
+__device__ __forceinline__ uint32_t gather2(const uint16_t *xr, int pa, int pb) {
+    const uint32_t a = pa >= 0 ? xr[pa] : 0u, b = pb >= 0 ? xr[pb] : 0u;
+    return a | (b << 16);
+}
+
+__global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int Kx,
+                                int K, uint16_t *__restrict__ ts) {
     const size_t total = static_cast<size_t>(M) * (K / 8);
     for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const size_t m = idx / (K / 8);
         const int j0 = static_cast<int>(idx % (K / 8)) * 8;
-        const uint16_t *xr = x + m * K;
+        const uint16_t *xr = x + m * Kx;
         const int4 p0 = *reinterpret_cast<const int4 *>(perm + j0);
         const int4 p1 = *reinterpret_cast<const int4 *>(perm + j0 + 4);
         uint4 v;
-        v.x = static_cast<uint32_t>(xr[p0.x]) | (static_cast<uint32_t>(xr[p0.y]) << 16);
-        v.y = static_cast<uint32_t>(xr[p0.z]) | (static_cast<uint32_t>(xr[p0.w]) << 16);
-        v.z = static_cast<uint32_t>(xr[p1.x]) | (static_cast<uint32_t>(xr[p1.y]) << 16);
-        v.w = static_cast<uint32_t>(xr[p1.z]) | (static_cast<uint32_t>(xr[p1.w]) << 16);
+        v.x = gather2(xr, p0.x, p0.y);
+        v.y = gather2(xr, p0.z, p0.w);
+        v.z = gather2(xr, p1.x, p1.y);
+        v.w = gather2(xr, p1.z, p1.w);
         *reinterpret_cast<uint4 *>(ts + m * K + j0) = v;
     }
 }
@@ -211,50 +220,50 @@ __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *_
 // gathered 16-byte writes are coalesced (the gather itself hits shared
 // memory).  Rows are taken round-robin by the CTAs.
 __global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__restrict__ x,
-                                                             const int32_t *__restrict__ perm, int M, int K,
+                                                             const int32_t *__restrict__ perm, int M, int Kx, int K,
                                                              uint16_t *__restrict__ ts) {
     extern __shared__ __align__(16) unsigned char sm[];
     int32_t *sp = reinterpret_cast<int32_t *>(sm);
     uint16_t *sx = reinterpret_cast<uint16_t *>(sm + static_cast<size_t>(K) * 4);
-    const int nv = K / 8;                                  // 16-byte vectors per row
+    const int nvx = Kx / 8, nv = K / 8;                    // 16-byte vectors per x row / temp_state row
     for (int i = threadIdx.x; i < K / 4; i += blockDim.x)
         reinterpret_cast<int4 *>(sp)[i] = reinterpret_cast<const int4 *>(perm)[i];
     for (int m = blockIdx.x; m < M; m += gridDim.x) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K);
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * Kx);
         __syncthreads();                                   // the previous row's gathers are done
-        for (int i = threadIdx.x; i < nv; i += blockDim.x) reinterpret_cast<uint4 *>(sx)[i] = xr[i];
+        for (int i = threadIdx.x; i < nvx; i += blockDim.x) reinterpret_cast<uint4 *>(sx)[i] = xr[i];
         __syncthreads();
         uint4 *out = reinterpret_cast<uint4 *>(ts + static_cast<size_t>(m) * K);
         for (int i = threadIdx.x; i < nv; i += blockDim.x) {
             const int4 p0 = reinterpret_cast<const int4 *>(sp)[2 * i];
             const int4 p1 = reinterpret_cast<const int4 *>(sp)[2 * i + 1];
             uint4 v;
-            v.x = static_cast<uint32_t>(sx[p0.x]) | (static_cast<uint32_t>(sx[p0.y]) << 16);
-            v.y = static_cast<uint32_t>(sx[p0.z]) | (static_cast<uint32_t>(sx[p0.w]) << 16);
-            v.z = static_cast<uint32_t>(sx[p1.x]) | (static_cast<uint32_t>(sx[p1.y]) << 16);
-            v.w = static_cast<uint32_t>(sx[p1.z]) | (static_cast<uint32_t>(sx[p1.w]) << 16);
+            v.x = gather2(sx, p0.x, p0.y);
+            v.y = gather2(sx, p0.z, p0.w);
+            v.z = gather2(sx, p1.x, p1.y);
+            v.w = gather2(sx, p1.z, p1.w);
             out[i] = v;
         }
     }
 }
 
-cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K, uint16_t *temp_state,
+cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
                             cudaStream_t s) {
-    const size_t rows_smem = static_cast<size_t>(K) * 6;   // permutation + one row
+    const size_t rows_smem = static_cast<size_t>(K) * 4 + static_cast<size_t>(Kx) * 2;   // permutation + one row
     if (M >= 32 && rows_smem <= 200 * 1024) {
         static cudaError_t attr =
             cudaFuncSetAttribute(xreorder_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (attr != cudaSuccess) return attr;
         const int per_sm = static_cast<int>((228 * 1024) / (rows_smem + 1024));
         const int ctas = std::min(M, kSMs * std::max(1, std::min(per_sm, 8)));
-        xreorder_rows_kernel<<<ctas, 256, rows_smem, s>>>(x, perm, M, K, temp_state);
+        xreorder_rows_kernel<<<ctas, 256, rows_smem, s>>>(x, perm, M, Kx, K, temp_state);
         return cudaGetLastError();
     }
     const size_t total = static_cast<size_t>(M) * (K / 8);
     const int threads = 256;
     const size_t want = (total + threads - 1) / threads;
     const int blocks = static_cast<int>(want < static_cast<size_t>(kSMs) * 16 ? want : static_cast<size_t>(kSMs) * 16);
-    xreorder_kernel<<<blocks > 0 ? blocks : 1, threads, 0, s>>>(x, perm, M, K, temp_state);
+    xreorder_kernel<<<blocks > 0 ? blocks : 1, threads, 0, s>>>(x, perm, M, Kx, K, temp_state);
     return cudaGetLastError();
 }
 

@@ -99,9 +99,14 @@ typedef struct gptq_q4_s *gptq_q4_handle;   /* opaque; owns device memory */
  * Validates the arguments; copies g_idx to the host, checks every entry is in
  * [0, G), and derives the act-order row permutation P with one stable argsort
  * (rows sorted by group, original order kept within a group).  An identity P
- * means no act-order.  Then repacks the codes, in P order, into a private
- * tile-ordered layout (same byte count as qweight), and the scales into a
- * private pairing; zero points keep the checkpoint layout.  All of it is
+ * means no act-order.  When the groups do not all hold the same whole number
+ * of 32-row blocks (g_idx with groups of unequal size, or a groupsize that is
+ * not a multiple of 32), every group is padded to the largest one rounded up
+ * to 32 rows: the padding rows hold code 0 and P = -1, and the activation
+ * gather writes 0 for them, so they add nothing to y.  Then repacks the codes,
+ * in P order, into a private tile-ordered layout (same byte count as qweight
+ * without padding), and the scales into a private pairing; zero points keep
+ * the checkpoint layout.  All of it is
  * copied into handle-owned device memory, so the caller may free or change its
  * tensors afterwards.  Also sizes the split-K workspace for M <= 16.
  * Synchronizes the device before returning.  The caller must have finished
@@ -112,9 +117,9 @@ typedef struct gptq_q4_s *gptq_q4_handle;   /* opaque; owns device memory */
  *                     != 0, groupsize not -1 and not a positive divisor of K,
  *                     a g_idx entry outside [0, G), a pointer that is not
  *                     device memory of the current device
- *   UNSUPPORTED       K % 64, N % 64 or (groupsize or K) % 32 != 0; an
- *                     act-order g_idx whose groups do not all hold exactly
- *                     groupsize rows; current device is not compute 10.3
+ *   UNSUPPORTED       K % 64 or N % 64 != 0; groups whose padding to the
+ *                     largest one would make the layout more than 4 x K
+ *                     rows; current device is not compute 10.3
  *   OUT_OF_MEMORY, CUDA_ERROR */
 gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros,
                             const uint16_t *scales, const int32_t *g_idx,

@@ -104,6 +104,24 @@ def make_layer(K: int, N: int, groupsize: int, *, act_order: bool = False,
     return LayerInputs(K, N, groupsize, qweight, qzeros, scales, g_idx, b, act_order)
 
 
+def uneven_group_index(K: int, G: int, key, empty_group: Optional[int] = None) -> np.ndarray:
+    """A g_idx whose G groups hold unequal numbers of rows, scattered over K.
+
+    Group sizes: K rows dealt to the groups with seeded random weights in
+    [0.3, 1.7] (and none to `empty_group`, if given); the rows of each group
+    are a seeded random subset of 0..K-1.
+    """
+    g = rng(*key)
+    w = g.uniform(0.3, 1.7, size=G)
+    if empty_group is not None:
+        w[empty_group] = 0.0
+    counts = np.floor(K * w / w.sum()).astype(np.int64)
+    for i in np.argsort(-w)[: K - int(counts.sum())]:
+        counts[i] += 1
+    groups = np.repeat(np.arange(G, dtype=np.int32), counts)
+    return groups[g.permutation(K)].astype(np.int32)
+
+
 def activations(M: int, K: int, g: Optional[np.random.Generator] = None, key=None) -> np.ndarray:
     """x ~ N(0, 1) rounded to fp16, shape [M, K]."""
     if g is None:

@@ -122,6 +122,69 @@ def test_ring_group_slots_match_oracle(q4, K, N, gs, act):
     mat.device_error()
 
 
+UNEVEN_CASES = [  # (K, N, groupsize, empty group)
+    (1024, 256, 128, None),
+    (2048, 320, 64, None),
+    (1024, 192, 256, 2),        # one group holds no row at all
+]
+
+
+@pytest.mark.parametrize("K,N,gs,empty", UNEVEN_CASES)
+def test_uneven_groups_match_oracle(q4, K, N, gs, empty):
+    """g_idx with groups of unequal size: the handle pads every group to the
+    largest one (whole 32-row blocks) with zero-x rows; codes, dequantized
+    weights and y on every path against the oracle, which takes any g_idx."""
+    import dataclasses
+    base = synthetic.make_layer(K, N, gs, bias=True, key=(29, K, N, gs))
+    gi = synthetic.uneven_group_index(K, K // gs, key=(29, K, gs), empty_group=empty)
+    assert len(set(np.bincount(gi, minlength=K // gs).tolist())) > 1
+    layer = dataclasses.replace(base, g_idx=gi, act_order=True)
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    info = mat.info()
+    assert info["K"] == K and info["act_order"]
+    q, z = mat.debug_unpack()
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), dq.q)
+    assert np.array_equal(z.cpu().numpy(), dq.z)
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "PREFILL"):
+        mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+        for M in (1, 5, 33, 300):
+            x = synthetic.activations(M, K, key=(29, K, N, M))
+            y = mat(to_dev(x))
+            torch.cuda.synchronize()
+            check_y(y, x, dq, layer.bias, K, f"uneven {path} K={K} N={N} g={gs} M={M}")
+    x = synthetic.activations(40, K, key=(29, K, N, 40))
+    yu = mat.matmul_unfused(to_dev(x))
+    torch.cuda.synchronize()
+    check_y(yu, x, dq, layer.bias, K, f"uneven unfused K={K} N={N} g={gs}")
+    mat.device_error()
+
+
+@pytest.mark.parametrize("act", [False, True])
+def test_groupsize_not_multiple_of_32(q4, act):
+    """groupsize 48: each group is padded to 64 rows inside the handle, with
+    or without act-order; every path against the oracle."""
+    K, N, gs = 960, 192, 48
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(30, K, N, gs, act))
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    assert mat.info()["K"] == K
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "PREFILL"):
+        mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+        for M in (1, 6, 40):
+            x = synthetic.activations(M, K, key=(30, K, N, M))
+            y = mat(to_dev(x))
+            torch.cuda.synchronize()
+            check_y(y, x, dq, layer.bias, K, f"g=48 {path} act={act} M={M}")
+    mat.device_error()
+
+
 V2_CASES = [  # (K, N, groupsize, act_order)
     (256, 128, 64, False),
     (1024, 448, 32, True),
@@ -286,9 +349,11 @@ def test_error_codes(q4):
     with pytest.raises(GPTQ4Error) as e:
         q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), gi.data_ptr(), 256, 256, 128)
     assert e.value.status == q4.GPTQ_Q4_INVALID_ARGUMENT
-    gi = (torch.arange(256, device=DEV, dtype=torch.int32) % 3 == 0).to(torch.int32)   # uneven groups
-    with pytest.raises(GPTQ4Error) as e:
-        q4.gptq_q4_make(qw.data_ptr(), qz.data_ptr(), sc.data_ptr(), gi.data_ptr(), 256, 256, 128)
+    gi = torch.zeros(256, dtype=torch.int32, device=DEV)   # eight groups of 32, all rows in the first:
+    qz8 = torch.zeros((8, 32), dtype=torch.int32, device=DEV)
+    sc8 = torch.ones((8, 256), dtype=torch.float16, device=DEV)
+    with pytest.raises(GPTQ4Error) as e:       # padding every group to 256 rows would be 8x the checkpoint
+        q4.gptq_q4_make(qw.data_ptr(), qz8.data_ptr(), sc8.data_ptr(), gi.data_ptr(), 256, 256, 32)
     assert e.value.status == q4.GPTQ_Q4_UNSUPPORTED
     host = np.zeros((32, 256), np.int32)
     with pytest.raises(GPTQ4Error) as e:       # host pointer
