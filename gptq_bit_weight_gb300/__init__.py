@@ -44,6 +44,7 @@ EXPORTED = [
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
     "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_make_fused", "gptq_q4_pack",
+    "gptq_q4_make8",
 ]
 
 _P = ctypes.c_void_p
@@ -58,6 +59,7 @@ def _sig(name, restype, *argtypes):
 
 
 _sig("gptq_q4_make", _P, _P, _P, _P, _P, _I, _I, _I)
+_sig("gptq_q4_make8", _P, _P, _P, _P, _P, _I, _I, _I)
 _sig("gptq_q4_set_bias", _I, _P, _P)
 _sig("gptq_q4_reserve", _I, _P, _I)
 _sig("gptq_q4_matmul", _I, _P, _P, _I, _P, _P)
@@ -101,6 +103,14 @@ def _check(rc: int) -> int:
 
 def gptq_q4_make(qweight: int, qzeros: int, scales: int, g_idx: int | None, K: int, N: int, groupsize: int) -> int:
     h = _lib.gptq_q4_make(qweight, qzeros, scales, g_idx or None, K, N, groupsize)
+    if not h:
+        raise GPTQ4Error(gptq_q4_last_status(), gptq_q4_last_error())
+    return h
+
+
+def gptq_q4_make8(qweight: int, qzeros: int, scales: int, g_idx: int | None, K: int, N: int, groupsize: int) -> int:
+    """An 8-bit GPTQ layer: qweight [K/4][N], qzeros [G][N/4] (device pointers)."""
+    h = _lib.gptq_q4_make8(qweight, qzeros, scales, g_idx or None, K, N, groupsize)
     if not h:
         raise GPTQ4Error(gptq_q4_last_status(), gptq_q4_last_error())
     return h
@@ -230,19 +240,21 @@ class Q4Matrix:
     of the Lorax ExLlama v1 layer).  Only moves pointers and shapes; the
     library does the work and copies what it keeps."""
 
-    def __init__(self, qweight, qzeros, scales, g_idx=None, bias=None, groupsize: int = 128):
+    def __init__(self, qweight, qzeros, scales, g_idx=None, bias=None, groupsize: int = 128, bits: int = 4):
         import torch
         assert qweight.is_cuda and qweight.dtype == torch.int32 and qweight.dim() == 2
-        K = qweight.shape[0] * 8
+        assert bits in (4, 8)
+        K = qweight.shape[0] * (32 // bits)
         N = qweight.shape[1]
         qweight, qzeros, scales = qweight.contiguous(), qzeros.contiguous(), scales.contiguous()
         assert scales.dtype == torch.float16
         g_idx = None if g_idx is None else g_idx.to(torch.int32).contiguous()
         torch.cuda.current_stream().synchronize()
-        self.K, self.N, self.groupsize = K, N, groupsize
+        self.K, self.N, self.groupsize, self.bits = K, N, groupsize, bits
         self.device = qweight.device
-        self.handle = gptq_q4_make(qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(),
-                                   None if g_idx is None else g_idx.data_ptr(), K, N, groupsize)
+        make = gptq_q4_make if bits == 4 else gptq_q4_make8
+        self.handle = make(qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(),
+                           None if g_idx is None else g_idx.data_ptr(), K, N, groupsize)
         if bias is not None:
             b = bias.to(torch.float16).contiguous()
             gptq_q4_set_bias(self.handle, b.data_ptr())

@@ -117,6 +117,7 @@ void release(gptq_q4_s *h) {
     cudaFree(h->s2);
     cudaFree(h->zeros);
     cudaFree(h->perm);
+    cudaFree(h->inv8);
     cudaFree(h->bias);
     cudaFree(h->status);
     cudaFree(h->ws);
@@ -137,6 +138,7 @@ q4::HandleView view(const gptq_q4_s *h) {
     v.s2 = h->s2;
     v.zeros = h->zeros;
     v.zero_offset = h->zero_offset;
+    v.zsplit = h->zsplit;
     v.perm = h->act_order ? h->perm : nullptr;
     v.bias = h->bias;
     v.status = h->status;
@@ -364,6 +366,116 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
     return h;
 }
 
+gptq_q4_handle gptq_q4_make8(const int32_t *qweight, const int32_t *qzeros, const uint16_t *scales,
+                             const int32_t *g_idx, int K, int N, int groupsize) {
+    if (!qweight || !qzeros || !scales) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "qweight, qzeros and scales must not be NULL");
+        return nullptr;
+    }
+    if (K <= 0 || N <= 0 || K % 8 || N % 8) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "K=%d and N=%d must be positive multiples of 8", K, N);
+        return nullptr;
+    }
+    if (!(groupsize == -1 || (groupsize > 0 && K % groupsize == 0))) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "groupsize=%d must be -1 or a positive divisor of K=%d", groupsize, K);
+        return nullptr;
+    }
+    const int geff = groupsize == -1 ? K : groupsize;
+    const int G = K / geff;
+    int dev = -1;
+    if (check_device_sm103(&dev) != GPTQ_Q4_OK) return nullptr;
+    if (check_device_ptr(qweight, dev, "qweight") || check_device_ptr(qzeros, dev, "qzeros") ||
+        check_device_ptr(scales, dev, "scales") || (g_idx && check_device_ptr(g_idx, dev, "g_idx")))
+        return nullptr;
+    if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, 2) || (g_idx && !aligned(g_idx, 4))) {
+        set_status(GPTQ_Q4_INVALID_ARGUMENT, "misaligned input pointer");
+        return nullptr;
+    }
+    // the groups of the split layer: row k -> g_idx[k], row K + k -> G + g_idx[k]
+    std::vector<int32_t> gi(2 * static_cast<size_t>(K));
+    if (g_idx) {
+        cudaError_t e = cudaMemcpy(gi.data(), g_idx, sizeof(int32_t) * K, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) {
+            cuda_fail(e, "copying g_idx to the host");
+            return nullptr;
+        }
+        for (int k = 0; k < K; ++k)
+            if (gi[k] < 0 || gi[k] >= G) {
+                set_status(GPTQ_Q4_INVALID_ARGUMENT, "g_idx[%d]=%d is outside [0, %d)", k, gi[k], G);
+                return nullptr;
+            }
+    } else {
+        for (int k = 0; k < K; ++k) gi[k] = k / geff;
+    }
+    for (int k = 0; k < K; ++k) gi[K + k] = G + gi[k];
+
+    // split checkpoint (temporary), then the ordinary 4-bit handle over 2K rows
+    int32_t *qw4 = nullptr, *qz4 = nullptr, *gi4 = nullptr;
+    uint16_t *sc4 = nullptr;
+    auto cleanup = [&]() {
+        cudaFree(qw4);
+        cudaFree(qz4);
+        cudaFree(sc4);
+        cudaFree(gi4);
+    };
+    if (dev_alloc(&qw4, static_cast<size_t>(2 * K / 8) * N, nullptr, "allocating the split codes") ||
+        dev_alloc(&qz4, static_cast<size_t>(2 * G) * (N / 8), nullptr, "allocating the split zeros") ||
+        dev_alloc(&sc4, static_cast<size_t>(2 * G) * N, nullptr, "allocating the split scales") ||
+        dev_alloc(&gi4, static_cast<size_t>(2 * K), nullptr, "allocating the split g_idx")) {
+        cleanup();
+        return nullptr;
+    }
+    cudaError_t e = cudaMemcpy(gi4, gi.data(), sizeof(int32_t) * 2 * K, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = q4::launch_split8(qweight, qzeros, scales, K, N, G, qw4, qz4, sc4, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cuda_fail(e, "splitting the 8-bit checkpoint");
+        cleanup();
+        return nullptr;
+    }
+    g_launches += 2;
+    gptq_q4_s *h = gptq_q4_make(qw4, qz4, sc4, gi4, 2 * K, N, geff);
+    cleanup();
+    if (!h) return nullptr;
+
+    // Private row order of the 2K split rows (the identity when make found no
+    // act-order), its inverse for the read-back kernels, and the column of x
+    // each private row reads: both halves read column k.
+    const int Kp = h->K;
+    std::vector<int32_t> perm(Kp);
+    if (h->act_order) e = cudaMemcpy(perm.data(), h->perm, sizeof(int32_t) * Kp, cudaMemcpyDeviceToHost);
+    else
+        for (int j = 0; j < Kp; ++j) perm[j] = j;
+    std::vector<int32_t> inv(2 * static_cast<size_t>(K), -1), xcol(Kp);
+    for (int j = 0; j < Kp; ++j) {
+        if (perm[j] >= 0) inv[perm[j]] = j;
+        xcol[j] = perm[j] < 0 ? -1 : perm[j] % K;
+    }
+    if (e == cudaSuccess && !h->act_order &&
+        dev_alloc(&h->perm, static_cast<size_t>(Kp), h, "allocating the activation gather") != GPTQ_Q4_OK) {
+        release(h);
+        return nullptr;
+    }
+    if (e == cudaSuccess && dev_alloc(&h->inv8, static_cast<size_t>(2 * K), h, "allocating the row map") != GPTQ_Q4_OK) {
+        release(h);
+        return nullptr;
+    }
+    if (e == cudaSuccess) e = cudaMemcpy(h->perm, xcol.data(), sizeof(int32_t) * Kp, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->inv8, inv.data(), sizeof(int32_t) * 2 * K, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "building the 8-bit row maps");
+        release(h);
+        return nullptr;
+    }
+    h->act_order = 1;
+    h->Kx = K;
+    h->groupsize = groupsize;
+    h->bits = 8;
+    h->zsplit = G;
+    ok();
+    return h;
+}
+
 gptq_q4_handle gptq_q4_make_fused(int parts, const int32_t *const *qweight, const int32_t *const *qzeros,
                                   const uint16_t *const *scales, const int32_t *g_idx, int K, const int *N,
                                   int groupsize) {
@@ -492,7 +604,7 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    if (path == GPTQ_Q4_PATH_DECODE_TC && q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
+    if (path == GPTQ_Q4_PATH_DECODE_TC && h->zsplit == 0 && q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
         Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
         ++g_launches;
         return ok();
@@ -543,7 +655,8 @@ int gptq_q4_dequant(gptq_q4_handle h, uint16_t *temp_dq, cudaStream_t stream) {
     if (int r = check_handle(h)) return r;
     if (!temp_dq) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must not be NULL");
     if (!aligned(temp_dq, 16)) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must be 16-byte aligned");
-    Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
+    if (h->bits == 8) Q4_CUDA(q4::launch_dequant8(view(h), h->inv8, h->Kx, temp_dq, stream), "dequant launch");
+    else Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
     ++g_launches;
     return ok();
 }
@@ -551,7 +664,8 @@ int gptq_q4_dequant(gptq_q4_handle h, uint16_t *temp_dq, cudaStream_t stream) {
 int gptq_q4_debug_unpack(gptq_q4_handle h, uint8_t *q, uint8_t *z, cudaStream_t stream) {
     if (int r = check_handle(h)) return r;
     if (!q && !z) return ok();
-    Q4_CUDA(q4::launch_debug_unpack(view(h), q, z, stream), "unpack launch");
+    if (h->bits == 8) Q4_CUDA(q4::launch_unpack8(view(h), h->inv8, h->Kx, h->zsplit, q, z, stream), "unpack launch");
+    else Q4_CUDA(q4::launch_debug_unpack(view(h), q, z, stream), "unpack launch");
     ++g_launches;
     return ok();
 }
@@ -576,7 +690,8 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
     if (M == 0) return ok();
     if (!temp_dq || !aligned(temp_dq, 16))
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "temp_dq must be a 16-byte aligned device buffer");
-    Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
+    if (h->bits == 8) Q4_CUDA(q4::launch_dequant8(view(h), h->inv8, h->Kx, temp_dq, stream), "dequant launch");
+    else Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
     ++g_launches;
     Q4_CUDA(q4::launch_gemm_f16(x, temp_dq, h->bias, M, h->Kx, h->N, out, h->status, stream), "gemm launch");
     ++g_launches;
@@ -659,7 +774,7 @@ int gptq_q4_info(gptq_q4_handle h, int *K, int *N, int *groupsize, int *G, int *
     if (K) *K = h->Kx;
     if (N) *N = h->N;
     if (groupsize) *groupsize = h->groupsize;
-    if (G) *G = h->G;
+    if (G) *G = h->bits == 8 ? h->zsplit : h->G;
     if (act_order) *act_order = h->act_order;
     if (device_bytes) *device_bytes = h->device_bytes;
     return ok();

@@ -298,12 +298,17 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         // the effective zero point of columns gq, gq + 8.
         float sc[kNTW][2], czl[kNTW][2], czh[kNTW][2];
         uint32_t nzlo[kNTW][2], nzhi[kNTW][2];
-        // neg_zlo / neg_zhi of (stored zero + zero_offset - 1) = stored zero
-        // times the pair stride plus these (32-bit wrap-around included)
-        const uint32_t lo_base = neg_zlo(static_cast<uint32_t>(h.zero_offset) - 1u);
-        const uint32_t hi_base = neg_zhi(static_cast<uint32_t>(h.zero_offset) - 1u);
+        // neg_zlo / neg_zhi of (stored zero + zero offset - 1) = stored zero
+        // times the pair stride plus these (32-bit wrap-around included); the
+        // groups below h.zsplit take zero offset 0
+        const uint32_t lo_base1 = neg_zlo(static_cast<uint32_t>(h.zero_offset) - 1u);
+        const uint32_t hi_base1 = neg_zhi(static_cast<uint32_t>(h.zero_offset) - 1u);
+        const uint32_t lo_base0 = neg_zlo(0xFFFFFFFFu), hi_base0 = neg_zhi(0xFFFFFFFFu);
         auto load_group = [&](int gl) {
             const uint32_t *base = gsz + gl * kGszStride;
+            const bool z0grp = g_base + gl < h.zsplit;
+            const uint32_t zoff = z0grp ? 0u : static_cast<uint32_t>(h.zero_offset);
+            const uint32_t lo_base = z0grp ? lo_base0 : lo_base1, hi_base = z0grp ? hi_base0 : hi_base1;
 #pragma unroll
             for (int nt = 0; nt < kNTW; ++nt) {
                 const uint32_t sp = base[nt * 8 + gq];
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
                 sc[nt][0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                 sc[nt][1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
                 const uint32_t z0s = (zw0 >> (4 * gq)) & 0xFu, z1s = (zw1 >> (4 * gq)) & 0xFu;   // stored
-                const uint32_t z0 = z0s + h.zero_offset, z1 = z1s + h.zero_offset;
+                const uint32_t z0 = z0s + zoff, z1 = z1s + zoff;
                 if (RAW) {
                     czl[nt][0] = -(1024.f + static_cast<float>(z0));
                     czl[nt][1] = -(1024.f + static_cast<float>(z1));

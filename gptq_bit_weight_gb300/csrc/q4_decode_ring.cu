@@ -97,6 +97,7 @@ struct RingArgs {
     const uint32_t *zeros;
     int bpg;             // 32-row blocks per group
     int zero_offset;     // effective zero = stored + zero_offset
+    int zsplit;          // groups [0, zsplit) take zero offset 0
     int slice_kb;        // stages per slice
     int splits;
 };
@@ -261,9 +262,10 @@ __global__ void __launch_bounds__(kThreads, 3)
                     float sc[2], czl[2], czh[2];
                     sc[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp & 0xFFFFu)));
                     sc[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sp >> 16)));
-                    // effective zero points (stored + zero_offset) of columns gq, gq + 8
-                    const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + a.zero_offset);
-                    const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + a.zero_offset);
+                    // effective zero points (stored + zero offset) of columns gq, gq + 8
+                    const uint32_t zoff = g_beg + gle < a.zsplit ? 0u : static_cast<uint32_t>(a.zero_offset);
+                    const float z0 = static_cast<float>(((zw0 >> (4 * gq)) & 0xFu) + zoff);
+                    const float z1 = static_cast<float>(((zw1 >> (4 * gq)) & 0xFu) + zoff);
                     czl[0] = -(1024.f + z0);
                     czl[1] = -(1024.f + z1);
                     czh[0] = -(64.f + z0);
@@ -543,7 +545,8 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &p, con
     if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
                        static_cast<uint64_t>(KC) * 512, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
-    RingArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, h.zero_offset, p.slice_kb, p.splits};
+    RingArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, h.zero_offset, h.zsplit,
+                  p.slice_kb, p.splits};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.tiles, p.splits, 1);
     cfg.blockDim = dim3(kThreads);

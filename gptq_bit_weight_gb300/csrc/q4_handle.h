@@ -15,6 +15,7 @@ struct gptq_q4_s {
     uint32_t *s2 = nullptr;
     uint32_t *zeros = nullptr;
     int32_t *perm = nullptr;
+    int32_t *inv8 = nullptr;    // 8-bit: private row of each split row (2 Kx entries)
     uint16_t *bias = nullptr;
     int *status = nullptr;
     float *ws = nullptr;
@@ -26,6 +27,8 @@ struct gptq_q4_s {
     int path = GPTQ_Q4_PATH_AUTO;
     int prefill_min_m = 0;
     int zero_offset = 1;    // GPTQ_Q4_FORMAT_GPTQ: effective zero = stored + 1
+    int bits = 4;           // 8: the handle holds an 8-bit layer as two 4-bit halves along K
+    int zsplit = 0;         // groups [0, zsplit) take zero offset 0 (8-bit: the high-nibble half)
     size_t device_bytes = 0;
 };
 

@@ -163,6 +163,8 @@ struct HandleView {
     const uint16_t *bias;   // device fp16 [N] or nullptr
     int *status;            // device status word
     int zero_offset;        // effective zero = stored + zero_offset (1: GPTQ, 0: GPTQ_V2)
+    int zsplit;             // groups [0, zsplit) take zero offset 0 instead (the high-nibble
+                            // half of an 8-bit layer), the rest zero_offset
 };
 
 struct DecodeWork {
@@ -243,6 +245,14 @@ cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws,
 cudaError_t launch_pack(const uint16_t *w, const uint16_t *scales, const int32_t *zeros, const int32_t *g_idx,
                         int K, int N, int geff, int G, int zero_offset, int32_t *qweight, int32_t *qzeros,
                         cudaStream_t s);
+// 8-bit layers as two 4-bit halves along K (q4_eight.cu): the split of the
+// checkpoint, and the read-back of codes / dequantized weights through the
+// inverse row map inv[k'] (private row of split row k')
+cudaError_t launch_split8(const int32_t *qw8, const int32_t *qz8, const uint16_t *sc, int K, int N, int G,
+                          int32_t *qw4, int32_t *qz4, uint16_t *sc4, cudaStream_t s);
+cudaError_t launch_unpack8(const HandleView &h, const int32_t *inv, int K8, int G8, uint8_t *q, uint8_t *z,
+                           cudaStream_t s);
+cudaError_t launch_dequant8(const HandleView &h, const int32_t *inv, int K8, uint16_t *temp_dq, cudaStream_t s);
 // test hook: a bounded mbarrier wait that runs out (q4_debug.cu)
 cudaError_t launch_wait_probe(int *status, uint64_t limit_ns, cudaStream_t s);
 

@@ -96,6 +96,7 @@ struct PfArgs {
     int bpg;                 // 32-row blocks per group
     int tiles_m, tiles_n;
     int zero_offset;         // effective zero = stored + zero_offset
+    int zsplit;              // groups [0, zsplit) take zero offset 0
     int splits;              // K slices per tile (> 1: one unit per CTA, cooperative launch)
     float *ws;               // fp32 partial tiles [tile][slice][BM][BN] when splits > 1
     int *tickets;            // one per tile, zero between calls
@@ -301,14 +302,15 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         const uint32_t sw0 = static_cast<uint32_t>((tq ^ gq) << 4);
         const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
         uint32_t c_s[2][2], c_nl[2][2], c_nh[2][2];   // [half J][column gq / gq+8]
-        auto load_consts = [&](const uint8_t *sz, int gl, int J) {
+        auto load_consts = [&](const uint8_t *sz, int gl, int J, int g) {   // g: the global group
             const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + gl * P::kSGroup + (wl * 8 + gq) * 4);
             const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + gl * P::kZGroup + wl * 8);
             c_s[J][0] = __byte_perm(sp, sp, 0x1010);
             c_s[J][1] = __byte_perm(sp, sp, 0x3232);
-            // effective zero points minus one (stored + zero_offset - 1)
-            const uint32_t z0 = ((zw.x >> (4 * gq)) & 0xFu) + a.zero_offset - 1u;
-            const uint32_t z1 = ((zw.y >> (4 * gq)) & 0xFu) + a.zero_offset - 1u;
+            // effective zero points minus one (stored + zero offset - 1)
+            const uint32_t zoff = g < a.zsplit ? 0u : static_cast<uint32_t>(a.zero_offset);
+            const uint32_t z0 = ((zw.x >> (4 * gq)) & 0xFu) + zoff - 1u;
+            const uint32_t z1 = ((zw.y >> (4 * gq)) & 0xFu) + zoff - 1u;
             c_nl[J][0] = neg_zlo(z0);
             c_nh[J][0] = neg_zhi(z0);
             c_nl[J][1] = neg_zlo(z1);
@@ -332,12 +334,12 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 // first block: a new group starts here (slot 0) or continues from the
                 // previous stage's second block, whose constants are already in slot 0
                 if (left == 0 || kb == kbeg) {      // a slice may start inside a group
-                    load_consts(sz, 0, 0);
+                    load_consts(sz, 0, 0, (2 * kb) / a.bpg);
                     left = kb == kbeg ? a.bpg - (2 * kbeg) % a.bpg : a.bpg;
                 }
                 --left;
                 const bool gl1 = left == 0;           // the second block starts a new group (slot 1)
-                if (gl1) { load_consts(sz, 1, 1); left = a.bpg; }
+                if (gl1) { load_consts(sz, 1, 1, (2 * kb + 1) / a.bpg); left = a.bpg; }
                 --left;
                 const uint4 wv = *reinterpret_cast<const uint4 *>(st + (wl * 32 + ls) * 16);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -539,7 +541,7 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
         cudaFuncSetAttribute(prefill_kernel<BM, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
     if (attr != cudaSuccess) return attr;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
-                (h.N + BN - 1) / BN, h.zero_offset, p.splits, ws, tickets};
+                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, p.splits, ws, tickets};
     const int nunits = args.tiles_m * args.tiles_n * p.splits;
     const int grid = nunits < sm_count() ? nunits : sm_count();
     cudaLaunchConfig_t cfg{};

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(HandleView h, uint16_t *__
             const int gr = (64 * kc + kl) / 32 / bpg;  // group of these eight rows
             const uint32_t w = wp[wp_index(nt, kc, lane, j, KC)];
             const uint32_t zw = h.zeros[static_cast<size_t>(gr) * (N / 8) + n / 8];
-            const int zeff = static_cast<int>((zw >> (4 * (n & 7))) & 0xFu) + h.zero_offset;
+            const int zeff = static_cast<int>((zw >> (4 * (n & 7))) & 0xFu) + (gr < h.zsplit ? 0 : h.zero_offset);
             const uint32_t sp = h.s2[(static_cast<size_t>(gr) * (N / 16) + nt) * 8 + gq];
             const uint16_t sbits = static_cast<uint16_t>((j & 1) ? (sp >> 16) : (sp & 0xFFFFu));
             const float s = __half2float(__ushort_as_half(sbits));

@@ -321,6 +321,26 @@ int gptq_q4_device_error(gptq_q4_handle h);
  * no-op. */
 void gptq_q4_free(gptq_q4_handle h);
 
+/* Q4Matrix handle for an 8-bit GPTQ layer ("Inference Backends", "GPTQ
+ * kernel contract": 8-bit codes pack four to an int32 along K).
+ *   qweight  device int32 [K/4][N]   four 8-bit codes per word along K,
+ *                                   lowest byte = lowest row
+ *   qzeros   device int32 [G][N/4]   four 8-bit zero points per word along N
+ *   scales   device fp16  [G][N], |scale| < 4094
+ *   g_idx, groupsize as for gptq_q4_make
+ * w[k][n] = scales[g][n] * (q[k][n] - (z[g][n] + 1)) (GPTQ; GPTQ_V2 after
+ * gptq_q4_set_format: q - z).  With q = 16 qh + ql and z = 16 zh + zl,
+ * s (q - z - 1) = 16 s (qh - zh) + s (ql - zl - 1) exactly, so the handle
+ * holds a 4-bit layer over 2K rows (the high nibbles with scale 16 s and zero
+ * offset 0, then the low nibbles with scale s) whose two halves read the same
+ * column of x; every matmul path, gptq_q4_dequant and gptq_q4_debug_unpack
+ * (8-bit codes and zero points, one byte each) work as for 4-bit handles,
+ * with twice the packed bytes.  gptq_q4_info reports the caller's K and G.
+ * Errors as for gptq_q4_make. */
+gptq_q4_handle gptq_q4_make8(const int32_t *qweight, const int32_t *qzeros,
+                             const uint16_t *scales, const int32_t *g_idx,
+                             int K, int N, int groupsize);
+
 /* Status and message of the last call made on this host thread. */
 int gptq_q4_last_status(void);
 const char *gptq_q4_last_error(void);

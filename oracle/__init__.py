@@ -70,6 +70,8 @@ def _load():
         lib.oracle_double_to_half_array.argtypes = [P, ctypes.c_size_t, P]
         lib.oracle_unpack_qweight.argtypes = [P, I, I, P]
         lib.oracle_unpack_qzeros.argtypes = [P, I, I, P]
+        lib.oracle_unpack_qweight8.argtypes = [P, I, I, P]
+        lib.oracle_unpack_qzeros8.argtypes = [P, I, I, P]
         lib.oracle_row_groups.argtypes = [P, I, I, P]
         lib.oracle_row_groups.restype = I
         lib.oracle_dequant.argtypes = [P, P, P, P, I, I, P, P, I]
@@ -122,6 +124,23 @@ def unpack_qzeros(qzeros: np.ndarray, G: int, N: int) -> np.ndarray:
     assert qz.shape == (G, N // 8)
     z = np.empty((G, N), np.uint8)
     _load().oracle_unpack_qzeros(_ptr(qz), G, N, _ptr(z))
+    return z
+
+
+def unpack_qweight8(qweight: np.ndarray, K: int, N: int) -> np.ndarray:
+    """8-bit codes: qweight [K/4, N], four per word along K, lowest byte first."""
+    qw = _c(qweight, np.int32)
+    assert qw.shape == (K // 4, N)
+    q = np.empty((K, N), np.uint8)
+    _load().oracle_unpack_qweight8(_ptr(qw), K, N, _ptr(q))
+    return q
+
+
+def unpack_qzeros8(qzeros: np.ndarray, G: int, N: int) -> np.ndarray:
+    qz = _c(qzeros, np.int32)
+    assert qz.shape == (G, N // 4)
+    z = np.empty((G, N), np.uint8)
+    _load().oracle_unpack_qzeros8(_ptr(qz), G, N, _ptr(z))
     return z
 
 
@@ -192,12 +211,12 @@ class Dequantized:
 
 
 def dequantize_layer(qweight, qzeros, scales, g_idx, K: int, N: int, groupsize: int,
-                     zero_offset: int = 1) -> Dequantized:
+                     zero_offset: int = 1, bits: int = 4) -> Dequantized:
     """Steps 1-3: unpack, group map, dequantize.  scales: fp16 array or its
-    bits.  zero_offset 1: GPTQ (v1) checkpoints, 0: GPTQ_V2."""
+    bits.  zero_offset 1: GPTQ (v1) checkpoints, 0: GPTQ_V2.  bits: 4 or 8."""
     gr, G = row_groups(g_idx, K, groupsize)
-    q = unpack_qweight(qweight, K, N)
-    z = unpack_qzeros(qzeros, G, N)
+    q = unpack_qweight(qweight, K, N) if bits == 4 else unpack_qweight8(qweight, K, N)
+    z = unpack_qzeros(qzeros, G, N) if bits == 4 else unpack_qzeros8(qzeros, G, N)
     sb = np.ascontiguousarray(scales).view(np.uint16) if np.asarray(scales).dtype != np.uint16 else scales
     w16, w64 = dequant(q, z, sb, gr, K, N, zero_offset=zero_offset)
     return Dequantized(q, z, gr, G, w16, w64)

@@ -35,7 +35,8 @@
  *    everything is fp64, bias is added after the k-sum.
  *
  * Precision: fp64 throughout.  The dequantized weight is formed exactly in
- * fp64 (an 11-bit significand times an integer in [-16, 15] fits easily)
+ * fp64 (an 11-bit significand times an integer in [-16, 15], or [-256, 255]
+ * for 8-bit codes, fits easily)
  * and then rounded once, to nearest-even, to fp16: that fp16 matrix (w16)
  * is the value a GPU dequantizer must reproduce bit for bit, and y_ref is
  * the fp64 product of the fp16 activations with w16.
@@ -133,6 +134,30 @@ void oracle_unpack_qzeros(const int32_t *qzeros, int G, int N, uint8_t *z)
         for (int n = 0; n < N; ++n) {
             uint32_t word = (uint32_t)qzeros[(size_t)i * (N / 8) + n / 8];
             z[(size_t)i * N + n] = (uint8_t)((word >> (4 * (n % 8))) & 0xFu);
+        }
+}
+
+/* 8-bit checkpoints.  "Inference Backends" declares GPTQ with 4 and 8 bits
+ * (GPTQ Marlin, Swordfish) without printing the 8-bit layout; read here as the
+ * same GPTQ packing with 32 / 8 = 4 codes per int32: qweight [K/4][N] holds
+ * four codes per word along K, lowest byte first, and qzeros [G][N/4] four
+ * zero points per word along N, lowest byte first.  oracle_dequant then
+ * applies unchanged (q and z up to 255). */
+void oracle_unpack_qweight8(const int32_t *qweight, int K, int N, uint8_t *q)
+{
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) {
+            uint32_t word = (uint32_t)qweight[(size_t)(k / 4) * N + n];
+            q[(size_t)k * N + n] = (uint8_t)((word >> (8 * (k % 4))) & 0xFFu);
+        }
+}
+
+void oracle_unpack_qzeros8(const int32_t *qzeros, int G, int N, uint8_t *z)
+{
+    for (int i = 0; i < G; ++i)
+        for (int n = 0; n < N; ++n) {
+            uint32_t word = (uint32_t)qzeros[(size_t)i * (N / 4) + n / 4];
+            z[(size_t)i * N + n] = (uint8_t)((word >> (8 * (n % 4))) & 0xFFu);
         }
 }
 

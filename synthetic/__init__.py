@@ -104,6 +104,23 @@ def make_layer(K: int, N: int, groupsize: int, *, act_order: bool = False,
     return LayerInputs(K, N, groupsize, qweight, qzeros, scales, g_idx, b, act_order)
 
 
+def make_layer8(K: int, N: int, groupsize: int, *, act_order: bool = False, bias: bool = False,
+                key=None) -> LayerInputs:
+    """Random 8-bit GPTQ layer: qweight [K/4, N] and qzeros [G, N/4] hold
+    uniform random bytes (codes and stored zeros 0..255), scales U[0.0002,
+    0.002] fp16 (an 8-bit code range is 16x a 4-bit one), act-order as in
+    make_layer."""
+    g = rng(*(key if key is not None else (97, K, N, groupsize, int(act_order))))
+    geff = K if groupsize == -1 else groupsize
+    G = K // geff
+    qweight = random_words(g, (K // 4, N))
+    qzeros = random_words(g, (G, N // 4))
+    scales = g.uniform(0.0002, 0.002, size=(G, N)).astype(np.float16)
+    g_idx = (g.permutation(K) // geff).astype(np.int32) if act_order else None
+    b = g.normal(0.0, 0.1, size=N).astype(np.float16) if bias else None
+    return LayerInputs(K, N, groupsize, qweight, qzeros, scales, g_idx, b, act_order, {"bits": 8})
+
+
 def uneven_group_index(K: int, G: int, key, empty_group: Optional[int] = None) -> np.ndarray:
     """A g_idx whose G groups hold unequal numbers of rows, scattered over K.
 

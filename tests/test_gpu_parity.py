@@ -185,6 +185,80 @@ def test_groupsize_not_multiple_of_32(q4, act):
     mat.device_error()
 
 
+EIGHT_BIT_CASES = [  # (K, N, groupsize, act_order)
+    (256, 128, 64, False),
+    (1024, 448, 32, True),
+    (1152, 320, 96, True),
+    (1024, 256, -1, False),
+    (2048, 960, 128, False),
+]
+
+
+@pytest.mark.parametrize("K,N,gs,act", EIGHT_BIT_CASES)
+def test_8bit_matches_oracle(q4, K, N, gs, act):
+    """8-bit checkpoints (qweight [K/4][N], qzeros [G][N/4]) held as two 4-bit
+    halves: the codes, zero points and dequantized weights bit for bit, y on
+    every path, GPTQ and GPTQ_V2 zero conventions."""
+    layer = synthetic.make_layer8(K, N, gs, act_order=act, bias=True, key=(31, K, N, gs & 0xFFFF, act))
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                      to_dev(layer.bias), gs, bits=8)
+    info = mat.info()
+    assert info["K"] == K and info["G"] == layer.G
+    for fmt, zo in ((q4.GPTQ_Q4_FORMAT_GPTQ, 1), (q4.GPTQ_Q4_FORMAT_GPTQ_V2, 0)):
+        mat.set_format(fmt)
+        dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs,
+                                     zero_offset=zo, bits=8)
+        q, z = mat.debug_unpack()
+        w = mat.dequant()
+        torch.cuda.synchronize()
+        assert np.array_equal(q.cpu().numpy(), dq.q)
+        assert np.array_equal(z.cpu().numpy(), dq.z)
+        assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+        for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "PREFILL"):
+            mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+            for M in (1, 3, 8, 16, 40):
+                x = synthetic.activations(M, K, key=(31, K, N, M))
+                y = mat(to_dev(x))
+                torch.cuda.synchronize()
+                check_y(y, x, dq, layer.bias, K, f"8-bit {path} fmt={fmt} K={K} N={N} g={gs} act={act} M={M}")
+        x = synthetic.activations(300, K, key=(31, K, N, 300))
+        mat.set_path(q4.GPTQ_Q4_PATH_AUTO)
+        y = mat(to_dev(x))
+        yu = mat.matmul_unfused(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, layer.bias, K, f"8-bit prefill fmt={fmt} M=300")
+        check_y(yu, x, dq, layer.bias, K, f"8-bit unfused fmt={fmt} M=300")
+    mat.device_error()
+    mat.close()
+
+
+def test_8bit_llama7b_shape(q4):
+    """An 8-bit 4096 x 11008 layer (g = 128): decode at M = 1 and 8 and the
+    fused prefill at M = 512 (oracle on a row sample)."""
+    K, N, gs = 4096, 11008, 128
+    layer = synthetic.make_layer8(K, N, gs, bias=True, key=(32, K, N))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, None, K, N, gs, bits=8)
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), None,
+                      to_dev(layer.bias), gs, bits=8)
+    w = mat.dequant()
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
+    del w
+    for M in (1, 8):
+        x = synthetic.activations(M, K, key=(32, K, N, M))
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check_y(y, x, dq, layer.bias, K, f"8-bit 7B M={M}")
+    M = 512
+    x = synthetic.activations(M, K, key=(32, K, N, M))
+    rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(36).choice(M, 16, replace=False)]))
+    y = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check_y(y[rows], x[rows], dq, layer.bias, K, "8-bit 7B M=512")
+    mat.device_error()
+    mat.close()
+
+
 V2_CASES = [  # (K, N, groupsize, act_order)
     (256, 128, 64, False),
     (1024, 448, 32, True),

@@ -120,6 +120,78 @@ def test_unpack_round_trip_all_values_all_positions():
     assert np.array_equal(oracle.unpack_qzeros(pack_cols(z), G, N), z)
 
 
+# ------------------------------------------------------------- 8-bit
+
+def pack_rows8(q: np.ndarray) -> np.ndarray:
+    """Test-side packer: 8-bit q [K, N] -> [K/4, N] int32, code 4i+r in bits 8r..8r+7."""
+    K, N = q.shape
+    words = np.zeros((K // 4, N), np.uint64)
+    for r in range(4):
+        words |= q[r::4, :].astype(np.uint64) << np.uint64(8 * r)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def pack_cols8(z: np.ndarray) -> np.ndarray:
+    G, N = z.shape
+    words = np.zeros((G, N // 4), np.uint64)
+    for r in range(4):
+        words |= z[:, r::4].astype(np.uint64) << np.uint64(8 * r)
+    return words.astype(np.uint32).view(np.int32)
+
+
+@pytest.mark.parametrize("word,codes", [
+    (0x04030201, [1, 2, 3, 4]),
+    (0xFF80007F, [0x7F, 0x00, 0x80, 0xFF]),       # a negative int32: the top byte is 255
+    (0x00000000, [0, 0, 0, 0]),
+    (0xF00F0FF0, [0xF0, 0x0F, 0x0F, 0xF0]),
+])
+def test_unpack8_hand_packed_words(word, codes):
+    w = np.array([word], np.uint32).view(np.int32)
+    q = oracle.unpack_qweight8(np.tile(w, (1, 4)).reshape(1, 4), 4, 4)
+    assert q[:, 0].tolist() == codes and (q == q[:, :1]).all()
+    z = oracle.unpack_qzeros8(w.reshape(1, 1), 1, 4)
+    assert z[0].tolist() == codes
+
+
+def test_unpack8_round_trip_all_byte_values():
+    g = np.random.default_rng(15)
+    K, N, G = 1024, 16, 4
+    q = g.integers(0, 256, size=(K, N)).astype(np.uint8)
+    for r in range(4):                   # every value at every byte position
+        q[r::4, 0] = (np.arange(K // 4) + r) % 256
+    z = g.integers(0, 256, size=(G, N)).astype(np.uint8)
+    assert np.array_equal(oracle.unpack_qweight8(pack_rows8(q), K, N), q)
+    assert np.array_equal(oracle.unpack_qzeros8(pack_cols8(z), G, N), z)
+
+
+def test_8bit_closed_forms():
+    """Every code 200, stored zero 100, unit scale: w = 200 - 101 (GPTQ) or
+    200 - 100 (GPTQ_V2); codes 255 against zero 255: -1 / 0."""
+    K, N = 32, 8
+    for code, zero in ((200, 100), (255, 255), (0, 255)):
+        qw = pack_rows8(np.full((K, N), code, np.uint8))
+        qz = pack_cols8(np.full((1, N), zero, np.uint8))
+        s = np.ones((1, N), np.float16)
+        for zo in (1, 0):
+            dq = oracle.dequantize_layer(qw, qz, s, None, K, N, -1, zero_offset=zo, bits=8)
+            assert (dq.w64 == float(code - zero - zo)).all()
+            assert (dq.w16.view(np.float16).astype(np.float64) == float(code - zero - zo)).all()
+
+
+def test_8bit_layer_with_nibble_codes_equals_4bit_layer():
+    """Codes and zeros below 16 packed as an 8-bit and as a 4-bit checkpoint
+    describe the same weights: both oracle routes agree bit for bit."""
+    g = np.random.default_rng(16)
+    K, N, gs = 256, 32, 64
+    q = g.integers(0, 16, size=(K, N)).astype(np.uint8)
+    z = g.integers(0, 16, size=(K // gs, N)).astype(np.uint8)
+    s = g.uniform(0.002, 0.02, size=(K // gs, N)).astype(np.float16)
+    gi = (g.permutation(K) // gs).astype(np.int32)
+    d4 = oracle.dequantize_layer(pack_rows(q), pack_cols(z), s, gi, K, N, gs)
+    d8 = oracle.dequantize_layer(pack_rows8(q), pack_cols8(z), s, gi, K, N, gs, bits=8)
+    assert np.array_equal(d4.w16, d8.w16) and np.array_equal(d4.q, d8.q) and np.array_equal(d4.z, d8.z)
+
+
 # ----------------------------------------------------------- group map
 
 def test_row_groups_trivial_and_errors():
