@@ -660,6 +660,24 @@ def run_next_rows(q4, torch, dev, stream, hbm_gbs):
     res["gptq_v2 4096x11008 M=1"] = {"gptq_us": round(t1 * 1e6, 2), "gptq_v2_us": round(t2 * 1e6, 2),
                                      "gptq_v2_TB/s": round(L.weight_bytes / t2 / 1e12, 3)}
     del mats
+    # 8-bit checkpoint of the same shape (two 4-bit halves along K): decode
+    # at M = 1 (weight bytes / time) and the fused prefill at M = 512
+    L8 = synthetic.make_layer8(4096, 11008, 128, key=(33, 4096, 11008))
+    mats = [q4.Q4Matrix(t(L8.qweight), t(L8.qzeros), t(L8.scales), None, None, 128, bits=8) for _ in range(6)]
+    t8 = _graph_time(torch, stream, issue) / len(mats)
+    bytes8 = 4096 * 11008 + (4096 // 128) * 11008 * 3   # codes + fp16 scales + 8-bit zeros
+    x512 = t(synthetic.activations(512, 4096, key=(33, 512)))
+    o512 = torch.empty((512, 11008), dtype=torch.float16, device=dev)
+    mats[0].reserve(512)
+
+    def issue512(sp):
+        q4.gptq_q4_matmul(mats[0].handle, x512.data_ptr(), 512, o512.data_ptr(), sp)
+
+    t512 = _graph_time(torch, stream, issue512)
+    res["8bit 4096x11008"] = {"M=1_us": round(t8 * 1e6, 2), "M=1_TB/s": round(bytes8 / t8 / 1e12, 3),
+                              "M=512_us": round(t512 * 1e6, 2),
+                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / t512 / 1e12, 1)}
+    del mats
     # GPU packer: float weights (fp16) + scales + zeros -> qweight/qzeros
     K, N, gs = 4096, 11008, 128
     g = np.random.default_rng(5)
