@@ -37,6 +37,8 @@ GPTQ_Q4_PATH_DECODE_TC = 4
 GPTQ_Q4_PATH_DECODE_RING = 5
 GPTQ_Q4_FORMAT_GPTQ = 0
 GPTQ_Q4_FORMAT_GPTQ_V2 = 1
+GPTQ_Q4_DTYPE_FP16 = 0
+GPTQ_Q4_DTYPE_BF16 = 1
 
 EXPORTED = [
     "gptq_q4_make", "gptq_q4_set_bias", "gptq_q4_reserve", "gptq_q4_matmul", "gptq_q4_dequant",
@@ -44,7 +46,7 @@ EXPORTED = [
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
     "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_make_fused", "gptq_q4_pack",
-    "gptq_q4_make8",
+    "gptq_q4_make8", "gptq_q4_set_act_dtype",
 ]
 
 _P = ctypes.c_void_p
@@ -70,6 +72,7 @@ _sig("gptq_q4_gemm_f16", _I, _P, _P, _P, _I, _I, _I, _P, _P)
 _sig("gptq_q4_set_path", _I, _P, _I)
 _sig("gptq_q4_set_prefill_min_m", _I, _P, _I)
 _sig("gptq_q4_set_format", _I, _P, _I)
+_sig("gptq_q4_set_act_dtype", _I, _P, _I)
 _sig("gptq_q4_make_fused", _P, _I, _P, _P, _P, _P, _I, _P, _I)
 _sig("gptq_q4_pack", _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P)
 _sig("gptq_q4_debug_wait_probe", _I, _P, ctypes.c_uint, _P)
@@ -192,6 +195,10 @@ def gptq_q4_set_format(h: int, fmt: int) -> int:
     return _check(_lib.gptq_q4_set_format(h, fmt))
 
 
+def gptq_q4_set_act_dtype(h: int, dtype: int) -> int:
+    return _check(_lib.gptq_q4_set_act_dtype(h, dtype))
+
+
 def gptq_q4_debug_wait_probe(status: int, limit_us: int, stream: int) -> int:
     return _check(_lib.gptq_q4_debug_wait_probe(status, limit_us, stream or None))
 
@@ -298,15 +305,27 @@ class Q4Matrix:
     def set_format(self, fmt: int) -> None:
         gptq_q4_set_format(self.handle, fmt)
 
+    def set_act_dtype(self, dtype) -> None:
+        """torch.float16 (default) or torch.bfloat16: the type of x and y."""
+        import torch
+        code = {torch.float16: GPTQ_Q4_DTYPE_FP16, torch.bfloat16: GPTQ_Q4_DTYPE_BF16}[dtype]
+        gptq_q4_set_act_dtype(self.handle, code)
+        self.act_dtype = dtype
+
+    def _act_dtype(self):
+        import torch
+        return getattr(self, "act_dtype", torch.float16)
+
     def matmul(self, x, out=None):
         import torch
+        dt = self._act_dtype()
         shape = x.shape
         x2 = x.reshape(-1, self.K)
-        if x2.dtype != torch.float16 or not x2.is_contiguous():
-            x2 = x2.to(torch.float16).contiguous()
+        if x2.dtype != dt or not x2.is_contiguous():
+            x2 = x2.to(dt).contiguous()
         M = x2.shape[0]
         if out is None:
-            out = torch.empty((M, self.N), dtype=torch.float16, device=x2.device)
+            out = torch.empty((M, self.N), dtype=dt, device=x2.device)
         gptq_q4_matmul(self.handle, x2.data_ptr(), M, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
         return out.reshape(*shape[:-1], self.N)
 
@@ -314,11 +333,12 @@ class Q4Matrix:
 
     def matmul_unfused(self, x, temp_dq=None):
         import torch
-        x2 = x.reshape(-1, self.K).to(torch.float16).contiguous()
+        dt = self._act_dtype()
+        x2 = x.reshape(-1, self.K).to(dt).contiguous()
         M = x2.shape[0]
         if temp_dq is None:
             temp_dq = torch.empty((self.K, self.N), dtype=torch.float16, device=x2.device)
-        out = torch.empty((M, self.N), dtype=torch.float16, device=x2.device)
+        out = torch.empty((M, self.N), dtype=dt, device=x2.device)
         gptq_q4_matmul_unfused(self.handle, x2.data_ptr(), M, temp_dq.data_ptr(), out.data_ptr(),
                                torch.cuda.current_stream().cuda_stream)
         return out

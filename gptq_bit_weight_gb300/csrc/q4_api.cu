@@ -21,7 +21,8 @@
 
 namespace q4 {
 cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
-                            uint16_t *out, int *status, cudaStream_t s);
+                            uint16_t *out, int *status, cudaStream_t s, const float *rowscale = nullptr,
+                            int out_bf16 = 0);
 int prefill_default_min_m();
 }  // namespace q4
 
@@ -123,6 +124,7 @@ void release(gptq_q4_s *h) {
     cudaFree(h->ws);
     cudaFree(h->tickets);
     cudaFree(h->temp_state);
+    cudaFree(h->rowscale);
     if (cur >= 0) cudaSetDevice(cur);
     delete h;
 }
@@ -196,7 +198,22 @@ int ensure_decode_work(gptq_q4_s *h, size_t ws_floats, int n_tickets, cudaStream
 
 int ensure_temp_state(gptq_q4_s *h, int M, cudaStream_t s, bool sync_alloc) {
     const size_t need = static_cast<size_t>(M) * h->K;
-    if (!h->act_order || need <= h->temp_state_elems) return GPTQ_Q4_OK;
+    if (h->act_bf16 && static_cast<size_t>(M) > h->rowscale_elems) {
+        if (h->rowscale) {
+            if (sync_alloc) cudaFree(h->rowscale);
+            else Q4_CUDA(cudaFreeAsync(h->rowscale, s), "cudaFreeAsync(rowscale)");
+            h->device_bytes -= h->rowscale_elems * sizeof(float);
+            h->rowscale = nullptr;
+            h->rowscale_elems = 0;
+        }
+        void *v = nullptr;
+        cudaError_t e = sync_alloc ? cudaMalloc(&v, M * sizeof(float)) : cudaMallocAsync(&v, M * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e, "allocating row scales");
+        h->rowscale = static_cast<float *>(v);
+        h->rowscale_elems = static_cast<size_t>(M);
+        h->device_bytes += M * sizeof(float);
+    }
+    if (!(h->act_order || h->act_bf16) || need <= h->temp_state_elems) return GPTQ_Q4_OK;
     if (h->temp_state) {
         if (sync_alloc) cudaFree(h->temp_state);
         else Q4_CUDA(cudaFreeAsync(h->temp_state, s), "cudaFreeAsync(temp_state)");
@@ -590,13 +607,26 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
 static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out, cudaStream_t stream,
                       int path) {
     const uint16_t *xin = x;
-    if (h->act_order) {
+    if (h->act_bf16) {
+        // bf16 x: scaled by a power of two per row and rounded once to fp16
+        // (gathered at the same time under act-order); the epilogues undo the scale
+        if (int r = ensure_temp_state(h, M, stream, false)) return r;
+        Q4_CUDA(q4::launch_xprep_bf16(x, h->act_order ? h->perm : nullptr, M, h->Kx, h->K, h->temp_state,
+                                      h->rowscale, stream),
+                "bf16 preparation launch");
+        ++g_launches;
+        xin = h->temp_state;
+    } else if (h->act_order) {
         if (int r = ensure_temp_state(h, M, stream, false)) return r;
         Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, h->temp_state, stream), "xreorder launch");
         ++g_launches;
         xin = h->temp_state;
     }
-    const q4::HandleView v = view(h);
+    q4::HandleView v = view(h);
+    if (h->act_bf16) {
+        v.rowscale = h->rowscale;
+        v.out_bf16 = 1;
+    }
     if (path == GPTQ_Q4_PATH_PREFILL) {
         const q4::PrefillPlan pp = q4::plan_prefill(M, h->K, h->N);
         if (int r = ensure_decode_work(h, pp.ws_floats, pp.n_tickets, stream, false)) return r;
@@ -604,7 +634,8 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    if (path == GPTQ_Q4_PATH_DECODE_TC && h->zsplit == 0 && q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
+    if (path == GPTQ_Q4_PATH_DECODE_TC && h->zsplit == 0 && !h->act_bf16 &&
+        q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
         Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
         ++g_launches;
         return ok();
@@ -693,7 +724,17 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
     if (h->bits == 8) Q4_CUDA(q4::launch_dequant8(view(h), h->inv8, h->Kx, temp_dq, stream), "dequant launch");
     else Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
     ++g_launches;
-    Q4_CUDA(q4::launch_gemm_f16(x, temp_dq, h->bias, M, h->Kx, h->N, out, h->status, stream), "gemm launch");
+    const uint16_t *xa = x;
+    if (h->act_bf16) {   // x in original order, scaled per row and rounded once to fp16
+        if (int r = ensure_temp_state(h, M, stream, false)) return r;
+        Q4_CUDA(q4::launch_xprep_bf16(x, nullptr, M, h->Kx, h->Kx, h->temp_state, h->rowscale, stream),
+                "bf16 preparation launch");
+        ++g_launches;
+        xa = h->temp_state;
+    }
+    Q4_CUDA(q4::launch_gemm_f16(xa, temp_dq, h->bias, M, h->Kx, h->N, out, h->status, stream,
+                                h->act_bf16 ? h->rowscale : nullptr, h->act_bf16),
+            "gemm launch");
     ++g_launches;
     return ok();
 }
@@ -757,6 +798,15 @@ int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "limit_us=%u outside [1, 2000000]", limit_us);
     Q4_CUDA(q4::launch_wait_probe(status, static_cast<uint64_t>(limit_us) * 1000ull, stream), "wait probe launch");
     ++g_launches;
+    return ok();
+}
+
+int gptq_q4_set_act_dtype(gptq_q4_handle h, int dtype) {
+    if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
+    if (dtype != GPTQ_Q4_DTYPE_FP16 && dtype != GPTQ_Q4_DTYPE_BF16)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "dtype=%d is neither GPTQ_Q4_DTYPE_FP16 nor GPTQ_Q4_DTYPE_BF16",
+                          dtype);
+    h->act_bf16 = dtype == GPTQ_Q4_DTYPE_BF16 ? 1 : 0;
     return ok();
 }
 

@@ -507,10 +507,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     auto store_out = [&](int e, float v) {
         int m, n;
         element_mn(e, m, n);
-        if (m < a.M) {
-            if (h.bias) v += __half2float(__ushort_as_half(h.bias[n]));
-            a.out[static_cast<size_t>(m) * N + n] = __half_as_ushort(__float2half_rn(v));
-        }
+        if (m < a.M)
+            a.out[static_cast<size_t>(m) * N + n] = out_one(v, h.rowscale ? h.rowscale[m] : 1.f, h.bias, n, h.out_bf16);
     };
 
     // CTA partial: the warps' partials summed in warp order, kept in red[0, E)

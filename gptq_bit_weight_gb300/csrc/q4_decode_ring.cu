@@ -98,6 +98,8 @@ struct RingArgs {
     int bpg;             // 32-row blocks per group
     int zero_offset;     // effective zero = stored + zero_offset
     int zsplit;          // groups [0, zsplit) take zero offset 0
+    const float *rowscale;   // epilogue: y = acc * rowscale[m] + bias (NULL: 1)
+    int out_bf16;            // output rounded to bf16 instead of fp16
     int slice_kb;        // stages per slice
     int splits;
 };
@@ -397,11 +399,9 @@ __global__ void __launch_bounds__(kThreads, 3)
                     for (int i = 0; i < 4; ++i) {
                         const int n = n0 + 16 * (kTPW * warp + t) + gq + 8 * (i >> 1);
                         const int m = m0 + mt * 8 + 2 * tq + (i & 1);
-                        if (m < a.M && n < a.N) {
-                            float v = acc[t][mt][i];
-                            if (a.bias) v += __half2float(__ushort_as_half(a.bias[n]));
-                            a.out[static_cast<size_t>(m) * a.N + n] = __half_as_ushort(__float2half_rn(v));
-                        }
+                        if (m < a.M && n < a.N)
+                            a.out[static_cast<size_t>(m) * a.N + n] =
+                                out_one(acc[t][mt][i], a.rowscale ? a.rowscale[m] : 1.f, a.bias, n, a.out_bf16);
                     }
         }
         return;
@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (e % a.splits != split || ml >= mrows || n0 + nl >= a.N) continue;
             float v = 0.f;
             for (int r = 0; r < a.splits; ++r) v += ld_dsmem_f32(red_local + e * 4, r);
-            if (a.bias) v += __half2float(__ushort_as_half(a.bias[n0 + nl]));
-            a.out[static_cast<size_t>(m0 + ml) * a.N + n0 + nl] = __half_as_ushort(__float2half_rn(v));
+            a.out[static_cast<size_t>(m0 + ml) * a.N + n0 + nl] =
+                out_one(v, a.rowscale ? a.rowscale[m0 + ml] : 1.f, a.bias, n0 + nl, a.out_bf16);
         }
     }
     cluster_sync();                                   // partials stay alive until all are read
@@ -546,7 +546,7 @@ cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &p, con
                        static_cast<uint64_t>(KC) * 512, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
     RingArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, h.zero_offset, h.zsplit,
-                  p.slice_kb, p.splits};
+                  h.rowscale, h.out_bf16, p.slice_kb, p.splits};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.tiles, p.splits, 1);
     cfg.blockDim = dim3(kThreads);

@@ -57,6 +57,8 @@ struct TcArgs {
     const uint32_t *s2;      // fused: scale pairs [G][N/16][8]
     const uint32_t *zeros;   // fused: zero words [G][N/8]
     int bpg;                 // fused: 32-row blocks per group
+    const float *rowscale;   // epilogue: y = acc * rowscale[m] + bias (NULL: 1)
+    int out_bf16;            // output rounded to bf16 instead of fp16
 };
 
 __device__ __forceinline__ void record_error(int *status, int bit, int *abort_flag) {
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 uint32_t r[32];
                 tmem_ld_x32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + c0, r);
                 if (row < a.M) {
+                    const float rs = a.rowscale ? a.rowscale[row] : 1.f;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int n = n0 + c0 + 8 * v;
@@ -176,14 +179,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                             uint32_t pk[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                float lo = __uint_as_float(r[8 * v + 2 * e]);
-                                float hi = __uint_as_float(r[8 * v + 2 * e + 1]);
-                                if (a.bias) {
-                                    lo += __half2float(__ushort_as_half(a.bias[n + 2 * e]));
-                                    hi += __half2float(__ushort_as_half(a.bias[n + 2 * e + 1]));
-                                }
-                                pk[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-                                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+                                pk[e] = out_pair(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]),
+                                                 rs, a.bias, n + 2 * e, a.out_bf16);
                             }
                             *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
                                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -244,7 +241,7 @@ cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr,
 }
 
 cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
-                            uint16_t *out, int *status, cudaStream_t s) {
+                            uint16_t *out, int *status, cudaStream_t s, const float *rowscale, int out_bf16) {
     CUtensorMap tmA, tmB;
     cudaError_t e;
     if ((e = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a, K, M, static_cast<uint64_t>(K) * 2, BK, BM,
@@ -254,7 +251,7 @@ cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t
                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
         return e;
     if ((e = ensure_smem_attr()) != cudaSuccess) return e;
-    TcArgs args{M, N, K, bias, out, status, nullptr, nullptr, 1};
+    TcArgs args{M, N, K, bias, out, status, nullptr, nullptr, 1, rowscale, out_bf16};
     dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
     tc_gemm_kernel<<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(tmA, tmB, args);
     return cudaGetLastError();

@@ -27,6 +27,8 @@
 // Zero points keep the checkpoint layout [G][N/8].
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace q4 {
@@ -165,7 +167,31 @@ struct HandleView {
     int zero_offset;        // effective zero = stored + zero_offset (1: GPTQ, 0: GPTQ_V2)
     int zsplit;             // groups [0, zsplit) take zero offset 0 instead (the high-nibble
                             // half of an 8-bit layer), the rest zero_offset
+    // output epilogue of this call: y = acc * rowscale[m] + bias, rounded once
+    // to fp16, or to bf16 when out_bf16 (rowscale NULL: 1)
+    const float *rowscale;
+    int out_bf16;
 };
+
+// One output value / pair of the epilogue above.
+__device__ __forceinline__ uint32_t out_bits(float v, bool bf16) {
+    return bf16 ? static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)))
+                : static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v)));
+}
+__device__ __forceinline__ uint16_t out_one(float acc, float rs, const uint16_t *bias, int n, bool bf16) {
+    float v = acc * rs;
+    if (bias) v += __half2float(__ushort_as_half(bias[n]));
+    return static_cast<uint16_t>(out_bits(v, bf16));
+}
+__device__ __forceinline__ uint32_t out_pair(float lo, float hi, float rs, const uint16_t *bias, int n, bool bf16) {
+    lo *= rs;
+    hi *= rs;
+    if (bias) {
+        lo += __half2float(__ushort_as_half(bias[n]));
+        hi += __half2float(__ushort_as_half(bias[n + 1]));
+    }
+    return out_bits(lo, bf16) | (out_bits(hi, bf16) << 16);
+}
 
 struct DecodeWork {
     float *ws;              // split-K partials
@@ -184,6 +210,11 @@ cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t 
 // values, temp_state rows K
 cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int Kx, int K,
                             uint16_t *temp_state, cudaStream_t s);
+// bf16 activations: per row m, e_m with max|x[m]| * 2^-e_m in [2^14, 2^15),
+// temp_state[m][j] = fp16(x[m][perm[j]] * 2^-e_m) (perm NULL: j; -1: 0) and
+// rowscale[m] = 2^e_m
+cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
+                              float *rowscale, cudaStream_t s);
 
 // decode (q4_decode.cu)
 struct DecodePlan {

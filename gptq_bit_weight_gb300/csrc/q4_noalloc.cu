@@ -68,8 +68,10 @@ extern "C" int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M
     const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N, h->geff);
     const size_t ticket_bytes = round_up_256(static_cast<size_t>(p.n_tickets) * sizeof(int));
     const size_t ws_bytes = round_up_256(p.ws_floats * sizeof(float));
-    const size_t ts_bytes = h->act_order ? round_up_256(static_cast<size_t>(M) * h->K * sizeof(uint16_t)) : 0;
-    const size_t need = ticket_bytes + ws_bytes + ts_bytes;
+    const size_t ts_bytes =
+        (h->act_order || h->act_bf16) ? round_up_256(static_cast<size_t>(M) * h->K * sizeof(uint16_t)) : 0;
+    const size_t rs_bytes = h->act_bf16 ? round_up_256(static_cast<size_t>(M) * sizeof(float)) : 0;
+    const size_t need = ticket_bytes + ws_bytes + ts_bytes + rs_bytes;
     if (need > kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
@@ -88,6 +90,7 @@ extern "C" int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M
     int *tickets = reinterpret_cast<int *>(scratch);
     float *ws = reinterpret_cast<float *>(scratch + ticket_bytes);
     uint16_t *temp_state = reinterpret_cast<uint16_t *>(scratch + ticket_bytes + ws_bytes);
+    float *rowscale = reinterpret_cast<float *>(scratch + ticket_bytes + ws_bytes + ts_bytes);
 
     // The tickets must start at zero; the array keeps whatever the last
     // call (on any handle) left in it.
@@ -95,14 +98,25 @@ extern "C" int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M
         return q4::api_cuda_fail(e, "clearing the scratch tickets");
 
     const uint16_t *xin = x;
-    if (h->act_order) {
+    if (h->act_bf16) {
+        if ((e = q4::launch_xprep_bf16(x, h->act_order ? h->perm : nullptr, M, h->Kx, h->K, temp_state, rowscale,
+                                       stream)) != cudaSuccess)
+            return q4::api_cuda_fail(e, "bf16 preparation launch");
+        q4::api_count_launches(1);
+        xin = temp_state;
+    } else if (h->act_order) {
         if ((e = q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, temp_state, stream)) != cudaSuccess)
             return q4::api_cuda_fail(e, "xreorder launch");
         q4::api_count_launches(1);
         xin = temp_state;
     }
     const q4::DecodeWork w{ws, p.ws_floats, tickets, p.n_tickets};
-    if ((e = q4::launch_decode(q4::api_view(h), p, w, xin, M, out, stream)) != cudaSuccess)
+    q4::HandleView v = q4::api_view(h);
+    if (h->act_bf16) {
+        v.rowscale = rowscale;
+        v.out_bf16 = 1;
+    }
+    if ((e = q4::launch_decode(v, p, w, xin, M, out, stream)) != cudaSuccess)
         return q4::api_cuda_fail(e, "decode launch");
     q4::api_count_launches(1);
     return q4::api_set_status(GPTQ_Q4_OK, nullptr);

@@ -267,4 +267,46 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
     return cudaGetLastError();
 }
 
+// --------------------------------------------------- bf16 activations
+// One CTA per row: the largest magnitude of the row picks a power of two
+// 2^e with max|x| * 2^-e in [2^14, 2^15); each value times 2^-e (exact in
+// fp32) is rounded once to fp16.  A bf16 value has an 8-bit significand, so
+// the fp16 value is exact unless it lies more than ~2^28 below the row's
+// largest.  The kernels' epilogues multiply the fp32 sums by 2^e (exact).
+__global__ void __launch_bounds__(256) xprep_bf16_kernel(const uint16_t *__restrict__ x,
+                                                         const int32_t *__restrict__ perm, int M, int Kx, int K,
+                                                         uint16_t *__restrict__ ts, float *__restrict__ rowscale) {
+    __shared__ float wmax[8];
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint16_t *xr = x + static_cast<size_t>(m) * Kx;
+        float mx = 0.f;
+        for (int k = threadIdx.x; k < Kx; k += blockDim.x)
+            mx = fmaxf(mx, fabsf(__uint_as_float(static_cast<uint32_t>(xr[k]) << 16)));
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        mx = wmax[0];
+        for (int w = 1; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+        __syncthreads();                               // wmax is reused by the next row
+        // e = ilogb(max) - 14, kept where 2^-e and 2^e are normal fp32 values
+        int e = 0;
+        if (mx > 0.f && mx <= 3.402823466e38f) e = min(max(ilogbf(mx) - 14, -110), 113);
+        const float down = __int_as_float((127 - e) << 23);   // 2^-e
+        if (threadIdx.x == 0) rowscale[m] = __int_as_float((127 + e) << 23);
+        uint16_t *tr = ts + static_cast<size_t>(m) * K;
+        for (int j = threadIdx.x; j < K; j += blockDim.x) {
+            const int k = perm ? perm[j] : j;
+            const float v = k >= 0 ? __uint_as_float(static_cast<uint32_t>(xr[k]) << 16) * down : 0.f;
+            tr[j] = __half_as_ushort(__float2half_rn(v));
+        }
+    }
+}
+
+cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
+                              float *rowscale, cudaStream_t s) {
+    const int ctas = std::min(M, kSMs * 8);
+    xprep_bf16_kernel<<<ctas > 0 ? ctas : 1, 256, 0, s>>>(x, perm, M, Kx, K, temp_state, rowscale);
+    return cudaGetLastError();
+}
+
 }  // namespace q4

@@ -302,6 +302,21 @@ gptq_q4_handle gptq_q4_make_fused(int parts, const int32_t *const *qweight, cons
 #define GPTQ_Q4_FORMAT_GPTQ_V2 1
 int gptq_q4_set_format(gptq_q4_handle h, int format);
 
+/* Type of x and out for later matmul calls on this handle ("Inference
+ * Backends": backends keep the activation/output dtype, fp16 or bf16, with
+ * fp16 scales and fp32 accumulation).  Default FP16.  With BF16, x and out are
+ * bf16 [M][K] / [M][N] (bias stays the handle's fp16); every row of x is
+ * first scaled by a power of two 2^-e (its largest magnitude times 2^-e in
+ * [2^14, 2^15)) and rounded once to fp16 (exact for values within ~2^28 of
+ * the row's largest: bf16 has an 8-bit significand), the fp16 kernels run
+ * unchanged, and each output is acc * 2^e + bias rounded once to bf16.
+ * Covers gptq_q4_matmul, gptq_q4_matmul_unfused and gptq_q4_matmul_noalloc;
+ * one extra launch per call prepares x (fused with the act-order gather).
+ * Errors: INVALID_ARGUMENT (NULL handle, unknown dtype). */
+#define GPTQ_Q4_DTYPE_FP16 0
+#define GPTQ_Q4_DTYPE_BF16 1
+int gptq_q4_set_act_dtype(gptq_q4_handle h, int dtype);
+
 /* Rows at and above which GPTQ_Q4_PATH_AUTO takes the prefill kernel (the
  * decode/prefill switch of the Lorax page's set_tuning_params).  Default 17:
  * decode covers up to 16 rows; measured on GB300, the fused prefill is faster

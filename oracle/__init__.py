@@ -69,6 +69,9 @@ def _load():
         lib.oracle_half_to_double_array.argtypes = [P, ctypes.c_size_t, P]
         lib.oracle_double_to_half_array.argtypes = [P, ctypes.c_size_t, P]
         lib.oracle_unpack_qweight.argtypes = [P, I, I, P]
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double_array.argtypes = [P, ctypes.c_size_t, P]
         lib.oracle_unpack_qzeros.argtypes = [P, I, I, P]
         lib.oracle_unpack_qweight8.argtypes = [P, I, I, P]
         lib.oracle_unpack_qzeros8.argtypes = [P, I, I, P]
@@ -110,6 +113,14 @@ def f64_to_half_bits(v: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- steps
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact fp64 values."""
+    b = _c(bits, np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_bf16_to_double_array(_ptr(b), b.size, _ptr(out))
+    return out
+
 
 def unpack_qweight(qweight: np.ndarray, K: int, N: int) -> np.ndarray:
     qw = _c(qweight, np.int32)
@@ -233,6 +244,25 @@ def reference_output(x_fp16, dq: Dequantized, bias_fp16=None, nthreads=None, exa
     w = dq.w64 if exact else half_bits_to_f64(dq.w16)
     b64 = None if bias_fp16 is None else half_bits_to_f64(_bits(bias_fp16))
     return linear_f64(x64, w, b64, nthreads)
+
+
+def reference_output_bf16(x_bf16_bits, dq: Dequantized, bias_fp16=None, nthreads=None):
+    """y_ref = x . w16 + bias with bf16 activations (bit patterns)."""
+    x64 = bf16_bits_to_f64(x_bf16_bits)
+    b64 = None if bias_fp16 is None else half_bits_to_f64(_bits(bias_fp16))
+    return linear_f64(x64, half_bits_to_f64(dq.w16), b64, nthreads)
+
+
+def tolerance_rows_bf16(x_bf16_bits, w16_bits, y_ref: np.ndarray, K: int) -> np.ndarray:
+    """tolerance() for bf16 outputs, with max|x| taken per row of x:
+    1e-2 sqrt(K) max|x[m]| max|w| / 64 + (2e-3 + 2^-8) |y_ref|.  The stated
+    bound is for fp16 outputs; rounding once to bf16 (an 8-bit significand)
+    alone can move a value by 2^-8 of itself, so that is added to the
+    relative term."""
+    xa = np.abs(bf16_bits_to_f64(x_bf16_bits))
+    xmax = xa.max(axis=1, keepdims=True) if xa.size else np.zeros((y_ref.shape[0], 1))
+    wmax = float(np.max(np.abs(half_bits_to_f64(_bits(w16_bits))))) if np.size(w16_bits) else 0.0
+    return 1e-2 * np.sqrt(K) * xmax * wmax / 64.0 + (2e-3 + 2.0 ** -8) * np.abs(y_ref)
 
 
 def tolerance(x_fp16, w16_bits, y_ref: np.ndarray, K: int) -> np.ndarray:

@@ -113,6 +113,22 @@ void oracle_double_to_half_array(const double *v, size_t n, uint16_t *out)
     for (size_t i = 0; i < n; ++i) out[i] = oracle_double_to_half(v[i]);
 }
 
+/* bf16 activations ("Inference Backends": backends keep the activation and
+ * output dtype, fp16 or bf16): a bf16 value is the upper 16 bits of an IEEE
+ * binary32, so it converts to double exactly. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+void oracle_bf16_to_double_array(const uint16_t *b, size_t n, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(b[i]);
+}
+
 /* ------------------------------------------------------------- unpack */
 
 /* q[k][n] = nibble (k mod 8) of qweight[k/8][n], lowest nibble first.

@@ -146,6 +146,18 @@ def activations(M: int, K: int, g: Optional[np.random.Generator] = None, key=Non
     return g.standard_normal((M, K)).astype(np.float16)
 
 
+def activations_bf16(M: int, K: int, key, row_scales=None) -> np.ndarray:
+    """x ~ N(0, 1) (times row_scales[m] per row, if given) rounded to bf16,
+    nearest-even, returned as uint16 bit patterns [M, K]."""
+    g = rng(*key)
+    v = g.standard_normal((M, K)).astype(np.float32)
+    if row_scales is not None:
+        v = (v * np.asarray(row_scales, np.float32)[:, None]).astype(np.float32)
+    u = v.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16          # round to nearest, ties to even
+    return u.astype(np.uint16)
+
+
 # ------------------------------------------------------------ workloads
 
 def single_layer():

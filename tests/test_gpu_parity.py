@@ -259,6 +259,70 @@ def test_8bit_llama7b_shape(q4):
     mat.close()
 
 
+BF16_CASES = [  # (K, N, groupsize, act_order)
+    (256, 128, 64, False),
+    (1024, 448, 32, True),
+    (1152, 320, 96, True),
+    (2048, 960, 128, False),
+]
+BF16_ROW_SCALES = [1.0, 1e6, 1e-6, 3e4]     # rows beyond fp16's range both ways
+
+
+def bf16_tensor(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def check_y_bf16(y_gpu, xb, dq, bias, K, what=""):
+    y_ref = oracle.reference_output_bf16(xb, dq, bias)
+    tol = oracle.tolerance_rows_bf16(xb, dq.w16, y_ref, K)
+    y = y_gpu.float().cpu().numpy().astype(np.float64)
+    err = np.abs(y - y_ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside tolerance; worst err/tol "
+                           f"{float(np.max(err / np.maximum(tol, 1e-300))):.3f}")
+
+
+@pytest.mark.parametrize("K,N,gs,act", BF16_CASES)
+def test_bf16_activations_match_oracle(q4, K, N, gs, act):
+    """bf16 x and y: every path (and the unfused route and the
+    allocation-free call) against the oracle, with rows of x scaled by 1e6 and
+    1e-6 (outside fp16's range), checked row by row."""
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(33, K, N, gs & 0xFFFF, act))
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    mat.set_act_dtype(torch.bfloat16)
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "PREFILL"):
+        mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+        for M in (1, 3, 8, 16, 40):
+            rs = [BF16_ROW_SCALES[m % 4] for m in range(M)]
+            xb = synthetic.activations_bf16(M, K, key=(33, K, N, M), row_scales=rs)
+            y = mat(bf16_tensor(xb))
+            torch.cuda.synchronize()
+            assert y.dtype == torch.bfloat16
+            check_y_bf16(y, xb, dq, layer.bias, K, f"bf16 {path} K={K} N={N} g={gs} act={act} M={M}")
+    M = 300
+    xb = synthetic.activations_bf16(M, K, key=(33, K, N, M), row_scales=[BF16_ROW_SCALES[m % 4] for m in range(M)])
+    mat.set_path(q4.GPTQ_Q4_PATH_AUTO)
+    y = mat(bf16_tensor(xb))
+    yu = mat.matmul_unfused(bf16_tensor(xb))
+    torch.cuda.synchronize()
+    check_y_bf16(y, xb, dq, layer.bias, K, "bf16 prefill M=300")
+    check_y_bf16(yu, xb, dq, layer.bias, K, "bf16 unfused M=300")
+    M = 4
+    xb = synthetic.activations_bf16(M, K, key=(34, K, N, M), row_scales=BF16_ROW_SCALES)
+    xt = bf16_tensor(xb)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    q4.gptq_q4_matmul_noalloc(mat.handle, xt.data_ptr(), M, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    check_y_bf16(out, xb, dq, layer.bias, K, "bf16 noalloc M=4")
+    mat.set_act_dtype(torch.float16)
+    x = synthetic.activations(5, K, key=(33, K, N, 5))
+    y = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check_y(y, x, dq, layer.bias, K, "back to fp16")
+    mat.device_error()
+
+
 V2_CASES = [  # (K, N, groupsize, act_order)
     (256, 128, 64, False),
     (1024, 448, 32, True),

@@ -120,6 +120,37 @@ def test_unpack_round_trip_all_values_all_positions():
     assert np.array_equal(oracle.unpack_qzeros(pack_cols(z), G, N), z)
 
 
+# --------------------------------------------------------------- bf16
+
+def test_bf16_to_double_exhaustive():
+    """Every bf16 pattern against numpy: the float32 whose upper half it is."""
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):                # signalling NaN patterns
+        expect = (bits << np.uint32(16)).view(np.float32).astype(np.float64)
+    got = oracle.bf16_bits_to_f64(bits.astype(np.uint16))
+    nan = np.isnan(expect)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], expect[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(expect[~nan]))
+
+
+def test_bf16_hand_values():
+    b = np.array([0x3F80, 0xC020, 0x0001, 0x7F7F, 0x4000, 0x3C00], np.uint16)
+    assert oracle.bf16_bits_to_f64(b).tolist() == [1.0, -2.5, 2.0 ** -133, (2 - 2 ** -7) * 2.0 ** 127, 2.0,
+                                                    2.0 ** -7]
+
+
+def test_bf16_tolerance_covers_output_rounding_only():
+    """The bf16 bound admits y_ref rounded to bf16 and rejects an error of a
+    whole bf16 unit in the last place on a value just above a power of two."""
+    y_ref = np.array([[1.0 + 2 ** -8 * 0.999, 3.0]])
+    x = np.zeros((1, 64), np.uint16)                   # x = 0: only the relative term is left
+    w16 = np.zeros((64, 2), np.uint16)
+    tol = oracle.tolerance_rows_bf16(x, w16, y_ref, 64)
+    assert (np.abs(np.array([[1.0, 3.0]]) - y_ref) <= tol).all()
+    assert not (np.abs(np.array([[1.0 + 2 ** -7 + 2 ** -6, 3.0]]) - y_ref) <= tol).all()
+
+
 # ------------------------------------------------------------- 8-bit
 
 def pack_rows8(q: np.ndarray) -> np.ndarray:
