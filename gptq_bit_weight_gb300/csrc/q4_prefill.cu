@@ -97,6 +97,8 @@ struct PfArgs {
     int tiles_m, tiles_n;
     int zero_offset;         // effective zero = stored + zero_offset
     int zsplit;              // groups [0, zsplit) take zero offset 0
+    const float *rowscale;   // epilogue: y = acc * rowscale[m] + bias (NULL: 1)
+    int out_bf16;            // output rounded to bf16 instead of fp16
     int splits;              // K slices per tile (> 1: one unit per CTA, cooperative launch)
     float *ws;               // fp32 partial tiles [tile][slice][BM][BN] when splits > 1
     int *tickets;            // one per tile, zero between calls
@@ -322,6 +324,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             int kbeg, kend;
             kb_range(u, kbeg, kend);
             int left = 0;                             // 32-row blocks left in the current group
+            int gcur = 0;                             // global group of the constants in slot 0
             for (int kb = kbeg; kb < kend; ++kb) {
                 if (aborted(abort_flag)) { ok = false; break; }
                 if (!mbar_wait(fullP(rp.s), rp.ph) || !mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
@@ -334,12 +337,13 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 // first block: a new group starts here (slot 0) or continues from the
                 // previous stage's second block, whose constants are already in slot 0
                 if (left == 0 || kb == kbeg) {      // a slice may start inside a group
-                    load_consts(sz, 0, 0, (2 * kb) / a.bpg);
-                    left = kb == kbeg ? a.bpg - (2 * kbeg) % a.bpg : a.bpg;
+                    gcur = kb == kbeg ? (2 * kbeg) / a.bpg : gcur + 1;
+                    load_consts(sz, 0, 0, gcur);
+                    left = kb == kbeg ? a.bpg - (2 * kbeg - gcur * a.bpg) : a.bpg;
                 }
                 --left;
                 const bool gl1 = left == 0;           // the second block starts a new group (slot 1)
-                if (gl1) { load_consts(sz, 1, 1, (2 * kb + 1) / a.bpg); left = a.bpg; }
+                if (gl1) { load_consts(sz, 1, 1, gcur + 1); left = a.bpg; }
                 --left;
                 const uint4 wv = *reinterpret_cast<const uint4 *>(st + (wl * 32 + ls) * 16);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -362,6 +366,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     mbar_arrive(emptyP(rp.s));        // every register loaded from it is consumed
                 }
                 if (gl1) {                            // that group continues into the next stage
+                    ++gcur;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         c_s[0][c] = c_s[1][c];
@@ -408,6 +413,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                         dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
                 } else if (row < a.M) {
+                    const float rs = a.rowscale ? a.rowscale[row] : 1.f;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int n = n0 + c0 + 8 * v;
@@ -415,14 +421,8 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                             uint32_t pk[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                float lo = __uint_as_float(r[8 * v + 2 * e]);
-                                float hi = __uint_as_float(r[8 * v + 2 * e + 1]);
-                                if (a.bias) {
-                                    lo += __half2float(__ushort_as_half(a.bias[n + 2 * e]));
-                                    hi += __half2float(__ushort_as_half(a.bias[n + 2 * e + 1]));
-                                }
-                                pk[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-                                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+                                pk[e] = out_pair(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]),
+                                                 rs, a.bias, n + 2 * e, a.out_bf16);
                             }
                             *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
                                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -490,16 +490,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
                 }
                 uint32_t pk[4];
+                const float rs = a.rowscale ? a.rowscale[row] : 1.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float lo = v[2 * e], hi = v[2 * e + 1];
-                    if (a.bias) {
-                        lo += __half2float(__ushort_as_half(a.bias[n + 2 * e]));
-                        hi += __half2float(__ushort_as_half(a.bias[n + 2 * e + 1]));
-                    }
-                    pk[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-                            (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
-                }
+                for (int e = 0; e < 4; ++e) pk[e] = out_pair(v[2 * e], v[2 * e + 1], rs, a.bias, n + 2 * e, a.out_bf16);
                 *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
@@ -541,7 +534,7 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
         cudaFuncSetAttribute(prefill_kernel<BM, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
     if (attr != cudaSuccess) return attr;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
-                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, p.splits, ws, tickets};
+                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, h.rowscale, h.out_bf16, p.splits, ws, tickets};
     const int nunits = args.tiles_m * args.tiles_n * p.splits;
     const int grid = nunits < sm_count() ? nunits : sm_count();
     cudaLaunchConfig_t cfg{};
