@@ -22,6 +22,7 @@
 #include <climits>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "q4_internal.cuh"
 #include "q4_tc.cuh"
@@ -171,21 +172,26 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 uint32_t r[32];
                 tmem_ld_x32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + c0, r);
                 if (row < a.M) {
-                    const float rs = a.rowscale ? a.rowscale[row] : 1.f;
+                    // one branch per 32 columns into fp16-only or bf16-only code
+                    auto store = [&](auto bf16c) {
+                        constexpr bool BF = decltype(bf16c)::value;
+                        const float rs = BF && a.rowscale ? a.rowscale[row] : 1.f;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int n = n0 + c0 + 8 * v;
-                        if (n < a.N) {
-                            uint32_t pk[4];
+                        for (int v = 0; v < 4; ++v) {
+                            const int n = n0 + c0 + 8 * v;
+                            if (n < a.N) {
+                                uint32_t pk[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                pk[e] = out_pair(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]),
-                                                 rs, a.bias, n + 2 * e, a.out_bf16);
+                                for (int e = 0; e < 4; ++e)
+                                    pk[e] = out_pair_t<BF>(__uint_as_float(r[8 * v + 2 * e]),
+                                                           __uint_as_float(r[8 * v + 2 * e + 1]), rs, a.bias, n + 2 * e);
+                                *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
+                                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
                             }
-                            *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
-                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
-                    }
+                    };
+                    if (a.out_bf16) store(std::true_type{});
+                    else store(std::false_type{});
                 }
             }
         }

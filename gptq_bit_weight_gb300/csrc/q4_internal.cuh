@@ -183,6 +183,20 @@ __device__ __forceinline__ uint16_t out_one(float acc, float rs, const uint16_t 
     if (bias) v += __half2float(__ushort_as_half(bias[n]));
     return static_cast<uint16_t>(out_bits(v, bf16));
 }
+// The same with the output type fixed at compile time (fp16: no row scale),
+// for epilogues on a kernel's critical path.
+template <bool BF16>
+__device__ __forceinline__ uint32_t out_pair_t(float lo, float hi, float rs, const uint16_t *bias, int n) {
+    if (BF16) {
+        lo *= rs;
+        hi *= rs;
+    }
+    if (bias) {
+        lo += __half2float(__ushort_as_half(bias[n]));
+        hi += __half2float(__ushort_as_half(bias[n + 1]));
+    }
+    return out_bits(lo, BF16) | (out_bits(hi, BF16) << 16);
+}
 __device__ __forceinline__ uint32_t out_pair(float lo, float hi, float rs, const uint16_t *bias, int n, bool bf16) {
     lo *= rs;
     hi *= rs;
