@@ -678,6 +678,30 @@ def run_next_rows(q4, torch, dev, stream, hbm_gbs):
                               "M=512_us": round(t512 * 1e6, 2),
                               "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / t512 / 1e12, 1)}
     del mats
+    # bf16 activations and outputs on the 4-bit layer (one preparation launch
+    # per call scales and rounds x to fp16): decode at M = 1, prefill at M = 512
+    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
+    for m in mats:
+        m.set_act_dtype(torch.bfloat16)
+        m.reserve(512)
+    xb1 = t(synthetic.activations_bf16(1, 4096, key=(35, 1)).view(np.int16)).view(torch.bfloat16)
+    xb512 = t(synthetic.activations_bf16(512, 4096, key=(35, 512)).view(np.int16)).view(torch.bfloat16)
+    ob1 = torch.empty((1, 11008), dtype=torch.bfloat16, device=dev)
+    ob512 = torch.empty((512, 11008), dtype=torch.bfloat16, device=dev)
+
+    def issue_b1(sp):
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, xb1.data_ptr(), 1, ob1.data_ptr(), sp)
+
+    def issue_b512(sp):
+        q4.gptq_q4_matmul(mats[0].handle, xb512.data_ptr(), 512, ob512.data_ptr(), sp)
+
+    tb1 = _graph_time(torch, stream, issue_b1) / len(mats)
+    tb512 = _graph_time(torch, stream, issue_b512)
+    res["bf16 4096x11008"] = {"M=1_us": round(tb1 * 1e6, 2), "M=1_TB/s": round(L.weight_bytes / tb1 / 1e12, 3),
+                              "M=512_us": round(tb512 * 1e6, 2),
+                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / tb512 / 1e12, 1)}
+    del mats
     # GPU packer: float weights (fp16) + scales + zeros -> qweight/qzeros
     K, N, gs = 4096, 11008, 128
     g = np.random.default_rng(5)
