@@ -186,6 +186,32 @@ cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t 
     return cudaGetLastError();
 }
 
+// Programmatic dependent launch for the activation kernels: the dependent
+// decode / prefill grid may launch at once (its weight prefetch needs nothing
+// from here), while these kernels wait for the preceding grid before they
+// read x or overwrite temp_state, which that grid may still be reading.
+// Used for M <= 8 (the register-streaming decode follows), where it measured
+// 10-30 % faster per call; at M = 16 (the TMA-ring decode) it measured slower.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(bool pdl, Kern kern, int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl && pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ------------------------------------------------------------- xreorder
 // temp_state[m][j] = x[m][P[j]] (0 where P[j] = -1, a padding row): eight
 // consecutive j per thread, written as one 16-byte store; the gathered reads
@@ -198,6 +224,7 @@ __device__ __forceinline__ uint32_t gather2(const uint16_t *xr, int pa, int pb) 
 
 __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int Kx,
                                 int K, uint16_t *__restrict__ ts) {
+    pdl_enter();
     const size_t total = static_cast<size_t>(M) * (K / 8);
     for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -223,6 +250,7 @@ __global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__re
                                                              const int32_t *__restrict__ perm, int M, int Kx, int K,
                                                              uint16_t *__restrict__ ts) {
     extern __shared__ __align__(16) unsigned char sm[];
+    pdl_enter();
     int32_t *sp = reinterpret_cast<int32_t *>(sm);
     uint16_t *sx = reinterpret_cast<uint16_t *>(sm + static_cast<size_t>(K) * 4);
     const int nvx = Kx / 8, nv = K / 8;                    // 16-byte vectors per x row / temp_state row
@@ -256,15 +284,14 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
         if (attr != cudaSuccess) return attr;
         const int per_sm = static_cast<int>((228 * 1024) / (rows_smem + 1024));
         const int ctas = std::min(M, kSMs * std::max(1, std::min(per_sm, 8)));
-        xreorder_rows_kernel<<<ctas, 256, rows_smem, s>>>(x, perm, M, Kx, K, temp_state);
-        return cudaGetLastError();
+        return launch_pdl(M <= 8, xreorder_rows_kernel, ctas, 256, rows_smem, s, x, perm, M, Kx, K, temp_state);
     }
     const size_t total = static_cast<size_t>(M) * (K / 8);
     const int threads = 256;
     const size_t want = (total + threads - 1) / threads;
     const int blocks = static_cast<int>(want < static_cast<size_t>(kSMs) * 16 ? want : static_cast<size_t>(kSMs) * 16);
-    xreorder_kernel<<<blocks > 0 ? blocks : 1, threads, 0, s>>>(x, perm, M, Kx, K, temp_state);
-    return cudaGetLastError();
+    return launch_pdl(M <= 8, xreorder_kernel, blocks > 0 ? blocks : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
+                      temp_state);
 }
 
 // --------------------------------------------------- bf16 activations
@@ -273,10 +300,12 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
 // fp32) is rounded once to fp16.  A bf16 value has an 8-bit significand, so
 // the fp16 value is exact unless it lies more than ~2^28 below the row's
 // largest.  The kernels' epilogues multiply the fp32 sums by 2^e (exact).
-__global__ void __launch_bounds__(256) xprep_bf16_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(1024) xprep_bf16_kernel(const uint16_t *__restrict__ x,
                                                          const int32_t *__restrict__ perm, int M, int Kx, int K,
                                                          uint16_t *__restrict__ ts, float *__restrict__ rowscale) {
-    __shared__ float wmax[8];
+    __shared__ float wmax[32];
+    pdl_enter();
+    const int nw = blockDim.x >> 5;
     for (int m = blockIdx.x; m < M; m += gridDim.x) {
         const uint16_t *xr = x + static_cast<size_t>(m) * Kx;
         float mx = 0.f;
@@ -286,7 +315,7 @@ __global__ void __launch_bounds__(256) xprep_bf16_kernel(const uint16_t *__restr
         if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
         __syncthreads();
         mx = wmax[0];
-        for (int w = 1; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+        for (int w = 1; w < nw; ++w) mx = fmaxf(mx, wmax[w]);
         __syncthreads();                               // wmax is reused by the next row
         // e = ilogb(max) - 14, kept where 2^-e and 2^e are normal fp32 values
         int e = 0;
@@ -304,9 +333,11 @@ __global__ void __launch_bounds__(256) xprep_bf16_kernel(const uint16_t *__restr
 
 cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
                               float *rowscale, cudaStream_t s) {
+    // one CTA per row; wide CTAs when there are few rows
     const int ctas = std::min(M, kSMs * 8);
-    xprep_bf16_kernel<<<ctas > 0 ? ctas : 1, 256, 0, s>>>(x, perm, M, Kx, K, temp_state, rowscale);
-    return cudaGetLastError();
+    const int threads = M <= kSMs ? 1024 : 256;
+    return launch_pdl(M <= 8, xprep_bf16_kernel, ctas > 0 ? ctas : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
+                      temp_state, rowscale);
 }
 
 }  // namespace q4
