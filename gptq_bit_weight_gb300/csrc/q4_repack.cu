@@ -192,8 +192,11 @@ cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t 
 // read x or overwrite temp_state, which that grid may still be reading.
 // Used for M <= 8 (the register-streaming decode follows), where it measured
 // 10-30 % faster per call; at M = 16 (the TMA-ring decode) it measured slower.
-__device__ __forceinline__ void pdl_enter() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+// (early: let the dependent grid launch now; otherwise it launches when this
+// grid ends, which keeps a TMA-ring decode from holding SM slots the gather
+// still needs.)
+__device__ __forceinline__ void pdl_enter(bool early) {
+    if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -224,7 +227,7 @@ __device__ __forceinline__ uint32_t gather2(const uint16_t *xr, int pa, int pb) 
 
 __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int Kx,
                                 int K, uint16_t *__restrict__ ts) {
-    pdl_enter();
+    pdl_enter(M <= 8);
     const size_t total = static_cast<size_t>(M) * (K / 8);
     for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__re
                                                              const int32_t *__restrict__ perm, int M, int Kx, int K,
                                                              uint16_t *__restrict__ ts) {
     extern __shared__ __align__(16) unsigned char sm[];
-    pdl_enter();
+    pdl_enter(M <= 8);
     int32_t *sp = reinterpret_cast<int32_t *>(sm);
     uint16_t *sx = reinterpret_cast<uint16_t *>(sm + static_cast<size_t>(K) * 4);
     const int nvx = Kx / 8, nv = K / 8;                    // 16-byte vectors per x row / temp_state row
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(1024) xprep_bf16_kernel(const uint16_t *__rest
                                                          const int32_t *__restrict__ perm, int M, int Kx, int K,
                                                          uint16_t *__restrict__ ts, float *__restrict__ rowscale) {
     __shared__ float wmax[32];
-    pdl_enter();
+    pdl_enter(M <= 8);
     const int nw = blockDim.x >> 5;
     for (int m = blockIdx.x; m < M; m += gridDim.x) {
         const uint16_t *xr = x + static_cast<size_t>(m) * Kx;
