@@ -81,7 +81,8 @@ extern "C" {
 #define GPTQ_Q4_PATH_PREFILL   2  /* always the fused shared-memory-dequant tensor-core kernel */
 #define GPTQ_Q4_PATH_DECODE_MMA 3 /* always the register-streaming decode kernel */
 #define GPTQ_Q4_PATH_DECODE_TC 4  /* decode on tcgen05 with one tensor-memory accumulator per
-                                     quantization group (M <= 16, else register-streaming) */
+                                     quantization group (M <= 16 on 4-bit handles with fp16
+                                     activations; otherwise as GPTQ_Q4_PATH_DECODE) */
 #define GPTQ_Q4_PATH_DECODE_RING 5 /* the TMA-ring decode kernel whenever the shape allows it
                                       (M <= 16, a K slice within 48 groups), else
                                       register-streaming */
