@@ -11,7 +11,10 @@ Metric: effective HBM bandwidth of decode, algorithmic bytes (qweight +
 qzeros + scales as stored) per second, whole job.  Also reported: the
 decode kernel's roofline fraction (per-launch CUDA events), the end-to-end
 figure through the C ABI with host buffers, the CPU oracle timed on this
-host, SM clocks during the run, and the prefill_7b tensor-core numbers.
+host, SM clocks during the run, the prefill_7b tensor-core numbers, the
+Llama-70B M = 1 layers and the act-order decode workload, and (next_rows)
+the rows past the hot path: fused Q/K/V projections, GPTQ_V2, 8-bit codes,
+bf16 activations and the GPU packer.
 
 --impl reference times the CPU oracle (the plain dequantize-then-matmul
 route) on the same workload, one shape per step.
