@@ -399,6 +399,10 @@ gptq_q4_handle gptq_q4_make8(const int32_t *qweight, const int32_t *qzeros, cons
     }
     const int geff = groupsize == -1 ? K : groupsize;
     const int G = K / geff;
+    if (K % 64 || N % 64) {   // the split layer has 2K rows, but x and the unfused route keep K
+        set_status(GPTQ_Q4_UNSUPPORTED, "the GPU kernels need K %% 64 == 0 and N %% 64 == 0 (K=%d N=%d)", K, N);
+        return nullptr;
+    }
     int dev = -1;
     if (check_device_sm103(&dev) != GPTQ_Q4_OK) return nullptr;
     if (check_device_ptr(qweight, dev, "qweight") || check_device_ptr(qzeros, dev, "qzeros") ||
