@@ -58,8 +58,26 @@ def test_null_handle_is_invalid_argument(lib_path):
     assert lib.gptq_q4_set_format(None, q4.GPTQ_Q4_FORMAT_GPTQ_V2) == q4.GPTQ_Q4_INVALID_ARGUMENT
     assert lib.gptq_q4_debug_wait_probe(None, 1000, None) == q4.GPTQ_Q4_INVALID_ARGUMENT
     assert lib.gptq_q4_info(None, None, None, None, None, None, None) == q4.GPTQ_Q4_INVALID_ARGUMENT
+    assert lib.gptq_q4_set_act_dtype(None, q4.GPTQ_Q4_DTYPE_BF16) == q4.GPTQ_Q4_INVALID_ARGUMENT
     assert q4.gptq_q4_last_status() == q4.GPTQ_Q4_INVALID_ARGUMENT
     q4.gptq_q4_free(None)
+
+
+def test_make_argument_errors_need_no_device(lib_path):
+    """Checks that come before any device call: NULL tensors, bad sizes."""
+    import gptq_bit_weight_gb300 as q4
+    lib = q4._lib
+    for make in (lib.gptq_q4_make, lib.gptq_q4_make8):
+        assert not make(None, None, None, None, 256, 256, 128)
+        assert q4.gptq_q4_last_status() == q4.GPTQ_Q4_INVALID_ARGUMENT
+        assert "NULL" in q4.gptq_q4_last_error()
+        p = ctypes.c_void_p(16)                      # never dereferenced: the sizes are checked first
+        assert not make(p, p, p, None, 256, 250, 128)
+        assert q4.gptq_q4_last_status() == q4.GPTQ_Q4_INVALID_ARGUMENT
+        assert not make(p, p, p, None, 256, 256, 100)   # groupsize must divide K
+        assert q4.gptq_q4_last_status() == q4.GPTQ_Q4_INVALID_ARGUMENT
+    assert not lib.gptq_q4_make8(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), None, 96, 256, 32)
+    assert q4.gptq_q4_last_status() == q4.GPTQ_Q4_UNSUPPORTED    # K % 64
 
 
 def test_missing_library_fails_loudly(tmp_path):
