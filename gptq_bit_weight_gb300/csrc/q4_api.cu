@@ -610,19 +610,30 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
 
 static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out, cudaStream_t stream,
                       int path) {
+    // Which decode kernel: measured on GB300 (CUDA-graph replays over more
+    // weights than L2), the register-streaming kernel (with its shared
+    // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
+    // layers below 64 Mi weights and at any M on layers below 24 Mi weights;
+    // the TMA-ring kernel is ahead everywhere else it applies.
+    const size_t weights = static_cast<size_t>(h->K) * h->N;
+    const bool small_layer =
+        M <= 4 || weights < (size_t{24} << 20) || (M <= 8 && weights < (size_t{64} << 20));
+    // the activation kernel lets the decode grid start early when that grid
+    // is the register-streaming kernel at M <= 8 (measured faster only there)
+    const bool early = M <= 8 && (path == GPTQ_Q4_PATH_DECODE_MMA || (path == GPTQ_Q4_PATH_DECODE && small_layer));
     const uint16_t *xin = x;
     if (h->act_bf16) {
         // bf16 x: scaled by a power of two per row and rounded once to fp16
         // (gathered at the same time under act-order); the epilogues undo the scale
         if (int r = ensure_temp_state(h, M, stream, false)) return r;
         Q4_CUDA(q4::launch_xprep_bf16(x, h->act_order ? h->perm : nullptr, M, h->Kx, h->K, h->temp_state,
-                                      h->rowscale, stream),
+                                      h->rowscale, stream, early),
                 "bf16 preparation launch");
         ++g_launches;
         xin = h->temp_state;
     } else if (h->act_order) {
         if (int r = ensure_temp_state(h, M, stream, false)) return r;
-        Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, h->temp_state, stream), "xreorder launch");
+        Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, h->temp_state, stream, early), "xreorder launch");
         ++g_launches;
         xin = h->temp_state;
     }
@@ -644,14 +655,6 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    // Which decode kernel: measured on GB300 (CUDA-graph replays over more
-    // weights than L2), the register-streaming kernel (with its shared
-    // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
-    // layers below 64 Mi weights and at any M on layers below 24 Mi weights;
-    // the TMA-ring kernel is ahead everywhere else it applies.
-    const size_t weights = static_cast<size_t>(h->K) * h->N;
-    const bool small_layer =
-        M <= 4 || weights < (size_t{24} << 20) || (M <= 8 && weights < (size_t{64} << 20));
     if ((path == GPTQ_Q4_PATH_DECODE && !small_layer) || path == GPTQ_Q4_PATH_DECODE_RING) {
         const q4::DecodeRingPlan rp = q4::plan_decode_ring(M, h->K, h->N, h->geff, q4::device_sm_count());
         if (rp.ok) {

@@ -222,13 +222,15 @@ cudaError_t launch_debug_unpack(const HandleView &h, uint8_t *q, uint8_t *z, cud
 cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t s);
 // temp_state[m][j] = x[m][perm[j]] (0 where perm[j] = -1); x rows hold Kx
 // values, temp_state rows K
+// (early: launched so that the next grid, a register-streaming decode, may
+// start now; only measured faster before that kernel)
 cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int Kx, int K,
-                            uint16_t *temp_state, cudaStream_t s);
+                            uint16_t *temp_state, cudaStream_t s, bool early = false);
 // bf16 activations: per row m, e_m with max|x[m]| * 2^-e_m in [2^14, 2^15),
 // temp_state[m][j] = fp16(x[m][perm[j]] * 2^-e_m) (perm NULL: j; -1: 0) and
 // rowscale[m] = 2^e_m
 cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
-                              float *rowscale, cudaStream_t s);
+                              float *rowscale, cudaStream_t s, bool early = false);
 
 // decode (q4_decode.cu)
 struct DecodePlan {

@@ -100,12 +100,12 @@ extern "C" int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M
     const uint16_t *xin = x;
     if (h->act_bf16) {
         if ((e = q4::launch_xprep_bf16(x, h->act_order ? h->perm : nullptr, M, h->Kx, h->K, temp_state, rowscale,
-                                       stream)) != cudaSuccess)
+                                       stream, M <= 8)) != cudaSuccess)
             return q4::api_cuda_fail(e, "bf16 preparation launch");
         q4::api_count_launches(1);
         xin = temp_state;
     } else if (h->act_order) {
-        if ((e = q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, temp_state, stream)) != cudaSuccess)
+        if ((e = q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, temp_state, stream, M <= 8)) != cudaSuccess)
             return q4::api_cuda_fail(e, "xreorder launch");
         q4::api_count_launches(1);
         xin = temp_state;

@@ -190,8 +190,9 @@ cudaError_t launch_dequant(const HandleView &h, uint16_t *temp_dq, cudaStream_t 
 // decode / prefill grid may launch at once (its weight prefetch needs nothing
 // from here), while these kernels wait for the preceding grid before they
 // read x or overwrite temp_state, which that grid may still be reading.
-// Used for M <= 8 (the register-streaming decode follows), where it measured
-// 10-30 % faster per call; at M = 16 (the TMA-ring decode) it measured slower.
+// Used when the register-streaming decode follows (early), where it measured
+// 10-30 % faster per call at M <= 8; before the TMA-ring decode (M = 16) it
+// measured slower.
 // (early: let the dependent grid launch now; otherwise it launches when this
 // grid ends, which keeps a TMA-ring decode from holding SM slots the gather
 // still needs.)
@@ -226,8 +227,8 @@ __device__ __forceinline__ uint32_t gather2(const uint16_t *xr, int pa, int pb) 
 }
 
 __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int Kx,
-                                int K, uint16_t *__restrict__ ts) {
-    pdl_enter(M <= 8);
+                                int K, uint16_t *__restrict__ ts, bool early) {
+    pdl_enter(early);
     const size_t total = static_cast<size_t>(M) * (K / 8);
     for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -251,9 +252,9 @@ __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *_
 // memory).  Rows are taken round-robin by the CTAs.
 __global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__restrict__ x,
                                                              const int32_t *__restrict__ perm, int M, int Kx, int K,
-                                                             uint16_t *__restrict__ ts) {
+                                                             uint16_t *__restrict__ ts, bool early) {
     extern __shared__ __align__(16) unsigned char sm[];
-    pdl_enter(M <= 8);
+    pdl_enter(early);
     int32_t *sp = reinterpret_cast<int32_t *>(sm);
     uint16_t *sx = reinterpret_cast<uint16_t *>(sm + static_cast<size_t>(K) * 4);
     const int nvx = Kx / 8, nv = K / 8;                    // 16-byte vectors per x row / temp_state row
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__re
 }
 
 cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool early) {
     const size_t rows_smem = static_cast<size_t>(K) * 4 + static_cast<size_t>(Kx) * 2;   // permutation + one row
     if (M >= 32 && rows_smem <= 200 * 1024) {
         static cudaError_t attr =
@@ -287,14 +288,14 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
         if (attr != cudaSuccess) return attr;
         const int per_sm = static_cast<int>((228 * 1024) / (rows_smem + 1024));
         const int ctas = std::min(M, kSMs * std::max(1, std::min(per_sm, 8)));
-        return launch_pdl(M <= 8, xreorder_rows_kernel, ctas, 256, rows_smem, s, x, perm, M, Kx, K, temp_state);
+        return launch_pdl(early, xreorder_rows_kernel, ctas, 256, rows_smem, s, x, perm, M, Kx, K, temp_state, early);
     }
     const size_t total = static_cast<size_t>(M) * (K / 8);
     const int threads = 256;
     const size_t want = (total + threads - 1) / threads;
     const int blocks = static_cast<int>(want < static_cast<size_t>(kSMs) * 16 ? want : static_cast<size_t>(kSMs) * 16);
-    return launch_pdl(M <= 8, xreorder_kernel, blocks > 0 ? blocks : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
-                      temp_state);
+    return launch_pdl(early, xreorder_kernel, blocks > 0 ? blocks : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
+                      temp_state, early);
 }
 
 // --------------------------------------------------- bf16 activations
@@ -305,9 +306,10 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
 // largest.  The kernels' epilogues multiply the fp32 sums by 2^e (exact).
 __global__ void __launch_bounds__(1024) xprep_bf16_kernel(const uint16_t *__restrict__ x,
                                                          const int32_t *__restrict__ perm, int M, int Kx, int K,
-                                                         uint16_t *__restrict__ ts, float *__restrict__ rowscale) {
+                                                         uint16_t *__restrict__ ts, float *__restrict__ rowscale,
+                                                         bool early) {
     __shared__ float wmax[32];
-    pdl_enter(M <= 8);
+    pdl_enter(early);
     const int nw = blockDim.x >> 5;
     for (int m = blockIdx.x; m < M; m += gridDim.x) {
         const uint16_t *xr = x + static_cast<size_t>(m) * Kx;
@@ -335,12 +337,12 @@ __global__ void __launch_bounds__(1024) xprep_bf16_kernel(const uint16_t *__rest
 }
 
 cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
-                              float *rowscale, cudaStream_t s) {
+                              float *rowscale, cudaStream_t s, bool early) {
     // one CTA per row; wide CTAs when there are few rows
     const int ctas = std::min(M, kSMs * 8);
     const int threads = M <= kSMs ? 1024 : 256;
-    return launch_pdl(M <= 8, xprep_bf16_kernel, ctas > 0 ? ctas : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
-                      temp_state, rowscale);
+    return launch_pdl(early, xprep_bf16_kernel, ctas > 0 ? ctas : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
+                      temp_state, rowscale, early);
 }
 
 }  // namespace q4
