@@ -209,6 +209,26 @@ def test_8bit_closed_forms():
             assert (dq.w16.view(np.float16).astype(np.float64) == float(code - zero - zo)).all()
 
 
+def test_8bit_uneven_groups_brute_force_tiny():
+    """A 16 x 8 layer with 8-bit codes and groups of 5 and 11 rows, element by
+    element from the packing (byte k % 4 of word k / 4; byte n % 4 of zero
+    word n / 4), rounded by numpy's float16 cast."""
+    g = np.random.default_rng(17)
+    K, N, gs = 16, 8, 8
+    qw = g.integers(0, 2**32, size=(K // 4, N), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    qz = g.integers(0, 2**32, size=(2, N // 4), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    s = g.uniform(0.0002, 0.002, size=(2, N)).astype(np.float16)
+    gi = np.array([0] * 5 + [1] * 11, np.int32)[g.permutation(K)]
+    dq = oracle.dequantize_layer(qw, qz, s, gi, K, N, gs, bits=8)
+    for k in range(K):
+        for n in range(N):
+            q = (int(qw.view(np.uint32)[k // 4, n]) >> (8 * (k % 4))) & 0xFF
+            z = (int(qz.view(np.uint32)[gi[k], n // 4]) >> (8 * (n % 4))) & 0xFF
+            w = float(s[gi[k], n]) * (q - z - 1)
+            assert dq.q[k, n] == q and dq.z[gi[k], n] == z
+            assert dq.w16[k, n] == np.float16(w).view(np.uint16)
+
+
 def test_8bit_layer_with_nibble_codes_equals_4bit_layer():
     """Codes and zeros below 16 packed as an 8-bit and as a 4-bit checkpoint
     describe the same weights: both oracle routes agree bit for bit."""
