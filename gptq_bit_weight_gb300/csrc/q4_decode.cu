@@ -43,10 +43,48 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <mutex>
+#include <vector>
 
 #include "q4_internal.cuh"
 
 namespace q4 {
+
+// Per (kernel, device, size): set a kernel's dynamic shared-memory limit.
+// The attribute belongs to the device that is current, so every device the
+// library runs on gets its own set-up; each is done once.  bytes < 0: the
+// largest the device allows beside the kernel's static shared memory.  The
+// limit set is returned in *set.
+cudaError_t dyn_smem_optin(const void *fn, int dev, int bytes, int *set) {
+    struct Entry {
+        const void *fn;
+        int dev;
+        int want;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &en : done)
+        if (en.fn == fn && en.dev == dev && en.want == bytes) {
+            if (set) *set = en.bytes;
+            return cudaSuccess;
+        }
+    int val = bytes;
+    cudaError_t e = cudaSuccess;
+    if (bytes < 0) {
+        int optin = 0;
+        cudaFuncAttributes fa{};
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, fn);
+        val = optin - static_cast<int>(fa.sharedSizeBytes);
+    }
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, val);
+    if (e != cudaSuccess) return e;
+    done.push_back(Entry{fn, dev, bytes, val});
+    if (set) *set = val;
+    return cudaSuccess;
+}
 
 namespace {
 
@@ -569,20 +607,15 @@ cudaError_t launch_mt(const HandleView &h, const DecodePlan &p, const DecodeWork
                       uint16_t *out, cudaStream_t s) {
     const int xrows = M < 8 * MT ? M : 8 * MT;
     const size_t smem = smem_bytes_for(MT, SR, XR, xrows, p.slice_chunks, max_groups_in_slice(p.slice_chunks, h.geff));
-    // Opt in once to the largest dynamic shared memory the device allows
-    // next to the kernel's static shared memory.
-    static int max_dyn = -1;
-    if (max_dyn < 0) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa{};
+    // Opt in, once per device, to the largest dynamic shared memory the
+    // device allows next to the kernel's static shared memory.
+    int max_dyn = 0;
+    {
+        int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_kernel<MT, RAW, SR, XR>);
-        const int want = optin - static_cast<int>(fa.sharedSizeBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_kernel<MT, RAW, SR, XR>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+            e = dyn_smem_optin(reinterpret_cast<const void *>(decode_kernel<MT, RAW, SR, XR>), dev, -1, &max_dyn);
         if (e != cudaSuccess) return e;
-        max_dyn = want;
     }
     if (smem > static_cast<size_t>(max_dyn)) return cudaErrorInvalidConfiguration;
     DecodeArgs a{x, out, w.ws, w.tickets, M, p.splits, p.slice_chunks, xrows, p.cluster};

@@ -436,9 +436,11 @@ __global__ void __launch_bounds__(kThreads, 3)
 
 template <int MT, int MP>
 cudaError_t ensure_attr() {
-    static cudaError_t e = cudaFuncSetAttribute(decode_ring_kernel<MT, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                RingCfg<MT>::kSmem);
-    return e;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return dyn_smem_optin(reinterpret_cast<const void *>(decode_ring_kernel<MT, MP>), dev, RingCfg<MT>::kSmem,
+                          nullptr);
 }
 
 // Rows of x per group slot for M rows (8: no slots)

@@ -274,6 +274,9 @@ struct DecodeRingPlan {
 DecodeRingPlan plan_decode_ring(int M, int K, int N, int geff, int sms);
 cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &plan, const uint16_t *x, int M,
                                uint16_t *out, cudaStream_t s);
+// Dynamic shared-memory limit of kernel fn on device dev, set once per
+// (fn, dev, bytes); bytes < 0 asks for the device's largest (q4_decode.cu)
+cudaError_t dyn_smem_optin(const void *fn, int dev, int bytes, int *set);
 // SMs of the current device (queried once)
 int device_sm_count();
 // programmatic dependent launch switch (GPTQ_Q4_PDL=0 turns it off)

@@ -19,6 +19,7 @@
 // The weights of the handle were copied at gptq_q4_make time, which does
 // allocate: only the per-call work is allocation-free.  This entry point has
 // no counterpart on the web pages the rest of the library follows.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -29,29 +30,75 @@
 namespace {
 
 constexpr size_t kScratchBytes = static_cast<size_t>(GPTQ_Q4_NOALLOC_SCRATCH_BYTES);
-constexpr int kMaxDevices = 64;
 
 // One array per device, shared by every call on that device; each call
 // leaves its contents behind for the next.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
 // In host code the name g_noalloc_scratch is only a host-side stand-in, not a
 // device address: a kernel handed it would fault or touch the wrong memory.
-// The device address comes from cudaGetSymbolAddress, once per device, with
-// that device current (the first call on each device does this).
-cudaError_t scratch_address(int dev, void **out) {
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+// The device address comes from cudaGetSymbolAddress, called with the device
+// current.  The address belongs to the CUDA context that is current, not
+// just to the device: a host framework may run this library inside a context
+// of its own, and a context destroyed by cudaDeviceReset takes its mapping
+// with it.  So the set-up runs once per context, and the cache is keyed by the
+// context's process-unique ID (cuCtxGetId; IDs are never reused, so a context
+// made after a reset never finds a stale entry).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_setup_mutex;
+ScratchEntry g_entries[kMaxContexts] = {};
+int g_used = 0, g_next_evict = 0;
+
+bool driver_fns(CtxGetCurrentFn *get_current, CtxGetIdFn *get_id) {
+    static CtxGetCurrentFn cur = nullptr;
+    static CtxGetIdFn id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+    });
+    *get_current = cur;
+    *get_id = id;
+    return cur && id;
+}
+
+// The array's device address in the current context (the caller has made the
+// handle's device current).  The first call in each context looks it up.
+cudaError_t scratch_address(void **out) {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+    if (!driver_fns(&get_current, &get_id)) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    unsigned long long ctx_id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &ctx_id) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    for (int i = 0; i < g_used; ++i)
+        if (g_entries[i].ctx_id == ctx_id) {
+            *out = g_entries[i].ptr;
+            return cudaSuccess;
+        }
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    int slot = g_used < kMaxContexts ? g_used++ : (g_next_evict++ % kMaxContexts);
+    g_entries[slot] = ScratchEntry{ctx_id, p};
+    *out = p;
     return cudaSuccess;
 }
 
@@ -80,11 +127,9 @@ extern "C" int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M
                  M, h->K, h->N, need, kScratchBytes);
         return q4::api_set_status(GPTQ_Q4_INVALID_ARGUMENT, msg);
     }
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return q4::api_cuda_fail(e, "cudaGetDevice");
     void *base = nullptr;
-    if ((e = scratch_address(dev, &base)) != cudaSuccess)
+    cudaError_t e;
+    if ((e = scratch_address(&base)) != cudaSuccess)
         return q4::api_cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
     unsigned char *scratch = static_cast<unsigned char *>(base);
     int *tickets = reinterpret_cast<int *>(scratch);

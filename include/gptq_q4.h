@@ -185,7 +185,11 @@ int gptq_q4_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
  * Errors: INVALID_ARGUMENT, CUDA_ERROR. */
 int gptq_q4_dequant(gptq_q4_handle h, uint16_t *temp_dq, cudaStream_t stream);
 
-/* The unpacked codes, read back from the handle's private layout:
+/* The unpacked codes, read back from the handle's private layout (a debug
+ * read-back; no passage of the pages defines it: "Inference Backends",
+ * "Packing, conversion, and runtime initialization" only says runtime
+ * initialization may repack into a private layout, and this call shows that
+ * the repack kept every code):
  *   q  device uint8 [K][N], q[k][n] in 0..15, ORIGINAL row order
  *   z  device uint8 [G][N], stored zero points (without the +1)
  * Either pointer may be NULL to skip it.  For checking the repack bit-exactly.
@@ -229,9 +233,12 @@ int gptq_q4_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias,
  * the library holds until the process exits.  Arguments, layouts and results
  * are those of gptq_q4_matmul (x, out: device fp16, 16-byte aligned).
  *
- *   - The first call on each device does a one-time set-up (it looks up the
- *     array's device address with cudaGetSymbolAddress, with that device
- *     current); make that first call before any stream capture.
+ *   - The first call in each CUDA context does a one-time set-up: it looks
+ *     up the array's device address with cudaGetSymbolAddress, with the
+ *     handle's device current, and keeps it keyed by the context's unique ID
+ *     (the primary context, or one the caller made current).  A context made
+ *     after cudaDeviceReset is a new context and gets its own set-up.  Make
+ *     the first call in a context before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents;
  *     the call clears what must start at zero (the tickets) on its stream.
  *     Calls that overlap on the GPU (other streams, other handles, other
@@ -334,11 +341,16 @@ int gptq_q4_info(gptq_q4_handle h, int *K, int *N, int *groupsize, int *G,
 int gptq_q4_device_error(gptq_q4_handle h);
 
 /* Release everything the handle owns (synchronizes its device).  NULL is a
- * no-op. */
+ * no-op.  Lifecycle only; the pages' nearest passage is "Inference
+ * Backends", "Runtime cache lifetime" (native runtime storage belongs to the
+ * handle, and nothing outlives it). */
 void gptq_q4_free(gptq_q4_handle h);
 
-/* Q4Matrix handle for an 8-bit GPTQ layer ("Inference Backends", "GPTQ
- * kernel contract": 8-bit codes pack four to an int32 along K).
+/* Q4Matrix handle for an 8-bit GPTQ layer.  "Inference Backends",
+ * "Hardware, dependency, and format requirements": the GPTQ Marlin row
+ * declares bits 4 and 8, and the Swordfish row says GPTQ supports 4/8-bit.
+ * The pages print no 8-bit layout; this library reads it as the 4-bit
+ * GPTQ packing with 32 / 8 = 4 codes per int32:
  *   qweight  device int32 [K/4][N]   four 8-bit codes per word along K,
  *                                   lowest byte = lowest row
  *   qzeros   device int32 [G][N/4]   four 8-bit zero points per word along N
@@ -357,7 +369,11 @@ gptq_q4_handle gptq_q4_make8(const int32_t *qweight, const int32_t *qzeros,
                              const uint16_t *scales, const int32_t *g_idx,
                              int K, int N, int groupsize);
 
-/* Status and message of the last call made on this host thread. */
+/* Status and message of the last call made on this host thread.
+ * "Inference Backends", "Hardware, dependency, and format requirements":
+ * device-validation errors keep the kernel's specific reason (an unsupported
+ * compute capability, a missing kernel image) instead of a generic one; the
+ * message names the argument or limit that failed. */
 int gptq_q4_last_status(void);
 const char *gptq_q4_last_error(void);
 

@@ -2,7 +2,9 @@
 groupsize and act-order combination at full size on the GPU, with the oracle
 evaluated on a seeded sample of 8-column blocks (a block is one qzeros word,
 so the oracle runs on exactly those columns of the real tensors) and, for
-the largest M, a seeded row sample."""
+the largest M, a seeded row sample.  Every M of the workload runs on every
+layer configuration through the default path; M = 16 and 64 also run the
+decode and prefill paths forced."""
 import numpy as np
 import pytest
 
@@ -55,8 +57,7 @@ def test_sweep_70b_sampled(q4, K, N, gs, act):
     assert np.array_equal(q_gpu[:, tcols].cpu().numpy(), dq.q)
     assert np.array_equal(w_gpu[:, tcols].cpu().numpy().view(np.uint16), dq.w16)
     del q_gpu, w_gpu
-    Ms = [1, 8, 64, 256, 2048] if gs == 128 else [1, 16, 2048]
-    for M in Ms:
+    for M in synthetic.SWEEP_70B_M:
         x = synthetic.workload_x("sweep_70b", K, N, gs, act, M)
         xd = to_dev(x)
         rows = np.arange(M) if M <= 256 else np.unique(np.concatenate(
@@ -64,7 +65,7 @@ def test_sweep_70b_sampled(q4, K, N, gs, act):
         y_ref = oracle.reference_output(x[rows], dq)
         tol = oracle.tolerance(x, dq.w16, y_ref, K)
         paths = [q4.GPTQ_Q4_PATH_AUTO]
-        if M == 64:
+        if M in (16, 64):
             paths += [q4.GPTQ_Q4_PATH_DECODE, q4.GPTQ_Q4_PATH_PREFILL]
         for path in paths:
             mat.set_path(path)

@@ -80,28 +80,39 @@ def test_prefill_fused_and_unfused_match_oracle(q4, K, N, gs, act):
     mat.device_error()
 
 
-@pytest.mark.parametrize("K,N,act", [(4096, 4096, False), (4096, 11008, True), (11008, 4096, False)])
+@pytest.mark.parametrize("act", [False, True])
+@pytest.mark.parametrize("K,N", synthetic.PREFILL_7B_SHAPES)
 def test_prefill_7b_workload_sampled(q4, K, N, act):
-    """prefill_7b shapes at M=512: full output, oracle on a row sample (all
-    N columns of 24 seeded rows, plus the first and last row)."""
-    M = 512
+    """Every prefill_7b case: the three Llama-7B shapes x {trivial, act-order}
+    x M in {512, 2048}, full output on the GPU by the fused prefill, the
+    unfused route and the decode path (past eight K slices: the last-arriver
+    reduction), oracle on a row sample (all N columns of 24 seeded rows, plus
+    the first and last row)."""
     layer = synthetic.workload_layer("prefill_7b", K, N, 128, act)
     dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, 128)
     mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
                       None, 128)
-    x = synthetic.workload_x("prefill_7b", K, N, 128, act, M)
-    rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(33).choice(M, 24, replace=False)]))
-    y_ref = oracle.reference_output(x[rows], dq)
-    tol = oracle.tolerance(x, dq.w16, y_ref, K)
-    mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
-    y = mat(to_dev(x))
-    yu = mat.matmul_unfused(to_dev(x))
-    mat.set_path(q4.GPTQ_Q4_PATH_DECODE)
-    yd = mat(to_dev(x))
-    torch.cuda.synchronize()
-    check(y[rows], y_ref, tol, f"fused {K}x{N}")
-    check(yu[rows], y_ref, tol, f"unfused {K}x{N}")
-    check(yd[rows], y_ref, tol, f"decode path {K}x{N}")
+    for M in synthetic.PREFILL_7B_M:
+        x = synthetic.workload_x("prefill_7b", K, N, 128, act, M)
+        rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(33 + M).choice(M, 24, replace=False)]))
+        y_ref = oracle.reference_output(x[rows], dq)
+        tol = oracle.tolerance(x, dq.w16, y_ref, K)
+        xd = to_dev(x)
+        mat.set_path(q4.GPTQ_Q4_PATH_AUTO)
+        ya = mat(xd)
+        mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
+        y = mat(xd)
+        yu = mat.matmul_unfused(xd)
+        mat.set_path(q4.GPTQ_Q4_PATH_DECODE)
+        yd = mat(xd)
+        torch.cuda.synchronize()
+        tr = torch.from_numpy(rows).to(DEV)
+        what = f"{K}x{N} act={act} M={M}"
+        check(ya[tr], y_ref, tol, f"default path {what}")
+        check(y[tr], y_ref, tol, f"fused {what}")
+        check(yu[tr], y_ref, tol, f"unfused {what}")
+        check(yd[tr], y_ref, tol, f"decode path {what}")
+        del ya, y, yu, yd
     mat.device_error()
 
 

@@ -525,3 +525,26 @@ def test_tolerance_catches_planted_mistakes():
     y_rev = oracle.reference_output(x, dq_rev)
     assert np.any(np.abs(y_rev - y_ref) > tol)
     del z
+
+
+def test_tolerance_hand_computed_values():
+    """The fp16 bound against values worked out by hand (not by re-evaluating
+    its formula).  K = 64, so sqrt(K) = 8.  x has two rows whose largest
+    magnitudes differ (|-4| in row 0, 0.5 in row 1); the largest |w| is |-2|.
+    With the maxima global over the whole x and w16:
+        1e-2 * 8 * 4 * 2 / 64 = 0.01
+    so every element's bound is 0.01 + 0.002 |y_ref|:
+        y_ref  =  1, -10,  0   |  100,  0.5,  -3
+        bound  = 0.012, 0.03, 0.01 | 0.21, 0.011, 0.016
+    A bound with K instead of sqrt(K) (0.08 + ...), without the /64
+    (0.64 + ...), with |y_ref| dropped, or with the maxima taken per row (row 1
+    would give 0.00125 + ...) misses these values."""
+    x = np.zeros((2, 64), np.float16)
+    x[0, 5], x[0, 9] = -4.0, 3.5
+    x[1, 0], x[1, 63] = 0.5, -0.25
+    w = np.zeros((64, 3), np.float16)
+    w[7, 1], w[40, 2] = -2.0, 1.75
+    y_ref = np.array([[1.0, -10.0, 0.0], [100.0, 0.5, -3.0]])
+    tol = oracle.tolerance(x.view(np.uint16), w.view(np.uint16), y_ref, 64)
+    expect = np.array([[0.012, 0.03, 0.01], [0.21, 0.011, 0.016]])
+    np.testing.assert_allclose(tol, expect, rtol=1e-12, atol=0)

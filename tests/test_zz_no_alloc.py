@@ -4,8 +4,9 @@ device memory, a service whose memory is budgeted up front, a loop that must
 not hit cudaMalloc's device-wide synchronization).  Its scratch lives in one
 fixed device array inside the library.
 
-Checked through the C ABI against the ordinary entry point, gptq_q4_matmul,
-on two calls in a row, within the tolerance the other parity tests use.
+Checked through the C ABI, on two calls in a row, element by element against
+the CPU oracle within the tolerance the other parity tests use, and against
+the ordinary entry point, gptq_q4_matmul, within the same tolerance.
 Collected last (file name) so that a run stopping at its first failure has
 already run every other test."""
 import numpy as np
@@ -56,7 +57,10 @@ def test_noalloc_matches_matmul_two_calls_in_a_row(q4, K, N, gs, act, M):
         out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
         q4.gptq_q4_matmul_noalloc(mat.handle, xd.data_ptr(), M, out.data_ptr(), stream)
         torch.cuda.synchronize()
-        diff = np.abs(out.float().cpu().numpy().astype(np.float64) - ref.float().cpu().numpy().astype(np.float64))
+        got = out.float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - y_oracle)
+        assert np.all(err <= tol), f"call {call}: worst |noalloc - oracle| / tol {float(np.max(err / tol)):.3f}"
+        diff = np.abs(got - ref.float().cpu().numpy().astype(np.float64))
         assert np.all(diff <= tol), f"call {call}: worst |noalloc - matmul| / tol {float(np.max(diff / tol)):.3f}"
     assert mat.info()["device_bytes"] == bytes_before
     mat.device_error()
@@ -71,11 +75,18 @@ def test_noalloc_never_grows_the_handle(q4):
     mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
                       None, gs)
     before = mat.info()["device_bytes"]
-    x = to_dev(synthetic.activations(M, K, key=(42, M)))
-    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
-    q4.gptq_q4_matmul_noalloc(mat.handle, x.data_ptr(), M, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    x = synthetic.activations(M, K, key=(42, M))
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    q4.gptq_q4_matmul_noalloc(mat.handle, to_dev(x).data_ptr(), M, out.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert mat.info()["device_bytes"] == before
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs)
+    y_oracle = oracle.reference_output(x, dq)
+    tol = oracle.tolerance(x, dq.w16, y_oracle, K)
+    err = np.abs(out.float().cpu().numpy().astype(np.float64) - y_oracle)
+    assert np.all(err <= tol), f"worst |noalloc - oracle| / tol {float(np.max(err / tol)):.3f}"
+    mat.device_error()
     mat.close()
 
 
