@@ -1,23 +1,28 @@
 """Benchmark of the fused GPTQ W4A16 linear layer on one GB300 (or N replicas).
 
-Workload (decode_7b): Llama-7B-shaped projection layers (K,N) in
-{(4096,4096), (4096,11008), (11008,4096), (4096,12288)}, groupsize 128,
-trivial g_idx, fp16 bias, x ~ N(0,1) fp16, with M in {1,2,4,8} rows.  One
-step runs every (shape, M) case once on each of R weight replicas, so that a
-weight set is touched once per step and the per-step working set (R * 81.7 MB)
-is several times the 129 MB L2: every call streams its weights from HBM.
+Headline workload (sweep_70b, M = 1): the Llama-70B projection shapes
+(K, N) in {(8192, 28672), (28672, 8192), (8192, 10240)} x groupsize in
+{32, 64, 128, -1} x {trivial, act-order g_idx} = 24 layer configurations,
+scales log-uniform [1e-3, 5e-2], x ~ N(0, 1) fp16, no bias.  Every layer
+configuration is made R times (R weight replicas, at least 3x the 129 MB L2
+per configuration), and one step is one M = 1 call on every replica of every
+configuration, captured once into a CUDA graph and replayed: each layer is
+touched once per step and ~10 GB of weights stream from HBM per step.
 
 Metric: effective HBM bandwidth of decode, algorithmic bytes (qweight +
-qzeros + scales as stored) per second, whole job.  Also reported: the
-decode kernel's roofline fraction (per-launch CUDA events), the end-to-end
-figure through the C ABI with host buffers, the CPU oracle timed on this
-host, SM clocks during the run, the prefill_7b tensor-core numbers, the
-Llama-70B M = 1 layers and the act-order decode workload, and (next_rows)
-the rows past the hot path: fused Q/K/V projections, GPTQ_V2, 8-bit codes,
-bf16 activations and the GPU packer.
+qzeros + scales as stored) per second, whole job.  Also on the line, kept
+short enough to be read whole: the roofline fraction of the decode kernels,
+the end-to-end figure through the C ABI with host buffers, the CPU oracle
+timed on this host (a seeded column sample of the same workload), SM clocks
+during the timed region, the binding-roofline fraction of the whole
+sweep_70b workload at every M (M = 2048 is the prefill), the prefill
+tensor-core numbers (sweep_70b M = 2048 and prefill_7b M = 512), and the
+decode_7b / actorder_7b workloads.  Per-case detail goes to stderr as one
+JSON line.
 
 --impl reference times the CPU oracle (the plain dequantize-then-matmul
-route) on the same workload, one shape per step.
+route) on the same workload: each step one layer configuration in turn, on a
+seeded sample of 256 of its columns.
 """
 from __future__ import annotations
 
@@ -41,6 +46,7 @@ METRIC = "W4A16 GEMM: decode eff. HBM TB/s (% roofline), prefill TFLOPS (% FP16 
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+SAMPLE_COLS = 256                     # columns per layer in the oracle's bounded sample
 
 
 def parse():
@@ -49,33 +55,34 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
-    p.add_argument("--replicas", type=int, default=8)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-extra", action="store_true", help="headline only (no sweep/prefill/7B legs)")
     p.add_argument("--soak-s", type=float, default=1.0)
-    p.add_argument("--only", choices=["decode", "prefill"], default=None,
-                   help="run one leg only (for profiling); the JSON line is then partial")
     p.add_argument("--sweep70b", action="store_true",
-                   help="also time all 240 sweep_70b cases (several minutes); adds a sweep_70b key")
-    p.add_argument("--single", default=None, metavar="K,N,M[,PATH]",
-                   help="profiling target instead of the bench: one synthetic g=128 layer, a 256 MB L2 "
-                        "flush before each of four calls on PATH (a GPTQ_Q4_PATH_* suffix, default DECODE)")
+                   help="also time every one of the 240 sweep_70b cases on its own (per-case detail on stderr)")
+    p.add_argument("--single", default=None, metavar="K,N,M[,PATH[,G[,ACT]]]",
+                   help="profiling target instead of the bench: one synthetic layer (groupsize G, default 128; "
+                        "ACT 1 for act-order), a 256 MB L2 flush before each of four calls on PATH (a "
+                        "GPTQ_Q4_PATH_* suffix, default AUTO)")
     return p.parse_args()
 
 
 def run_single(spec: str) -> None:
     """Four calls of one layer, each after an L2 flush: a short, fixed launch
-    sequence for ncu captures (-s 3 -c 1 takes the fourth call)."""
+    sequence for ncu captures (-s <launches before> -c 1 takes the fourth call)."""
     import torch
     import gptq_bit_weight_gb300 as q4
     parts = spec.split(",")
     K, N, M = int(parts[0]), int(parts[1]), int(parts[2])
-    path = getattr(q4, "GPTQ_Q4_PATH_" + (parts[3].upper() if len(parts) > 3 else "DECODE"))
-    layer = synthetic.make_layer(K, N, 128, bias=True, key=(77, K, N))
+    path = getattr(q4, "GPTQ_Q4_PATH_" + (parts[3].upper() if len(parts) > 3 and parts[3] else "AUTO"))
+    gs = int(parts[4]) if len(parts) > 4 else 128
+    act = len(parts) > 5 and parts[5] == "1"
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(77, K, N, gs & 0xFFFF, int(act)))
     dev = torch.device("cuda", 0)
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    mat = q4.Q4Matrix(t(layer.qweight), t(layer.qzeros), t(layer.scales), None, t(layer.bias), 128)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    mat = q4.Q4Matrix(t(layer.qweight), t(layer.qzeros), t(layer.scales), t(layer.g_idx), t(layer.bias), gs)
     mat.set_path(path)
+    mat.reserve(M)
     x = t(synthetic.activations(M, K, key=(77, K, N, M)))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(4):
@@ -86,25 +93,23 @@ def run_single(spec: str) -> None:
     print(json.dumps({"single": spec, "max_abs_y": float(y.float().abs().max())}))
 
 
-# DRAM bytes the decode kernels move per algorithmic byte, from an ncu launch
-# list of the decode_7b leg (dram__bytes_read.sum + dram__bytes_write.sum over
-# 1216 launches / their K*N/2 + G*N*2.5 bytes); the kernels read every packed
-# word, scale and zero once.
-DECODE_DRAM_PER_ALGORITHMIC_BYTE = 24957.7e6 / 24841.4e6
-
-
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
     except Exception:
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def r3(v, n=3):
+    return None if v is None else round(float(v), n)
 
 
 # --------------------------------------------------------- replicas (N > 1)
@@ -186,89 +191,155 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# --------------------------------------------------------------- reference
+# --------------------------------------------------------------- the oracle
+
+SWEEP_CONFIGS = [(K, N, g, a) for (K, N) in synthetic.SWEEP_70B_SHAPES for g in synthetic.SWEEP_70B_G
+                 for a in (False, True)]
+
+
+def sample_columns(N: int, key) -> np.ndarray:
+    """A seeded sample of SAMPLE_COLS columns in whole 8-column blocks (one
+    qzeros word each), so the oracle runs on exactly those columns."""
+    blocks = np.sort(synthetic.rng(*key).choice(N // 8, size=SAMPLE_COLS // 8, replace=False))
+    return (blocks[:, None] * 8 + np.arange(8)[None, :]).reshape(-1), blocks
+
+
+def oracle_step(cfg, cores, L=None):
+    """The oracle as it stands on one sweep_70b M = 1 configuration, on a
+    column sample: unpack + dequantize the sampled columns, then y in fp64.
+    Returns the sampled columns' weight bytes (qweight + qzeros + scales) and
+    the seconds that took (input generation is not timed)."""
+    import oracle
+    K, N, g, act = cfg
+    if L is None:
+        L = synthetic.workload_layer("sweep_70b", K, N, g, act)
+    cols, blocks = sample_columns(N, (90, K, N, g & 0xFFFF, int(act)))
+    qw = np.ascontiguousarray(L.qweight[:, cols])
+    qz = np.ascontiguousarray(L.qzeros[:, blocks])
+    sc = np.ascontiguousarray(L.scales[:, cols])
+    x = synthetic.workload_x("sweep_70b", K, N, g, act, 1)
+    t0 = time.perf_counter()
+    dq = oracle.dequantize_layer(qw, qz, sc, L.g_idx, K, cols.size, g)
+    oracle.reference_output(x, dq, None, nthreads=cores)
+    return qw.nbytes + qz.nbytes + sc.nbytes, time.perf_counter() - t0
+
 
 def run_reference(args):
-    """The CPU oracle on the decode_7b workload: one shape (all four M) per step."""
+    """The CPU oracle on the headline workload (sweep_70b, M = 1): each step
+    one layer configuration in turn, on a seeded sample of its columns."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
-    shapes = synthetic.DECODE_7B_SHAPES
-    layers = {s: synthetic.workload_layer("decode_7b", s[0], s[1], 128, False) for s in shapes}
-    xs = {(s, M): synthetic.workload_x("decode_7b", s[0], s[1], 128, False, M) for s in shapes
-          for M in synthetic.DECODE_7B_M}
-
-    def step(i):
-        s = shapes[i % len(shapes)]
-        L = layers[s]
-        dq = oracle.dequantize_layer(L.qweight, L.qzeros, L.scales, None, s[0], s[1], 128)
-        for M in synthetic.DECODE_7B_M:
-            oracle.reference_output(xs[(s, M)], dq, L.bias, nthreads=cores)
-        return L.weight_bytes * len(synthetic.DECODE_7B_M)
-
     for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    nbytes = 0
+        oracle_step(SWEEP_CONFIGS[i % len(SWEEP_CONFIGS)], cores)
+    nbytes, secs = 0, 0.0
     for i in range(args.steps):
-        nbytes += step(args.warmup + i)
-    dt = time.perf_counter() - t0
-    value = nbytes / dt / 1e12
+        b, s = oracle_step(SWEEP_CONFIGS[(args.warmup + i) % len(SWEEP_CONFIGS)], cores)
+        nbytes += b
+        secs += s
+    value = nbytes / secs / 1e12
+    sample = (f"each step: one sweep_70b M=1 layer configuration in turn, {SAMPLE_COLS} seeded columns "
+              f"(unpack, dequantize, fp64 products on {cores} threads; input generation untimed)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "decode_7b", "shapes": [list(s) for s in shapes], "M": synthetic.DECODE_7B_M,
-                   "groupsize": 128, "step": "one shape, all four M, dequantize once then fp64 products"},
-        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
-                         "sample": "each step: one decode_7b shape, all four M (shapes in turn)"},
+        "config": headline_config(),
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
-def cpu_baseline_sample(budget_s: float = 25.0):
-    """The oracle as it stands on the decode_7b cases, shape by shape, within a time budget."""
+def cpu_baseline_sample(layers, budget_s: float = 12.0):
+    """The oracle as it stands, timed on this host's cores, on column samples
+    of the headline configurations in turn (round robin) until the budget is
+    spent.  layers: the configurations' host tensors, already drawn."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
-    t0 = time.perf_counter()
-    nbytes, ncases, shapes_done = 0, 0, []
-    for (K, N) in synthetic.DECODE_7B_SHAPES:
-        L = synthetic.workload_layer("decode_7b", K, N, 128, False)
-        dq = oracle.dequantize_layer(L.qweight, L.qzeros, L.scales, None, K, N, 128)
-        for M in synthetic.DECODE_7B_M:
-            x = synthetic.workload_x("decode_7b", K, N, 128, False, M)
-            oracle.reference_output(x, dq, L.bias, nthreads=cores)
-            nbytes += L.weight_bytes
-            ncases += 1
-        shapes_done.append([K, N])
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{ncases} decode_7b cases (shapes {shapes_done}, M 1/2/4/8; dequantize once per shape, "
-                      f"fp64 products on {cores} threads), {dt:.1f} s"}
+    nbytes, secs, n = 0, 0.0, 0
+    while secs < budget_s and n < 50 * len(SWEEP_CONFIGS):
+        i = n % len(SWEEP_CONFIGS)
+        b, s = oracle_step(SWEEP_CONFIGS[i], cores, layers[i])
+        nbytes += b
+        secs += s
+        n += 1
+    return {"value": nbytes / secs / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} sweep_70b M=1 layer configs in turn x {SAMPLE_COLS} seeded columns, {secs:.1f} s"}
+
+
+def headline_config():
+    return {"workload": "sweep_70b", "M": 1, "shapes": [list(s) for s in synthetic.SWEEP_70B_SHAPES],
+            "groupsize": synthetic.SWEEP_70B_G, "g_idx": ["trivial", "act-order"], "layer_configs": 24,
+            "bias": False}
 
 
 # ------------------------------------------------------------------ native
+
+class Sweep:
+    """The 24 sweep_70b layer configurations on the device, R replicas each
+    (R * weight bytes >= 3x L2)."""
+
+    def __init__(self, q4, torch, dev, reserve_m):
+        t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.cfgs = []
+        for (K, N, g, act) in SWEEP_CONFIGS:
+            L = synthetic.workload_layer("sweep_70b", K, N, g, act)
+            qw, qz, sc, gi = t(L.qweight), t(L.qzeros), t(L.scales), t(L.g_idx)
+            R = max(2, int(np.ceil(3 * L2_BYTES / L.weight_bytes)))
+            mats = [q4.Q4Matrix(qw, qz, sc, gi, None, g) for _ in range(R)]
+            for m in mats:
+                m.reserve(reserve_m)
+            del qw, qz, sc, gi
+            self.cfgs.append({"K": K, "N": N, "g": g, "act": act, "mats": mats, "wb": L.weight_bytes,
+                              "x": {}, "o": {}, "L": L})
+        self.torch, self.dev = torch, dev
+
+    def xo(self, c, M):
+        if M not in c["x"]:
+            t = self.torch
+            c["x"][M] = t.from_numpy(synthetic.workload_x("sweep_70b", c["K"], c["N"], c["g"], c["act"], M)).to(self.dev)
+            c["o"][M] = t.empty((M, c["N"]), dtype=t.float16, device=self.dev)
+        return c["x"][M], c["o"][M]
+
+    def drop_m(self, M):
+        for c in self.cfgs:
+            c["x"].pop(M, None)
+            c["o"].pop(M, None)
+
+
+def capture(torch, q4, issue):
+    """One CUDA graph of issue(stream_ptr); returns (graph, our launches in it)."""
+    issue(torch.cuda.current_stream().cuda_stream)     # nothing allocates during capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = q4.gptq_q4_launch_count()
+    with torch.cuda.graph(g):
+        issue(torch.cuda.current_stream().cuda_stream)
+    return g, q4.gptq_q4_launch_count() - n0
+
+
+def graph_seconds(torch, stream, g, reps):
+    for _ in range(3):
+        g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e-3 / reps
+
 
 def run_native(args):
     import torch
 
     import gptq_bit_weight_gb300 as q4
-
-    if args.only == "prefill":
-        dev = torch.device("cuda", 0)
-        torch.cuda.set_device(dev)
-        _, bf16_tf, _, peak_src = peaks()
-        print(json.dumps({"prefill": run_prefill(q4, torch, dev, torch.cuda.current_stream(), bf16_tf, peak_src)}),
-              flush=True)
-        return
 
     rank, world, local = dist_env()
     if world > 1:
@@ -277,34 +348,19 @@ def run_native(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    sptr = stream.cuda_stream
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
+    detail = {}
 
-    shapes = synthetic.DECODE_7B_SHAPES
-    Ms = synthetic.DECODE_7B_M
-    R = args.replicas
-    mats, wbytes = {}, {}
-    for (K, N) in shapes:
-        L = synthetic.workload_layer("decode_7b", K, N, 128, False)
-        qw = torch.from_numpy(L.qweight).to(dev)
-        qz = torch.from_numpy(L.qzeros).to(dev)
-        sc = torch.from_numpy(L.scales).to(dev)
-        b = torch.from_numpy(L.bias).to(dev)
-        mats[(K, N)] = [q4.Q4Matrix(qw, qz, sc, None, b, 128) for _ in range(R)]
-        for m in mats[(K, N)]:
-            m.reserve(max(Ms))
-        wbytes[(K, N)] = L.weight_bytes
-        del qw, qz, sc
-    xs = {(s, M): torch.from_numpy(synthetic.workload_x("decode_7b", s[0], s[1], 128, False, M)).to(dev)
-          for s in shapes for M in Ms}
-    outs = {(s, M): torch.empty((M, s[1]), dtype=torch.float16, device=dev) for s in shapes for M in Ms}
-    calls = [(s, M, r) for r in range(R) for M in Ms for s in shapes]
-    step_bytes = sum(wbytes[s] for (s, M, r) in calls)
-    l2_defeated = R * sum(wbytes.values()) > 2 * L2_BYTES
+    sw = Sweep(q4, torch, dev, reserve_m=256)
+    step_bytes = sum(c["wb"] * len(c["mats"]) for c in sw.cfgs)
 
-    def issue(call_list, stream_ptr):
-        for (s, M, r) in call_list:
-            q4.gptq_q4_matmul(mats[s][r].handle, xs[(s, M)].data_ptr(), M, outs[(s, M)].data_ptr(), stream_ptr)
+    def issue_m(M, cfgs):
+        def issue(sp):
+            for c in cfgs:
+                x, o = sw.xo(c, M)
+                for m in c["mats"]:
+                    q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), sp)
+        return issue
 
     def barrier():
         rank_barrier(world)
@@ -313,20 +369,7 @@ def run_native(args):
     def max_over_ranks(v):
         return max_over_ranks_value(v, world, dev)
 
-    # One step is captured once into a CUDA graph and replayed: the kernels
-    # then run back to back as in a model's decode loop, instead of waiting
-    # on Python + ctypes + the launch API for every call (~11 us a call).
-    def capture(call_list):
-        g = torch.cuda.CUDAGraph()
-        issue(call_list, sptr)                  # make sure nothing allocates during capture
-        torch.cuda.synchronize()
-        n0 = q4.gptq_q4_launch_count()
-        with torch.cuda.graph(g):
-            issue(call_list, torch.cuda.current_stream().cuda_stream)
-        return g, q4.gptq_q4_launch_count() - n0
-
-    step_graph, launches_per_step = capture(calls)
-
+    step_graph, launches_per_step = capture(torch, q4, issue_m(1, sw.cfgs))
     with ClockSampler(local) as clk:
         t_end = time.perf_counter() + args.soak_s
         for _ in range(max(3, args.warmup)):
@@ -343,67 +386,52 @@ def run_native(args):
             step_graph.replay()
         e1.record(stream)
         barrier()
-        launches = launches_per_step * args.steps
         ms = max_over_ranks(e0.elapsed_time(e1))
-        # ---- the same steps launched eagerly, call by call, for comparison
-        barrier()
-        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2.record(stream)
-        for _ in range(args.steps):
-            issue(calls, sptr)
-        e3.record(stream)
-        barrier()
-        eager_ms = max_over_ranks(e2.elapsed_time(e3))
     clocks = clk.summary()
-
+    launches = launches_per_step * args.steps
     value = job_throughput(step_bytes, args.steps, world, ms * 1e-3)
-    eager_value = job_throughput(step_bytes, args.steps, world, eager_ms * 1e-3)
-    # The timed region holds nothing but decode kernels, back to back: the
-    # average launch duration is the region's time over its launches.
-    achieved_gbs = step_bytes * args.steps / (ms * 1e-3) / 1e9
 
-    # per-case figures: a graph of the R replicas of one case, replayed
-    per_case = {}
-    for s in shapes:
-        for M in Ms:
-            g, n = capture([(s, M, r) for r in range(R)])
-            for _ in range(3):
-                g.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 20
-            a.record(stream)
-            for _ in range(reps):
-                g.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / (reps * R)
-            per_case[f"{s[0]}x{s[1]} M={M}"] = {"us": round(us, 2), "TB/s": round(wbytes[s] / (us * 1e-6) / 1e12, 3)}
-            del g
+    # ---- roofline of the decode kernels: a graph of the trivial-g_idx configs
+    # (only decode kernels launch there; act-order calls add the x gather)
+    triv = [c for c in sw.cfgs if not c["act"]]
+    g_triv, n_triv = capture(torch, q4, issue_m(1, triv))
+    triv_bytes = sum(c["wb"] * len(c["mats"]) for c in triv)
+    triv_s = graph_seconds(torch, stream, g_triv, max(5, args.steps // 2))
+    del g_triv
+    achieved_gbs = triv_bytes / triv_s / 1e9
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region.
-    # One step, as a decode loop would run it: the step's inputs copied host -> device (one copy
-    # per distinct input; the replicas of a case share it), every C-ABI matmul, the results copied
-    # device -> host, all captured once into a CUDA graph and replayed; timed on the host clock
-    # up to the completed device -> host copies.
-    hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
-    ho = {k: torch.empty(v.shape, dtype=torch.float16).pin_memory() for k, v in outs.items()}
-    dx = {k: torch.empty_like(v) for k, v in xs.items()}
+    # ---- per layer configuration at M = 1: a graph of its R replicas
+    m1 = {}
+    for c in sw.cfgs:
+        g1, _ = capture(torch, q4, issue_m(1, [c]))
+        s = graph_seconds(torch, stream, g1, 10) / len(c["mats"])
+        m1[(c["K"], c["N"], c["g"], c["act"])] = s
+        del g1
+    fr1 = {k: sw_cfg_bytes(k) / s / 1e9 / hbm_gbs for k, s in m1.items()}
+    detail["m1_us"] = {cfg_name(k): round(s * 1e6, 2) for k, s in m1.items()}
+    detail["m1_frac"] = {cfg_name(k): r3(f) for k, f in fr1.items()}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies
+    # inside the timed region: every step copies each configuration's x host ->
+    # device, runs every C-ABI call, and copies every output device -> host;
+    # one CUDA graph per step, timed on the host clock to the completed copies
+    hx = {id(c): sw.xo(c, 1)[0].cpu().pin_memory() for c in sw.cfgs}
+    ho = {id(c): torch.empty((1, c["N"]), dtype=torch.float16).pin_memory() for c in sw.cfgs}
+    dx = {id(c): torch.empty_like(sw.xo(c, 1)[0]) for c in sw.cfgs}
     h2d = sum(t.numel() * 2 for t in hx.values())
     d2h = sum(t.numel() * 2 for t in ho.values())
 
-    def e2e_issue(stream_ptr):
-        for k in hx:
-            dx[k].copy_(hx[k], non_blocking=True)
-        for (s, M, r) in calls:
-            q4.gptq_q4_matmul(mats[s][r].handle, dx[(s, M)].data_ptr(), M, outs[(s, M)].data_ptr(), stream_ptr)
-        for k in ho:
-            ho[k].copy_(outs[k], non_blocking=True)
+    def e2e_issue(sp):
+        for c in sw.cfgs:
+            dx[id(c)].copy_(hx[id(c)], non_blocking=True)
+        for c in sw.cfgs:
+            o = sw.xo(c, 1)[1]
+            for m in c["mats"]:
+                q4.gptq_q4_matmul(m.handle, dx[id(c)].data_ptr(), 1, o.data_ptr(), sp)
+        for c in sw.cfgs:
+            ho[id(c)].copy_(sw.xo(c, 1)[1], non_blocking=True)
 
-    e2e_issue(sptr)
-    torch.cuda.synchronize()
-    e2e_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(e2e_graph):
-        e2e_issue(torch.cuda.current_stream().cuda_stream)
+    e2e_graph, _ = capture(torch, q4, e2e_issue)
     for _ in range(max(3, args.warmup)):
         e2e_graph.replay()
     torch.cuda.synchronize()
@@ -415,391 +443,220 @@ def run_native(args):
     barrier()
     e2e_s = max_over_ranks(time.perf_counter() - t0)
     e2e_value = job_throughput(step_bytes, args.steps, world, e2e_s)
-    assert all(torch.equal(ho[k], outs[k].cpu()) for k in ho), "e2e results did not reach the host"
+    assert all(torch.equal(ho[id(c)], sw.xo(c, 1)[1].cpu()) for c in sw.cfgs), "e2e results did not reach the host"
+    del e2e_graph
 
-    decode_70b = None
-    if args.only is None:
-        decode_70b = run_decode_70b(q4, torch, dev, stream, hbm_gbs)
-        actorder = run_actorder_decode(q4, torch, dev, stream, hbm_gbs, bf16_tf)
-        next_rows = run_next_rows(q4, torch, dev, stream, hbm_gbs)
-        sweep70 = run_sweep_70b(q4, torch, dev, stream, hbm_gbs, bf16_tf) if args.sweep70b else None
-
-    prefill = None
-    if not args.no_prefill and args.only != "decode":
-        prefill = run_prefill(q4, torch, dev, stream, bf16_tf, peak_src)
+    line_extra = {}
+    if not args.no_extra:
+        line_extra, d2 = run_extra_legs(q4, torch, dev, stream, sw, hbm_gbs, bf16_tf, issue_m, args)
+        detail.update(d2)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only is None:
-        cpu = cpu_baseline_sample()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample([c["L"] for c in sw.cfgs])
 
     if rank == 0:
+        fr = list(fr1.values())
+        cfg = headline_config()
+        cfg.update({"replicas": "R per config, R x weight bytes >= 3x L2",
+                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.1f} GB of weights per step, each replica "
+                          f"touched once per step (129 MB L2)",
+                    "bytes_per_step": step_bytes, "calls_per_step": launches_per_step,
+                    "launch": "one CUDA graph per step (captured C-ABI calls)", "parallelism": f"replicas x{world}"})
         line = {
-            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16 x int4 -> f32 accumulate", "data": "synthetic",
-            "config": {"workload": "decode_7b", "shapes": [list(s) for s in shapes], "M": Ms, "groupsize": 128,
-                       "g_idx": "trivial", "bias": True, "replicas": R,
-                       "calls_per_step": len(calls), "launch": "one CUDA graph per step (captured C-ABI calls)",
-                       "l2": (f"inputs larger than L2: {R} weight replicas, {R * sum(wbytes.values()) / 1e6:.0f} MB "
-                              f"per step vs 129 MB L2, each replica touched once per step") if l2_defeated else
-                             f"NOT defeated: {R} replicas = {R * sum(wbytes.values()) / 1e6:.0f} MB (profiling run)",
-                       "bytes_per_step": step_bytes, "soak_s": args.soak_s,
-                       "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": achieved_gbs / hbm_gbs,
-                         # DRAM bytes (read + write) per step: the algorithmic bytes times the ratio
-                         # ncu measured over every decode_7b launch of the bench
-                         "traffic": round(step_bytes * DECODE_DRAM_PER_ALGORITHMIC_BYTE),
-                         "traffic_unit": "bytes per step",
-                         "kernel": ("decode_kernel<1,*> (register-streaming with a shared-memory weight ring; "
-                                    "every decode_7b case)"),
-                         "peak_source": peak_src,
-                         "how": "algorithmic bytes of the timed region / its CUDA-event time (only decode kernels run in it)"},
-            "eager": {"value": eager_value, "unit": "TB/s",
-                      "how": "the same steps launched call by call from Python through the C ABI"},
-            "per_case": per_case,
-            "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "metric": METRIC, "value": r3(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r3(ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 x int4 -> f32 accumulate", "data": "synthetic",
+            "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": r3(achieved_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": r3(achieved_gbs / hbm_gbs), "traffic": None, "peak_source": peak_src,
+                         "kernel": "decode kernels on the 12 trivial-g_idx configs (graph of only decode launches)"},
+            "m1_frac": {"min": r3(min(fr)), "mean": r3(float(np.mean(fr))), "max": r3(max(fr)),
+                        "by_g": {str(g): r3(float(np.mean([f for k, f in fr1.items() if k[2] == g])))
+                                 for g in synthetic.SWEEP_70B_G},
+                        "act": r3(float(np.mean([f for k, f in fr1.items() if k[3]])))},
+            "e2e": {"value": r3(e2e_value, 4), "unit": "TB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "clocks": clocks,
         }
-        if decode_70b:
-            line["decode_70b"] = decode_70b
-            line["actorder_7b"] = actorder
-            line["next_rows"] = next_rows
-            if sweep70:
-                line["sweep_70b"] = sweep70
-        if prefill:
-            line["prefill"] = prefill
+        line.update(line_extra)
         if cpu:
             line["cpu_baseline"] = cpu
-        print(json.dumps(line), flush=True)
+        print(json.dumps({"detail": detail}, separators=(",", ":")), file=sys.stderr, flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def run_decode_70b(q4, torch, dev, stream, hbm_gbs, reps=10):
-    """M=1 decode on the Llama-70B projection shapes (sweep_70b, g=128,
-    trivial g_idx): per shape, enough weight replicas to exceed L2, captured
-    in one CUDA graph and replayed; eff. TB/s on the stored weight bytes."""
-    out = {}
-    tot_bytes, tot_s = 0.0, 0.0
-    for (K, N) in synthetic.SWEEP_70B_SHAPES:
-        L = synthetic.workload_layer("sweep_70b", K, N, 128, False)
-        qw, qz, sc = (torch.from_numpy(a).to(dev) for a in (L.qweight, L.qzeros, L.scales))
-        R = max(2, int(np.ceil(3 * L2_BYTES / L.weight_bytes)))
-        mats = [q4.Q4Matrix(qw, qz, sc, None, None, 128) for _ in range(R)]
-        del qw, qz, sc
-        x = torch.from_numpy(synthetic.workload_x("sweep_70b", K, N, 128, False, 1)).to(dev)
-        o = torch.empty((1, N), dtype=torch.float16, device=dev)
-        for m in mats:
-            q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), stream.cuda_stream)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for m in mats:
-                q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), torch.cuda.current_stream().cuda_stream)
-        for _ in range(3):
-            g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * R)
-        tbs = L.weight_bytes / (us * 1e-6) / 1e12
-        out[f"{K}x{N} M=1"] = {"us": round(us, 2), "TB/s": round(tbs, 3), "frac": round(tbs * 1e3 / hbm_gbs, 3)}
-        tot_bytes += L.weight_bytes
-        tot_s += us * 1e-6
-        del g, mats
-    return {"workload": "sweep_70b M=1, g=128, trivial g_idx", "value": tot_bytes / tot_s / 1e12, "unit": "TB/s",
-            "frac_of_hbm_peak": tot_bytes / tot_s / 1e9 / hbm_gbs, "cases": out,
-            "how": "weight bytes / per-call time from CUDA-graph replays of >= 3x L2 of weight replicas"}
+def sw_cfg_bytes(k):
+    K, N, g, _ = k
+    G = 1 if g == -1 else K // g
+    return K * N // 2 + G * N * 2 + G * N // 2
 
 
-def time_layer_cases(q4, torch, dev, stream, workload, K, N, g, act, Ms, hbm_gbs, tf_peak, reps=10):
-    """One layer configuration of a workload at several M through the default
-    path (GPTQ_Q4_PATH_AUTO): enough weight replicas to exceed L2 three times,
-    each M captured in one CUDA graph over the replicas and replayed.  Per
-    case: time per call, eff. TB/s on the stored weight bytes, TFLOP/s, and the
-    fraction of the roofline that binds, max(bytes/HBM, flops/tensor)/time."""
-    L = synthetic.workload_layer(workload, K, N, g, act)
+def cfg_name(k):
+    K, N, g, act = k
+    return f"{K}x{N} g{g}{' act' if act else ''}"
+
+
+def run_extra_legs(q4, torch, dev, stream, sw, hbm_gbs, bf16_tf, issue_m, args):
+    """The rest of the workloads, summarised for the JSON line (detail for stderr)."""
+    line, detail = {}, {}
+    # sweep_70b at every M: binding-roofline fraction summed over the 24 configs,
+    # sum(max(bytes / HBM, flops / tensor)) / sum(time), one graph of every
+    # replica of every config per M (M = 2048: the prefill leg below)
+    by_m = {}
+    for M in synthetic.SWEEP_70B_M:
+        if M == 2048:
+            continue
+        g, _ = capture(torch, q4, issue_m(M, sw.cfgs))
+        s = graph_seconds(torch, stream, g, 5)
+        del g
+        bound = sum(max(c["wb"] / (hbm_gbs * 1e9), 2.0 * M * c["K"] * c["N"] / (bf16_tf * 1e12)) * len(c["mats"])
+                    for c in sw.cfgs)
+        by_m[M] = bound / s
+        if M > 1:
+            sw.drop_m(M)
+    # prefill: sweep_70b M = 2048 on one replica of each config
+    pf = {}
+    tot_f, tot_s = 0.0, 0.0
+    for c in sw.cfgs:
+        M = 2048
+        m = c["mats"][0]
+        x = torch.from_numpy(synthetic.workload_x("sweep_70b", c["K"], c["N"], c["g"], c["act"], M)).to(dev)
+        o = torch.empty((M, c["N"]), dtype=torch.float16, device=dev)
+        m.reserve(M)
+        g, _ = capture(torch, q4, lambda sp: q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), sp))
+        s = graph_seconds(torch, stream, g, 10)
+        del g, x, o
+        fl = 2.0 * M * c["K"] * c["N"]
+        pf[(c["K"], c["N"], c["g"], c["act"])] = fl / s / 1e12
+        tot_f += fl
+        tot_s += s
+    by_m[2048] = tot_f / tot_s / 1e12 / bf16_tf
+    pfr = [v / bf16_tf for v in pf.values()]
+    detail["prefill_70b_m2048_tflops"] = {cfg_name(k): round(v, 1) for k, v in pf.items()}
+    line["sweep_frac_by_M"] = {str(M): r3(f) for M, f in sorted(by_m.items())}
+    p7, d7 = run_prefill_7b(q4, torch, dev, stream, bf16_tf)
+    detail["prefill_7b"] = d7
+    line["prefill"] = {"m2048_70b": {"TFLOP/s": r3(tot_f / tot_s / 1e12, 1), "frac": r3(tot_f / tot_s / 1e12 / bf16_tf),
+                                     "min_frac": r3(min(pfr)), "max_frac": r3(max(pfr))},
+                       "m512_7b": p7["m512"], "m2048_7b": p7["m2048"], "unfused_7b_TFLOP/s": p7["unfused"],
+                       "peak": bf16_tf, "peak_kind": "bf16 burst (fp16 dense rate is the same)"}
+    # 7B decode workloads (secondary)
+    line["decode_7b"], detail["decode_7b"] = run_7b_decode(q4, torch, dev, stream, hbm_gbs, "decode_7b",
+                                                           synthetic.DECODE_7B_SHAPES, synthetic.DECODE_7B_M, False)
+    line["actorder_7b"], detail["actorder_7b"] = run_7b_decode(q4, torch, dev, stream, hbm_gbs, "actorder_7b",
+                                                               synthetic.ACTORDER_7B_SHAPES, synthetic.ACTORDER_7B_M,
+                                                               True)
+    if args.sweep70b:
+        detail["sweep_70b_cases"] = run_sweep_70b_cases(q4, torch, dev, stream, sw, hbm_gbs, bf16_tf)
+    return line, detail
+
+
+def run_7b_decode(q4, torch, dev, stream, hbm_gbs, workload, shapes, Ms, act):
+    """A 7B decode workload through the default path: per shape, replicas
+    >= 3x L2, one graph per M over the replicas; TB/s on the weight bytes
+    (any x gather inside the calls)."""
     t = lambda a: None if a is None else torch.from_numpy(a).to(dev)
-    qw, qz, sc, gi = t(L.qweight), t(L.qzeros), t(L.scales), t(L.g_idx)
-    R = max(2, int(np.ceil(3 * L2_BYTES / L.weight_bytes)))
-    mats = [q4.Q4Matrix(qw, qz, sc, gi, None, g) for _ in range(R)]
-    del qw, qz, sc, gi
-    for m in mats:
-        m.reserve(max(Ms))
-    res = {}
-    for M in Ms:
-        x = t(synthetic.workload_x(workload, K, N, g, act, M))
-        o = torch.empty((M, N), dtype=torch.float16, device=dev)
+    tot_b, tot_s, cases = 0.0, 0.0, {}
+    for (K, N) in shapes:
+        L = synthetic.workload_layer(workload, K, N, 128, act)
+        R = max(2, int(np.ceil(3 * L2_BYTES / L.weight_bytes)))
+        qw, qz, sc, gi, b = t(L.qweight), t(L.qzeros), t(L.scales), t(L.g_idx), t(L.bias)
+        mats = [q4.Q4Matrix(qw, qz, sc, gi, b, 128) for _ in range(R)]
         for m in mats:
-            q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), stream.cuda_stream)
-        torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            for m in mats:
-                q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), torch.cuda.current_stream().cuda_stream)
-        for _ in range(3):
-            gr.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            gr.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        sec = a.elapsed_time(b) * 1e-3 / (reps * R)
-        flops = 2.0 * M * K * N
-        t_bw, t_tc = L.weight_bytes / (hbm_gbs * 1e9), flops / (tf_peak * 1e12)
-        res[M] = {"us": round(sec * 1e6, 2), "TB/s": round(L.weight_bytes / sec / 1e12, 3),
-                  "TFLOP/s": round(flops / sec / 1e12, 1), "bound": "hbm" if t_bw >= t_tc else "tensor",
-                  "frac": round(max(t_bw, t_tc) / sec, 3)}
-        del gr
-    del mats
-    torch.cuda.empty_cache()
-    return L.weight_bytes, res
+            m.reserve(max(Ms))
+        for M in Ms:
+            x = t(synthetic.workload_x(workload, K, N, 128, act, M))
+            o = torch.empty((M, N), dtype=torch.float16, device=dev)
+
+            def issue(sp):
+                for m in mats:
+                    q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), sp)
+
+            g, _ = capture(torch, q4, issue)
+            s = graph_seconds(torch, stream, g, 10) / R
+            del g
+            cases[f"{K}x{N} M={M}"] = round(s * 1e6, 2)
+            tot_b += L.weight_bytes
+            tot_s += s
+        del mats
+    v = tot_b / tot_s / 1e12
+    return {"TB/s": r3(v), "frac": r3(v * 1e3 / hbm_gbs)}, cases
 
 
-def run_actorder_decode(q4, torch, dev, stream, hbm_gbs, tf_peak):
-    """actorder_7b: decode with a scattered act-order g_idx, M in {1, 4, 16},
-    on (4096, 11008) and (11008, 4096); the x reorder runs inside each call."""
-    cases, tot_b, tot_s = {}, 0.0, 0.0
-    for (K, N) in synthetic.ACTORDER_7B_SHAPES:
-        wb, res = time_layer_cases(q4, torch, dev, stream, "actorder_7b", K, N, 128, True, synthetic.ACTORDER_7B_M,
-                                   hbm_gbs, tf_peak)
-        for M, r in res.items():
-            cases[f"{K}x{N} M={M}"] = r
-            tot_b += wb
-            tot_s += r["us"] * 1e-6
-    return {"workload": "actorder_7b", "value": tot_b / tot_s / 1e12, "unit": "TB/s",
-            "frac_of_hbm_peak": tot_b / tot_s / 1e9 / hbm_gbs, "cases": cases,
-            "how": "weight bytes / per-call time (x reorder included) from CUDA-graph replays of >= 3x L2 of replicas"}
-
-
-def run_sweep_70b(q4, torch, dev, stream, hbm_gbs, tf_peak):
-    """sweep_70b in full: 3 shapes x 4 group sizes x {trivial, act-order} x
-    10 values of M (240 cases), through the default path."""
-    cases = {}
-    for (K, N) in synthetic.SWEEP_70B_SHAPES:
-        for g in synthetic.SWEEP_70B_G:
-            for act in (False, True):
-                _, res = time_layer_cases(q4, torch, dev, stream, "sweep_70b", K, N, g, act, synthetic.SWEEP_70B_M,
-                                          hbm_gbs, tf_peak, reps=5)
-                for M, r in res.items():
-                    cases[f"{K}x{N} g={g} act={int(act)} M={M}"] = r
-    fr = [r["frac"] for r in cases.values()]
-    return {"workload": "sweep_70b (all 240 cases)", "cases": cases, "median_frac": float(np.median(fr)),
-            "min_frac": float(np.min(fr)), "max_frac": float(np.max(fr))}
-
-
-def _graph_time(torch, stream, issue, reps=20):
-    """Per-replay seconds of a CUDA graph of issue(stream_ptr)."""
-    issue(stream.cuda_stream)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        issue(torch.cuda.current_stream().cuda_stream)
-    for _ in range(3):
-        g.replay()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e-3 / reps
-
-
-def run_next_rows(q4, torch, dev, stream, hbm_gbs):
-    """Measurements of the rows added past the hot path, on Llama-7B shapes:
-    projection fusion (Q, K, V of one input as one handle vs three), the
-    GPTQ_V2 zero convention (same kernels; must cost the same), and the GPU
-    packer (float weights -> checkpoint words)."""
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    res = {}
-    K, Nq = 4096, 4096
-    R = 6                                                   # 6 x 3 x 8.7 MB = 157 MB of weights > 129 MB L2
-    layers = [synthetic.workload_layer("decode_7b", K, Nq, 128, False) for _ in range(3)]
-    sep = [[q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for L in layers] for _ in range(R)]
-    fused = [q4.Q4Matrix.fused([(t(L.qweight), t(L.qzeros), t(L.scales)) for L in layers], None, None, 128)
-             for _ in range(R)]
-    wbytes = 3 * layers[0].weight_bytes
-    for M in (1, 8):
-        x = t(synthetic.workload_x("decode_7b", K, Nq, 128, False, M))
-        o1 = torch.empty((M, Nq), dtype=torch.float16, device=dev)
-        o3 = torch.empty((M, 3 * Nq), dtype=torch.float16, device=dev)
-
-        def issue_sep(sp):
-            for r in range(R):
-                for m in sep[r]:
-                    q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o1.data_ptr(), sp)
-
-        def issue_fused(sp):
-            for r in range(R):
-                q4.gptq_q4_matmul(fused[r].handle, x.data_ptr(), M, o3.data_ptr(), sp)
-
-        ts = _graph_time(torch, stream, issue_sep) / R
-        tf = _graph_time(torch, stream, issue_fused) / R
-        res[f"qkv_7b M={M}"] = {"separate_us": round(ts * 1e6, 2), "fused_us": round(tf * 1e6, 2),
-                                "separate_TB/s": round(wbytes / ts / 1e12, 3), "fused_TB/s": round(wbytes / tf / 1e12, 3)}
-    del sep, fused
-    # GPTQ_V2: the same layer read as a V2 checkpoint
-    L = synthetic.workload_layer("decode_7b", 4096, 11008, 128, False)
-    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
-    x = t(synthetic.workload_x("decode_7b", 4096, 11008, 128, False, 1))
-    o = torch.empty((1, 11008), dtype=torch.float16, device=dev)
-
-    def issue(sp):
-        for m in mats:
-            q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), sp)
-
-    t1 = _graph_time(torch, stream, issue) / len(mats)
-    for m in mats:
-        m.set_format(q4.GPTQ_Q4_FORMAT_GPTQ_V2)
-    t2 = _graph_time(torch, stream, issue) / len(mats)
-    res["gptq_v2 4096x11008 M=1"] = {"gptq_us": round(t1 * 1e6, 2), "gptq_v2_us": round(t2 * 1e6, 2),
-                                     "gptq_v2_TB/s": round(L.weight_bytes / t2 / 1e12, 3)}
-    del mats
-    # 8-bit checkpoint of the same shape (two 4-bit halves along K): decode
-    # at M = 1 (weight bytes / time) and the fused prefill at M = 512
-    L8 = synthetic.make_layer8(4096, 11008, 128, key=(33, 4096, 11008))
-    mats = [q4.Q4Matrix(t(L8.qweight), t(L8.qzeros), t(L8.scales), None, None, 128, bits=8) for _ in range(6)]
-    t8 = _graph_time(torch, stream, issue) / len(mats)
-    bytes8 = 4096 * 11008 + (4096 // 128) * 11008 * 3   # codes + fp16 scales + 8-bit zeros
-    x512 = t(synthetic.activations(512, 4096, key=(33, 512)))
-    o512 = torch.empty((512, 11008), dtype=torch.float16, device=dev)
-    mats[0].reserve(512)
-
-    def issue512(sp):
-        q4.gptq_q4_matmul(mats[0].handle, x512.data_ptr(), 512, o512.data_ptr(), sp)
-
-    t512 = _graph_time(torch, stream, issue512)
-    res["8bit 4096x11008"] = {"M=1_us": round(t8 * 1e6, 2), "M=1_TB/s": round(bytes8 / t8 / 1e12, 3),
-                              "M=512_us": round(t512 * 1e6, 2),
-                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / t512 / 1e12, 1)}
-    del mats
-    # bf16 activations and outputs on the 4-bit layer (one preparation launch
-    # per call scales and rounds x to fp16): decode at M = 1, prefill at M = 512
-    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
-    for m in mats:
-        m.set_act_dtype(torch.bfloat16)
-        m.reserve(512)
-    xb1 = t(synthetic.activations_bf16(1, 4096, key=(35, 1)).view(np.int16)).view(torch.bfloat16)
-    xb512 = t(synthetic.activations_bf16(512, 4096, key=(35, 512)).view(np.int16)).view(torch.bfloat16)
-    ob1 = torch.empty((1, 11008), dtype=torch.bfloat16, device=dev)
-    ob512 = torch.empty((512, 11008), dtype=torch.bfloat16, device=dev)
-
-    def issue_b1(sp):
-        for m in mats:
-            q4.gptq_q4_matmul(m.handle, xb1.data_ptr(), 1, ob1.data_ptr(), sp)
-
-    def issue_b512(sp):
-        q4.gptq_q4_matmul(mats[0].handle, xb512.data_ptr(), 512, ob512.data_ptr(), sp)
-
-    tb1 = _graph_time(torch, stream, issue_b1) / len(mats)
-    tb512 = _graph_time(torch, stream, issue_b512)
-    res["bf16 4096x11008"] = {"M=1_us": round(tb1 * 1e6, 2), "M=1_TB/s": round(L.weight_bytes / tb1 / 1e12, 3),
-                              "M=512_us": round(tb512 * 1e6, 2),
-                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / tb512 / 1e12, 1)}
-    del mats
-    # GPU packer: float weights (fp16) + scales + zeros -> qweight/qzeros
-    K, N, gs = 4096, 11008, 128
-    g = np.random.default_rng(5)
-    w = torch.from_numpy(g.normal(0, 0.05, (K, N)).astype(np.float16)).to(dev)
-    sc = torch.from_numpy(g.uniform(0.002, 0.02, (K // gs, N)).astype(np.float16)).to(dev)
-    zs = torch.from_numpy(g.integers(0, 16, (K // gs, N)).astype(np.int32)).to(dev)
-    qw = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
-    qz = torch.empty((K // gs, N // 8), dtype=torch.int32, device=dev)
-
-    def issue_pack(sp):
-        q4.gptq_q4_pack(w.data_ptr(), sc.data_ptr(), zs.data_ptr(), None, K, N, gs, 0, qw.data_ptr(), qz.data_ptr(), sp)
-
-    tp = _graph_time(torch, stream, issue_pack, reps=10)
-    moved = K * N * 2 + K * N // 2 + (K // gs) * N * 6 + (K // gs) * N // 2
-    res["pack 4096x11008"] = {"us": round(tp * 1e6, 2), "TB/s": round(moved / tp / 1e12, 3),
-                              "frac_of_hbm_peak": round(moved / tp / 1e9 / hbm_gbs, 3),
-                              "bytes": "w fp16 read + qweight written + scales/zeros read + qzeros written"}
-    return res
-
-
-def run_prefill(q4, torch, dev, stream, bf16_tf, peak_src, reps=10):
-    """prefill_7b: M in {512, 2048} x the three 7B shapes x {trivial, act-order}.
-
-    Fused (shared-memory dequantization inside the tcgen05 GEMM) against the
-    unfused route (dequantize to temp_dq, then the tcgen05 GEMM on it).  Each
-    case is one call captured in a CUDA graph, replayed `reps` times back to
-    back after a warm-up and timed with CUDA events around the replays; the
-    work is compute-bound, so the 129 MB L2 does not flatter it."""
-    sptr = stream.cuda_stream
-    cases, tot_flops, tot_fused, tot_unf = {}, 0.0, 0.0, 0.0
-    per_launch = []
+def run_prefill_7b(q4, torch, dev, stream, bf16_tf):
+    """prefill_7b: fused (shared-memory dequantization inside the tcgen05
+    GEMM) at M in {512, 2048} x the three 7B shapes x {trivial, act-order};
+    the unfused route (dequantize to temp_dq, then the tcgen05 GEMM) beside it
+    on the trivial cases.  One call per graph, replayed back to back."""
+    out, detail = {}, {}
+    f_tot = {512: [0.0, 0.0], 2048: [0.0, 0.0]}
+    u_tot = [0.0, 0.0]
+    fr = {512: [], 2048: []}
     for act in (False, True):
         for (K, N) in synthetic.PREFILL_7B_SHAPES:
             L = synthetic.workload_layer("prefill_7b", K, N, 128, act)
-            mat = q4.Q4Matrix(torch.from_numpy(L.qweight).to(dev), torch.from_numpy(L.qzeros).to(dev),
-                              torch.from_numpy(L.scales).to(dev),
-                              None if L.g_idx is None else torch.from_numpy(L.g_idx).to(dev), None, 128)
+            t = lambda a: None if a is None else torch.from_numpy(a).to(dev)
+            mat = q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), t(L.g_idx), None, 128)
             mat.reserve(max(synthetic.PREFILL_7B_M))
             temp_dq = torch.empty((K, N), dtype=torch.float16, device=dev)
             for M in synthetic.PREFILL_7B_M:
-                x = torch.from_numpy(synthetic.workload_x("prefill_7b", K, N, 128, act, M)).to(dev)
-                out = torch.empty((M, N), dtype=torch.float16, device=dev)
-
-                def fused(sp):
-                    q4.gptq_q4_matmul(mat.handle, x.data_ptr(), M, out.data_ptr(), sp)
-
-                def unfused(sp):
-                    q4.gptq_q4_matmul_unfused(mat.handle, x.data_ptr(), M, temp_dq.data_ptr(), out.data_ptr(), sp)
-
-                mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
-                times = {}
-                for name, fn in (("fused", fused), ("unfused", unfused)):
-                    # one call captured in a CUDA graph and replayed back to back, so that the
-                    # host's launch cost does not show as device time on the short cases
-                    for _ in range(3):
-                        fn(sptr)
-                    torch.cuda.synchronize()
-                    g = torch.cuda.CUDAGraph()
-                    with torch.cuda.graph(g):
-                        fn(torch.cuda.current_stream().cuda_stream)
-                    g.replay()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    for _ in range(reps):
-                        g.replay()
-                    b.record(stream)
-                    torch.cuda.synchronize()
-                    times[name] = a.elapsed_time(b) / reps
-                    del g
-                flops = 2.0 * M * K * N
-                tot_flops += flops
-                tot_fused += times["fused"]
-                tot_unf += times["unfused"]
+                x = t(synthetic.workload_x("prefill_7b", K, N, 128, act, M))
+                o = torch.empty((M, N), dtype=torch.float16, device=dev)
+                g, _ = capture(torch, q4, lambda sp: q4.gptq_q4_matmul(mat.handle, x.data_ptr(), M, o.data_ptr(), sp))
+                s = graph_seconds(torch, stream, g, 10)
+                del g
+                fl = 2.0 * M * K * N
+                f_tot[M][0] += fl
+                f_tot[M][1] += s
+                fr[M].append(fl / s / 1e12 / bf16_tf)
+                name = f"{K}x{N} M={M}{' act' if act else ''}"
+                detail[name] = {"us": round(s * 1e6, 1), "TFLOP/s": round(fl / s / 1e12, 1)}
                 if not act:
-                    per_launch.append((flops, times["fused"]))
-                cases[f"{K}x{N} M={M}{' act' if act else ''}"] = {
-                    "fused_us": round(times["fused"] * 1e3, 1),
-                    "fused_TFLOPS": round(flops / (times["fused"] * 1e-3) / 1e12, 1),
-                    "unfused_us": round(times["unfused"] * 1e3, 1),
-                    "unfused_TFLOPS": round(flops / (times["unfused"] * 1e-3) / 1e12, 1)}
+                    g, _ = capture(torch, q4, lambda sp: q4.gptq_q4_matmul_unfused(
+                        mat.handle, x.data_ptr(), M, temp_dq.data_ptr(), o.data_ptr(), sp))
+                    su = graph_seconds(torch, stream, g, 10)
+                    del g
+                    u_tot[0] += fl
+                    u_tot[1] += su
+                    detail[name]["unfused_us"] = round(su * 1e6, 1)
             mat.close()
             del temp_dq
-    fused_tf = tot_flops / (tot_fused * 1e-3) / 1e12
-    kern_flops = sum(f for f, _ in per_launch)
-    kern_ms = sum(t for _, t in per_launch)
-    achieved = kern_flops / (kern_ms * 1e-3) / 1e12
-    return {
-        "workload": "prefill_7b", "metric": "prefill TFLOPS (2*M*K*N / time)", "value": fused_tf,
-        "unit": "TFLOP/s", "unfused_value": tot_flops / (tot_unf * 1e-3) / 1e12,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
-                     "frac": achieved / bf16_tf, "traffic": None, "kernel": "prefill_kernel (fused prefill)",
-                     "peak_source": f"{peak_src} bf16 burst x 1 (fp16 and bf16 dense rates are equal)",
-                     "how": "trivial-g_idx cases: 2*M*K*N summed / per-call time (CUDA-graph replays) summed"},
-        "cases": cases,
-    }
+    for M in (512, 2048):
+        v = f_tot[M][0] / f_tot[M][1] / 1e12
+        out[f"m{M}"] = {"TFLOP/s": r3(v, 1), "frac": r3(v / bf16_tf), "min_frac": r3(min(fr[M])),
+                        "max_frac": r3(max(fr[M]))}
+    out["unfused"] = r3(u_tot[0] / u_tot[1] / 1e12, 1)
+    return out, detail
+
+
+def run_sweep_70b_cases(q4, torch, dev, stream, sw, hbm_gbs, tf_peak):
+    """Every sweep_70b case on its own: per (config, M) a graph over the
+    config's replicas; binding-roofline fraction per case."""
+    cases = {}
+    for c in sw.cfgs:
+        for M in synthetic.SWEEP_70B_M:
+            mats = c["mats"] if M < 2048 else c["mats"][:1]
+            x = torch.from_numpy(synthetic.workload_x("sweep_70b", c["K"], c["N"], c["g"], c["act"], M)).to(dev)
+            o = torch.empty((M, c["N"]), dtype=torch.float16, device=dev)
+            for m in mats:
+                m.reserve(M)
+
+            def issue(sp):
+                for m in mats:
+                    q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o.data_ptr(), sp)
+
+            g, _ = capture(torch, q4, issue)
+            s = graph_seconds(torch, stream, g, 5) / len(mats)
+            del g
+            t_bw = c["wb"] / (hbm_gbs * 1e9)
+            t_tc = 2.0 * M * c["K"] * c["N"] / (tf_peak * 1e12)
+            cases[f"{cfg_name((c['K'], c['N'], c['g'], c['act']))} M={M}"] = {
+                "us": round(s * 1e6, 2), "frac": round(max(t_bw, t_tc) / s, 3)}
+    return cases
 
 
 def main():
