@@ -35,6 +35,7 @@ GPTQ_Q4_PATH_PREFILL = 2
 GPTQ_Q4_PATH_DECODE_MMA = 3
 GPTQ_Q4_PATH_DECODE_TC = 4
 GPTQ_Q4_PATH_DECODE_RING = 5
+GPTQ_Q4_PATH_DECODE_STREAM = 6
 GPTQ_Q4_FORMAT_GPTQ = 0
 GPTQ_Q4_FORMAT_GPTQ_V2 = 1
 GPTQ_Q4_DTYPE_FP16 = 0

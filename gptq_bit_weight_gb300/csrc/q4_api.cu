@@ -377,7 +377,10 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
     cudaStreamDestroy(s);
     s = nullptr;
     const q4::DecodePlan p = q4::plan_decode(decode_max_ws_rows(), Kp, N, gpad);
-    if (ensure_decode_work(h, p.ws_floats, p.n_tickets, nullptr, true)) return fail(0);
+    const q4::DecodeSkPlan sp = q4::plan_decode_sk(1, Kp, N, q4::device_sm_count());
+    if (ensure_decode_work(h, std::max(p.ws_floats, sp.ws_floats), std::max(p.n_tickets, sp.n_tickets), nullptr,
+                           true))
+        return fail(0);
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail(cuda_fail(e, "make"));
     ok();
     return h;
@@ -597,6 +600,11 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
         ws = std::max(ws, p.ws_floats);
         nt = std::max(nt, p.n_tickets);
     }
+    if (max_m >= 1) {       // the stream-K decode: the same workspace at every M <= 8
+        const q4::DecodeSkPlan sp = q4::plan_decode_sk(1, h->K, h->N, q4::device_sm_count());
+        ws = std::max(ws, sp.ws_floats);
+        nt = std::max(nt, sp.n_tickets);
+    }
     if (max_m > 64) {
         const q4::DecodePlan p = q4::plan_decode(max_m, h->K, h->N, h->geff);
         ws = std::max(ws, p.ws_floats);
@@ -654,6 +662,15 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
         ++g_launches;
         return ok();
+    }
+    if (path == GPTQ_Q4_PATH_DECODE_STREAM && M <= 8) {
+        const q4::DecodeSkPlan sp = q4::plan_decode_sk(M, h->K, h->N, q4::device_sm_count());
+        if (sp.ok) {
+            if (int r = ensure_decode_work(h, sp.ws_floats, sp.n_tickets, stream, false)) return r;
+            Q4_CUDA(q4::launch_decode_sk(v, sp, h->ws, h->tickets, xin, M, out, stream), "decode launch");
+            ++g_launches;
+            return ok();
+        }
     }
     if ((path == GPTQ_Q4_PATH_DECODE && !small_layer) || path == GPTQ_Q4_PATH_DECODE_RING) {
         const q4::DecodeRingPlan rp = q4::plan_decode_ring(M, h->K, h->N, h->geff, q4::device_sm_count());
@@ -748,7 +765,7 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
 
 int gptq_q4_set_path(gptq_q4_handle h, int path) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
-    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_RING)
+    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_STREAM)
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "unknown path %d", path);
     h->path = path;
     return ok();

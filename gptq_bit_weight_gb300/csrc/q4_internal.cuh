@@ -274,6 +274,22 @@ struct DecodeRingPlan {
 DecodeRingPlan plan_decode_ring(int M, int K, int N, int geff, int sms);
 cudaError_t launch_decode_ring(const HandleView &h, const DecodeRingPlan &plan, const uint16_t *x, int M,
                                uint16_t *out, cudaStream_t s);
+// stream-K decode with group slots (q4_decode_sk.cu), M <= 8
+struct DecodeSkPlan {
+    int ok;            // 0: shape not supported
+    int mp;            // rows per group slot (M rounded up to a power of two)
+    int ntw;           // n16 tiles per unit
+    int T, KC;         // tiles of 16 ntw columns, 64-row chunks per tile
+    long long U;       // units (tile, chunk)
+    int workers;       // warps with work
+    int ctas;
+    int smax;          // most segments of one tile
+    size_t ws_floats;  // fp32 partials [T][smax][8][16 ntw]
+    int n_tickets;     // one per tile
+};
+DecodeSkPlan plan_decode_sk(int M, int K, int N, int sms);
+cudaError_t launch_decode_sk(const HandleView &h, const DecodeSkPlan &p, float *ws, int *tickets, const uint16_t *x,
+                             int M, uint16_t *out, cudaStream_t s);
 // Dynamic shared-memory limit of kernel fn on device dev, set once per
 // (fn, dev, bytes); bytes < 0 asks for the device's largest (q4_decode.cu)
 cudaError_t dyn_smem_optin(const void *fn, int dev, int bytes, int *set);

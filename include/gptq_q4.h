@@ -86,6 +86,10 @@ extern "C" {
 #define GPTQ_Q4_PATH_DECODE_RING 5 /* the TMA-ring decode kernel whenever the shape allows it
                                       (M <= 16, a K slice within 48 groups), else
                                       register-streaming */
+#define GPTQ_Q4_PATH_DECODE_STREAM 6 /* the stream-K decode kernel (M <= 8): every warp of the
+                                        grid streams an equal run of 32-column x 64-row units,
+                                        quantization groups ride in the MMAs' spare columns;
+                                        larger M as GPTQ_Q4_PATH_DECODE */
 
 typedef struct gptq_q4_s *gptq_q4_handle;   /* opaque; owns device memory */
 

@@ -77,7 +77,7 @@ def test_unpack_and_dequant_bit_exact(q4, K, N, gs, act):
     mat.device_error()
 
 
-@pytest.mark.parametrize("path", ["DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC"])
+@pytest.mark.parametrize("path", ["DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "DECODE_STREAM"])
 @pytest.mark.parametrize("K,N,gs,act", SMALL)
 def test_decode_matches_oracle(q4, K, N, gs, act, path):
     """Every decode kernel: DECODE_RING runs the TMA-ring kernel for M <= 16
