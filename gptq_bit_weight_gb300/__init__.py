@@ -40,6 +40,7 @@ GPTQ_Q4_FORMAT_GPTQ = 0
 GPTQ_Q4_FORMAT_GPTQ_V2 = 1
 GPTQ_Q4_DTYPE_FP16 = 0
 GPTQ_Q4_DTYPE_BF16 = 1
+GPTQ_Q4_DTYPE_FP32 = 2
 
 EXPORTED = [
     "gptq_q4_make", "gptq_q4_set_bias", "gptq_q4_reserve", "gptq_q4_matmul", "gptq_q4_dequant",
@@ -307,9 +308,10 @@ class Q4Matrix:
         gptq_q4_set_format(self.handle, fmt)
 
     def set_act_dtype(self, dtype) -> None:
-        """torch.float16 (default) or torch.bfloat16: the type of x and y."""
+        """torch.float16 (default), torch.bfloat16 or torch.float32: the type of x and y."""
         import torch
-        code = {torch.float16: GPTQ_Q4_DTYPE_FP16, torch.bfloat16: GPTQ_Q4_DTYPE_BF16}[dtype]
+        code = {torch.float16: GPTQ_Q4_DTYPE_FP16, torch.bfloat16: GPTQ_Q4_DTYPE_BF16,
+                torch.float32: GPTQ_Q4_DTYPE_FP32}[dtype]
         gptq_q4_set_act_dtype(self.handle, code)
         self.act_dtype = dtype
 

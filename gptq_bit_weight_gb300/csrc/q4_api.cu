@@ -125,6 +125,7 @@ void release(gptq_q4_s *h) {
     cudaFree(h->tickets);
     cudaFree(h->temp_state);
     cudaFree(h->rowscale);
+    cudaFree(h->part);
     if (cur >= 0) cudaSetDevice(cur);
     delete h;
 }
@@ -198,7 +199,7 @@ int ensure_decode_work(gptq_q4_s *h, size_t ws_floats, int n_tickets, cudaStream
 
 int ensure_temp_state(gptq_q4_s *h, int M, cudaStream_t s, bool sync_alloc) {
     const size_t need = static_cast<size_t>(M) * h->K;
-    if (h->act_bf16 && static_cast<size_t>(M) > h->rowscale_elems) {
+    if ((h->act_bf16 || h->act_f32) && static_cast<size_t>(M) > h->rowscale_elems) {
         if (h->rowscale) {
             if (sync_alloc) cudaFree(h->rowscale);
             else Q4_CUDA(cudaFreeAsync(h->rowscale, s), "cudaFreeAsync(rowscale)");
@@ -213,7 +214,7 @@ int ensure_temp_state(gptq_q4_s *h, int M, cudaStream_t s, bool sync_alloc) {
         h->rowscale_elems = static_cast<size_t>(M);
         h->device_bytes += M * sizeof(float);
     }
-    if (!(h->act_order || h->act_bf16) || need <= h->temp_state_elems) return GPTQ_Q4_OK;
+    if (!(h->act_order || h->act_bf16 || h->act_f32) || need <= h->temp_state_elems) return GPTQ_Q4_OK;
     if (h->temp_state) {
         if (sync_alloc) cudaFree(h->temp_state);
         else Q4_CUDA(cudaFreeAsync(h->temp_state, s), "cudaFreeAsync(temp_state)");
@@ -227,6 +228,25 @@ int ensure_temp_state(gptq_q4_s *h, int M, cudaStream_t s, bool sync_alloc) {
     h->temp_state = static_cast<uint16_t *>(v);
     h->temp_state_elems = need;
     h->device_bytes += need * 2;
+    return GPTQ_Q4_OK;
+}
+
+// fp32 activations: room for the raw fp32 sums of 2M rows
+int ensure_part(gptq_q4_s *h, size_t elems, cudaStream_t s, bool sync_alloc) {
+    if (elems <= h->part_elems) return GPTQ_Q4_OK;
+    if (h->part) {
+        if (sync_alloc) cudaFree(h->part);
+        else Q4_CUDA(cudaFreeAsync(h->part, s), "cudaFreeAsync(partial rows)");
+        h->device_bytes -= h->part_elems * sizeof(float);
+        h->part = nullptr;
+        h->part_elems = 0;
+    }
+    void *v = nullptr;
+    cudaError_t e = sync_alloc ? cudaMalloc(&v, elems * sizeof(float)) : cudaMallocAsync(&v, elems * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "allocating the fp32 partial rows");
+    h->part = static_cast<float *>(v);
+    h->part_elems = elems;
+    h->device_bytes += elems * sizeof(float);
     return GPTQ_Q4_OK;
 }
 
@@ -616,40 +636,10 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
     return ok();
 }
 
-static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out, cudaStream_t stream,
-                      int path) {
-    // Which decode kernel: measured on GB300 (CUDA-graph replays over more
-    // weights than L2), the register-streaming kernel (with its shared
-    // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
-    // layers below 64 Mi weights and at any M on layers below 24 Mi weights;
-    // the TMA-ring kernel is ahead everywhere else it applies.
-    const size_t weights = static_cast<size_t>(h->K) * h->N;
-    const bool small_layer =
-        M <= 4 || weights < (size_t{24} << 20) || (M <= 8 && weights < (size_t{64} << 20));
-    // the activation kernel lets the decode grid start early when that grid
-    // is the register-streaming kernel at M <= 8 (measured faster only there)
-    const bool early = M <= 8 && (path == GPTQ_Q4_PATH_DECODE_MMA || (path == GPTQ_Q4_PATH_DECODE && small_layer));
-    const uint16_t *xin = x;
-    if (h->act_bf16) {
-        // bf16 x: scaled by a power of two per row and rounded once to fp16
-        // (gathered at the same time under act-order); the epilogues undo the scale
-        if (int r = ensure_temp_state(h, M, stream, false)) return r;
-        Q4_CUDA(q4::launch_xprep_bf16(x, h->act_order ? h->perm : nullptr, M, h->Kx, h->K, h->temp_state,
-                                      h->rowscale, stream, early),
-                "bf16 preparation launch");
-        ++g_launches;
-        xin = h->temp_state;
-    } else if (h->act_order) {
-        if (int r = ensure_temp_state(h, M, stream, false)) return r;
-        Q4_CUDA(q4::launch_xreorder(x, h->perm, M, h->Kx, h->K, h->temp_state, stream, early), "xreorder launch");
-        ++g_launches;
-        xin = h->temp_state;
-    }
-    q4::HandleView v = view(h);
-    if (h->act_bf16) {
-        v.rowscale = h->rowscale;
-        v.out_bf16 = 1;
-    }
+// One of the kernels on prepared fp16 rows xin [M][K] (K the private
+// layout's rows), epilogue as v says.
+static int run_path(gptq_q4_handle h, const q4::HandleView &v, const uint16_t *xin, int M, uint16_t *out,
+                    cudaStream_t stream, int path, bool small_layer) {
     if (path == GPTQ_Q4_PATH_PREFILL) {
         const q4::PrefillPlan pp = q4::plan_prefill(M, h->K, h->N);
         if (int r = ensure_decode_work(h, pp.ws_floats, pp.n_tickets, stream, false)) return r;
@@ -657,7 +647,7 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
         ++g_launches;
         return ok();
     }
-    if (path == GPTQ_Q4_PATH_DECODE_TC && h->zsplit == 0 && !h->act_bf16 &&
+    if (path == GPTQ_Q4_PATH_DECODE_TC && h->zsplit == 0 && v.out_bf16 == q4::kOutF16 &&
         q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
         Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
         ++g_launches;
@@ -688,6 +678,60 @@ static int run_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
     return ok();
 }
 
+static int run_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStream_t stream, int path) {
+    // fp32 activations: the kernels see 2M fp16 rows (each row's hi and lo
+    // parts) and write raw fp32 sums; a last pass adds each row's two parts
+    const int Mk = h->act_f32 ? 2 * M : M;
+    // Which decode kernel: measured on GB300 (CUDA-graph replays over more
+    // weights than L2), the register-streaming kernel (with its shared
+    // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
+    // layers below 64 Mi weights and at any M on layers below 24 Mi weights;
+    // the TMA-ring kernel is ahead everywhere else it applies.
+    const size_t weights = static_cast<size_t>(h->K) * h->N;
+    const bool small_layer =
+        Mk <= 4 || weights < (size_t{24} << 20) || (Mk <= 8 && weights < (size_t{64} << 20));
+    // the activation kernel lets the decode grid start early when that grid
+    // is the register-streaming kernel at M <= 8 (measured faster only there)
+    const bool early = Mk <= 8 && (path == GPTQ_Q4_PATH_DECODE_MMA || (path == GPTQ_Q4_PATH_DECODE && small_layer));
+    const uint16_t *xin = static_cast<const uint16_t *>(x);
+    q4::HandleView v = view(h);
+    if (h->act_f32) {
+        if (int r = ensure_temp_state(h, Mk, stream, false)) return r;
+        if (int r = ensure_part(h, static_cast<size_t>(Mk) * h->N, stream, false)) return r;
+        Q4_CUDA(q4::launch_xprep_f32(static_cast<const float *>(x), h->act_order ? h->perm : nullptr, M, h->Kx, h->K,
+                                     h->temp_state, h->rowscale, stream),
+                "fp32 preparation launch");
+        ++g_launches;
+        xin = h->temp_state;
+        v.out_bf16 = q4::kOutF32;
+        v.bias = nullptr;
+        if (int r = run_path(h, v, xin, Mk, reinterpret_cast<uint16_t *>(h->part), stream, path, small_layer))
+            return r;
+        Q4_CUDA(q4::launch_combine_f32(h->part, h->rowscale, h->bias, M, h->N, static_cast<float *>(out), stream),
+                "fp32 combine launch");
+        ++g_launches;
+        return ok();
+    }
+    if (h->act_bf16) {
+        // bf16 x: scaled by a power of two per row and rounded once to fp16
+        // (gathered at the same time under act-order); the epilogues undo the scale
+        if (int r = ensure_temp_state(h, M, stream, false)) return r;
+        Q4_CUDA(q4::launch_xprep_bf16(xin, h->act_order ? h->perm : nullptr, M, h->Kx, h->K, h->temp_state,
+                                      h->rowscale, stream, early),
+                "bf16 preparation launch");
+        ++g_launches;
+        xin = h->temp_state;
+        v.rowscale = h->rowscale;
+        v.out_bf16 = q4::kOutBF16;
+    } else if (h->act_order) {
+        if (int r = ensure_temp_state(h, M, stream, false)) return r;
+        Q4_CUDA(q4::launch_xreorder(xin, h->perm, M, h->Kx, h->K, h->temp_state, stream, early), "xreorder launch");
+        ++g_launches;
+        xin = h->temp_state;
+    }
+    return run_path(h, v, xin, M, static_cast<uint16_t *>(out), stream, path, small_layer);
+}
+
 static int check_matmul_args(gptq_q4_handle h, const void *x, int M, const void *out) {
     if (int r = check_handle(h)) return r;
     if (M < 0) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "M=%d < 0", M);
@@ -698,11 +742,12 @@ static int check_matmul_args(gptq_q4_handle h, const void *x, int M, const void 
     return GPTQ_Q4_OK;
 }
 
-int gptq_q4_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out, cudaStream_t stream) {
+int gptq_q4_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStream_t stream) {
     if (int r = check_matmul_args(h, x, M, out)) return r;
     if (M == 0) return ok();
     int path = h->path;
-    if (path == GPTQ_Q4_PATH_AUTO) path = (M >= h->prefill_min_m) ? GPTQ_Q4_PATH_PREFILL : GPTQ_Q4_PATH_DECODE;
+    const int Mk = h->act_f32 ? 2 * M : M;            // rows the kernels see
+    if (path == GPTQ_Q4_PATH_AUTO) path = (Mk >= h->prefill_min_m) ? GPTQ_Q4_PATH_PREFILL : GPTQ_Q4_PATH_DECODE;
     return run_matmul(h, x, M, out, stream, path);
 }
 
@@ -739,7 +784,7 @@ int gptq_q4_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias,
     return ok();
 }
 
-int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *temp_dq, uint16_t *out,
+int gptq_q4_matmul_unfused(gptq_q4_handle h, const void *x, int M, uint16_t *temp_dq, void *out,
                            cudaStream_t stream) {
     if (int r = check_matmul_args(h, x, M, out)) return r;
     if (M == 0) return ok();
@@ -748,15 +793,29 @@ int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M, uint16_t 
     if (h->bits == 8) Q4_CUDA(q4::launch_dequant8(view(h), h->inv8, h->Kx, temp_dq, stream), "dequant launch");
     else Q4_CUDA(q4::launch_dequant(view(h), temp_dq, stream), "dequant launch");
     ++g_launches;
-    const uint16_t *xa = x;
+    const uint16_t *xa = static_cast<const uint16_t *>(x);
+    if (h->act_f32) {    // x in original order, split into hi and lo fp16 rows
+        if (int r = ensure_temp_state(h, 2 * M, stream, false)) return r;
+        if (int r = ensure_part(h, static_cast<size_t>(2 * M) * h->N, stream, false)) return r;
+        Q4_CUDA(q4::launch_xprep_f32(static_cast<const float *>(x), nullptr, M, h->Kx, h->Kx, h->temp_state,
+                                     h->rowscale, stream),
+                "fp32 preparation launch");
+        Q4_CUDA(q4::launch_gemm_f16(h->temp_state, temp_dq, nullptr, 2 * M, h->Kx, h->N,
+                                    reinterpret_cast<uint16_t *>(h->part), h->status, stream, nullptr, q4::kOutF32),
+                "gemm launch");
+        Q4_CUDA(q4::launch_combine_f32(h->part, h->rowscale, h->bias, M, h->N, static_cast<float *>(out), stream),
+                "fp32 combine launch");
+        g_launches += 3;
+        return ok();
+    }
     if (h->act_bf16) {   // x in original order, scaled per row and rounded once to fp16
         if (int r = ensure_temp_state(h, M, stream, false)) return r;
-        Q4_CUDA(q4::launch_xprep_bf16(x, nullptr, M, h->Kx, h->Kx, h->temp_state, h->rowscale, stream),
+        Q4_CUDA(q4::launch_xprep_bf16(xa, nullptr, M, h->Kx, h->Kx, h->temp_state, h->rowscale, stream),
                 "bf16 preparation launch");
         ++g_launches;
         xa = h->temp_state;
     }
-    Q4_CUDA(q4::launch_gemm_f16(xa, temp_dq, h->bias, M, h->Kx, h->N, out, h->status, stream,
+    Q4_CUDA(q4::launch_gemm_f16(xa, temp_dq, h->bias, M, h->Kx, h->N, static_cast<uint16_t *>(out), h->status, stream,
                                 h->act_bf16 ? h->rowscale : nullptr, h->act_bf16),
             "gemm launch");
     ++g_launches;
@@ -827,10 +886,11 @@ int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream
 
 int gptq_q4_set_act_dtype(gptq_q4_handle h, int dtype) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
-    if (dtype != GPTQ_Q4_DTYPE_FP16 && dtype != GPTQ_Q4_DTYPE_BF16)
-        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "dtype=%d is neither GPTQ_Q4_DTYPE_FP16 nor GPTQ_Q4_DTYPE_BF16",
-                          dtype);
+    if (dtype != GPTQ_Q4_DTYPE_FP16 && dtype != GPTQ_Q4_DTYPE_BF16 && dtype != GPTQ_Q4_DTYPE_FP32)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT,
+                          "dtype=%d is none of GPTQ_Q4_DTYPE_FP16, GPTQ_Q4_DTYPE_BF16, GPTQ_Q4_DTYPE_FP32", dtype);
     h->act_bf16 = dtype == GPTQ_Q4_DTYPE_BF16 ? 1 : 0;
+    h->act_f32 = dtype == GPTQ_Q4_DTYPE_FP32 ? 1 : 0;
     return ok();
 }
 

@@ -545,8 +545,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
     auto store_out = [&](int e, float v) {
         int m, n;
         element_mn(e, m, n);
-        if (m < a.M)
-            a.out[static_cast<size_t>(m) * N + n] = out_one(v, h.rowscale ? h.rowscale[m] : 1.f, h.bias, n, h.out_bf16);
+        if (m < a.M) {
+            if (h.out_bf16 == kOutF32) reinterpret_cast<float *>(a.out)[static_cast<size_t>(m) * N + n] = v;
+            else a.out[static_cast<size_t>(m) * N + n] = out_one(v, h.rowscale ? h.rowscale[m] : 1.f, h.bias, n, h.out_bf16);
+        }
     };
 
     // CTA partial: the warps' partials summed in warp order, kept in red[0, E)

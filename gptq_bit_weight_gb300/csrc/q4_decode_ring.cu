@@ -399,9 +399,13 @@ __global__ void __launch_bounds__(kThreads, 3)
                     for (int i = 0; i < 4; ++i) {
                         const int n = n0 + 16 * (kTPW * warp + t) + gq + 8 * (i >> 1);
                         const int m = m0 + mt * 8 + 2 * tq + (i & 1);
-                        if (m < a.M && n < a.N)
-                            a.out[static_cast<size_t>(m) * a.N + n] =
-                                out_one(acc[t][mt][i], a.rowscale ? a.rowscale[m] : 1.f, a.bias, n, a.out_bf16);
+                        if (m < a.M && n < a.N) {
+                            if (a.out_bf16 == kOutF32)
+                                reinterpret_cast<float *>(a.out)[static_cast<size_t>(m) * a.N + n] = acc[t][mt][i];
+                            else
+                                a.out[static_cast<size_t>(m) * a.N + n] =
+                                    out_one(acc[t][mt][i], a.rowscale ? a.rowscale[m] : 1.f, a.bias, n, a.out_bf16);
+                        }
                     }
         }
         return;
@@ -427,8 +431,11 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (e % a.splits != split || ml >= mrows || n0 + nl >= a.N) continue;
             float v = 0.f;
             for (int r = 0; r < a.splits; ++r) v += ld_dsmem_f32(red_local + e * 4, r);
-            a.out[static_cast<size_t>(m0 + ml) * a.N + n0 + nl] =
-                out_one(v, a.rowscale ? a.rowscale[m0 + ml] : 1.f, a.bias, n0 + nl, a.out_bf16);
+            if (a.out_bf16 == kOutF32)
+                reinterpret_cast<float *>(a.out)[static_cast<size_t>(m0 + ml) * a.N + n0 + nl] = v;
+            else
+                a.out[static_cast<size_t>(m0 + ml) * a.N + n0 + nl] =
+                    out_one(v, a.rowscale ? a.rowscale[m0 + ml] : 1.f, a.bias, n0 + nl, a.out_bf16);
         }
     }
     cluster_sync();                                   // partials stay alive until all are read

@@ -299,8 +299,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
         const int wf = owner(tu0, a.U, a.workers), wl = owner(tu0 + KC - 1, a.U, a.workers);
         const int n0 = kCols * seg_t;
         auto store = [&](int row, int col, float val) {
-            a.out[static_cast<size_t>(row) * N + n0 + col] =
-                out_one(val, h.rowscale ? h.rowscale[row] : 1.f, h.bias, n0 + col, h.out_bf16);
+            if (h.out_bf16 == kOutF32) reinterpret_cast<float *>(a.out)[static_cast<size_t>(row) * N + n0 + col] = val;
+            else
+                a.out[static_cast<size_t>(row) * N + n0 + col] =
+                    out_one(val, h.rowscale ? h.rowscale[row] : 1.f, h.bias, n0 + col, h.out_bf16);
         };
         if (wf == wl) {
 #pragma unroll

@@ -30,8 +30,11 @@ struct gptq_q4_s {
     int bits = 4;           // 8: the handle holds an 8-bit layer as two 4-bit halves along K
     int zsplit = 0;         // groups [0, zsplit) take zero offset 0 (8-bit: the high-nibble half)
     int act_bf16 = 0;       // x and out are bf16 (GPTQ_Q4_DTYPE_BF16)
-    float *rowscale = nullptr;  // bf16: 2^e per row of the current call
+    int act_f32 = 0;        // x and out are fp32 (GPTQ_Q4_DTYPE_FP32)
+    float *rowscale = nullptr;  // bf16 / fp32: 2^e per row of the current call
     size_t rowscale_elems = 0;
+    float *part = nullptr;      // fp32: the raw sums of the hi and lo rows, [2M][N]
+    size_t part_elems = 0;
     size_t device_bytes = 0;
 };
 

@@ -167,11 +167,16 @@ struct HandleView {
     int zero_offset;        // effective zero = stored + zero_offset (1: GPTQ, 0: GPTQ_V2)
     int zsplit;             // groups [0, zsplit) take zero offset 0 instead (the high-nibble
                             // half of an 8-bit layer), the rest zero_offset
-    // output epilogue of this call: y = acc * rowscale[m] + bias, rounded once
-    // to fp16, or to bf16 when out_bf16 (rowscale NULL: 1)
+    // output epilogue of this call (out_bf16 is the output mode):
+    //   kOutF16  y = acc * rowscale[m] + bias, rounded once to fp16
+    //   kOutBF16 the same rounded once to bf16 (rowscale NULL: 1)
+    //   kOutF32  the fp32 sum acc itself, no bias and no row scale, stored as
+    //            float (out points to M x N floats); the fp32-activation route
+    //            combines two such rows per output row afterwards
     const float *rowscale;
     int out_bf16;
 };
+constexpr int kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2;
 
 // One output value / pair of the epilogue above.
 __device__ __forceinline__ uint32_t out_bits(float v, bool bf16) {
@@ -232,6 +237,15 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
 cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
                               float *rowscale, cudaStream_t s, bool early = false);
 
+// fp32 activations: per row m, e_m with max|x[m]| * 2^-e_m in [2^14, 2^15);
+// v = x[m][perm[j]] * 2^-e_m (perm NULL: j; -1: 0), temp_state[m][j] =
+// fp16(v) (hi) and temp_state[M + m][j] = fp16(v - hi) (lo, exact residual
+// rounded once); rowscale[m] = 2^e_m
+cudaError_t launch_xprep_f32(const float *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
+                             float *rowscale, cudaStream_t s);
+// y[m][n] = (part[m][n] + part[M + m][n]) * rowscale[m] + bias[n] in fp32
+cudaError_t launch_combine_f32(const float *part, const float *rowscale, const uint16_t *bias, int M, int N, float *y,
+                               cudaStream_t s);
 // decode (q4_decode.cu)
 struct DecodePlan {
     int mt;            // 8-row m tiles per CTA (1, 2 or 4)

@@ -110,6 +110,10 @@ extern "C" int gptq_q4_matmul_noalloc(gptq_q4_handle h, const uint16_t *x, int M
                                       cudaStream_t stream) {
     if (int r = q4::api_check_matmul_args(h, x, M, out)) return r;
     if (M == 0) return q4::api_set_status(GPTQ_Q4_OK, nullptr);
+    if (h->act_f32)
+        return q4::api_set_status(GPTQ_Q4_UNSUPPORTED,
+                                  "gptq_q4_matmul_noalloc does not take fp32 activations (its scratch holds no "
+                                  "partial rows); use gptq_q4_matmul");
 
     // Carve the scratch: tickets | split-K partials | temp_state.
     const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N, h->geff);

@@ -432,7 +432,21 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                             }
                         }
                     };
-                    if (a.out_bf16) store(std::true_type{});
+                    if (a.out_bf16 == kOutF32) {
+                        // raw fp32 sums, 32 bytes per 8 columns
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int n = n0 + c0 + 8 * v;
+                            if (n < a.N) {
+                                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) +
+                                                                         static_cast<size_t>(row) * a.N + n);
+                                dst[0] = make_float4(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1]),
+                                                     __uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                                dst[1] = make_float4(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]),
+                                                     __uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            }
+                        }
+                    } else if (a.out_bf16) store(std::true_type{});
                     else store(std::false_type{});
                 }
             }
@@ -494,6 +508,13 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     const float4 p0 = __ldcg(src), p1 = __ldcg(src + 32);
                     v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
                     v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+                }
+                if (a.out_bf16 == kOutF32) {
+                    float4 *dst =
+                        reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + static_cast<size_t>(row) * a.N + n);
+                    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                    continue;
                 }
                 uint32_t pk[4];
                 const float rs = a.rowscale ? a.rowscale[row] : 1.f;

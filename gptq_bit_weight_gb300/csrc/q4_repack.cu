@@ -345,4 +345,88 @@ cudaError_t launch_xprep_bf16(const uint16_t *x, const int32_t *perm, int M, int
                       temp_state, rowscale, early);
 }
 
+// --------------------------------------------------- fp32 activations
+// One CTA per row.  As for bf16, the row's largest magnitude picks 2^e with
+// max|x| * 2^-e in [2^14, 2^15); v = x * 2^-e is exact in fp32.  hi = v
+// rounded once to fp16; v - hi is exact in fp32 (hi is within half an fp16
+// unit of v), and lo = that residual rounded once to fp16.  hi + lo carries
+// v to about 2^-22 of itself, so the fp16 kernels run on 2M rows (hi rows,
+// then lo rows) and the two results of each row are summed afterwards.
+__global__ void __launch_bounds__(1024) xprep_f32_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
+                                                        int M, int Kx, int K, uint16_t *__restrict__ ts,
+                                                        float *__restrict__ rowscale) {
+    __shared__ float wmax[32];
+    pdl_enter(false);
+    const int nw = blockDim.x >> 5;
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
+        const float *xr = x + static_cast<size_t>(m) * Kx;
+        float mx = 0.f;
+        for (int k = threadIdx.x; k < Kx; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        mx = wmax[0];
+        for (int w = 1; w < nw; ++w) mx = fmaxf(mx, wmax[w]);
+        __syncthreads();                               // wmax is reused by the next row
+        // e = ilogb(max) - 14, kept where 2^-e and 2^e are normal fp32 values
+        int e = 0;
+        if (mx > 0.f && mx <= 3.402823466e38f) e = min(max(ilogbf(mx) - 14, -110), 113);
+        const float down = __int_as_float((127 - e) << 23);   // 2^-e
+        if (threadIdx.x == 0) rowscale[m] = __int_as_float((127 + e) << 23);
+        uint16_t *hi_row = ts + static_cast<size_t>(m) * K;
+        uint16_t *lo_row = ts + static_cast<size_t>(M + m) * K;
+        for (int j = threadIdx.x; j < K; j += blockDim.x) {
+            const int k = perm ? perm[j] : j;
+            const float v = k >= 0 ? xr[k] * down : 0.f;
+            const __half hi = __float2half_rn(v);
+            const float r = v - __half2float(hi);
+            hi_row[j] = __half_as_ushort(hi);
+            lo_row[j] = __half_as_ushort(__float2half_rn(r));
+        }
+    }
+}
+
+cudaError_t launch_xprep_f32(const float *x, const int32_t *perm, int M, int Kx, int K, uint16_t *temp_state,
+                             float *rowscale, cudaStream_t s) {
+    const int ctas = std::min(M, kSMs * 8);
+    const int threads = M <= kSMs ? 1024 : 256;
+    return launch_pdl(false, xprep_f32_kernel, ctas > 0 ? ctas : 1, threads, size_t{0}, s, x, perm, M, Kx, K,
+                      temp_state, rowscale);
+}
+
+// y[m][n] = (part[m][n] + part[M + m][n]) * rowscale[m] + bias[n]: the hi and
+// lo results of a row summed in fp32, the row's power of two restored
+// (exact), bias added; no rounding beyond fp32.  Four columns per thread.
+__global__ void combine_f32_kernel(const float *__restrict__ part, const float *__restrict__ rowscale,
+                                   const uint16_t *__restrict__ bias, int M, int N, float *__restrict__ y) {
+    pdl_enter(false);
+    const size_t total = static_cast<size_t>(M) * (N / 4);
+    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t m = idx / (N / 4);
+        const int n = static_cast<int>(idx % (N / 4)) * 4;
+        const float4 a = *reinterpret_cast<const float4 *>(part + m * N + n);
+        const float4 b = *reinterpret_cast<const float4 *>(part + (m + M) * N + n);
+        const float rs = rowscale[m];
+        float4 o = make_float4((a.x + b.x) * rs, (a.y + b.y) * rs, (a.z + b.z) * rs, (a.w + b.w) * rs);
+        if (bias) {
+            o.x += __half2float(__ushort_as_half(bias[n]));
+            o.y += __half2float(__ushort_as_half(bias[n + 1]));
+            o.z += __half2float(__ushort_as_half(bias[n + 2]));
+            o.w += __half2float(__ushort_as_half(bias[n + 3]));
+        }
+        *reinterpret_cast<float4 *>(y + m * N + n) = o;
+    }
+}
+
+cudaError_t launch_combine_f32(const float *part, const float *rowscale, const uint16_t *bias, int M, int N, float *y,
+                               cudaStream_t s) {
+    const size_t total = static_cast<size_t>(M) * (N / 4);
+    const int threads = 256;
+    const size_t want = (total + threads - 1) / threads;
+    const int blocks = static_cast<int>(std::min<size_t>(want, static_cast<size_t>(kSMs) * 16));
+    return launch_pdl(false, combine_f32_kernel, blocks > 0 ? blocks : 1, threads, size_t{0}, s, part, rowscale, bias,
+                      M, N, y);
+}
+
 }  // namespace q4

@@ -148,8 +148,10 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m);
 
 /* out = x . W + bias  (q4_matmul; the Lorax page's "Description").
  *
- *   x    device fp16 [M][K], 16-byte aligned
- *   out  device fp16 [M][N], 16-byte aligned; written entirely, never read
+ *   x    device [M][K] of the handle's activation type (fp16 by default;
+ *        bf16 or fp32 after gptq_q4_set_act_dtype), 16-byte aligned
+ *   out  device [M][N] of the same type, 16-byte aligned; written entirely,
+ *        never read
  *   M    rows; 0 is a valid no-op
  *
  * With act-order, x is first gathered into temp_state (temp_state[m][j] =
@@ -177,7 +179,7 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m);
  * Errors: INVALID_ARGUMENT (NULL handle/pointers with M > 0, M < 0,
  * misaligned x or out, handle made on another device), OUT_OF_MEMORY (growing
  * a work buffer), CUDA_ERROR (launch failure). */
-int gptq_q4_matmul(gptq_q4_handle h, const uint16_t *x, int M, uint16_t *out,
+int gptq_q4_matmul(gptq_q4_handle h, const void *x, int M, void *out,
                    cudaStream_t stream);
 
 /* temp_dq[k][n] = fp16(scales[g][n] * (q[k][n] - (z[g][n] + 1))), rounded
@@ -205,8 +207,8 @@ int gptq_q4_debug_unpack(gptq_q4_handle h, uint8_t *q, uint8_t *z, cudaStream_t 
  * out = x . temp_dq + bias by the tcgen05 GEMM below.  Same arguments as
  * gptq_q4_matmul plus temp_dq (device fp16 [K][N], caller-owned scratch).
  * Errors: as gptq_q4_matmul and gptq_q4_dequant. */
-int gptq_q4_matmul_unfused(gptq_q4_handle h, const uint16_t *x, int M,
-                           uint16_t *temp_dq, uint16_t *out, cudaStream_t stream);
+int gptq_q4_matmul_unfused(gptq_q4_handle h, const void *x, int M,
+                           uint16_t *temp_dq, void *out, cudaStream_t stream);
 
 /* Dense fp16 GEMM on the 5th-generation tensor cores (tcgen05, accumulators
  * in tensor memory, operands staged by TMA): out = a . b + bias with fp32
@@ -315,18 +317,30 @@ gptq_q4_handle gptq_q4_make_fused(int parts, const int32_t *const *qweight, cons
 int gptq_q4_set_format(gptq_q4_handle h, int format);
 
 /* Type of x and out for later matmul calls on this handle ("Inference
- * Backends": backends keep the activation/output dtype, fp16 or bf16, with
- * fp16 scales and fp32 accumulation).  Default FP16.  With BF16, x and out are
- * bf16 [M][K] / [M][N] (bias stays the handle's fp16); every row of x is
- * first scaled by a power of two 2^-e (its largest magnitude times 2^-e in
- * [2^14, 2^15)) and rounded once to fp16 (exact for values within ~2^28 of
- * the row's largest: bf16 has an 8-bit significand), the fp16 kernels run
- * unchanged, and each output is acc * 2^e + bias rounded once to bf16.
- * Covers gptq_q4_matmul, gptq_q4_matmul_unfused and gptq_q4_matmul_noalloc;
- * one extra launch per call prepares x (fused with the act-order gather).
+ * Backends", "Hardware, dependency, and format requirements": the ExLlama v2
+ * row declares FP16/BF16/FP32 activation dtypes, keeps the activation/output
+ * dtype, fp16 scales and fp32 accumulation).  Default FP16.  bias stays the
+ * handle's fp16.
+ *   BF16: x and out are bf16 [M][K] / [M][N]; every row of x is first scaled
+ *     by a power of two 2^-e (its largest magnitude times 2^-e in [2^14,
+ *     2^15)) and rounded once to fp16 (exact for values within ~2^28 of the
+ *     row's largest: bf16 has an 8-bit significand), the fp16 kernels run
+ *     unchanged, and each output is acc * 2^e + bias rounded once to bf16.
+ *     Covers gptq_q4_matmul, gptq_q4_matmul_unfused and
+ *     gptq_q4_matmul_noalloc; one extra launch per call prepares x (fused
+ *     with the act-order gather).
+ *   FP32: x and out are fp32 [M][K] / [M][N]; every row is scaled by 2^-e
+ *     as above and split into two fp16 rows, hi = fp16(v) and lo = fp16(v -
+ *     hi) (v - hi is exact, so hi + lo carries v to about 2^-22 of itself);
+ *     the fp16 kernels run on the 2M rows and write their raw fp32 sums, and
+ *     a last launch forms out = (sum_hi + sum_lo) * 2^e + bias in fp32 (no
+ *     rounding to a narrower type).  Covers gptq_q4_matmul and
+ *     gptq_q4_matmul_unfused (two extra launches per call);
+ *     gptq_q4_matmul_noalloc returns UNSUPPORTED for an FP32 handle.
  * Errors: INVALID_ARGUMENT (NULL handle, unknown dtype). */
 #define GPTQ_Q4_DTYPE_FP16 0
 #define GPTQ_Q4_DTYPE_BF16 1
+#define GPTQ_Q4_DTYPE_FP32 2
 int gptq_q4_set_act_dtype(gptq_q4_handle h, int dtype);
 
 /* Rows at and above which GPTQ_Q4_PATH_AUTO takes the prefill kernel (the

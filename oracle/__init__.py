@@ -72,6 +72,9 @@ def _load():
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_double.restype = ctypes.c_double
         lib.oracle_bf16_to_double_array.argtypes = [P, ctypes.c_size_t, P]
+        lib.oracle_f32_to_double.argtypes = [ctypes.c_uint32]
+        lib.oracle_f32_to_double.restype = ctypes.c_double
+        lib.oracle_f32_to_double_array.argtypes = [P, ctypes.c_size_t, P]
         lib.oracle_unpack_qzeros.argtypes = [P, I, I, P]
         lib.oracle_unpack_qweight8.argtypes = [P, I, I, P]
         lib.oracle_unpack_qzeros8.argtypes = [P, I, I, P]
@@ -119,6 +122,14 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     b = _c(bits, np.uint16)
     out = np.empty(b.shape, np.float64)
     _load().oracle_bf16_to_double_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def f32_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """fp32 bit patterns (uint32) -> exact fp64 values, from the binary32 definition."""
+    b = _c(bits, np.uint32)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_f32_to_double_array(_ptr(b), b.size, _ptr(out))
     return out
 
 
@@ -251,6 +262,24 @@ def reference_output_bf16(x_bf16_bits, dq: Dequantized, bias_fp16=None, nthreads
     x64 = bf16_bits_to_f64(x_bf16_bits)
     b64 = None if bias_fp16 is None else half_bits_to_f64(_bits(bias_fp16))
     return linear_f64(x64, half_bits_to_f64(dq.w16), b64, nthreads)
+
+
+def reference_output_f32(x_f32_bits, dq: Dequantized, bias_fp16=None, nthreads=None):
+    """y_ref = x . w16 + bias with fp32 activations (bit patterns, uint32)."""
+    x64 = f32_bits_to_f64(x_f32_bits)
+    b64 = None if bias_fp16 is None else half_bits_to_f64(_bits(bias_fp16))
+    return linear_f64(x64, half_bits_to_f64(dq.w16), b64, nthreads)
+
+
+def tolerance_rows_f32(x_f32_bits, w16_bits, y_ref: np.ndarray, K: int) -> np.ndarray:
+    """tolerance() for fp32 activations and outputs, with max|x| taken per
+    row of x:  1e-2 sqrt(K) max|x[m]| max|w| / 64 + 2e-3 |y_ref|.  An fp32
+    output adds no rounding of its own, so the relative term is the stated
+    one; the per-row max keeps rows scaled far below the others as strict."""
+    xa = np.abs(f32_bits_to_f64(x_f32_bits))
+    xmax = xa.max(axis=1, keepdims=True) if xa.size else np.zeros((y_ref.shape[0], 1))
+    wmax = float(np.max(np.abs(half_bits_to_f64(_bits(w16_bits))))) if np.size(w16_bits) else 0.0
+    return 1e-2 * np.sqrt(K) * xmax * wmax / 64.0 + 2e-3 * np.abs(y_ref)
 
 
 def tolerance_rows_bf16(x_bf16_bits, w16_bits, y_ref: np.ndarray, K: int) -> np.ndarray:

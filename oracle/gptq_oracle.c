@@ -129,6 +129,32 @@ void oracle_bf16_to_double_array(const uint16_t *b, size_t n, double *out)
     for (size_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(b[i]);
 }
 
+/* fp32 activations ("Inference Backends", "Hardware, dependency, and format
+ * requirements": the ExLlama v2 row declares FP16/BF16/FP32 activation
+ * dtypes).  An IEEE binary32 bit pattern to its exact double, from the
+ * format's definition: sign, 8-bit exponent with bias 127, 23-bit fraction;
+ * exponent 0 is zero or subnormal (f 2^-149), 255 is infinity or NaN. */
+double oracle_f32_to_double(uint32_t u)
+{
+    int sign = (int)(u >> 31);
+    int e = (int)((u >> 23) & 0xffu);
+    uint32_t f = u & 0x7fffffu;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -149);                /* zero or subnormal */
+    } else if (e == 255) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(0x800000u + f), e - 150);   /* (1 + f/2^23) 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+void oracle_f32_to_double_array(const uint32_t *u, size_t n, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = oracle_f32_to_double(u[i]);
+}
+
 /* ------------------------------------------------------------- unpack */
 
 /* q[k][n] = nibble (k mod 8) of qweight[k/8][n], lowest nibble first.

@@ -158,6 +158,16 @@ def activations_bf16(M: int, K: int, key, row_scales=None) -> np.ndarray:
     return u.astype(np.uint16)
 
 
+def activations_f32(M: int, K: int, key, row_scales=None) -> np.ndarray:
+    """x ~ N(0, 1) (times row_scales[m] per row, if given) as fp32, returned
+    as uint32 bit patterns [M, K]."""
+    g = rng(*key)
+    v = g.standard_normal((M, K))
+    if row_scales is not None:
+        v = v * np.asarray(row_scales, np.float64)[:, None]
+    return v.astype(np.float32).view(np.uint32)
+
+
 # ------------------------------------------------------------ workloads
 
 def single_layer():

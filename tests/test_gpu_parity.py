@@ -323,6 +323,81 @@ def test_bf16_activations_match_oracle(q4, K, N, gs, act):
     mat.device_error()
 
 
+def f32_tensor(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.float32)).to(DEV)
+
+
+def check_y_f32(y_gpu, xf, dq, bias, K, what=""):
+    y_ref = oracle.reference_output_f32(xf, dq, bias)
+    tol = oracle.tolerance_rows_f32(xf, dq.w16, y_ref, K)
+    y = y_gpu.cpu().numpy().astype(np.float64)
+    err = np.abs(y - y_ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside tolerance; worst err/tol "
+                           f"{float(np.max(err / np.maximum(tol, 1e-300))):.3f}")
+
+
+@pytest.mark.parametrize("K,N,gs,act", BF16_CASES)
+def test_f32_activations_match_oracle(q4, K, N, gs, act):
+    """fp32 x and y: every path and the unfused route against the oracle,
+    with rows of x scaled by 1e6 and 1e-6 (outside fp16's range), checked
+    row by row; the allocation-free call refuses an fp32 handle."""
+    layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(36, K, N, gs & 0xFFFF, act))
+    dq = oracle_dq(layer)
+    mat = make(q4, layer)
+    mat.set_act_dtype(torch.float32)
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "DECODE_STREAM", "PREFILL"):
+        mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+        for M in (1, 3, 8, 16, 40):
+            rs = [BF16_ROW_SCALES[m % 4] for m in range(M)]
+            xf = synthetic.activations_f32(M, K, key=(36, K, N, M), row_scales=rs)
+            y = mat(f32_tensor(xf))
+            torch.cuda.synchronize()
+            assert y.dtype == torch.float32
+            check_y_f32(y, xf, dq, layer.bias, K, f"fp32 {path} K={K} N={N} g={gs} act={act} M={M}")
+    M = 300
+    xf = synthetic.activations_f32(M, K, key=(36, K, N, M), row_scales=[BF16_ROW_SCALES[m % 4] for m in range(M)])
+    mat.set_path(q4.GPTQ_Q4_PATH_AUTO)
+    y = mat(f32_tensor(xf))
+    yu = mat.matmul_unfused(f32_tensor(xf))
+    torch.cuda.synchronize()
+    check_y_f32(y, xf, dq, layer.bias, K, "fp32 prefill M=300")
+    check_y_f32(yu, xf, dq, layer.bias, K, "fp32 unfused M=300")
+    out = torch.empty((4, N), dtype=torch.float32, device=DEV)
+    xt = f32_tensor(synthetic.activations_f32(4, K, key=(37, K, N, 4)))
+    with pytest.raises(q4.GPTQ4Error) as e:
+        q4.gptq_q4_matmul_noalloc(mat.handle, xt.data_ptr(), 4, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == q4.GPTQ_Q4_UNSUPPORTED
+    mat.set_act_dtype(torch.float16)
+    x = synthetic.activations(5, K, key=(36, K, N, 5))
+    y = mat(to_dev(x))
+    torch.cuda.synchronize()
+    check_y(y, x, dq, layer.bias, K, "back to fp16")
+    mat.device_error()
+
+
+def test_f32_activations_70b_shape(q4):
+    """fp32 activations on a Llama-70B projection (8192 x 10240, act-order,
+    g = 128) at decode and prefill sizes; oracle on a column sample."""
+    K, N, gs = 8192, 10240, 128
+    layer = synthetic.workload_layer("sweep_70b", K, N, gs, True)
+    g = np.random.default_rng(38)
+    blocks = np.sort(g.choice(N // 8, size=16, replace=False))
+    cols = (blocks[:, None] * 8 + np.arange(8)[None, :]).reshape(-1)
+    dq = oracle.dequantize_layer(layer.qweight[:, cols], layer.qzeros[:, blocks], layer.scales[:, cols],
+                                 layer.g_idx, K, cols.size, gs)
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                      None, gs)
+    mat.set_act_dtype(torch.float32)
+    tcols = torch.from_numpy(cols).to(DEV)
+    for M in (1, 4, 64):
+        xf = synthetic.activations_f32(M, K, key=(38, M), row_scales=[BF16_ROW_SCALES[m % 4] for m in range(M)])
+        y = mat(f32_tensor(xf))
+        torch.cuda.synchronize()
+        check_y_f32(y[:, tcols], xf, dq, None, K, f"fp32 70B M={M}")
+    mat.device_error()
+
+
 V2_CASES = [  # (K, N, groupsize, act_order)
     (256, 128, 64, False),
     (1024, 448, 32, True),

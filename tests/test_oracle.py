@@ -548,3 +548,69 @@ def test_tolerance_hand_computed_values():
     tol = oracle.tolerance(x.view(np.uint16), w.view(np.uint16), y_ref, 64)
     expect = np.array([[0.012, 0.03, 0.01], [0.21, 0.011, 0.016]])
     np.testing.assert_allclose(tol, expect, rtol=1e-12, atol=0)
+
+
+# ------------------------------------------------------------- fp32 x
+
+def test_f32_to_double_matches_numpy_on_sampled_patterns():
+    """The binary32 decoder against numpy's float32 reinterpretation: 2^20
+    seeded random bit patterns plus every exponent at the fraction's ends,
+    signed zeros, the subnormal range's ends, the largest finite values and
+    infinities; NaN patterns decode to NaN."""
+    g = np.random.default_rng(21)
+    rnd = g.integers(0, 2**32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    e = np.arange(256, dtype=np.uint32) << 23
+    ends = np.concatenate([e, e | 1, e | 0x7FFFFF, e | 0x400000])
+    special = np.array([0, 0x80000000, 1, 0x80000001, 0x007FFFFF, 0x00800000, 0x7F7FFFFF, 0xFF7FFFFF,
+                        0x7F800000, 0xFF800000], np.uint32)
+    bits = np.concatenate([rnd, ends, ends | 0x80000000, special])
+    got = oracle.f32_bits_to_f64(bits)
+    with np.errstate(invalid="ignore"):
+        want = bits.view(np.float32).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_f32_hand_values():
+    """Values worked out from the binary32 layout by hand."""
+    cases = {0x3F800000: 1.0, 0xC0000000: -2.0, 0x00000001: 2.0 ** -149, 0x00800000: 2.0 ** -126,
+             0x7F7FFFFF: (2.0 - 2.0 ** -23) * 2.0 ** 127, 0x3EAAAAAB: 11184811 * 2.0 ** -25,
+             0x00400000: 2.0 ** -127}
+    for bits, v in cases.items():
+        assert oracle.f32_bits_to_f64(np.array([bits], np.uint32))[0] == v, hex(bits)
+
+
+def test_f32_tolerance_hand_computed_values():
+    """The fp32-activation bound (per-row max|x|) against hand-worked values.
+    K = 64 (sqrt 8), largest |w| = 2.  Row 0 has max|x| = 4, row 1 has 0.5:
+        row 0: 1e-2 * 8 * 4 * 2 / 64 = 0.01      row 1: ... * 0.5 ... = 0.00125
+    plus 0.002 |y_ref|:  y_ref = 1, -10 | 100, 0.5
+        bound = 0.012, 0.03 | 0.20125, 0.00225"""
+    x = np.zeros((2, 64), np.float32)
+    x[0, 3], x[0, 8] = -4.0, 2.5
+    x[1, 1] = 0.5
+    w = np.zeros((64, 2), np.float16)
+    w[10, 0] = -2.0
+    y_ref = np.array([[1.0, -10.0], [100.0, 0.5]])
+    tol = oracle.tolerance_rows_f32(x.view(np.uint32), w.view(np.uint16), y_ref, 64)
+    np.testing.assert_allclose(tol, np.array([[0.012, 0.03], [0.20125, 0.00225]]), rtol=1e-12, atol=0)
+
+
+def test_f32_reference_is_the_definition_on_a_tiny_layer():
+    """y for fp32 x by brute force: explicit nested sums over the exact
+    double values of x and of the dequantized weights."""
+    K, N, gs = 16, 8, 8
+    layer = synthetic.make_layer(K, N, gs, key=(23,))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, None, K, N, gs)
+    xb = synthetic.activations_f32(3, K, key=(23, 3), row_scales=[1.0, 1e6, 1e-6])
+    x = xb.view(np.float32).astype(np.float64)
+    w = dq.w16.view(np.float16).astype(np.float64)
+    y = oracle.reference_output_f32(xb, dq)
+    for m in range(3):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += x[m, k] * w[k, n]
+            assert y[m, n] == acc
