@@ -678,10 +678,29 @@ static int run_path(gptq_q4_handle h, const q4::HandleView &v, const uint16_t *x
     return ok();
 }
 
+// GPTQ_Q4_PATH_DECODE: where the stream-K kernel is ahead, measured on GB300
+// over the Llama-7B and Llama-70B projection layers at M = 1, 2, 4, 8
+// (CUDA-graph replays over more weights than L2):
+//   - a tall layer whose 32-column tiles cannot fill the GPU (K >= 2 N and
+//     fewer than two tiles per SM; 28672 x 8192) at M <= 2 with groups of
+//     at most 128 rows: the other kernels leave SMs short of warps;
+//   - M >= 5 on a wide layer (at least two tiles per SM) with groups of 32
+//     rows, or of 64 rows on layers of at least 100 Mi weights: the group
+//     slots save most of the per-group work there.
+static bool prefer_stream(const gptq_q4_s *h, int M) {
+    const long long tiles = h->N / 32, sms = q4::device_sm_count();
+    const size_t weights = static_cast<size_t>(h->K) * h->N;
+    if (M <= 2) return h->K >= 2LL * h->N && tiles < 2 * sms && h->geff <= 128;
+    if (M >= 5 && M <= 8 && tiles >= 2 * sms)
+        return h->geff <= 32 || (h->geff <= 64 && weights >= (size_t{100} << 20));
+    return false;
+}
+
 static int run_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStream_t stream, int path) {
     // fp32 activations: the kernels see 2M fp16 rows (each row's hi and lo
     // parts) and write raw fp32 sums; a last pass adds each row's two parts
     const int Mk = h->act_f32 ? 2 * M : M;
+    if (path == GPTQ_Q4_PATH_DECODE && prefer_stream(h, Mk)) path = GPTQ_Q4_PATH_DECODE_STREAM;
     // Which decode kernel: measured on GB300 (CUDA-graph replays over more
     // weights than L2), the register-streaming kernel (with its shared
     // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on

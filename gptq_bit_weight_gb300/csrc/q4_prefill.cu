@@ -557,9 +557,11 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
     if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
                        static_cast<uint64_t>(KC) * 512, 128, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
-    static cudaError_t attr =
-        cudaFuncSetAttribute(prefill_kernel<BM, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kSmem);
-    if (attr != cudaSuccess) return attr;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = dyn_smem_optin(reinterpret_cast<const void *>(prefill_kernel<BM, BN>), dev, P::kSmem, nullptr)) !=
+        cudaSuccess)
+        return e;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
                 (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, h.rowscale, h.out_bf16, p.splits, ws, tickets};
     const int nunits = args.tiles_m * args.tiles_n * p.splits;
