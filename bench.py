@@ -270,13 +270,17 @@ def cpu_baseline_sample(layers, budget_s: float = 12.0):
         secs += s
         n += 1
     return {"value": nbytes / secs / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} sweep_70b M=1 layer configs in turn x {SAMPLE_COLS} seeded columns, {secs:.1f} s"}
+            "sample": f"{n} sweep_70b M=1 configs x {SAMPLE_COLS} cols, {secs:.1f} s"}
 
 
 def headline_config():
-    return {"workload": "sweep_70b", "M": 1, "shapes": [list(s) for s in synthetic.SWEEP_70B_SHAPES],
-            "groupsize": synthetic.SWEEP_70B_G, "g_idx": ["trivial", "act-order"], "layer_configs": 24,
-            "bias": False}
+    return {"workload": "sweep_70b", "M": 1, "layer_configs": "3 shapes x g{32,64,128,-1} x {trivial,act-order}"}
+
+
+# DRAM bytes per step of the decode kernels (the roofline's traffic), from an
+# ncu capture of the same kernels; None until one has been taken of the
+# kernels as they stand.
+DECODE_TRAFFIC = None
 
 
 # ------------------------------------------------------------------ native
@@ -458,19 +462,17 @@ def run_native(args):
     if rank == 0:
         fr = list(fr1.values())
         cfg = headline_config()
-        cfg.update({"replicas": "R per config, R x weight bytes >= 3x L2",
-                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.1f} GB of weights per step, each replica "
-                          f"touched once per step (129 MB L2)",
-                    "bytes_per_step": step_bytes, "calls_per_step": launches_per_step,
-                    "launch": "one CUDA graph per step (captured C-ABI calls)", "parallelism": f"replicas x{world}"})
+        cfg.update({"bytes_per_step": step_bytes,
+                    "l2": f"inputs > L2: {step_bytes / 1e9:.1f} GB weights/step (>=3x L2 per config), each once",
+                    "launch": "CUDA graph of C-ABI calls", "parallelism": f"replicas x{world}"})
         line = {
             "metric": METRIC, "value": r3(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r3(ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 x int4 -> f32 accumulate", "data": "synthetic",
             "config": cfg,
             "roofline": {"bound": "hbm", "achieved": r3(achieved_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": r3(achieved_gbs / hbm_gbs), "traffic": None, "peak_source": peak_src,
-                         "kernel": "decode kernels on the 12 trivial-g_idx configs (graph of only decode launches)"},
+                         "frac": r3(achieved_gbs / hbm_gbs), "traffic": DECODE_TRAFFIC, "peak_source": peak_src,
+                         "kernel": "decode, 12 trivial-g_idx configs"},
             "m1_frac": {"min": r3(min(fr)), "mean": r3(float(np.mean(fr))), "max": r3(max(fr)),
                         "by_g": {str(g): r3(float(np.mean([f for k, f in fr1.items() if k[2] == g])))
                                  for g in synthetic.SWEEP_70B_G},
@@ -540,10 +542,11 @@ def run_extra_legs(q4, torch, dev, stream, sw, hbm_gbs, bf16_tf, issue_m, args):
     line["sweep_frac_by_M"] = {str(M): r3(f) for M, f in sorted(by_m.items())}
     p7, d7 = run_prefill_7b(q4, torch, dev, stream, bf16_tf)
     detail["prefill_7b"] = d7
-    line["prefill"] = {"m2048_70b": {"TFLOP/s": r3(tot_f / tot_s / 1e12, 1), "frac": r3(tot_f / tot_s / 1e12 / bf16_tf),
-                                     "min_frac": r3(min(pfr)), "max_frac": r3(max(pfr))},
-                       "m512_7b": p7["m512"], "m2048_7b": p7["m2048"], "unfused_7b_TFLOP/s": p7["unfused"],
-                       "peak": bf16_tf, "peak_kind": "bf16 burst (fp16 dense rate is the same)"}
+    line["prefill"] = {"fields": "TFLOP/s,frac,min,max", "m2048_70b": [r3(tot_f / tot_s / 1e12, 1),
+                                                                        r3(tot_f / tot_s / 1e12 / bf16_tf),
+                                                                        r3(min(pfr)), r3(max(pfr))],
+                       "m512_7b": p7["m512"], "m2048_7b": p7["m2048"], "unfused_7b": p7["unfused"],
+                       "peak": bf16_tf}
     # 7B decode workloads (secondary)
     line["decode_7b"], detail["decode_7b"] = run_7b_decode(q4, torch, dev, stream, hbm_gbs, "decode_7b",
                                                            synthetic.DECODE_7B_SHAPES, synthetic.DECODE_7B_M, False)
@@ -627,8 +630,7 @@ def run_prefill_7b(q4, torch, dev, stream, bf16_tf):
             del temp_dq
     for M in (512, 2048):
         v = f_tot[M][0] / f_tot[M][1] / 1e12
-        out[f"m{M}"] = {"TFLOP/s": r3(v, 1), "frac": r3(v / bf16_tf), "min_frac": r3(min(fr[M])),
-                        "max_frac": r3(max(fr[M]))}
+        out[f"m{M}"] = [r3(v, 1), r3(v / bf16_tf), r3(min(fr[M])), r3(max(fr[M]))]
     out["unfused"] = r3(u_tot[0] / u_tot[1] / 1e12, 1)
     return out, detail
 

@@ -314,9 +314,11 @@ bool pdl_enabled();
 // fused prefill (q4_prefill.cu): tile shape, K split and split workspace
 struct PrefillPlan {
     int bm, bn;        // tile
-    int splits;        // K slices per tile (1: none)
-    size_t ws_floats;  // fp32 partial tiles when splits > 1
-    int n_tickets;     // one per tile when splits > 1
+    int sk;            // 1: stream-K over the tiles x k-blocks space (cooperative launch)
+    int grid;          // stream-K: CTAs
+    int pmax;          // stream-K: most pieces of one tile
+    size_t ws_floats;  // fp32 partial tiles when tiles are cut into pieces
+    int n_tickets;     // one per tile when tiles are cut into pieces
 };
 PrefillPlan plan_prefill(int M, int K, int N);
 cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets, const uint16_t *x,

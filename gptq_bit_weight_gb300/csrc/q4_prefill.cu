@@ -6,9 +6,11 @@
 // to the fp32 sum before the single rounding to fp16 ("Inference Backends",
 // "Numeric epilogues and input gradients").
 //
-// Persistent kernel, one CTA per SM, 128 x BN output tiles taken round-robin
-// (m fastest, so the CTAs working at the same time share weight tiles in L2);
-// BN = 256, or 128 when 256-wide tiles would leave SMs idle (small M).  The
+// Persistent kernel, one CTA per SM.  Work: BM x BN output tiles taken round
+// robin (m fastest, so the CTAs working at the same time share weight tiles
+// in L2) when there are enough of them; otherwise stream-K, every CTA one
+// contiguous range of the tiles x k-blocks space, the tiles cut at range
+// ends summed after the main loop (cooperative launch, bounded waits).  The
 // roles below are for BN = 256 (BN = 128: 8 dequant warps, 256 TMEM columns).
 //
 //   warp 0       one thread: TMA loads into a 6-stage ring of {x tile 128x64
@@ -40,6 +42,13 @@
 
 #include "q4_internal.cuh"
 #include "q4_tc.cuh"
+
+// 1: stream-K for tile-starved shapes that an even k split cannot serve; 0:
+// round robin over 128-row tiles there (kept to measure the two against
+// each other)
+#ifndef Q4_PREFILL_SK
+#define Q4_PREFILL_SK 1
+#endif
 
 namespace q4 {
 
@@ -100,10 +109,48 @@ struct PfArgs {
     int zsplit;              // groups [0, zsplit) take zero offset 0
     const float *rowscale;   // epilogue: y = acc * rowscale[m] + bias (NULL: 1)
     int out_bf16;            // output rounded to bf16 instead of fp16
-    int splits;              // K slices per tile (> 1: one unit per CTA, cooperative launch)
-    float *ws;               // fp32 partial tiles [tile][slice][BM][BN] when splits > 1
+    int sk;                  // 1: stream-K (every CTA one contiguous range of the (tile, k
+                             // block) space, cooperative launch); 0: whole tiles round robin
+    int pmax;                // stream-K: most pieces (CTAs) any tile is cut into
+    float *ws;               // stream-K: fp32 partial tiles [tile][piece][BM][BN]
     int *tickets;            // one per tile, zero between calls
 };
+
+// One unit of a CTA's work: tile t, k blocks [kb0, kb1), piece p of the np
+// pieces the tile is cut into (np = 1: the whole tile).
+struct PfUnit {
+    int t, kb0, kb1, p, np;
+};
+
+// The i-th unit of CTA c (false past the last).  Round robin: tile c + i G.
+// Stream-K: the CTA's range [c W / G, (c + 1) W / G) of the W = tiles x KB
+// (tile, k block) pairs, tile by tile; piece p of tile t is the CTA's index
+// minus that of the first CTA whose range touches t.
+__device__ __forceinline__ bool pf_unit(const PfArgs &a, int KB, int i, PfUnit &u) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int ntiles = a.tiles_m * a.tiles_n;
+    if (!a.sk) {
+        u.t = c + i * G;
+        u.kb0 = 0;
+        u.kb1 = KB;
+        u.p = 0;
+        u.np = 1;
+        return u.t < ntiles;
+    }
+    const long long W = static_cast<long long>(ntiles) * KB;
+    const long long w0 = c * W / G, w1 = (c + 1) * W / G;
+    const int t = static_cast<int>(w0 / KB) + i;
+    const long long tb = static_cast<long long>(t) * KB;
+    if (tb >= w1 || w0 >= w1) return false;
+    u.t = t;
+    u.kb0 = static_cast<int>(w0 > tb ? w0 - tb : 0);
+    u.kb1 = static_cast<int>(w1 < tb + KB ? w1 - tb : KB);
+    auto owner = [&](long long w) { return static_cast<int>(((w + 1) * G - 1) / W); };
+    const int f = owner(tb);
+    u.p = c - f;
+    u.np = owner(tb + KB - 1) - f + 1;
+    return true;
+}
 
 __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
     if (status) atomicOr(status, bit);
@@ -152,13 +199,6 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = a.K / BK;
     const int NT16 = a.N >> 4;
-    const int ntiles = a.tiles_m * a.tiles_n;
-    const int nunits = ntiles * a.splits;                 // (tile, K slice) work units
-    auto kb_range = [&](int u, int &kb0, int &kb1) {
-        const int ks = u % a.splits;
-        kb0 = (KB * ks) / a.splits;
-        kb1 = (KB * (ks + 1)) / a.splits;
-    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSX; ++s) {
@@ -192,10 +232,10 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             RingPos r;
             int issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-                const int t = u / a.splits;
-                int kbeg, kend;
-                kb_range(u, kbeg, kend);
+            PfUnit un;
+            for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui) {
+                const int t = un.t;
+                const int kbeg = un.kb0, kend = un.kb1;
                 const int nt0 = (t / a.tiles_m) * (BN / 16);
                 const int tiles16 = min(BN / 16, NT16 - nt0);
                 const uint32_t sbytes = tiles16 * 32u, zbytes = tiles16 * 8u;
@@ -232,10 +272,10 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             RingPos r;
             int issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-                const int t = u / a.splits;
-                int kbeg, kend;
-                kb_range(u, kbeg, kend);
+            PfUnit un;
+            for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui) {
+                const int t = un.t;
+                const int kbeg = un.kb0, kend = un.kb1;
                 const int m0 = (t % a.tiles_m) * BM;
                 for (int kb = kbeg; kb < kend; ++kb) {
                     if (aborted(abort_flag)) { ok = false; break; }
@@ -256,9 +296,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             RingPos rx, rb;
             int lt = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x, ++lt) {
-                int kbeg, kend;
-                kb_range(u, kbeg, kend);
+            PfUnit un;
+            for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui, ++lt) {
+                const int kbeg = un.kb0, kend = un.kb1;
                 const int acc = lt % kAccBufs;
                 const uint32_t aph = (lt / kAccBufs) & 1;
                 if (aborted(abort_flag) || !mbar_wait(accE(acc), aph ^ 1)) {
@@ -321,9 +361,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         };
         RingPos rp, rb;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-            int kbeg, kend;
-            kb_range(u, kbeg, kend);
+        PfUnit un;
+        for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui) {
+            const int kbeg = un.kb0, kend = un.kb1;
             int left = 0;                             // 32-row blocks left in the current group
             int gcur = 0;                             // global group of the constants in slot 0
             for (int kb = kbeg; kb < kend; ++kb) {
@@ -383,8 +423,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         // ------------------------------------------------------ epilogue
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. +31
         int lt = 0;
-        for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lt) {
-            const int t = u / a.splits;
+        PfUnit un;
+        for (int ui = 0; pf_unit(a, KB, ui, un); ++ui, ++lt) {
+            const int t = un.t;
             const int acc = lt % kAccBufs;
             const uint32_t aph = (lt / kAccBufs) & 1;
             bool ok = !aborted(abort_flag) && mbar_wait(accF(acc), aph);
@@ -403,12 +444,13 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 uint32_t r[32];
                 tmem_ld_x32(tmem + static_cast<uint32_t>(acc * kHalves * BN + hc) + (static_cast<uint32_t>(32 * quad) << 16),
                             r);
-                if (a.splits > 1) {
-                    // the fp32 partial of this K slice, whole tile, lane-major so that
-                    // each warp store is 512 contiguous bytes:
-                    // float4 index (((u * (kHalves*BN/32) + hc/32) * 4 + quad) * 8 + v) * 32 + lane
+                if (un.np > 1) {
+                    // the fp32 partial of this piece, whole tile, lane-major so that
+                    // each warp store is 512 contiguous bytes: slot sl = t pmax + p,
+                    // float4 index (((sl * (kHalves*BN/32) + hc/32) * 4 + quad) * 8 + v) * 32 + lane
+                    const size_t sl = static_cast<size_t>(t) * a.pmax + un.p;
                     float4 *dst = reinterpret_cast<float4 *>(a.ws) +
-                                  ((static_cast<size_t>(u) * (kHalves * BN / 32) + hc / 32) * 4 + quad) * 8 * 32 + lane;
+                                  ((sl * (kHalves * BN / 32) + hc / 32) * 4 + quad) * 8 * 32 + lane;
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
@@ -464,69 +506,79 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
 
-    if (a.splits > 1 && blockIdx.x < nunits) {
-        // K slices of one tile: every unit has written its partial tile; once
-        // all have (a bounded wait: the cooperative launch keeps every unit
-        // resident), each unit finishes rows [ks*BM/S, (ks+1)*BM/S) of the
-        // tile, summing the partials in slice order, adding bias, rounding once.
-        const int u = blockIdx.x, t = u / a.splits, ks = u % a.splits, S = a.splits;
+    if (a.sk) {
+        // Stream-K fixup, after the main loop so that no CTA waits before it
+        // has written all of its pieces (only a range's first and last unit
+        // can be a piece of a shared tile).  Every piece is in the workspace;
+        // each CTA first announces its pieces, then, per piece, waits (bounded:
+        // the cooperative launch keeps every CTA resident) for the tile's
+        // other pieces and finishes rows [p BM / np, (p + 1) BM / np) of the
+        // tile, summing the pieces in order, adding bias, rounding once.
+        __threadfence();
+        __syncthreads();
+        PfUnit un;
+        if (threadIdx.x == 0)
+            for (int ui = 0; pf_unit(a, KB, ui, un); ++ui)
+                if (un.np > 1) atomicAdd(a.tickets + un.t, 1);
         __shared__ int s_ready;
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(a.tickets + t, 1);
-            bool ready = true;
-            const uint64_t t0 = globaltimer();
-            while (atomicAdd(a.tickets + t, 0) < S) {
-                if (aborted(abort_flag) || globaltimer() - t0 > 2000000000ull) {
-                    ready = false;
-                    break;
+        for (int ui = 0; pf_unit(a, KB, ui, un); ++ui) {
+            if (un.np == 1) continue;
+            const int t = un.t, S = un.np, ks = un.p;
+            if (threadIdx.x == 0) {
+                bool ready = true;
+                const uint64_t t0 = globaltimer();
+                while (atomicAdd(a.tickets + t, 0) < S) {
+                    if (aborted(abort_flag) || globaltimer() - t0 > 2000000000ull) {
+                        ready = false;
+                        break;
+                    }
+                    __nanosleep(256);
                 }
-                __nanosleep(256);
+                __threadfence();
+                s_ready = ready;
+                if (!ready) fail(a.status, 0x100, abort_flag);
             }
-            __threadfence();
-            s_ready = ready;
-            if (!ready) fail(a.status, 0x100, abort_flag);
-        }
-        __syncthreads();
-        if (s_ready) {
-            const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
-            const int r0 = (BM * ks) / S, r1 = (BM * (ks + 1)) / S, rows = r1 - r0;
-            const float4 *ws4 = reinterpret_cast<const float4 *>(a.ws);
-            // consecutive threads take consecutive rows of one 8-column group: their
-            // loads of the lane-major partials are contiguous
-            for (int i = threadIdx.x; i < rows * (BN / 8); i += blockDim.x) {
-                const int rl = r0 + i % rows, c = 8 * (i / rows);
-                const int row = m0 + rl, n = n0 + c;
-                if (row >= a.M || n >= a.N) continue;
-                const int hm = rl / 128, q = (rl % 128) / 32, ln = rl % 32;
-                const int hc = hm * BN + c;
-                float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (int j = 0; j < S; ++j) {
-                    const float4 *src =
-                        ws4 + ((static_cast<size_t>(t * S + j) * (kHalves * BN / 32) + hc / 32) * 4 + q) * 8 * 32 +
-                        ((hc % 32) / 4) * 32 + ln;
-                    const float4 p0 = __ldcg(src), p1 = __ldcg(src + 32);
-                    v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-                    v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
-                }
-                if (a.out_bf16 == kOutF32) {
-                    float4 *dst =
-                        reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + static_cast<size_t>(row) * a.N + n);
-                    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-                    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-                    continue;
-                }
-                uint32_t pk[4];
-                const float rs = a.rowscale ? a.rowscale[row] : 1.f;
+            __syncthreads();
+            if (s_ready) {
+                const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
+                const int r0 = (BM * ks) / S, r1 = (BM * (ks + 1)) / S, rows = r1 - r0;
+                const float4 *ws4 = reinterpret_cast<const float4 *>(a.ws);
+                // consecutive threads take consecutive rows of one 8-column group: their
+                // loads of the lane-major partials are contiguous
+                for (int i = threadIdx.x; i < rows * (BN / 8); i += blockDim.x) {
+                    const int rl = r0 + i % rows, c = 8 * (i / rows);
+                    const int row = m0 + rl, n = n0 + c;
+                    if (row >= a.M || n >= a.N) continue;
+                    const int hm = rl / 128, q = (rl % 128) / 32, ln = rl % 32;
+                    const int hc = hm * BN + c;
+                    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    for (int j = 0; j < S; ++j) {
+                        const size_t sl = static_cast<size_t>(t) * a.pmax + j;
+                        const float4 *src = ws4 + ((sl * (kHalves * BN / 32) + hc / 32) * 4 + q) * 8 * 32 +
+                                            ((hc % 32) / 4) * 32 + ln;
+                        const float4 p0 = __ldcg(src), p1 = __ldcg(src + 32);
+                        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+                        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+                    }
+                    if (a.out_bf16 == kOutF32) {
+                        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) +
+                                                                 static_cast<size_t>(row) * a.N + n);
+                        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                        continue;
+                    }
+                    uint32_t pk[4];
+                    const float rs = a.rowscale ? a.rowscale[row] : 1.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pk[e] = out_pair(v[2 * e], v[2 * e + 1], rs, a.bias, n + 2 * e, a.out_bf16);
-                *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    for (int e = 0; e < 4; ++e) pk[e] = out_pair(v[2 * e], v[2 * e + 1], rs, a.bias, n + 2 * e, a.out_bf16);
+                    *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
             }
+            __syncthreads();
+            // second arrival: the last of the 2 S resets the ticket for the next call
+            if (threadIdx.x == 0 && atomicAdd(a.tickets + t, 1) == 2 * S - 1) atomicExch(a.tickets + t, 0);
         }
-        __syncthreads();
-        // second arrival: the last of the 2S resets the ticket for the next call
-        if (threadIdx.x == 0 && atomicAdd(a.tickets + t, 1) == 2 * S - 1) atomicExch(a.tickets + t, 0);
     }
 }
 
@@ -563,9 +615,9 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
         cudaSuccess)
         return e;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
-                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, h.rowscale, h.out_bf16, p.splits, ws, tickets};
-    const int nunits = args.tiles_m * args.tiles_n * p.splits;
-    const int grid = nunits < sm_count() ? nunits : sm_count();
+                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, h.rowscale, h.out_bf16, p.sk, p.pmax, ws, tickets};
+    const int ntiles = args.tiles_m * args.tiles_n;
+    const int grid = p.sk ? p.grid : (ntiles < sm_count() ? ntiles : sm_count());
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(P::kThreads);
@@ -575,17 +627,23 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
     at.id = cudaLaunchAttributeCooperative;         // split units wait on each other: all resident
     at.val.cooperative = 1;
     cfg.attrs = &at;
-    cfg.numAttrs = p.splits > 1 ? 1 : 0;
+    cfg.numAttrs = p.sk ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_kernel<BM, BN>, tmA, tmW, args);
 }
 
 }  // namespace
 
-// Tile shape and K split by tile count (c = SMs): 256 x 256 when those tiles
-// give every SM at least three quarters of a tile's work; else 256 x 256 with
-// the K range split S ways (S = floor(c / tiles) <= 8, every unit resident at
-// once, at least 8 stages each) when that makes at least two slices; else
-// 128 x 256; else 128 x 128 (small M), at the same cost per flop as 128 x 256.
+// Tile shape and work split by tile count (c = SMs), measured on GB300:
+//   - 256 x 256 tiles round robin when there are enough of them to give
+//     every SM at least three quarters of a tile's work;
+//   - else, when that gives at least two pieces per tile, every 256 x 256
+//     tile cut into S = floor(c / tiles) <= 8 equal k ranges, one CTA each
+//     (the stream-K walk below with S CTAs per tile);
+//   - else stream-K over 256 x 256 tiles: one CTA per SM (fewer when that
+//     would leave a CTA under 8 k blocks), each a contiguous range of the
+//     tiles x k-blocks space, tiles cut into pieces at the range ends and
+//     summed after the main loop.  256-row tiles let one dequantized B tile
+//     feed two M = 128 MMAs.
 PrefillPlan plan_prefill(int M, int K, int N) {
     PrefillPlan p{};
     const long long c = sm_count();
@@ -593,19 +651,30 @@ PrefillPlan plan_prefill(int M, int K, int N) {
     const long long t256x256 = static_cast<long long>((M + 255) / 256) * n256;
     const long long t128x256 = static_cast<long long>((M + 127) / 128) * n256;
     const int KB = K / BK;
-    p.splits = 1;
-    if (4 * t256x256 >= 3 * c) {
-        p.bm = 256, p.bn = 256;
-    } else if (c / t256x256 >= 2 && KB / 2 >= 8) {
-        p.bm = 256, p.bn = 256;
-        p.splits = static_cast<int>(std::min<long long>(8, c / t256x256));
-        while (p.splits > 2 && KB / p.splits < 8) --p.splits;
-        p.ws_floats = static_cast<size_t>(t256x256) * p.splits * 256 * 256;
-        p.n_tickets = static_cast<int>(t256x256);
-    } else if (4 * t128x256 >= 3 * c) {
-        p.bm = 128, p.bn = 256;
+    p.bm = 256, p.bn = 256;
+    if (4 * t256x256 >= 3 * c) return p;
+    const long long W = t256x256 * KB;
+    p.sk = 1;
+    if (c / t256x256 >= 2 && KB / 2 >= 8) {
+        int S = static_cast<int>(std::min<long long>(8, c / t256x256));
+        while (S > 2 && KB / S < 8) --S;
+        p.grid = static_cast<int>(t256x256) * S;
+    } else if (!Q4_PREFILL_SK) {
+        // round robin over 128-row tiles (the alternative measured against stream-K)
+        p.sk = 0;
+        p.bm = 128;
+        p.bn = 4 * t128x256 >= 3 * c ? 256 : 128;
+        return p;
     } else {
-        p.bm = 128, p.bn = 128;
+        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(c, W / 8)));
+    }
+    auto owner = [&](long long w) { return static_cast<int>(((w + 1) * p.grid - 1) / W); };
+    p.pmax = 1;
+    for (long long t = 0; t < t256x256; ++t)
+        p.pmax = std::max(p.pmax, owner(t * KB + KB - 1) - owner(t * KB) + 1);
+    if (p.pmax > 1) {
+        p.ws_floats = static_cast<size_t>(t256x256) * p.pmax * 256 * 256;
+        p.n_tickets = static_cast<int>(t256x256);
     }
     return p;
 }
