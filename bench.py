@@ -277,10 +277,12 @@ def headline_config():
     return {"workload": "sweep_70b", "M": 1, "layer_configs": "3 shapes x g{32,64,128,-1} x {trivial,act-order}"}
 
 
-# DRAM bytes per step of the decode kernels (the roofline's traffic), from an
-# ncu capture of the same kernels; None until one has been taken of the
-# kernels as they stand.
-DECODE_TRAFFIC = None
+# The roofline's traffic: DRAM bytes (read + write) of one launch of the
+# dominant decode kernel, from an ncu capture of
+#   bench.py --single 8192,28672,1,DECODE,128   (the fourth call, after an L2 flush)
+# whose algorithmic bytes are 122,028,032; ncu read 122.15 MB and wrote 2.95 MB.
+DECODE_TRAFFIC = {"bytes": 125_100_000, "launch": "decode_kernel<1,0,1,0>, 8192x28672 g128 M=1",
+                  "algorithmic_bytes": 122_028_032}
 
 
 # ------------------------------------------------------------------ native
@@ -471,7 +473,8 @@ def run_native(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 x int4 -> f32 accumulate", "data": "synthetic",
             "config": cfg,
             "roofline": {"bound": "hbm", "achieved": r3(achieved_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": r3(achieved_gbs / hbm_gbs), "traffic": DECODE_TRAFFIC, "peak_source": peak_src,
+                         "frac": r3(achieved_gbs / hbm_gbs), "traffic": DECODE_TRAFFIC["bytes"],
+                         "traffic_launch": DECODE_TRAFFIC["launch"], "peak_source": peak_src,
                          "kernel": "decode, 12 trivial-g_idx configs"},
             "m1_frac": {"min": r3(min(fr)), "mean": r3(float(np.mean(fr))), "max": r3(max(fr)),
                         "by_g": {str(g): r3(float(np.mean([f for k, f in fr1.items() if k[2] == g])))

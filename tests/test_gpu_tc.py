@@ -119,9 +119,10 @@ def test_prefill_7b_workload_sampled(q4, K, N, act):
 @pytest.mark.parametrize("K,N,gs,act,M", [(1152, 576, 96, False, 4900), (1024, 448, 32, True, 7300),
                                           (1152, 576, 96, False, 9700), (1024, 448, 32, True, 14600)])
 def test_prefill_wide_tiles_sampled(q4, K, N, gs, act, M):
-    """Enough rows that the fused prefill takes 128 x 256 tiles (the first two
-    cases) or 256 x 256 tiles (the last two) on a narrow layer, with a ragged
-    last column tile and a ragged last row tile; oracle on a row sample."""
+    """Many rows on a narrow layer, with a ragged last column tile and a
+    ragged last row tile: 256 x 256 tiles cut into two equal k ranges (the
+    first two cases) or taken whole, round robin (the last two); oracle on a
+    row sample."""
     layer = synthetic.make_layer(K, N, gs, act_order=act, bias=True, key=(34, K, N, gs & 0xFFFF, act))
     dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs)
     mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
