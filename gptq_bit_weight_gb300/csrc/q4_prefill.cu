@@ -636,7 +636,7 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
 //     would leave a CTA under 8 k blocks), each a contiguous range of the
 //     tiles x k-blocks space, tiles cut into pieces at the range ends and
 //     summed after the main loop.  256-row tiles let one dequantized B tile
-//     feed two M = 128 MMAs.
+//     feed two M = 128 MMAs; up to 128 rows take 128 x 256 tiles instead.
 PrefillPlan plan_prefill(int M, int K, int N) {
     PrefillPlan p{};
     const long long c = sm_count();
@@ -645,12 +645,16 @@ PrefillPlan plan_prefill(int M, int K, int N) {
     const int KB = K / BK;
     p.bm = 256, p.bn = 256;
     if (4 * t256x256 >= 3 * c) return p;
-    const long long W = t256x256 * KB;
+    // up to 128 rows: one 128-row tile holds them all (256-row MMAs would
+    // spend half or more of the tensor pipe on rows that do not exist)
+    if (M <= 128) p.bm = 128;
+    const long long tiles = static_cast<long long>((M + p.bm - 1) / p.bm) * n256;
+    const long long W = tiles * KB;
     p.sk = 1;
-    if (c / t256x256 >= 2 && KB / 2 >= 8) {
-        int S = static_cast<int>(std::min<long long>(8, c / t256x256));
+    if (c / tiles >= 2 && KB / 2 >= 8) {
+        int S = static_cast<int>(std::min<long long>(8, c / tiles));
         while (S > 2 && KB / S < 8) --S;
-        p.grid = static_cast<int>(t256x256) * S;
+        p.grid = static_cast<int>(tiles) * S;
     } else {
         // (measured against round robin over 128-row tiles, the choice before
         // stream-K: 1.4x-1.9x faster on 8192 x 28672 at M <= 256, 8192 x 10240
@@ -659,18 +663,19 @@ PrefillPlan plan_prefill(int M, int K, int N) {
     }
     auto owner = [&](long long w) { return static_cast<int>(((w + 1) * p.grid - 1) / W); };
     p.pmax = 1;
-    for (long long t = 0; t < t256x256; ++t)
+    for (long long t = 0; t < tiles; ++t)
         p.pmax = std::max(p.pmax, owner(t * KB + KB - 1) - owner(t * KB) + 1);
     if (p.pmax > 1) {
-        p.ws_floats = static_cast<size_t>(t256x256) * p.pmax * 256 * 256;
-        p.n_tickets = static_cast<int>(t256x256);
+        p.ws_floats = static_cast<size_t>(tiles) * p.pmax * p.bm * p.bn;
+        p.n_tickets = static_cast<int>(tiles);
     }
     return p;
 }
 
 cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets, const uint16_t *x,
                            int M, uint16_t *out, cudaStream_t s) {
-    if (p.bm != 256 || p.bn != 256) return cudaErrorInvalidValue;
+    if (p.bn != 256) return cudaErrorInvalidValue;
+    if (p.bm == 128) return launch_prefill_tile<128, 256>(h, p, ws, tickets, x, M, out, s);
     return launch_prefill_tile<256, 256>(h, p, ws, tickets, x, M, out, s);
 }
 
