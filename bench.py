@@ -18,7 +18,8 @@ during the timed region, the binding-roofline fraction of the whole
 sweep_70b workload at every M (M = 2048 is the prefill), the prefill
 tensor-core numbers (sweep_70b M = 2048 and prefill_7b M = 512), and the
 decode_7b / actorder_7b workloads.  Per-case detail goes to stderr as one
-JSON line.
+JSON line, with the rows past the hot path (fused Q/K/V projections, GPTQ_V2,
+8-bit codes, bf16 and fp32 activations, the GPU packer).
 
 --impl reference times the CPU oracle (the plain dequantize-then-matmul
 route) on the same workload: each step one layer configuration in turn, on a
@@ -556,9 +557,164 @@ def run_extra_legs(q4, torch, dev, stream, sw, hbm_gbs, bf16_tf, issue_m, args):
     line["actorder_7b"], detail["actorder_7b"] = run_7b_decode(q4, torch, dev, stream, hbm_gbs, "actorder_7b",
                                                                synthetic.ACTORDER_7B_SHAPES, synthetic.ACTORDER_7B_M,
                                                                True)
+    detail["next_rows"] = run_next_rows(q4, torch, dev, stream, hbm_gbs)
     if args.sweep70b:
         detail["sweep_70b_cases"] = run_sweep_70b_cases(q4, torch, dev, stream, sw, hbm_gbs, bf16_tf)
     return line, detail
+
+
+def _graph_time(torch, stream, issue, reps=20):
+    """Per-replay seconds of a CUDA graph of issue(stream_ptr)."""
+    issue(stream.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        issue(torch.cuda.current_stream().cuda_stream)
+    for _ in range(3):
+        g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e-3 / reps
+
+
+def run_next_rows(q4, torch, dev, stream, hbm_gbs):
+    """Measurements of the rows added past the hot path, on Llama-7B shapes:
+    projection fusion (Q, K, V of one input as one handle vs three), the
+    GPTQ_V2 zero convention (same kernels; must cost the same), and the GPU
+    packer (float weights -> checkpoint words)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    res = {}
+    K, Nq = 4096, 4096
+    R = 6                                                   # 6 x 3 x 8.7 MB = 157 MB of weights > 129 MB L2
+    layers = [synthetic.workload_layer("decode_7b", K, Nq, 128, False) for _ in range(3)]
+    sep = [[q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for L in layers] for _ in range(R)]
+    fused = [q4.Q4Matrix.fused([(t(L.qweight), t(L.qzeros), t(L.scales)) for L in layers], None, None, 128)
+             for _ in range(R)]
+    wbytes = 3 * layers[0].weight_bytes
+    for M in (1, 8):
+        x = t(synthetic.workload_x("decode_7b", K, Nq, 128, False, M))
+        o1 = torch.empty((M, Nq), dtype=torch.float16, device=dev)
+        o3 = torch.empty((M, 3 * Nq), dtype=torch.float16, device=dev)
+
+        def issue_sep(sp):
+            for r in range(R):
+                for m in sep[r]:
+                    q4.gptq_q4_matmul(m.handle, x.data_ptr(), M, o1.data_ptr(), sp)
+
+        def issue_fused(sp):
+            for r in range(R):
+                q4.gptq_q4_matmul(fused[r].handle, x.data_ptr(), M, o3.data_ptr(), sp)
+
+        ts = _graph_time(torch, stream, issue_sep) / R
+        tf = _graph_time(torch, stream, issue_fused) / R
+        res[f"qkv_7b M={M}"] = {"separate_us": round(ts * 1e6, 2), "fused_us": round(tf * 1e6, 2),
+                                "separate_TB/s": round(wbytes / ts / 1e12, 3), "fused_TB/s": round(wbytes / tf / 1e12, 3)}
+    del sep, fused
+    # GPTQ_V2: the same layer read as a V2 checkpoint
+    L = synthetic.workload_layer("decode_7b", 4096, 11008, 128, False)
+    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
+    x = t(synthetic.workload_x("decode_7b", 4096, 11008, 128, False, 1))
+    o = torch.empty((1, 11008), dtype=torch.float16, device=dev)
+
+    def issue(sp):
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, x.data_ptr(), 1, o.data_ptr(), sp)
+
+    t1 = _graph_time(torch, stream, issue) / len(mats)
+    for m in mats:
+        m.set_format(q4.GPTQ_Q4_FORMAT_GPTQ_V2)
+    t2 = _graph_time(torch, stream, issue) / len(mats)
+    res["gptq_v2 4096x11008 M=1"] = {"gptq_us": round(t1 * 1e6, 2), "gptq_v2_us": round(t2 * 1e6, 2),
+                                     "gptq_v2_TB/s": round(L.weight_bytes / t2 / 1e12, 3)}
+    del mats
+    # 8-bit checkpoint of the same shape (two 4-bit halves along K): decode
+    # at M = 1 (weight bytes / time) and the fused prefill at M = 512
+    L8 = synthetic.make_layer8(4096, 11008, 128, key=(33, 4096, 11008))
+    mats = [q4.Q4Matrix(t(L8.qweight), t(L8.qzeros), t(L8.scales), None, None, 128, bits=8) for _ in range(6)]
+    t8 = _graph_time(torch, stream, issue) / len(mats)
+    bytes8 = 4096 * 11008 + (4096 // 128) * 11008 * 3   # codes + fp16 scales + 8-bit zeros
+    x512 = t(synthetic.activations(512, 4096, key=(33, 512)))
+    o512 = torch.empty((512, 11008), dtype=torch.float16, device=dev)
+    mats[0].reserve(512)
+
+    def issue512(sp):
+        q4.gptq_q4_matmul(mats[0].handle, x512.data_ptr(), 512, o512.data_ptr(), sp)
+
+    t512 = _graph_time(torch, stream, issue512)
+    res["8bit 4096x11008"] = {"M=1_us": round(t8 * 1e6, 2), "M=1_TB/s": round(bytes8 / t8 / 1e12, 3),
+                              "M=512_us": round(t512 * 1e6, 2),
+                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / t512 / 1e12, 1)}
+    del mats
+    # bf16 activations and outputs on the 4-bit layer (one preparation launch
+    # per call scales and rounds x to fp16): decode at M = 1, prefill at M = 512
+    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
+    for m in mats:
+        m.set_act_dtype(torch.bfloat16)
+        m.reserve(512)
+    xb1 = t(synthetic.activations_bf16(1, 4096, key=(35, 1)).view(np.int16)).view(torch.bfloat16)
+    xb512 = t(synthetic.activations_bf16(512, 4096, key=(35, 512)).view(np.int16)).view(torch.bfloat16)
+    ob1 = torch.empty((1, 11008), dtype=torch.bfloat16, device=dev)
+    ob512 = torch.empty((512, 11008), dtype=torch.bfloat16, device=dev)
+
+    def issue_b1(sp):
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, xb1.data_ptr(), 1, ob1.data_ptr(), sp)
+
+    def issue_b512(sp):
+        q4.gptq_q4_matmul(mats[0].handle, xb512.data_ptr(), 512, ob512.data_ptr(), sp)
+
+    tb1 = _graph_time(torch, stream, issue_b1) / len(mats)
+    tb512 = _graph_time(torch, stream, issue_b512)
+    res["bf16 4096x11008"] = {"M=1_us": round(tb1 * 1e6, 2), "M=1_TB/s": round(L.weight_bytes / tb1 / 1e12, 3),
+                              "M=512_us": round(tb512 * 1e6, 2),
+                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / tb512 / 1e12, 1)}
+    del mats
+    # fp32 activations and outputs on the 4-bit layer (hi/lo fp16 rows, raw
+    # fp32 sums, one combine launch): decode at M = 1, prefill at M = 512
+    mats = [q4.Q4Matrix(t(L.qweight), t(L.qzeros), t(L.scales), None, None, 128) for _ in range(6)]
+    for m in mats:
+        m.set_act_dtype(torch.float32)
+        m.reserve(512)
+    xf1 = t(synthetic.activations_f32(1, 4096, key=(39, 1)).view(np.float32))
+    xf512 = t(synthetic.activations_f32(512, 4096, key=(39, 512)).view(np.float32))
+    of1 = torch.empty((1, 11008), dtype=torch.float32, device=dev)
+    of512 = torch.empty((512, 11008), dtype=torch.float32, device=dev)
+
+    def issue_f1(sp):
+        for m in mats:
+            q4.gptq_q4_matmul(m.handle, xf1.data_ptr(), 1, of1.data_ptr(), sp)
+
+    def issue_f512(sp):
+        q4.gptq_q4_matmul(mats[0].handle, xf512.data_ptr(), 512, of512.data_ptr(), sp)
+
+    tf1 = _graph_time(torch, stream, issue_f1) / len(mats)
+    tf512 = _graph_time(torch, stream, issue_f512)
+    res["fp32 4096x11008"] = {"M=1_us": round(tf1 * 1e6, 2), "M=1_TB/s": round(L.weight_bytes / tf1 / 1e12, 3),
+                              "M=512_us": round(tf512 * 1e6, 2),
+                              "M=512_TFLOP/s": round(2 * 512 * 4096 * 11008 / tf512 / 1e12, 1)}
+    del mats
+    # GPU packer: float weights (fp16) + scales + zeros -> qweight/qzeros
+    K, N, gs = 4096, 11008, 128
+    g = np.random.default_rng(5)
+    w = torch.from_numpy(g.normal(0, 0.05, (K, N)).astype(np.float16)).to(dev)
+    sc = torch.from_numpy(g.uniform(0.002, 0.02, (K // gs, N)).astype(np.float16)).to(dev)
+    zs = torch.from_numpy(g.integers(0, 16, (K // gs, N)).astype(np.int32)).to(dev)
+    qw = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
+    qz = torch.empty((K // gs, N // 8), dtype=torch.int32, device=dev)
+
+    def issue_pack(sp):
+        q4.gptq_q4_pack(w.data_ptr(), sc.data_ptr(), zs.data_ptr(), None, K, N, gs, 0, qw.data_ptr(), qz.data_ptr(), sp)
+
+    tp = _graph_time(torch, stream, issue_pack, reps=10)
+    moved = K * N * 2 + K * N // 2 + (K // gs) * N * 6 + (K // gs) * N // 2
+    res["pack 4096x11008"] = {"us": round(tp * 1e6, 2), "TB/s": round(moved / tp / 1e12, 3),
+                              "frac_of_hbm_peak": round(moved / tp / 1e9 / hbm_gbs, 3),
+                              "bytes": "w fp16 read + qweight written + scales/zeros read + qzeros written"}
+    return res
 
 
 def run_7b_decode(q4, torch, dev, stream, hbm_gbs, workload, shapes, Ms, act):
