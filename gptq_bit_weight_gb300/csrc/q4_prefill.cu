@@ -43,6 +43,23 @@
 #include "q4_internal.cuh"
 #include "q4_tc.cuh"
 
+// Ring depths (stages): x tiles, packed words, fp16 B tiles, per tile height.
+#ifndef Q4_PF_SX128
+#define Q4_PF_SX128 5
+#endif
+#ifndef Q4_PF_SB128
+#define Q4_PF_SB128 3
+#endif
+#ifndef Q4_PF_SX256
+#define Q4_PF_SX256 3
+#endif
+#ifndef Q4_PF_SB256
+#define Q4_PF_SB256 2
+#endif
+#ifndef Q4_PF_SP
+#define Q4_PF_SP 4
+#endif
+
 namespace q4 {
 
 cudaError_t encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
@@ -67,9 +84,9 @@ struct PfCfg {
     static constexpr int BM = BM_, BN = BN_;
     static constexpr int kHalves = BM / 128;           // M = 128 MMAs per k step
     static constexpr int kAccBufs = BM == 128 ? 2 : 1; // accumulator sets (double-buffered when they fit)
-    static constexpr int kSX = BM == 128 ? 5 : 3;      // x-tile ring (released by the MMAs)
-    static constexpr int kSP = 4;                      // packed-word ring (released by the dequantizers)
-    static constexpr int kSB = BM == 128 ? 3 : 2;      // fp16 B ring
+    static constexpr int kSX = BM == 128 ? Q4_PF_SX128 : Q4_PF_SX256;   // x-tile ring (released by the MMAs)
+    static constexpr int kSP = Q4_PF_SP;               // packed-word ring (released by the dequantizers)
+    static constexpr int kSB = BM == 128 ? Q4_PF_SB128 : Q4_PF_SB256;   // fp16 B ring
     static constexpr int kXStage = BM * BK * 2;
     static constexpr int kSGroup = BN * 2, kZGroup = BN / 2;
     static constexpr int kSzOff = BN * 32;             // within a packed stage

@@ -149,7 +149,7 @@ def test_uneven_groups_match_oracle(q4, K, N, gs, empty):
     assert np.array_equal(q.cpu().numpy(), dq.q)
     assert np.array_equal(z.cpu().numpy(), dq.z)
     assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
-    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "PREFILL"):
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_STREAM", "PREFILL"):
         mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
         for M in (1, 5, 33, 300):
             x = synthetic.activations(M, K, key=(29, K, N, M))
@@ -175,7 +175,7 @@ def test_groupsize_not_multiple_of_32(q4, act):
     w = mat.dequant()
     torch.cuda.synchronize()
     assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
-    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "PREFILL"):
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_STREAM", "PREFILL"):
         mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
         for M in (1, 6, 40):
             x = synthetic.activations(M, K, key=(30, K, N, M))
@@ -214,7 +214,7 @@ def test_8bit_matches_oracle(q4, K, N, gs, act):
         assert np.array_equal(q.cpu().numpy(), dq.q)
         assert np.array_equal(z.cpu().numpy(), dq.z)
         assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
-        for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "PREFILL"):
+        for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "DECODE_STREAM", "PREFILL"):
             mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
             for M in (1, 3, 8, 16, 40):
                 x = synthetic.activations(M, K, key=(31, K, N, M))
@@ -291,7 +291,7 @@ def test_bf16_activations_match_oracle(q4, K, N, gs, act):
     dq = oracle_dq(layer)
     mat = make(q4, layer)
     mat.set_act_dtype(torch.bfloat16)
-    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "PREFILL"):
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "DECODE_STREAM", "PREFILL"):
         mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
         for M in (1, 3, 8, 16, 40):
             rs = [BF16_ROW_SCALES[m % 4] for m in range(M)]
@@ -420,7 +420,7 @@ def test_gptq_v2_format_matches_oracle(q4, K, N, gs, act):
     w = mat.dequant()
     torch.cuda.synchronize()
     assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
-    for path in ("DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "PREFILL"):
+    for path in ("DECODE", "DECODE_RING", "DECODE_MMA", "DECODE_TC", "DECODE_STREAM", "PREFILL"):
         mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
         for M in (1, 3, 8, 16, 40):
             x = synthetic.activations(M, K, key=(25, K, N, M))
@@ -455,15 +455,22 @@ def test_trivial_gidx_same_as_none(q4):
     assert torch.equal(ya, yb)
 
 
-def test_deterministic_repeat(q4):
-    K, N, gs = 4096, 1024, 128
+@pytest.mark.parametrize("path", ["AUTO", "DECODE_STREAM", "DECODE_MMA", "PREFILL"])
+def test_deterministic_repeat(q4, path):
+    """Split reductions sum in a fixed order (slices, segments or pieces),
+    never in arrival order: repeated calls give identical bits.  28672 rows
+    cut the stream-K decode's tiles into several segments and the fused
+    prefill's into several pieces."""
+    K, N, gs = 28672, 1024, 128
     layer = synthetic.make_layer(K, N, gs, act_order=True, bias=True, key=(24,))
     mat = make(q4, layer)
-    x = to_dev(synthetic.activations(4, K, key=(24, 4)))
-    y1 = mat(x).clone()
-    y2 = mat(x).clone()
-    torch.cuda.synchronize()
-    assert torch.equal(y1, y2)
+    mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
+    for M in (1, 4, 300):
+        x = to_dev(synthetic.activations(M, K, key=(24, M)))
+        y1 = mat(x).clone()
+        y2 = mat(x).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2), f"{path} M={M}"
 
 
 def test_zero_rows_is_noop(q4):
@@ -607,7 +614,7 @@ def test_fused_projections_match_oracle(q4, act):
     w = mat.dequant()
     torch.cuda.synchronize()
     assert np.array_equal(w.cpu().numpy().view(np.uint16), dq.w16)
-    for path in ("AUTO", "DECODE", "DECODE_RING", "PREFILL"):
+    for path in ("AUTO", "DECODE", "DECODE_RING", "DECODE_STREAM", "PREFILL"):
         mat.set_path(getattr(q4, "GPTQ_Q4_PATH_" + path))
         for M in (1, 8, 33):
             x = synthetic.activations(M, K, key=(26, K, M))
