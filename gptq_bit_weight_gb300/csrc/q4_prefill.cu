@@ -10,26 +10,31 @@
 // robin (m fastest, so the CTAs working at the same time share weight tiles
 // in L2) when there are enough of them; otherwise stream-K, every CTA one
 // contiguous range of the tiles x k-blocks space, the tiles cut at range
-// ends summed after the main loop (cooperative launch, bounded waits).  The
-// roles below are for BN = 256 (BN = 128: 8 dequant warps, 256 TMEM columns).
+// ends summed after the main loop (cooperative launch, bounded waits).
+// Roles, for BN = 256 (BM = 128 or 256):
 //
-//   warp 0       one thread: TMA loads into a 6-stage ring of {x tile 128x64
-//                fp16 (128-byte swizzle), packed-word tile 256x64 (8 KB), the
-//                stage's scale pairs and zero words}
-//   warp 1       allocates 512 TMEM columns (two 128x256 fp32 accumulators);
-//                one thread issues tcgen05.mma M=128 N=256 K=16 and commits
-//                stages back to the producer and the dequantizers
-//   warps 2-17   dequantize each stage's packed words into a 2-stage ring of
-//                fp16 B tiles (K-major, 128-byte swizzle: the UMMA operand
-//                layout), w16 = fp16(s * (q - z - 1)) rounded once; each
-//                thread one 16-byte vector (four words) per stage
-//   warps 18-21  epilogue: tcgen05.ld an accumulator, add bias, round to fp16,
-//                store; then hand the accumulator back, so the epilogue of
-//                one tile overlaps the main loop of the next.
+//   warp 0       one thread: TMA loads of the packed-word stages (8 KB of
+//                packed words per 64 rows) with their scale pairs and zero
+//                words, a 4-slot ring
+//   warp 1       allocates TMEM (two 128x256 fp32 accumulators at BM = 128,
+//                one 256x256 pair at BM = 256); one thread issues tcgen05.mma
+//                M=128 N=256 K=16 (two per k step at BM = 256, sharing the B
+//                tile) and commits each stage back to the x producer and the
+//                dequantizers
+//   warp 2       one thread: TMA loads of the x tiles (BM x 64 fp16, 128-byte
+//                swizzle), a 5-slot ring at BM = 128, 3 at BM = 256
+//   warp 3       waits for each stage's x and B tiles and hands the stage to
+//                warp 1 through a named barrier
+//   warps 4-19   dequantize each packed stage into the fp16 B ring (3 slots
+//                at BM = 128, 2 at BM = 256; K-major, 128-byte swizzle: the
+//                UMMA operand layout), w16 = fp16(s * (q - z - 1)) rounded
+//                once; each thread one 16-byte vector (four words) per stage,
+//                unpacked and scaled before its B slot is free
+//   warps 20-23  epilogue: tcgen05.ld an accumulator, add bias, round to fp16,
+//                store (or write a stream-K piece's fp32 partial); then hand
+//                the accumulator back, so the epilogue of one tile overlaps
+//                the main loop of the next.
 //
-// Only the 24 KB of x and packed words per 64-row stage travel through TMA
-// (the 32 KB fp16 tile is made on chip), so six stages keep ~150 KB in flight
-// per SM, enough to cover the L2 round trip at the tensor-core rate.
 // Every mbarrier wait is bounded (~2 s); a wait that runs out records an
 // error bit in the handle's status word, the CTA lets its copies land, frees
 // its TMEM and returns.
@@ -99,7 +104,7 @@ struct PfCfg {
     static constexpr int kNumBars = 2 * kSX + 2 * kSP + 2 * kSB + 4;
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr int kDqWarps = BN / 16;
-    static constexpr int kDq0 = 3;                     // first dequant warp
+    static constexpr int kDq0 = 4;                     // first dequant warp
     static constexpr int kThreads = 32 * (kDq0 + kDqWarps + kEpiWarps);
     static constexpr uint32_t kTmemCols = kAccBufs * kHalves * BN;
     static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -299,46 +304,62 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             if (aborted(abort_flag))
                 for (int j = issued > kSX ? issued - kSX : 0; j < issued; ++j) mbar_wait(fullX(j % kSX), (j / kSX) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(128, BN, false);
-            RingPos rx, rb;
-            int lt = 0;
-            bool ok = true;
-            PfUnit un;
-            for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui, ++lt) {
-                const int kbeg = un.kb0, kend = un.kb1;
-                const int acc = lt % kAccBufs;
-                const uint32_t aph = (lt / kAccBufs) & 1;
-                if (aborted(abort_flag) || !mbar_wait(accE(acc), aph ^ 1)) {
-                    fail(a.status, 0x20, abort_flag);
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------- MMA issuer (warp 1) and its poller (warp 3)
+        // One thread issues every tcgen05.mma, and the tensor core queues only
+        // about two of them, so whatever that thread does between stages
+        // leaves the tensor pipe idle.  An mbarrier poll right after an MMA
+        // measured ~200 cycles on sm_103a, a named-barrier hand-off ~45: warp
+        // 3 waits for each stage's x and B tiles and hands the stage over
+        // through named barrier 1 (a reduction that also carries either
+        // side's failure, so both leave the loop at the same point); warp 1
+        // issues its MMAs and commits.  The operand descriptors are formed
+        // once (slot 0 of each ring) and advanced by constant address offsets
+        // (the descriptor's low field is the shared address / 16; every
+        // address here is below 256 KB, so the field never carries).
+        const bool issuer = warp == 1;
+        constexpr uint32_t idesc = idesc_f16(128, BN, false);
+        const uint64_t dA0 = smem_desc_sw128(base, 16, 1024);
+        const uint64_t dB0 = smem_desc_sw128(base + kRingB, 16, 1024);
+        RingPos rx, rb;
+        int lt = 0;
+        bool ok = true;
+        PfUnit un;
+        for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui, ++lt) {
+            const int kbeg = un.kb0, kend = un.kb1;
+            const int acc = lt % kAccBufs;
+            const uint32_t aph = (lt / kAccBufs) & 1;
+            // the issuer needs the accumulator set drained by the epilogue
+            bool mine = true;
+            if (issuer && lane == 0) mine = !aborted(abort_flag) && mbar_wait(accE(acc), aph ^ 1);
+            const uint32_t d = tmem + static_cast<uint32_t>(acc * kHalves * BN);
+            for (int kb = kbeg; kb < kend; ++kb) {
+                if (!issuer && lane == 0) mine = mbar_wait(fullX(rx.s), rx.ph) && mbar_wait(fullB(rb.s), rb.ph);
+                __syncwarp();
+                if (!bar_and(1, 64, mine)) {
+                    if (lane == 0) fail(a.status, 0x20, abort_flag);
+                    ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * kHalves * BN);
-                for (int kb = kbeg; kb < kend; ++kb) {
-                    if (aborted(abort_flag) || !mbar_poll(fullX(rx.s), rx.ph) || !mbar_poll(fullB(rb.s), rb.ph)) {
-                        fail(a.status, 0x20, abort_flag);
-                        ok = false;
-                        break;
-                    }
+                if (issuer && lane == 0) {
                     tc_fence_after();
-                    const uint32_t sa = base + rx.s * kXStage;
-                    const uint32_t sbb = base + kRingB + rb.s * kBStage;
+                    const uint64_t da = dA0 + static_cast<uint32_t>((rx.s * kXStage) >> 4);
+                    const uint64_t db = dB0 + static_cast<uint32_t>((rb.s * kBStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
 #pragma unroll
                         for (int hm = 0; hm < kHalves; ++hm)    // rows 128*hm.. of the x tile, same B tile
-                            umma_f16(d + hm * BN, smem_desc_sw128(sa + hm * 16384 + kk * 32, 16, 1024),
-                                     smem_desc_sw128(sbb + kk * 32, 16, 1024), idesc, (kb != kbeg) || (kk != 0));
+                            umma_f16(d + hm * BN, da + ((hm * 16384 + kk * 32) >> 4), db + ((kk * 32) >> 4), idesc,
+                                     (kb != kbeg) || (kk != 0));
                     umma_commit(emptyX(rx.s));
                     umma_commit(emptyB(rb.s));
-                    rx.next(kSX);
-                    rb.next(kSB);
                 }
-                if (ok) umma_commit(accF(acc));
+                __syncwarp();
+                mine = true;
+                rx.next(kSX);
+                rb.next(kSB);
             }
+            if (ok && issuer && lane == 0) umma_commit(accF(acc));
         }
     } else if (warp < kDq0 + kDqWarps) {
         // ------------------------------------------------------ dequantizers
@@ -378,7 +399,12 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             int gcur = 0;                             // global group of the constants in slot 0
             for (int kb = kbeg; kb < kend; ++kb) {
                 if (aborted(abort_flag)) { ok = false; break; }
-                if (!mbar_wait(fullP(rp.s), rp.ph) || !mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
+                // The B slot is freed only when the MMAs of the stage kSB back
+                // complete, so that wait is on the tensor pipe's critical loop:
+                // everything that needs only the packed stage (loads, unpack,
+                // scale) runs before it, leaving the stores, the proxy fence
+                // and the arrival after it.
+                if (!mbar_wait(fullP(rp.s), rp.ph)) {
                     fail(a.status, 0x40, abort_flag);
                     ok = false;
                     break;
@@ -398,7 +424,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 --left;
                 const uint4 wv = *reinterpret_cast<const uint4 *>(st + (wl * 32 + ls) * 16);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                uint8_t *brow = sbase + kRingB + rb.s * kBStage + 2 * wl * 1024 + gq * 128;
+                uint4 bv[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int J = j >> 1, jj = j & 1;
@@ -407,15 +433,22 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     const uint32_t nh = (J && gl1) ? c_nh[1][jj] : c_nh[0][jj];
                     uint32_t q[4];
                     unpack_qz(w[j], nl, nh, q);
-                    *reinterpret_cast<uint4 *>(brow + jj * 1024 + (J ? sw1 : sw0)) =
-                        make_uint4(hmul2(q[0], sp), hmul2(q[1], sp), hmul2(q[2], sp), hmul2(q[3], sp));
+                    bv[j] = make_uint4(hmul2(q[0], sp), hmul2(q[1], sp), hmul2(q[2], sp), hmul2(q[3], sp));
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(emptyP(rp.s));   // every value read from it is in registers
+                if (!mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
+                    fail(a.status, 0x40, abort_flag);
+                    ok = false;
+                    break;
+                }
+                uint8_t *brow = sbase + kRingB + rb.s * kBStage + 2 * wl * 1024 + gq * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(brow + (j & 1) * 1024 + ((j >> 1) ? sw1 : sw0)) = bv[j];
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(fullB(rb.s));
-                    mbar_arrive(emptyP(rp.s));        // every register loaded from it is consumed
-                }
+                if (lane == 0) mbar_arrive(fullB(rb.s));
                 if (gl1) {                            // that group continues into the next stage
                     ++gcur;
 #pragma unroll

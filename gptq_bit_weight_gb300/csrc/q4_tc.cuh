@@ -74,6 +74,20 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
         if (globaltimer() - t0 > 2000000000ull) return false;
     }
 }
+// Named barrier `id` over `nthreads` threads (whole warps, each converged
+// before the call) that also returns the AND of every thread's predicate.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
