@@ -28,8 +28,10 @@
 //   warps 4-19   dequantize each packed stage into the fp16 B ring (3 slots
 //                at BM = 128, 2 at BM = 256; K-major, 128-byte swizzle: the
 //                UMMA operand layout), w16 = fp16(s * (q - z - 1)) rounded
-//                once; each thread one 16-byte vector (four words) per stage,
-//                unpacked and scaled before its B slot is free
+//                once, unpacked and scaled before its B slot is free; at
+//                BM = 256 every warp takes one n16 tile of every stage, at
+//                BM = 128 two groups of eight warps take alternate stages,
+//                two n16 tiles per warp
 //   warps 20-23  epilogue: tcgen05.ld an accumulator, add bias, round to fp16,
 //                store (or write a stream-K piece's fp32 partial); then hand
 //                the accumulator back, so the epilogue of one tile overlaps
@@ -104,6 +106,10 @@ struct PfCfg {
     static constexpr int kNumBars = 2 * kSX + 2 * kSP + 2 * kSB + 4;
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr int kDqWarps = BN / 16;
+    // 128-row tiles: two dequant groups on alternate stages, two n16 tiles
+    // per warp (measured 5-7 % faster there, 3 % slower with 256-row tiles)
+    static constexpr int kDqGroups = BM == 128 ? 2 : 1;
+    static constexpr int kDqHalf = kDqWarps / kDqGroups;   // warps per dequant group
     static constexpr int kDq0 = 4;                     // first dequant warp
     static constexpr int kThreads = 32 * (kDq0 + kDqWarps + kEpiWarps);
     static constexpr uint32_t kTmemCols = kAccBufs * kHalves * BN;
@@ -193,7 +199,8 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
     constexpr int kSX = P::kSX, kSP = P::kSP, kSB = P::kSB, kHalves = P::kHalves, kAccBufs = P::kAccBufs;
     constexpr int kXStage = P::kXStage, kPStage = P::kPStage, kBStage = P::kBStage;
     constexpr int kRingP = P::kRingP, kRingB = P::kRingB, kBarOff = P::kBarOff;
-    constexpr int kNumBars = P::kNumBars, kDqWarps = P::kDqWarps, kDq0 = P::kDq0;
+    constexpr int kNumBars = P::kNumBars, kDqWarps = P::kDqWarps, kDq0 = P::kDq0, kDqHalf = P::kDqHalf;
+    constexpr int kDqGroups = P::kDqGroups;
     constexpr uint32_t kTmemCols = P::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -222,10 +229,10 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         }
         for (int s = 0; s < kSP; ++s) {
             mbar_init(fullP(s), 1);
-            mbar_init(emptyP(s), kDqWarps);          // every dequant warp has read it
+            mbar_init(emptyP(s), kDqHalf);           // every warp of the stage's dequant group has read it
         }
         for (int s = 0; s < kSB; ++s) {
-            mbar_init(fullB(s), kDqWarps);
+            mbar_init(fullB(s), kDqHalf);
             mbar_init(emptyB(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -363,101 +370,111 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         }
     } else if (warp < kDq0 + kDqWarps) {
         // ------------------------------------------------------ dequantizers
+        // kDqGroups groups of kDqHalf warps take the stages in turn, and warp
+        // wg of a group owns kDqGroups n16 tiles of its stages: every stage
+        // costs its warps two barrier waits and two arrivals whatever its
+        // work, so with 128-row tiles (half the MMA work per stage) two
+        // groups on alternate stages keep up better than all sixteen warps
+        // on every stage.
         // Lane -> packed-word assignment: in every 8-lane phase (p = lane >> 3)
         // the lanes take columns gq in {p, p ^ 5} and all four tq, so the
         // 16-byte loads of packed words and the 16-byte stores into the
         // swizzled B tile both hit eight distinct bank groups per phase.
-        // Warp wl owns n16 tile wl of the tile.
         const int wl = warp - kDq0;
+        const int grp = wl / kDqHalf, wg = wl % kDqHalf;
         const int pq = lane >> 3;
         const int gq = ((lane >> 2) & 1) ? (pq ^ 5) : pq;
         const int tq = lane & 3;
         const int ls = 4 * gq + tq;
         const uint32_t sw0 = static_cast<uint32_t>((tq ^ gq) << 4);
         const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
-        uint32_t c_s[2][2], c_nl[2][2], c_nh[2][2];   // [half J][column gq / gq+8]
-        auto load_consts = [&](const uint8_t *sz, int gl, int J, int g) {   // g: the global group
-            const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + gl * P::kSGroup + (wl * 8 + gq) * 4);
-            const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + gl * P::kZGroup + wl * 8);
-            c_s[J][0] = __byte_perm(sp, sp, 0x1010);
-            c_s[J][1] = __byte_perm(sp, sp, 0x3232);
-            // effective zero points minus one (stored + zero offset - 1)
-            const uint32_t zoff = g < a.zsplit ? 0u : static_cast<uint32_t>(a.zero_offset);
-            const uint32_t z0 = ((zw.x >> (4 * gq)) & 0xFu) + zoff - 1u;
-            const uint32_t z1 = ((zw.y >> (4 * gq)) & 0xFu) + zoff - 1u;
-            c_nl[J][0] = neg_zlo(z0);
-            c_nh[J][0] = neg_zhi(z0);
-            c_nl[J][1] = neg_zlo(z1);
-            c_nh[J][1] = neg_zhi(z1);
+        // one n16 tile of a stage: the constants of the stage's one or two
+        // groups, the words, and the scaled fp16 pairs (four 16-byte vectors)
+        auto dequant_tile = [&](const uint8_t *st, int nt, int g0, bool gl1, uint4 (&bv)[4]) {
+            const uint8_t *sz = st + kSzOff;
+            uint32_t c_s[2][2], c_nl[2][2], c_nh[2][2];   // [group slot][column gq / gq+8]
+#pragma unroll
+            for (int gl = 0; gl < 2; ++gl) {
+                if (gl == 1 && !gl1) break;
+                const int g = g0 + gl;
+                const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + gl * P::kSGroup + (nt * 8 + gq) * 4);
+                const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + gl * P::kZGroup + nt * 8);
+                c_s[gl][0] = __byte_perm(sp, sp, 0x1010);
+                c_s[gl][1] = __byte_perm(sp, sp, 0x3232);
+                // effective zero points minus one (stored + zero offset - 1)
+                const uint32_t zoff = g < a.zsplit ? 0u : static_cast<uint32_t>(a.zero_offset);
+                const uint32_t z0 = ((zw.x >> (4 * gq)) & 0xFu) + zoff - 1u;
+                const uint32_t z1 = ((zw.y >> (4 * gq)) & 0xFu) + zoff - 1u;
+                c_nl[gl][0] = neg_zlo(z0);
+                c_nh[gl][0] = neg_zhi(z0);
+                c_nl[gl][1] = neg_zlo(z1);
+                c_nh[gl][1] = neg_zhi(z1);
+            }
+            const uint4 wv = *reinterpret_cast<const uint4 *>(st + (nt * 32 + ls) * 16);
+            const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int J = j >> 1, jj = j & 1;     // J: the 32-row block
+                const uint32_t sp = (J && gl1) ? c_s[1][jj] : c_s[0][jj];
+                const uint32_t nl = (J && gl1) ? c_nl[1][jj] : c_nl[0][jj];
+                const uint32_t nh = (J && gl1) ? c_nh[1][jj] : c_nh[0][jj];
+                uint32_t q[4];
+                unpack_qz(w[j], nl, nh, q);
+                bv[j] = make_uint4(hmul2(q[0], sp), hmul2(q[1], sp), hmul2(q[2], sp), hmul2(q[3], sp));
+            }
         };
         RingPos rp, rb;
         bool ok = true;
+        int si = 0;                                   // stage index over the CTA's units
         PfUnit un;
         for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui) {
             const int kbeg = un.kb0, kend = un.kb1;
             int left = 0;                             // 32-row blocks left in the current group
-            int gcur = 0;                             // global group of the constants in slot 0
-            for (int kb = kbeg; kb < kend; ++kb) {
-                if (aborted(abort_flag)) { ok = false; break; }
-                // The B slot is freed only when the MMAs of the stage kSB back
-                // complete, so that wait is on the tensor pipe's critical loop:
-                // everything that needs only the packed stage (loads, unpack,
-                // scale) runs before it, leaving the stores, the proxy fence
-                // and the arrival after it.
-                if (!mbar_wait(fullP(rp.s), rp.ph)) {
-                    fail(a.status, 0x40, abort_flag);
-                    ok = false;
-                    break;
-                }
-                const uint8_t *st = sbase + kRingP + rp.s * kPStage;
-                const uint8_t *sz = st + kSzOff;
-                // first block: a new group starts here (slot 0) or continues from the
-                // previous stage's second block, whose constants are already in slot 0
-                if (left == 0 || kb == kbeg) {      // a slice may start inside a group
+            int gcur = 0;                             // group of the stage's first block
+            for (int kb = kbeg; kb < kend; ++kb, ++si) {
+                if (left == 0 || kb == kbeg) {        // a slice may start inside a group
                     gcur = kb == kbeg ? (2 * kbeg) / a.bpg : gcur + 1;
-                    load_consts(sz, 0, 0, gcur);
                     left = kb == kbeg ? a.bpg - (2 * kbeg - gcur * a.bpg) : a.bpg;
                 }
                 --left;
-                const bool gl1 = left == 0;           // the second block starts a new group (slot 1)
-                if (gl1) { load_consts(sz, 1, 1, gcur + 1); left = a.bpg; }
+                const bool gl1 = left == 0;           // the second block starts a new group
+                const int g0 = gcur;
+                if (gl1) left = a.bpg;
                 --left;
-                const uint4 wv = *reinterpret_cast<const uint4 *>(st + (wl * 32 + ls) * 16);
-                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                uint4 bv[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int J = j >> 1, jj = j & 1;
-                    const uint32_t sp = (J && gl1) ? c_s[1][jj] : c_s[0][jj];
-                    const uint32_t nl = (J && gl1) ? c_nl[1][jj] : c_nl[0][jj];
-                    const uint32_t nh = (J && gl1) ? c_nh[1][jj] : c_nh[0][jj];
-                    uint32_t q[4];
-                    unpack_qz(w[j], nl, nh, q);
-                    bv[j] = make_uint4(hmul2(q[0], sp), hmul2(q[1], sp), hmul2(q[2], sp), hmul2(q[3], sp));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(emptyP(rp.s));   // every value read from it is in registers
-                if (!mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
-                    fail(a.status, 0x40, abort_flag);
-                    ok = false;
-                    break;
-                }
-                uint8_t *brow = sbase + kRingB + rb.s * kBStage + 2 * wl * 1024 + gq * 128;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(brow + (j & 1) * 1024 + ((j >> 1) ? sw1 : sw0)) = bv[j];
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(fullB(rb.s));
-                if (gl1) {                            // that group continues into the next stage
-                    ++gcur;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        c_s[0][c] = c_s[1][c];
-                        c_nl[0][c] = c_nl[1][c];
-                        c_nh[0][c] = c_nh[1][c];
+                if (si % kDqGroups == grp) {
+                    if (aborted(abort_flag)) { ok = false; break; }
+                    // The B slot is freed only when the MMAs of the stage kSB back
+                    // complete, so that wait is on the tensor pipe's critical loop:
+                    // everything that needs only the packed stage runs before it,
+                    // leaving the stores, the proxy fence and the arrival after it.
+                    if (!mbar_wait(fullP(rp.s), rp.ph)) {
+                        fail(a.status, 0x40, abort_flag);
+                        ok = false;
+                        break;
                     }
+                    const uint8_t *st = sbase + kRingP + rp.s * kPStage;
+                    uint4 bv[kDqGroups][4];
+#pragma unroll
+                    for (int i = 0; i < kDqGroups; ++i) dequant_tile(st, kDqGroups * wg + i, g0, gl1, bv[i]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(emptyP(rp.s));   // every value read from it is in registers
+                    if (!mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
+                        fail(a.status, 0x40, abort_flag);
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kDqGroups; ++i) {
+                        uint8_t *brow = sbase + kRingB + rb.s * kBStage + 2 * (kDqGroups * wg + i) * 1024 + gq * 128;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint4 *>(brow + (j & 1) * 1024 + ((j >> 1) ? sw1 : sw0)) = bv[i][j];
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(fullB(rb.s));
                 }
+                if (gl1) ++gcur;                      // that group continues into the next stage
                 rp.next(kSP);
                 rb.next(kSB);
             }
