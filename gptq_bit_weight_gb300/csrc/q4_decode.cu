@@ -342,7 +342,22 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         const uint32_t lo_base1 = neg_zlo(static_cast<uint32_t>(h.zero_offset) - 1u);
         const uint32_t hi_base1 = neg_zhi(static_cast<uint32_t>(h.zero_offset) - 1u);
         const uint32_t lo_base0 = neg_zlo(0xFFFFFFFFu), hi_base0 = neg_zhi(0xFFFFFFFFu);
+        // Group slots (raw pairs).  An m16n8k16 MMA has 8 B columns and the
+        // rows of x fill MP of them (MP = 2 for one or two rows, else M rounded
+        // up to a power of two); the others carry the next groups: B column c
+        // holds x row c % MP while the run is in group c / MP of the current
+        // batch of S = 8 / MP groups, zeros otherwise.  Each group then
+        // accumulates in its own columns and the per-group step (zero point,
+        // scale) runs once per batch; a lane's two accumulator columns belong
+        // to slot 2 tq / MP, whose group's constants it loads.  The slots of
+        // each row are summed across the lanes at the end.
+        const int MP = mrows <= 2 ? 2 : (mrows <= 4 ? 4 : 8);
+        const int S = 8 / MP;
+        const int lslot = (2 * tq) / MP;
+        const int ng_slice = (c_end * 64 - 1) / geff + 1 - g_base;   // groups staged for the slice
+        int slot = 0;
         auto load_group = [&](int gl) {
+            if (RAW) gl = min(gl + lslot, ng_slice - 1);   // past the run's last group: zero sums
             const uint32_t *base = gsz + gl * kGszStride;
             const bool z0grp = g_base + gl < h.zsplit;
             const uint32_t zoff = z0grp ? 0u : static_cast<uint32_t>(h.zero_offset);
@@ -403,20 +418,35 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
         // 32-row block of the run.
         const uint16_t *xp[MT];
         bool xv[MT];
+        const int rraw = gq & (MP - 1);                // raw pairs: the lane's x row in its slot
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const int r = mt * 8 + gq;
-            xv[mt] = r < mrows;
-            xp[mt] = xs + (xv[mt] ? r : 0) * XS + 2 * (wc_beg - c_beg) * 32 + 8 * tq;
+            const int r = mt * 8 + (RAW ? rraw : gq);
+            xv[mt] = r < mrows && (!RAW || gq / MP == slot);
+            xp[mt] = xs + (r < mrows ? r : 0) * XS + 2 * (wc_beg - c_beg) * 32 + 8 * tq;
         }
+        // shared ring: offset from the lane's own x row to the row it reads
+        const int xring_off = RAW ? (rraw - gq) * 128 : 0;
+        bool xsel = RAW ? xv[0] : xrow;
 
         const unsigned char *xcur = myx;               // shared ring: x fragments of the current chunk
         auto run_chunk = [&](int c, const uint4 (&w)[kNTW]) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 if (left == 0) {
-                    flush();
-                    load_group(++gl);
+                    if (RAW) {
+                        if (++slot == S) {
+                            flush();
+                            gl += S;
+                            slot = 0;
+                            load_group(gl);
+                        }
+                        xsel = gq / MP == slot && rraw < mrows;
+                        xv[0] = xsel;
+                    } else {
+                        flush();
+                        load_group(++gl);
+                    }
                     left = bpg;
                 }
                 --left;
@@ -424,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     if (XR)
-                        xb[mt] = xrow ? *reinterpret_cast<const uint4 *>(xcur + hh * 64) : make_uint4(0u, 0u, 0u, 0u);
+                        xb[mt] = xsel ? *reinterpret_cast<const uint4 *>(xcur + xring_off + hh * 64)
+                                      : make_uint4(0u, 0u, 0u, 0u);
                     else
                         xb[mt] = xv[mt] ? *reinterpret_cast<const uint4 *>(xp[mt] + (2 * c + hh) * 32)
                                         : make_uint4(0u, 0u, 0u, 0u);
@@ -520,6 +551,19 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT, RAW)) decode_kernel(H
             }
         }
         flush();
+    }
+    if (RAW && mrows <= 4) {
+        // raw pairs: sum each row's group slots across the lanes (xor 1 and 2
+        // with two slot columns per row set of four lanes, xor 2 with four rows)
+#pragma unroll
+        for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float v = acc[nt][0][i];
+                if (mrows <= 2) v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+                acc[nt][0][i] = v;
+            }
     }
 
     // ---- fixed-order reduction over the CTA's warps; warp w's partials go to
