@@ -728,9 +728,16 @@ static DecodePlan plan_decode_arith(int M, int K, int N, int geff, bool raw, boo
     // each x line and carrying x per chunk measured faster), else carried
     // per chunk.
     const int max_slice = sr ? KC : std::min(KC, std::max(8, std::min(64, 512 / xrows)));
+    // Also carried per chunk when staging it would cost a resident CTA per SM
+    // (small groups stage more scale words: 8192x10240 g32 M = 1 measured
+    // 22.2 -> 18.7 us at three CTAs per SM instead of two).
     auto xr_for = [&](int slice) {
         const long long xb = static_cast<long long>(xrows) * slice * 128;
-        return sr && (xb > kXStageBytes || (p.ctas_n * p.zdim <= kSMs && xb > kXStageBytes / 2));
+        if (!sr) return false;
+        if (xb > kXStageBytes || (p.ctas_n * p.zdim <= kSMs && xb > kXStageBytes / 2)) return true;
+        const int mg = max_groups_in_slice(slice, geff);
+        return resident_ctas(p.mt, raw, smem_bytes_for(p.mt, sr, false, xrows, slice, mg)) <
+               resident_ctas(p.mt, raw, smem_bytes_for(p.mt, sr, true, xrows, slice, mg));
     };
     const int base = p.ctas_n * p.zdim;
     const int min_splits = (KC + max_slice - 1) / max_slice;
