@@ -228,15 +228,28 @@ __device__ __forceinline__ uint32_t gather2(const uint16_t *xr, int pa, int pb) 
 
 __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int M, int Kx,
                                 int K, uint16_t *__restrict__ ts, bool early) {
-    pdl_enter(early);
+    if (early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const size_t total = static_cast<size_t>(M) * (K / 8);
-    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    // The permutation is a handle constant: the thread's first vectors of it
+    // are read before the preceding grid has finished, leaving only the
+    // gather from x on the path after it.
+    int4 p0 = make_int4(-1, -1, -1, -1), p1 = p0;
+    if (idx < total) {
+        const int j0 = static_cast<int>(idx % (K / 8)) * 8;
+        p0 = *reinterpret_cast<const int4 *>(perm + j0);
+        p1 = *reinterpret_cast<const int4 *>(perm + j0 + 4);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (bool first = true; idx < total; idx += stride, first = false) {
         const size_t m = idx / (K / 8);
         const int j0 = static_cast<int>(idx % (K / 8)) * 8;
         const uint16_t *xr = x + m * Kx;
-        const int4 p0 = *reinterpret_cast<const int4 *>(perm + j0);
-        const int4 p1 = *reinterpret_cast<const int4 *>(perm + j0 + 4);
+        if (!first) {
+            p0 = *reinterpret_cast<const int4 *>(perm + j0);
+            p1 = *reinterpret_cast<const int4 *>(perm + j0 + 4);
+        }
         uint4 v;
         v.x = gather2(xr, p0.x, p0.y);
         v.y = gather2(xr, p0.z, p0.w);
