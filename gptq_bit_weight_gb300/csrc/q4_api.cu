@@ -710,8 +710,11 @@ static int run_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStr
     const bool small_layer =
         Mk <= 4 || weights < (size_t{24} << 20) || (Mk <= 8 && weights < (size_t{64} << 20));
     // the activation kernel lets the decode grid start early when that grid
-    // is the register-streaming kernel at M <= 8 (measured faster only there)
-    const bool early = Mk <= 8 && (path == GPTQ_Q4_PATH_DECODE_MMA || (path == GPTQ_Q4_PATH_DECODE && small_layer));
+    // is the register-streaming kernel at M <= 8, or the stream-K kernel at
+    // one row (28672x8192 act-order M = 1: 39.0 -> 37.0 us; measured slower
+    // elsewhere, 1-3 % for the stream-K kernel at two rows)
+    const bool early = Mk <= 8 && (path == GPTQ_Q4_PATH_DECODE_MMA || (path == GPTQ_Q4_PATH_DECODE_STREAM && Mk == 1) ||
+                                   (path == GPTQ_Q4_PATH_DECODE && small_layer));
     const uint16_t *xin = static_cast<const uint16_t *>(x);
     q4::HandleView v = view(h);
     if (h->act_f32) {
