@@ -62,8 +62,14 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 // ring slots per warp (depth - 1 units in flight), a power of two: 8, or 4
 // with eight rows of x per slot (two CTAs per SM must fit in shared memory)
-constexpr int depth_for(int mp) { return mp == 8 ? 4 : 8; }
-constexpr int kCtasPerSm = 2;
+#ifndef Q4_SK_DEPTH
+#define Q4_SK_DEPTH 8
+#endif
+#ifndef Q4_SK_CTAS
+#define Q4_SK_CTAS 2
+#endif
+constexpr int depth_for(int mp) { return mp == 8 ? (Q4_SK_DEPTH < 4 ? Q4_SK_DEPTH : 4) : Q4_SK_DEPTH; }
+constexpr int kCtasPerSm = Q4_SK_CTAS;
 constexpr int kMinUnits = 4;            // fewest units per worker
 
 // Ring slot: the unit's packed words (NTW x 512 bytes), its x fragments (MP
