@@ -23,7 +23,7 @@ namespace q4 {
 cudaError_t launch_gemm_f16(const uint16_t *a, const uint16_t *b, const uint16_t *bias, int M, int K, int N,
                             uint16_t *out, int *status, cudaStream_t s, const float *rowscale = nullptr,
                             int out_bf16 = 0);
-int prefill_default_min_m();
+int prefill_default_min_m(int K, int N, int geff);
 }  // namespace q4
 
 #include "q4_handle.h"
@@ -359,7 +359,7 @@ gptq_q4_handle gptq_q4_make(const int32_t *qweight, const int32_t *qzeros, const
     h->geff = gpad;
     h->G = G;
     h->act_order = act ? 1 : 0;
-    h->prefill_min_m = q4::prefill_default_min_m();
+    h->prefill_min_m = q4::prefill_default_min_m(Kp, N, gpad);
 
     cudaStream_t s = nullptr;
     auto fail = [&](int) -> gptq_q4_handle {

@@ -746,6 +746,15 @@ cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws,
     return launch_prefill_tile<256, 256>(h, p, ws, tickets, x, M, out, s);
 }
 
-int prefill_default_min_m() { return 17; }
+// Rows from which the fused prefill beats the decode kernels, measured on
+// GB300 (CUDA-graph replays over more weights than L2): 17 in general; 9 with
+// 32-row groups (8192x28672 M = 9-16: 75 against 112-125 us), and with 64-row
+// groups on layers of 100 Mi weights or more (69 against 74-78 us), where the
+// decode kernels' per-group step weighs most.
+int prefill_default_min_m(int K, int N, int geff) {
+    const size_t weights = static_cast<size_t>(K) * N;
+    if (geff <= 32 || (geff <= 64 && weights >= (size_t{100} << 20))) return 9;
+    return 17;
+}
 
 }  // namespace q4

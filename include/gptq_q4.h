@@ -348,9 +348,10 @@ int gptq_q4_set_format(gptq_q4_handle h, int format);
 int gptq_q4_set_act_dtype(gptq_q4_handle h, int dtype);
 
 /* Rows at and above which GPTQ_Q4_PATH_AUTO takes the prefill kernel (the
- * decode/prefill switch of the Lorax page's set_tuning_params).  Default 17:
- * decode covers up to 16 rows; measured on GB300, the fused prefill is faster
- * than the decode kernels beyond that.  Results never depend on it. */
+ * decode/prefill switch of the Lorax page's set_tuning_params).  Default 17,
+ * or 9 for groups of at most 32 rows and for groups of at most 64 rows on
+ * layers of 100 Mi weights or more: measured on GB300, the fused prefill is
+ * faster than the decode kernels from there.  Results never depend on it. */
 int gptq_q4_set_prefill_min_m(gptq_q4_handle h, int min_m);
 
 /* Facts about a handle (host outputs; any pointer may be NULL). */
