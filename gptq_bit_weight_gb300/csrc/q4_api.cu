@@ -679,21 +679,21 @@ static int run_path(gptq_q4_handle h, const q4::HandleView &v, const uint16_t *x
 }
 
 // GPTQ_Q4_PATH_DECODE: where the stream-K kernel is ahead, measured on GB300
-// over the Llama-7B and Llama-70B projection layers at M = 1, 2, 4, 8
-// (CUDA-graph replays over more weights than L2):
-//   - a tall layer whose 32-column tiles cannot fill the GPU (K >= 2 N and
-//     fewer than two tiles per SM; 28672 x 8192) at M <= 2 with groups of
-//     at most 128 rows: the other kernels leave SMs short of warps;
-//   - M >= 5 on a wide layer (at least two tiles per SM) with groups of 32
-//     rows, or of 64 rows on layers of at least 100 Mi weights: the group
-//     slots save most of the per-group work there.
+// over the Llama-70B projection layers at M = 1, 2, 4, 8 (CUDA-graph replays
+// over more weights than L2): only on a tall layer whose 32-column tiles
+// cannot fill the GPU (K >= 2 N and fewer than two tiles per SM; 28672 x
+// 8192), where the other kernels leave SMs short of warps: at one row with
+// groups of at most 128 rows, at two rows with 32-row groups, and at 3-8 rows
+// with groups of 128 rows or more (28672 x 8192 g128 M = 8: 42.1 against
+// 45.8 us).
 static bool prefer_stream(const gptq_q4_s *h, int M) {
     const long long tiles = h->N / 32, sms = q4::device_sm_count();
-    const size_t weights = static_cast<size_t>(h->K) * h->N;
-    if (M <= 2) return h->K >= 2LL * h->N && tiles < 2 * sms && h->geff <= 128;
-    if (M >= 5 && M <= 8 && tiles >= 2 * sms)
-        return h->geff <= 32 || (h->geff <= 64 && weights >= (size_t{100} << 20));
-    return false;
+    // tall layers whose 32-column tiles cannot fill the GPU (28672 x 8192)
+    const bool tall = h->K >= 2LL * h->N && tiles < 2 * sms;
+    if (!tall || M > 8) return false;
+    if (M == 1) return h->geff <= 128;
+    if (M == 2) return h->geff <= 32;
+    return h->geff >= 128;
 }
 
 static int run_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStream_t stream, int path) {
@@ -704,11 +704,13 @@ static int run_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStr
     // Which decode kernel: measured on GB300 (CUDA-graph replays over more
     // weights than L2), the register-streaming kernel (with its shared
     // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
-    // layers below 64 Mi weights and at any M on layers below 24 Mi weights;
-    // the TMA-ring kernel is ahead everywhere else it applies.
+    // layers below 64 Mi weights or with groups of at most 64 rows
+    // (8192 x 28672 g32 M = 8: 45.0 against 89.3 us) and at any M on layers
+    // below 24 Mi weights; the TMA-ring kernel is ahead everywhere else it
+    // applies.
     const size_t weights = static_cast<size_t>(h->K) * h->N;
-    const bool small_layer =
-        Mk <= 4 || weights < (size_t{24} << 20) || (Mk <= 8 && weights < (size_t{64} << 20));
+    const bool small_layer = Mk <= 4 || weights < (size_t{24} << 20) ||
+                             (Mk <= 8 && (weights < (size_t{64} << 20) || h->geff <= 64));
     // the activation kernel lets the decode grid start early when that grid
     // is the register-streaming kernel at M <= 8, or the stream-K kernel at
     // one row (28672x8192 act-order M = 1: 39.0 -> 37.0 us; measured slower
