@@ -262,10 +262,15 @@ __global__ void xreorder_kernel(const uint16_t *__restrict__ x, const int32_t *_
 // Many rows: the permutation is staged once per CTA and each row of x is
 // staged in shared memory with 16-byte loads, so that both the reads and the
 // gathered 16-byte writes are coalesced (the gather itself hits shared
-// memory).  Rows are taken round-robin by the CTAs.
-__global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__restrict__ x,
-                                                             const int32_t *__restrict__ perm, int M, int Kx, int K,
-                                                             uint16_t *__restrict__ ts, bool early) {
+// memory).  Rows are taken round-robin by the CTAs.  Each thread's loads of a
+// row are all issued before any is stored, and rows wide enough to leave one
+// CTA per SM get 1024 threads, so that a row costs about one memory round
+// trip (with 256 threads and one load at a time a 28672-wide row took ~14:
+// Llama-70B act-order prefill at M = 2048 on 28672 x 8192 1.31 -> 1.42
+// PFLOP/s).
+__global__ void __launch_bounds__(1024) xreorder_rows_kernel(const uint16_t *__restrict__ x,
+                                                              const int32_t *__restrict__ perm, int M, int Kx, int K,
+                                                              uint16_t *__restrict__ ts, bool early) {
     extern __shared__ __align__(16) unsigned char sm[];
     pdl_enter(early);
     int32_t *sp = reinterpret_cast<int32_t *>(sm);
@@ -273,10 +278,23 @@ __global__ void __launch_bounds__(256) xreorder_rows_kernel(const uint16_t *__re
     const int nvx = Kx / 8, nv = K / 8;                    // 16-byte vectors per x row / temp_state row
     for (int i = threadIdx.x; i < K / 4; i += blockDim.x)
         reinterpret_cast<int4 *>(sp)[i] = reinterpret_cast<const int4 *>(perm)[i];
+    constexpr int kBatch = 4;                              // loads in flight per thread
     for (int m = blockIdx.x; m < M; m += gridDim.x) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * Kx);
         __syncthreads();                                   // the previous row's gathers are done
-        for (int i = threadIdx.x; i < nvx; i += blockDim.x) reinterpret_cast<uint4 *>(sx)[i] = xr[i];
+        for (int i0 = threadIdx.x; i0 < nvx; i0 += kBatch * blockDim.x) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = i0 + b * blockDim.x;
+                if (i < nvx) v[b] = xr[i];
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = i0 + b * blockDim.x;
+                if (i < nvx) reinterpret_cast<uint4 *>(sx)[i] = v[b];
+            }
+        }
         __syncthreads();
         uint4 *out = reinterpret_cast<uint4 *>(ts + static_cast<size_t>(m) * K);
         for (int i = threadIdx.x; i < nv; i += blockDim.x) {
@@ -300,8 +318,13 @@ cudaError_t launch_xreorder(const uint16_t *x, const int32_t *perm, int M, int K
             cudaFuncSetAttribute(xreorder_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (attr != cudaSuccess) return attr;
         const int per_sm = static_cast<int>((228 * 1024) / (rows_smem + 1024));
+        // one CTA per SM (a wide row and its permutation fill shared memory):
+        // 1024 threads; else 256 threads and several CTAs per SM (measured
+        // faster on 4096- and 11008-wide rows)
+        const int threads = per_sm <= 1 ? 1024 : 256;
         const int ctas = std::min(M, kSMs * std::max(1, std::min(per_sm, 8)));
-        return launch_pdl(early, xreorder_rows_kernel, ctas, 256, rows_smem, s, x, perm, M, Kx, K, temp_state, early);
+        return launch_pdl(early, xreorder_rows_kernel, ctas, threads, rows_smem, s, x, perm, M, Kx, K, temp_state,
+                          early);
     }
     const size_t total = static_cast<size_t>(M) * (K / 8);
     const int threads = 256;
