@@ -682,16 +682,13 @@ static int run_path(gptq_q4_handle h, const q4::HandleView &v, const uint16_t *x
 // over the Llama-7B and Llama-70B projection layers at M = 1, 2, 4, 8
 // (CUDA-graph replays over more weights than L2): only on a large tall layer
 // whose 32-column tiles cannot fill the GPU (K >= 2 N, fewer than two tiles
-// per SM, 100 Mi weights or more; 28672 x 8192), where the other kernels
-// leave SMs short of warps: at one row with
-// groups of at most 128 rows, at two rows with 32-row groups, and at 3-8 rows
-// with groups of 128 rows or more (28672 x 8192 g128 M = 8: 42.1 against
-// 45.8 us).
+// per SM, 100 Mi weights or more: 28672 x 8192; on 11008 x 4096 the
+// register-streaming kernel is ahead, M = 1 9.4 against 12.7 us), where the
+// other kernels leave SMs short of warps: at one row with groups of at most
+// 128 rows, at two rows with 32-row groups, and at 3-8 rows with groups of
+// 128 rows or more (28672 x 8192 g128 M = 8: 42.1 against 45.8 us).
 static bool prefer_stream(const gptq_q4_s *h, int M) {
     const long long tiles = h->N / 32, sms = q4::device_sm_count();
-    // tall layers of 100 Mi weights or more whose 32-column tiles cannot fill
-    // the GPU (28672 x 8192; on 11008 x 4096 the register-streaming kernel is
-    // ahead: M = 1 9.4 against 12.7 us)
     const bool tall = h->K >= 2LL * h->N && tiles < 2 * sms &&
                       static_cast<size_t>(h->K) * h->N >= (size_t{100} << 20);
     if (!tall || M > 8) return false;

@@ -74,12 +74,13 @@ extern "C" {
 
 /* Paths gptq_q4_matmul can take (see gptq_q4_set_path). */
 #define GPTQ_Q4_PATH_AUTO      0  /* decode below the prefill threshold, fused prefill above */
-#define GPTQ_Q4_PATH_DECODE    1  /* always decode: the stream-K kernel on tall layers that the
-                                     column tiles cannot fill (K >= 2 N, fewer than two 32-column
-                                     tiles per SM) at M <= 2 with groups of at most 128 rows, and
-                                     at M = 5..8 on wide layers with 32-row groups (64-row groups
-                                     from 100 Mi weights); otherwise the register-streaming kernel
-                                     at M <= 4, at M <= 8 on layers below 64 Mi weights and on any
+#define GPTQ_Q4_PATH_DECODE    1  /* always decode: the stream-K kernel on tall layers of 100 Mi
+                                     weights or more that the column tiles cannot fill (K >= 2 N,
+                                     fewer than two 32-column tiles per SM) at M = 1 with groups of
+                                     at most 128 rows, at M = 2 with 32-row groups and at M = 3..8
+                                     with groups of 128 rows or more; otherwise the
+                                     register-streaming kernel at M <= 4, at M <= 8 on layers below
+                                     64 Mi weights or with groups of at most 64 rows, and on any
                                      layer below 24 Mi weights; the TMA-ring kernel (M <= 16)
                                      elsewhere, where the shape allows it */
 #define GPTQ_Q4_PATH_PREFILL   2  /* always the fused shared-memory-dequant tensor-core kernel */
