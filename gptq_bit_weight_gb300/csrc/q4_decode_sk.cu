@@ -72,19 +72,19 @@ constexpr int depth_for(int mp) { return mp == 8 ? (Q4_SK_DEPTH < 4 ? Q4_SK_DEPT
 constexpr int kCtasPerSm = Q4_SK_CTAS;
 constexpr int kMinUnits = 4;            // fewest units per worker
 
-// Ring slot: the unit's packed words (NTW x 512 bytes), its x fragments (MP
-// rows x 128 bytes), and 128 bytes of zeros that lanes outside the current
-// group slot read instead of x (so no select is needed per MMA).
+// Ring slot: the unit's packed words (NTW x 512 bytes) and its x fragments
+// (MP rows x 128 bytes).  After the ring, per warp: the segment's fp32
+// accumulators, NTW x 16 bytes per lane (touched only when a batch of groups
+// is flushed), and 128 bytes of zeros that lanes outside the current group
+// slot read instead of x (so no select is needed per MMA).
 template <int MP, int NTW>
 struct SkCfg {
     static constexpr int kDepth = depth_for(MP);
     static constexpr int kXOff = NTW * 512;
-    static constexpr int kZeroOff = kXOff + MP * 128;
-    static constexpr int kSlot = kZeroOff + 128;      // multiple of 16
-    // after the ring: the segment's fp32 accumulators, NTW x 16 bytes per lane
-    // (touched only when a batch of groups is flushed)
+    static constexpr int kSlot = kXOff + MP * 128;    // multiple of 16
     static constexpr int kAccOff = kDepth * kSlot;
-    static constexpr int kWarpBytes = kAccOff + NTW * 512;
+    static constexpr int kZeroOff = kAccOff + NTW * 512;
+    static constexpr int kWarpBytes = kZeroOff + 128;
     static constexpr int kSmem = kWarps * kWarpBytes;
 };
 
@@ -136,9 +136,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
     const long long u1 = static_cast<long long>(wid + 1) * a.U / a.workers;
     const int n_units = static_cast<int>(u1 - u0);
     unsigned char *ring = smem + warp * C::kWarpBytes;
-    // zero areas of every slot
-    for (int v = lane; v < kDepth * 8; v += 32)
-        *reinterpret_cast<uint4 *>(ring + (v >> 3) * C::kSlot + C::kZeroOff + (v & 7) * 16) = make_uint4(0, 0, 0, 0);
+    // the warp's zero area
+    if (lane < 8) *reinterpret_cast<uint4 *>(ring + C::kZeroOff + lane * 16) = make_uint4(0, 0, 0, 0);
+    __syncwarp();
 
     // Fill cursor: word offset (in 16-byte vectors) of the next unit's first
     // n16 tile, (NTW t KC + c) 32, and its chunk c.
@@ -205,12 +205,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
     uint32_t csc[NTW], cz0[NTW], cz1[NTW];
     uint32_t gzoff;
     int seg_t = 0, gb0 = 0, slot = 0, left = 0;
-    // lanes whose B column belongs to the current slot read x, the others the
-    // zero area (offset within a ring slot)
+    // lanes whose B column belongs to the current slot read x (at this offset
+    // within a ring slot), the others the warp's zero area
     const int x_real = C::kXOff + (gq % MP) * 128 + tq * 16;
-    const int x_zero = C::kZeroOff + tq * 16;
-    int xoff = x_real;
-    auto set_xoff = [&]() { xoff = (S == 1 || gq / MP == slot) && (gq % MP) < a.M ? x_real : x_zero; };
+    const unsigned char *const xzero = ring + C::kZeroOff + tq * 16;
+    bool xuse = true;
+    auto set_xoff = [&]() { xuse = (S == 1 || gq / MP == slot) && (gq % MP) < a.M; };
     auto clear_partials = [&]() {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -357,9 +357,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
     int t = t_first, c = static_cast<int>(u0 - static_cast<long long>(t_first) * KC);
     begin_segment(t, c);
     cp_async_wait<0>();
+    int s = 0;                                        // ring slot of unit i
 #pragma unroll 1
     for (int i = 0; i < n_units; ++i) {
-        const int s = i & (kDepth - 1);
         cp_async_wait<kDepth - 2>();
         __syncwarp();                                 // every lane's x copy of unit i has landed
         const unsigned char *slot_base = ring + s * C::kSlot;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
         for (int nt = 0; nt < NTW; ++nt) w[nt] = *reinterpret_cast<const uint4 *>(slot_base + lane * 16 + nt * 512);
         // refill the slot consumed by unit i - 1 with unit i + kDepth - 1
         if (i + kDepth - 1 < n_units) {
-            const int fs = (i + kDepth - 1) & (kDepth - 1);
+            const int fs = s == 0 ? kDepth - 1 : s - 1;
             copy_w(fs);
             copy_x(fs, fc);
             advance();
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
         // tile the A fragments straight from the code pairs (rows (0,1),
         // (4,5) as 1024 + q, rows (2,3), (6,7) as 1024 + 16 q) into the MMAs
         auto block = [&](int hh) {
-            const uint4 xb = *reinterpret_cast<const uint4 *>(slot_base + xoff + hh * 64);
+            const uint4 xb = *reinterpret_cast<const uint4 *>((xuse ? slot_base + x_real : xzero) + hh * 64);
             mma_f32(slo, ones, xb.x, xb.z);
             mma_f32(shi, ones, xb.y, xb.w);
 #pragma unroll
@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_sk_kernel(HandleV
                 begin_segment(t, 0);
             }
         }
+        if (++s == kDepth) s = 0;
     }
     cp_async_wait<0>();
 }
