@@ -33,6 +33,10 @@
 // which lets both operands come from single 16-byte loads; a sum does not
 // depend on the order of its terms beyond rounding.  The scale is factored
 // out of each group: a fresh fp32 partial per group, then acc += s * partial.
+// The raw-pair variant (RAW) enters the code pairs as raw 1024 + q / 1024 +
+// 16 q, removes the zero points per group from MMA-accumulated sums of x, and
+// puts successive groups in the spare B columns of its MMAs (group slots), so
+// that its per-group step runs once per batch of 8 / MP groups.
 //
 // Reduction.  Warps of a CTA are summed in a fixed order through shared
 // memory.  With more than one K slice, each CTA writes its fp32 partial tile
