@@ -317,6 +317,7 @@ struct PrefillPlan {
     int sk;            // 1: stream-K over the tiles x k-blocks space (cooperative launch)
     int grid;          // stream-K: CTAs
     int pmax;          // stream-K: most pieces of one tile
+    int fin0;          // stream-K, one range per CTA: piece 0's CTA finishes each cut tile
     size_t ws_floats;  // fp32 partial tiles when tiles are cut into pieces
     int n_tickets;     // one per tile when tiles are cut into pieces
 };

@@ -78,6 +78,17 @@ using namespace tc;
 
 constexpr int BK = 64;
 constexpr int kEpiWarps = 4;
+// Stream-K pieces.  With one range per CTA over the tiles x k-blocks space,
+// a tile is cut into at most three pieces, and all but piece 0 (the tile's
+// first k blocks, the last unit of its CTA's range) are the first units of
+// their CTAs' ranges, written early in the main loop: the CTA holding piece 0
+// keeps it in tensor memory and finishes the tile, adding the others
+// (8192 x 28672 at M = 256-512, 4096 x 11008 and 8192 x 10240 at M = 1024:
+// 5-12 % faster than every piece's CTA summing a share of the rows).  With
+// the even K split every piece ends at the same time, one reader per tile is
+// slower (4096 x 4096 at M = 1024: 43.3 against 39.6 us), and the pieces'
+// CTAs share the sum.
+constexpr int kFinishMax = 3;
 
 // Per tile BM x BN: BN = 256, or 128 where 256-wide tiles leave SMs idle (one
 // dequant warp per 16 columns); BM = 128, or 256 (two M = 128 MMAs per k step
@@ -133,6 +144,7 @@ struct PfArgs {
     int sk;                  // 1: stream-K (every CTA one contiguous range of the (tile, k
                              // block) space, cooperative launch); 0: whole tiles round robin
     int pmax;                // stream-K: most pieces (CTAs) any tile is cut into
+    int fin0;                // stream-K: piece 0's CTA finishes each cut tile (else all pieces' CTAs)
     float *ws;               // stream-K: fp32 partial tiles [tile][piece][BM][BN]
     int *tickets;            // one per tile, zero between calls
 };
@@ -178,6 +190,45 @@ __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
     atomicExch(abort_flag, 1);
 }
 __device__ __forceinline__ bool aborted(int *abort_flag) { return *reinterpret_cast<volatile int *>(abort_flag) != 0; }
+
+// 32 consecutive accumulator columns of one output row, the first at column
+// n: the row scale, bias and one rounding to fp16 or bf16, or the raw fp32
+// sums; columns at or past N are skipped.
+template <bool BF>
+__device__ __forceinline__ void store_row32_t(const PfArgs &a, int row, int n, const uint32_t (&r)[32]) {
+    const float rs = BF && a.rowscale ? a.rowscale[row] : 1.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int nv = n + 8 * v;
+        if (nv < a.N) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pk[e] = out_pair_t<BF>(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]), rs,
+                                       a.bias, nv + 2 * e);
+            *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + nv) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+}
+__device__ __forceinline__ void store_row32(const PfArgs &a, int row, int n, const uint32_t (&r)[32]) {
+    if (a.out_bf16 == kOutF32) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int nv = n + 8 * v;
+            if (nv < a.N) {
+                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + static_cast<size_t>(row) * a.N + nv);
+                dst[0] = make_float4(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1]), __uint_as_float(r[8 * v + 2]),
+                                     __uint_as_float(r[8 * v + 3]));
+                dst[1] = make_float4(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]),
+                                     __uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+            }
+        }
+    } else if (a.out_bf16) {
+        store_row32_t<true>(a, row, n, r);
+    } else {
+        store_row32_t<false>(a, row, n, r);
+    }
+}
 
 // Ring position: slot and the parity of its current phase.
 struct RingPos {
@@ -489,12 +540,18 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             const int acc = lt % kAccBufs;
             const uint32_t aph = (lt / kAccBufs) & 1;
             bool ok = !aborted(abort_flag) && mbar_wait(accF(acc), aph);
-            ok = __all_sync(0xffffffffu, ok);
+            __syncwarp();
+            ok = bar_and(2, 32 * kEpiWarps, ok);        // the four epilogue warps agree
             if (!ok) {
                 if (lane == 0) fail(a.status, 0x80, abort_flag);
                 break;
             }
             tc_fence_after();
+            // With fin0, piece 0 of a tile cut into 2..kFinishMax pieces (its
+            // first k blocks; always the CTA's last unit) stays in tensor
+            // memory: the CTA finishes that tile after the main loop.
+            PfUnit nx;
+            if (a.fin0 && un.np > 1 && un.np <= kFinishMax && un.p == 0 && !pf_unit(a, KB, ui + 1, nx)) break;
             const int m0 = (t % a.tiles_m) * BM;
             const int n0 = (t / a.tiles_m) * BN;
 #pragma unroll 1
@@ -516,43 +573,18 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                         dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
                 } else if (row < a.M) {
-                    // one branch per 32 columns into fp16-only or bf16-only code
-                    auto store = [&](auto bf16c) {
-                        constexpr bool BF = decltype(bf16c)::value;
-                        const float rs = BF && a.rowscale ? a.rowscale[row] : 1.f;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int n = n0 + c0 + 8 * v;
-                            if (n < a.N) {
-                                uint32_t pk[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    pk[e] = out_pair_t<BF>(__uint_as_float(r[8 * v + 2 * e]),
-                                                           __uint_as_float(r[8 * v + 2 * e + 1]), rs, a.bias, n + 2 * e);
-                                *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row) * a.N + n) =
-                                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            }
-                        }
-                    };
-                    if (a.out_bf16 == kOutF32) {
-                        // raw fp32 sums, 32 bytes per 8 columns
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int n = n0 + c0 + 8 * v;
-                            if (n < a.N) {
-                                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) +
-                                                                         static_cast<size_t>(row) * a.N + n);
-                                dst[0] = make_float4(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1]),
-                                                     __uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                                dst[1] = make_float4(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]),
-                                                     __uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                            }
-                        }
-                    } else if (a.out_bf16) store(std::true_type{});
-                    else store(std::false_type{});
+                    store_row32(a, row, n0 + c0, r);
                 }
             }
             tc_fence_before();
+            if (un.np > 1) {
+                // this piece's partial is written: count it for the CTAs that
+                // finish the tile
+                __threadfence();
+                __syncwarp();
+                bar_and(2, 32 * kEpiWarps, true);
+                if (quad == 0 && lane == 0) atomicAdd(a.tickets + t, 1);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(accE(acc));
         }
@@ -560,30 +592,89 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-
     if (a.sk) {
-        // Stream-K fixup, after the main loop so that no CTA waits before it
-        // has written all of its pieces (only a range's first and last unit
-        // can be a piece of a shared tile).  Every piece is in the workspace;
-        // each CTA first announces its pieces, then, per piece, waits (bounded:
-        // the cooperative launch keeps every CTA resident) for the tile's
-        // other pieces and finishes rows [p BM / np, (p + 1) BM / np) of the
-        // tile, summing the pieces in order, adding bias, rounding once.
-        __threadfence();
-        __syncthreads();
-        PfUnit un;
-        if (threadIdx.x == 0)
-            for (int ui = 0; pf_unit(a, KB, ui, un); ++ui)
-                if (un.np > 1) atomicAdd(a.tickets + un.t, 1);
-        __shared__ int s_ready;
+        // Stream-K.  Every piece of a tile cut into pieces is counted in the
+        // tile's ticket by its own CTA's epilogue as soon as it is written,
+        // and no CTA waits before writing its pieces, so no wait below
+        // depends on another (bounded waits all the same; the cooperative
+        // launch keeps every CTA resident).
+        //
+        // (a) With fin0, this CTA's last unit is piece 0 of a tile cut into
+        // at most kFinishMax pieces, still in tensor memory: wait for the tile's
+        // other pieces, stage them through the idle ring memory and add them
+        // in piece order, all warps at once (warp w reads TMEM lanes
+        // 32 (w % 4) ..), then add bias and round once.
+        PfUnit un, last{};
+        int nu = 0;
+        for (; pf_unit(a, KB, nu, un); ++nu) last = un;
+        constexpr int CP = kHalves * BN / 32;          // 32-column chunks per piece, 16 KB each
+        constexpr int kStage = kBarOff / 16384;        // chunks the ring memory holds
+        const bool fin = a.fin0 != 0;
+        if (fin && nu > 0 && last.np > 1 && last.np <= kFinishMax && last.p == 0) {
+            const int t = last.t, S = last.np;
+            __shared__ int s_ready;
+            if (threadIdx.x == 0) {
+                bool ready = !aborted(abort_flag) && S - 1 <= kStage;
+                const uint64_t t0 = globaltimer();
+                while (ready && atomicAdd(a.tickets + t, 0) < S - 1) {
+                    if (aborted(abort_flag) || globaltimer() - t0 > 2000000000ull) ready = false;
+                    else __nanosleep(128);
+                }
+                __threadfence();
+                if (ready) a.tickets[t] = 0;            // every other piece has arrived: ready for the next call
+                else fail(a.status, 0x100, abort_flag);
+                s_ready = ready;
+            }
+            __syncthreads();
+            if (s_ready) {
+                tc_fence_after();
+                const int C = kStage / (S - 1);            // chunks per pass
+                const int quad = warp & 3, nw = static_cast<int>(blockDim.x) / 128;
+                const uint32_t tacc = tmem + static_cast<uint32_t>(((nu - 1) % kAccBufs) * kHalves * BN) +
+                                      (static_cast<uint32_t>(32 * quad) << 16);
+                const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
+                // piece j of tile t: float4 ((t pmax + j) CP + chunk) 1024 + (quad 8 + v) 32 + lane
+                const float4 *ws4 = reinterpret_cast<const float4 *>(a.ws) + static_cast<size_t>(t) * a.pmax * CP * 1024;
+                float4 *st4 = reinterpret_cast<float4 *>(sbase);
+                for (int c0 = 0; c0 < CP; c0 += C) {
+                    const int nc = min(C, CP - c0), per = nc * 1024;
+                    for (int i = threadIdx.x; i < (S - 1) * per; i += blockDim.x) {
+                        const int j = i / per;
+                        cp_async_16(st4 + i, ws4 + (static_cast<size_t>(j + 1) * CP + c0) * 1024 + (i - j * per));
+                    }
+                    cp_async_commit();
+                    cp_async_wait_all();
+                    __syncthreads();
+                    for (int ch = c0 + (warp >> 2); ch < c0 + nc; ch += nw) {
+                        uint32_t r[32];
+                        tmem_ld_x32(tacc + static_cast<uint32_t>(32 * ch), r);
+                        for (int j = 0; j < S - 1; ++j) {
+                            const float4 *src = st4 + j * per + ((ch - c0) * 4 + quad) * 256 + lane;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const float4 q = src[v * 32];
+                                r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) + q.x);
+                                r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + q.y);
+                                r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + q.z);
+                                r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q.w);
+                            }
+                        }
+                        const int row = m0 + 128 * ((32 * ch) / BN) + 32 * quad + lane;
+                        if (row < a.M) store_row32(a, row, n0 + (32 * ch) % BN, r);
+                    }
+                    __syncthreads();                       // before the next pass overwrites the stage
+                }
+            }
+        }
+        // (b) Otherwise (the even K split: S equal k ranges, one CTA each):
+        // once all S are counted, every piece's CTA finishes rows
+        // [p BM / S, (p + 1) BM / S) of the tile, summing the pieces in order,
+        // adding bias, rounding once; the second round of counts lets the
+        // last of the 2 S reset the ticket for the next call.
         for (int ui = 0; pf_unit(a, KB, ui, un); ++ui) {
-            if (un.np == 1) continue;
+            if (un.np == 1 || (fin && un.np <= kFinishMax)) continue;
             const int t = un.t, S = un.np, ks = un.p;
+            __shared__ int s_all;
             if (threadIdx.x == 0) {
                 bool ready = true;
                 const uint64_t t0 = globaltimer();
@@ -595,11 +686,11 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     __nanosleep(256);
                 }
                 __threadfence();
-                s_ready = ready;
+                s_all = ready;
                 if (!ready) fail(a.status, 0x100, abort_flag);
             }
             __syncthreads();
-            if (s_ready) {
+            if (s_all) {
                 const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
                 const int r0 = (BM * ks) / S, r1 = (BM * (ks + 1)) / S, rows = r1 - r0;
                 const float4 *ws4 = reinterpret_cast<const float4 *>(a.ws);
@@ -614,8 +705,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                     for (int j = 0; j < S; ++j) {
                         const size_t sl = static_cast<size_t>(t) * a.pmax + j;
-                        const float4 *src = ws4 + ((sl * (kHalves * BN / 32) + hc / 32) * 4 + q) * 8 * 32 +
-                                            ((hc % 32) / 4) * 32 + ln;
+                        const float4 *src = ws4 + ((sl * CP + hc / 32) * 4 + q) * 8 * 32 + ((hc % 32) / 4) * 32 + ln;
                         const float4 p0 = __ldcg(src), p1 = __ldcg(src + 32);
                         v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
                         v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
@@ -636,9 +726,15 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 }
             }
             __syncthreads();
-            // second arrival: the last of the 2 S resets the ticket for the next call
             if (threadIdx.x == 0 && atomicAdd(a.tickets + t, 1) == 2 * S - 1) atomicExch(a.tickets + t, 0);
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -675,7 +771,7 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
         cudaSuccess)
         return e;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
-                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, h.rowscale, h.out_bf16, p.sk, p.pmax, ws, tickets};
+                (h.N + BN - 1) / BN, h.zero_offset, h.zsplit, h.rowscale, h.out_bf16, p.sk, p.pmax, p.fin0, ws, tickets};
     const int ntiles = args.tiles_m * args.tiles_n;
     const int grid = p.sk ? p.grid : (ntiles < sm_count() ? ntiles : sm_count());
     cudaLaunchConfig_t cfg{};
@@ -732,6 +828,7 @@ PrefillPlan plan_prefill(int M, int K, int N) {
         // stream-K: 1.4x-1.9x faster on 8192 x 28672 at M <= 256, 8192 x 10240
         // and 4096 x 11008 at M = 512, the same elsewhere)
         p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(c, W / 8)));
+        p.fin0 = 1;
     }
     auto owner = [&](long long w) { return static_cast<int>(((w + 1) * p.grid - 1) / W); };
     p.pmax = 1;
