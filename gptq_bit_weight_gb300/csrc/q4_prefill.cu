@@ -114,7 +114,7 @@ struct PfCfg {
     static constexpr int kRingP = kSX * kXStage;
     static constexpr int kRingB = (kRingP + kSP * kPStage + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kRingB + kSB * kBStage;
-    static constexpr int kNumBars = 2 * kSX + 2 * kSP + 2 * kSB + 4;
+    static constexpr int kNumBars = 2 * kSX + 2 * kSP + 2 * kSB + 5;
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr int kDqWarps = BN / 16;
     // 128-row tiles: two dequant groups on alternate stages, two n16 tiles
@@ -191,9 +191,10 @@ __device__ __forceinline__ void fail(int *status, int bit, int *abort_flag) {
 }
 __device__ __forceinline__ bool aborted(int *abort_flag) { return *reinterpret_cast<volatile int *>(abort_flag) != 0; }
 
-// 32 consecutive accumulator columns of one output row, the first at column
-// n: the row scale, bias and one rounding to fp16 or bf16, or the raw fp32
-// sums; columns at or past N are skipped.
+// 32 consecutive accumulator columns of one output row (one lane's share of
+// a tensor-memory load), the first at column n: the row scale, bias and one
+// rounding to fp16 or bf16, or the raw fp32 sums; columns at or past N are
+// skipped.
 template <bool BF>
 __device__ __forceinline__ void store_row32_t(const PfArgs &a, int row, int n, const uint32_t (&r)[32]) {
     const float rs = BF && a.rowscale ? a.rowscale[row] : 1.f;
@@ -227,6 +228,65 @@ __device__ __forceinline__ void store_row32(const PfArgs &a, int row, int n, con
         store_row32_t<true>(a, row, n, r);
     } else {
         store_row32_t<false>(a, row, n, r);
+    }
+}
+// The same for a warp's 32 rows (lane = row row0 + lane) through 2 KB of the
+// warp's shared memory (16-byte slots XOR-swizzled by row pair: no bank
+// conflicts either way), so that each store instruction writes 8 rows x 64
+// contiguous bytes instead of 32 rows x 16 bytes: measured faster where many
+// warps write at once (the stream-K finish), slower for the epilogue's four.
+template <bool BF>
+__device__ __forceinline__ void store_block16_t(const PfArgs &a, int row0, int n, const uint32_t (&r)[32], uint8_t *stage,
+                                                int lane) {
+    const int row = row0 + lane;
+    const float rs = BF && a.rowscale && row < a.M ? a.rowscale[row] : 1.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = n + 8 * v + 2 * e;
+            pk[e] = c < a.N ? out_pair_t<BF>(__uint_as_float(r[8 * v + 2 * e]), __uint_as_float(r[8 * v + 2 * e + 1]), rs,
+                                             a.bias, c)
+                            : 0u;
+        }
+        *reinterpret_cast<uint4 *>(stage + lane * 64 + 16 * (v ^ ((lane >> 1) & 3))) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rr = 8 * it + (lane >> 2), sg = lane & 3;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + 16 * (sg ^ ((rr >> 1) & 3)));
+        if (row0 + rr < a.M && n + 8 * sg < a.N)
+            *reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(row0 + rr) * a.N + n + 8 * sg) = val;
+    }
+    __syncwarp();
+}
+__device__ __forceinline__ void store_block(const PfArgs &a, int row0, int n, const uint32_t (&r)[32], uint8_t *stage,
+                                            int lane) {
+    if (a.out_bf16 == kOutF32) {
+        float *out = reinterpret_cast<float *>(a.out);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {               // 16 columns (64 bytes) per round
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                *reinterpret_cast<uint4 *>(stage + lane * 64 + 16 * (v ^ ((lane >> 1) & 3))) =
+                    make_uint4(r[16 * h + 4 * v], r[16 * h + 4 * v + 1], r[16 * h + 4 * v + 2], r[16 * h + 4 * v + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int rr = 8 * it + (lane >> 2), sg = lane & 3;
+                const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + 16 * (sg ^ ((rr >> 1) & 3)));
+                const int c = n + 16 * h + 4 * sg;
+                if (row0 + rr < a.M && c < a.N)
+                    *reinterpret_cast<uint4 *>(out + static_cast<size_t>(row0 + rr) * a.N + c) = val;
+            }
+            __syncwarp();
+        }
+    } else if (a.out_bf16) {
+        store_block16_t<true>(a, row0, n, r, stage, lane);
+    } else {
+        store_block16_t<false>(a, row0, n, r, stage, lane);
     }
 }
 
@@ -266,6 +326,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
     auto emptyB = [&](int s) { return bar0 + 8u * (2 * kSX + 2 * kSP + kSB + s); };
     auto accF = [&](int i) { return bar0 + 8u * (2 * kSX + 2 * kSP + 2 * kSB + i); };
     auto accE = [&](int i) { return bar0 + 8u * (2 * kSX + 2 * kSP + 2 * kSB + 2 + i); };
+    const uint32_t stageB = bar0 + 8u * (2 * kSX + 2 * kSP + 2 * kSB + 4);   // stream-K pieces staged after the loop
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + kBarOff + kNumBars * 8);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -290,6 +351,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             mbar_init(accF(i), 1);
             mbar_init(accE(i), kEpiWarps);
         }
+        mbar_init(stageB, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -592,26 +654,31 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (a.sk) {
-        // Stream-K.  Every piece of a tile cut into pieces is counted in the
-        // tile's ticket by its own CTA's epilogue as soon as it is written,
-        // and no CTA waits before writing its pieces, so no wait below
-        // depends on another (bounded waits all the same; the cooperative
-        // launch keeps every CTA resident).
-        //
-        // (a) With fin0, this CTA's last unit is piece 0 of a tile cut into
-        // at most kFinishMax pieces, still in tensor memory: wait for the tile's
-        // other pieces, stage them through the idle ring memory and add them
-        // in piece order, all warps at once (warp w reads TMEM lanes
-        // 32 (w % 4) ..), then add bias and round once.
-        PfUnit un, last{};
+    // Stream-K.  Every piece of a tile cut into pieces is counted in the
+    // tile's ticket as soon as its CTA's epilogue has written it, and no CTA
+    // waits before writing its pieces, so no wait below depends on another
+    // (bounded waits all the same; the cooperative launch keeps every CTA
+    // resident).
+    //
+    // (a) With fin0, when this CTA's last unit is piece 0 of a tile cut into
+    // at most kFinishMax pieces (still in tensor memory): wait for the tile's
+    // other pieces, stage them through the idle ring memory (one bulk copy
+    // per piece and pass) and add them in piece order, all warps at once
+    // (warp w reads TMEM lanes 32 (w % 4) ..), then add bias and round once.
+    constexpr int CP = kHalves * BN / 32;              // 32-column chunks of a tile, 16 KB of fp32 each
+    constexpr int kStage = kBarOff / 16384;            // chunks the ring memory holds
+    const bool fin = a.sk && a.fin0 != 0;
+    PfUnit un;
+    if (fin) {
+        PfUnit last{};
         int nu = 0;
         for (; pf_unit(a, KB, nu, un); ++nu) last = un;
-        constexpr int CP = kHalves * BN / 32;          // 32-column chunks per piece, 16 KB each
-        constexpr int kStage = kBarOff / 16384;        // chunks the ring memory holds
-        const bool fin = a.fin0 != 0;
-        if (fin && nu > 0 && last.np > 1 && last.np <= kFinishMax && last.p == 0) {
-            const int t = last.t, S = last.np;
+        if (nu > 0 && last.np > 1 && last.np <= kFinishMax && last.p == 0) {
+            const int t = last.t, quad = warp & 3, nw = static_cast<int>(blockDim.x) / 128;
+            const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
+            const uint32_t tacc = tmem + static_cast<uint32_t>(((nu - 1) % kAccBufs) * kHalves * BN) +
+                                  (static_cast<uint32_t>(32 * quad) << 16);
+            const int S = last.np;
             __shared__ int s_ready;
             if (threadIdx.x == 0) {
                 bool ready = !aborted(abort_flag) && S - 1 <= kStage;
@@ -629,22 +696,26 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
             if (s_ready) {
                 tc_fence_after();
                 const int C = kStage / (S - 1);            // chunks per pass
-                const int quad = warp & 3, nw = static_cast<int>(blockDim.x) / 128;
-                const uint32_t tacc = tmem + static_cast<uint32_t>(((nu - 1) % kAccBufs) * kHalves * BN) +
-                                      (static_cast<uint32_t>(32 * quad) << 16);
-                const int m0 = (t % a.tiles_m) * BM, n0 = (t / a.tiles_m) * BN;
                 // piece j of tile t: float4 ((t pmax + j) CP + chunk) 1024 + (quad 8 + v) 32 + lane
                 const float4 *ws4 = reinterpret_cast<const float4 *>(a.ws) + static_cast<size_t>(t) * a.pmax * CP * 1024;
                 float4 *st4 = reinterpret_cast<float4 *>(sbase);
-                for (int c0 = 0; c0 < CP; c0 += C) {
+                for (int c0 = 0, pass = 0; c0 < CP; c0 += C, ++pass) {
                     const int nc = min(C, CP - c0), per = nc * 1024;
-                    for (int i = threadIdx.x; i < (S - 1) * per; i += blockDim.x) {
-                        const int j = i / per;
-                        cp_async_16(st4 + i, ws4 + (static_cast<size_t>(j + 1) * CP + c0) * 1024 + (i - j * per));
+                    // one bulk copy per piece (its chunks [c0, c0 + nc) are contiguous),
+                    // after every thread's last reads of this memory (barrier above);
+                    // the pieces were published by other CTAs' plain stores
+                    if (threadIdx.x == 0) {
+                        asm volatile("fence.proxy.async.global;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+                        mbar_arrive_expect_tx(stageB, static_cast<uint32_t>((S - 1) * nc) * 16384u);
+                        for (int j = 0; j < S - 1; ++j)
+                            bulk_load(base + static_cast<uint32_t>(j * per) * 16u,
+                                      ws4 + (static_cast<size_t>(j + 1) * CP + c0) * 1024, static_cast<uint32_t>(nc) * 16384u,
+                                      stageB);
                     }
-                    cp_async_commit();
-                    cp_async_wait_all();
-                    __syncthreads();
+                    if (!__syncthreads_and(mbar_wait(stageB, pass & 1))) {
+                        if (threadIdx.x == 0) fail(a.status, 0x100, abort_flag);
+                        break;
+                    }
                     for (int ch = c0 + (warp >> 2); ch < c0 + nc; ch += nw) {
                         uint32_t r[32];
                         tmem_ld_x32(tacc + static_cast<uint32_t>(32 * ch), r);
@@ -659,13 +730,19 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                                 r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q.w);
                             }
                         }
-                        const int row = m0 + 128 * ((32 * ch) / BN) + 32 * quad + lane;
-                        if (row < a.M) store_row32(a, row, n0 + (32 * ch) % BN, r);
+                        // this warp's slice of the first staged piece, read only by this warp
+                        __syncwarp();
+                        const int row0 = m0 + 128 * ((32 * ch) / BN) + 32 * quad;
+                        if (row0 < a.M)
+                            store_block(a, row0, n0 + (32 * ch) % BN, r,
+                                        reinterpret_cast<uint8_t *>(st4 + ((ch - c0) * 4 + quad) * 256), lane);
                     }
                     __syncthreads();                       // before the next pass overwrites the stage
                 }
             }
         }
+    }
+    if (a.sk) {
         // (b) Otherwise (the even K split: S equal k ranges, one CTA each):
         // once all S are counted, every piece's CTA finishes rows
         // [p BM / S, (p + 1) BM / S) of the tile, summing the pieces in order,
