@@ -909,6 +909,21 @@ int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream
     return ok();
 }
 
+int gptq_q4_debug_prefill_plan(int M, int K, int N, int sms, int *out) {
+    if (!out) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "out must not be NULL");
+    if (M < 1 || K <= 0 || N <= 0 || K % 64 || N % 64 || sms < 1)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "M=%d K=%d N=%d sms=%d: need M >= 1, K and N positive multiples of 64, sms >= 1",
+                          M, K, N, sms);
+    const q4::PrefillPlan p = q4::plan_prefill(M, K, N, sms);
+    out[0] = p.bm;
+    out[1] = p.bn;
+    out[2] = p.sk;
+    out[3] = p.sk ? p.grid : 0;
+    out[4] = p.sk ? p.pmax : 1;
+    out[5] = p.fin0;
+    return ok();
+}
+
 int gptq_q4_set_act_dtype(gptq_q4_handle h, int dtype) {
     if (!h) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "handle is NULL");
     if (dtype != GPTQ_Q4_DTYPE_FP16 && dtype != GPTQ_Q4_DTYPE_BF16 && dtype != GPTQ_Q4_DTYPE_FP32)

@@ -332,7 +332,8 @@ struct PrefillPlan {
     size_t ws_floats;  // fp32 partial tiles when tiles are cut into pieces
     int n_tickets;     // one per tile when tiles are cut into pieces
 };
-PrefillPlan plan_prefill(int M, int K, int N);
+// sms: SMs to plan for (0: this device's)
+PrefillPlan plan_prefill(int M, int K, int N, int sms = 0);
 cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets, const uint16_t *x,
                            int M, uint16_t *out, cudaStream_t s);
 // float weights + scales + zero points -> GPTQ checkpoint words (q4_pack.cu)

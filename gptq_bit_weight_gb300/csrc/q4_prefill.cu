@@ -877,9 +877,9 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
 //     tiles x k-blocks space, tiles cut into pieces at the range ends and
 //     summed after the main loop.  256-row tiles let one dequantized B tile
 //     feed two M = 128 MMAs; up to 128 rows take 128 x 256 tiles instead.
-PrefillPlan plan_prefill(int M, int K, int N) {
+PrefillPlan plan_prefill(int M, int K, int N, int sms) {
     PrefillPlan p{};
-    const long long c = sm_count();
+    const long long c = sms > 0 ? sms : sm_count();
     const long long n256 = (N + 255) / 256;
     const long long t256x256 = static_cast<long long>((M + 255) / 256) * n256;
     const int KB = K / BK;

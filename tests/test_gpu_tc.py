@@ -136,3 +136,40 @@ def test_prefill_wide_tiles_sampled(q4, K, N, gs, act, M):
     torch.cuda.synchronize()
     check(y[rows], y_ref, tol, f"fused wide tiles K={K} N={N} g={gs} act={act} M={M}")
     mat.device_error()
+
+
+def test_prefill_stream_k_finish_matches_oracle(q4):
+    """Stream-K ranges with tiles cut into two or three pieces, finished by
+    the CTA holding each tile's piece 0 (from tensor memory, the other pieces
+    staged into its ring memory): 80 column tiles of 256 on the GPU's SMs
+    (fewer than two SMs per tile), a ragged last tile, bias, act-order, and
+    fp16, bf16 (rows outside fp16's range) and fp32 activations, at 128- and
+    256-row tiles."""
+    K, N, gs = 1024, 20416, 128
+    layer = synthetic.make_layer(K, N, gs, act_order=True, bias=True, key=(41, K, N))
+    dq = oracle.dequantize_layer(layer.qweight, layer.qzeros, layer.scales, layer.g_idx, K, N, gs)
+    mat = q4.Q4Matrix(to_dev(layer.qweight), to_dev(layer.qzeros), to_dev(layer.scales), to_dev(layer.g_idx),
+                      to_dev(layer.bias), gs)
+    mat.set_path(q4.GPTQ_Q4_PATH_PREFILL)
+    scales = [1.0, 1e6, 1e-6, 3e4]
+    for M in (40, 200, 300):
+        x = synthetic.activations(M, K, key=(41, M))
+        y_ref = oracle.reference_output(x, dq, layer.bias)
+        y = mat(to_dev(x))
+        torch.cuda.synchronize()
+        check(y, y_ref, oracle.tolerance(x, dq.w16, y_ref, K), f"fp16 M={M}")
+        rs = [scales[m % 4] for m in range(M)]
+        mat.set_act_dtype(torch.bfloat16)
+        xb = synthetic.activations_bf16(M, K, key=(42, M), row_scales=rs)
+        yb = mat(torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(DEV).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        yb_ref = oracle.reference_output_bf16(xb, dq, layer.bias)
+        check(yb, yb_ref, oracle.tolerance_rows_bf16(xb, dq.w16, yb_ref, K), f"bf16 M={M}")
+        mat.set_act_dtype(torch.float32)
+        xf = synthetic.activations_f32(M, K, key=(43, M), row_scales=rs)
+        yf = mat(torch.from_numpy(np.ascontiguousarray(xf).view(np.float32)).to(DEV))
+        torch.cuda.synchronize()
+        yf_ref = oracle.reference_output_f32(xf, dq, layer.bias)
+        check(yf, yf_ref, oracle.tolerance_rows_f32(xf, dq.w16, yf_ref, K), f"fp32 M={M}")
+        mat.set_act_dtype(torch.float16)
+    mat.device_error()
