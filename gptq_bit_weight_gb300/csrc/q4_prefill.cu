@@ -8,9 +8,12 @@
 //
 // Persistent kernel, one CTA per SM.  Work: BM x BN output tiles taken round
 // robin (m fastest, so the CTAs working at the same time share weight tiles
-// in L2) when there are enough of them; otherwise stream-K, every CTA one
-// contiguous range of the tiles x k-blocks space, the tiles cut at range
-// ends summed after the main loop (cooperative launch, bounded waits).
+// in L2) when there are enough of them; otherwise stream-K (cooperative
+// launch, bounded waits): every tile cut into equal k ranges, one CTA each,
+// whose CTAs each finish a share of its rows after the main loop; or every
+// CTA one contiguous range of the tiles x k-blocks space, each tile cut at
+// range ends finished by the CTA holding its first k blocks, which keeps
+// them in tensor memory and adds the other pieces after its main loop.
 // Roles, for BN = 256 (BM = 128 or 256):
 //
 //   warp 0       one thread: TMA loads of the packed-word stages (8 KB of
