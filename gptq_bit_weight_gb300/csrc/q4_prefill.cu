@@ -84,8 +84,9 @@ constexpr int kEpiWarps = 4;
 // Stream-K pieces.  With one range per CTA over the tiles x k-blocks space,
 // a tile is cut into at most three pieces, and all but piece 0 (the tile's
 // first k blocks, the last unit of its CTA's range) are the first units of
-// their CTAs' ranges, written early in the main loop: the CTA holding piece 0
-// keeps it in tensor memory and finishes the tile, adding the others
+// their CTAs' ranges, written as soon as they are done (mid-loop unless the
+// range ends inside the same tile): the CTA holding piece 0 keeps it in
+// tensor memory and finishes the tile, adding the others
 // (8192 x 28672 at M = 256-512, 4096 x 11008 and 8192 x 10240 at M = 1024:
 // 5-12 % faster than every piece's CTA summing a share of the rows).  With
 // the even K split every piece ends at the same time, one reader per tile is
