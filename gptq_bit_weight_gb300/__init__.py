@@ -47,7 +47,7 @@ EXPORTED = [
     "gptq_q4_debug_unpack", "gptq_q4_matmul_unfused", "gptq_q4_gemm_f16", "gptq_q4_set_path",
     "gptq_q4_set_prefill_min_m", "gptq_q4_info", "gptq_q4_device_error", "gptq_q4_free",
     "gptq_q4_last_status", "gptq_q4_last_error", "gptq_q4_launch_count", "gptq_q4_matmul_noalloc",
-    "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_debug_prefill_plan", "gptq_q4_make_fused", "gptq_q4_pack",
+    "gptq_q4_set_format", "gptq_q4_debug_wait_probe", "gptq_q4_debug_prefill_plan", "gptq_q4_debug_dispatch", "gptq_q4_make_fused", "gptq_q4_pack",
     "gptq_q4_make8", "gptq_q4_set_act_dtype",
 ]
 
@@ -79,6 +79,7 @@ _sig("gptq_q4_make_fused", _P, _I, _P, _P, _P, _P, _I, _P, _I)
 _sig("gptq_q4_pack", _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P)
 _sig("gptq_q4_debug_wait_probe", _I, _P, ctypes.c_uint, _P)
 _sig("gptq_q4_debug_prefill_plan", _I, _I, _I, _I, _I, _P)
+_sig("gptq_q4_debug_dispatch", _I, _I, _I, _I, _I, _I, _I, _P)
 _sig("gptq_q4_info", _I, _P, _P, _P, _P, _P, _P, _P)
 _sig("gptq_q4_device_error", _I, _P)
 _sig("gptq_q4_free", None, _P)
@@ -204,6 +205,15 @@ def gptq_q4_set_act_dtype(h: int, dtype: int) -> int:
 
 def gptq_q4_debug_wait_probe(status: int, limit_us: int, stream: int) -> int:
     return _check(_lib.gptq_q4_debug_wait_probe(status, limit_us, stream or None))
+
+
+KERNELS = ("prefill", "decode_reg", "decode_stream", "decode_ring", "decode_tc")
+
+
+def gptq_q4_debug_dispatch(M: int, K: int, N: int, groupsize: int, path: int, sms: int) -> str:
+    k = ctypes.c_int()
+    _check(_lib.gptq_q4_debug_dispatch(M, K, N, groupsize, path, sms, ctypes.byref(k)))
+    return KERNELS[k.value]
 
 
 def gptq_q4_debug_prefill_plan(M: int, K: int, N: int, sms: int) -> dict:

@@ -636,44 +636,61 @@ int gptq_q4_reserve(gptq_q4_handle h, int max_m) {
     return ok();
 }
 
+// The kernels a call can run.
+enum class Kern { Prefill = 0, Reg = 1, Stream = 2, Ring = 3, Tc = 4 };
+
+// Which kernel run_path launches for `path` on M rows (host logic only):
+// the requested kernel where its planner accepts the shape, else the
+// register-streaming decode.  tc_ok: fp16 output and GPTQ zero points, the
+// tcgen05 decode's only case.  The plan of the chosen stream-K or TMA-ring
+// kernel is returned through sk / rp.
+static Kern kernel_for(int path, int M, int K, int N, int geff, bool tc_ok, bool small_layer, int sms,
+                       q4::DecodeSkPlan *sk, q4::DecodeRingPlan *rp) {
+    if (path == GPTQ_Q4_PATH_PREFILL) return Kern::Prefill;
+    if (path == GPTQ_Q4_PATH_DECODE_TC && tc_ok && q4::decode_tc_supported(M, K, N, geff)) return Kern::Tc;
+    if (path == GPTQ_Q4_PATH_DECODE_STREAM && M <= 8) {
+        *sk = q4::plan_decode_sk(M, K, N, sms);
+        if (sk->ok) return Kern::Stream;
+    }
+    if ((path == GPTQ_Q4_PATH_DECODE && !small_layer) || path == GPTQ_Q4_PATH_DECODE_RING) {
+        *rp = q4::plan_decode_ring(M, K, N, geff, sms);
+        if (rp->ok) return Kern::Ring;
+    }
+    return Kern::Reg;
+}
+
 // One of the kernels on prepared fp16 rows xin [M][K] (K the private
 // layout's rows), epilogue as v says.
 static int run_path(gptq_q4_handle h, const q4::HandleView &v, const uint16_t *xin, int M, uint16_t *out,
                     cudaStream_t stream, int path, bool small_layer) {
-    if (path == GPTQ_Q4_PATH_PREFILL) {
-        const q4::PrefillPlan pp = q4::plan_prefill(M, h->K, h->N);
-        if (int r = ensure_decode_work(h, pp.ws_floats, pp.n_tickets, stream, false)) return r;
-        Q4_CUDA(q4::launch_prefill(v, pp, h->ws, h->tickets, xin, M, out, stream), "prefill launch");
-        ++g_launches;
-        return ok();
-    }
-    if (path == GPTQ_Q4_PATH_DECODE_TC && h->zsplit == 0 && v.out_bf16 == q4::kOutF16 &&
-        q4::decode_tc_supported(M, h->K, h->N, h->geff)) {
-        Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
-        ++g_launches;
-        return ok();
-    }
-    if (path == GPTQ_Q4_PATH_DECODE_STREAM && M <= 8) {
-        const q4::DecodeSkPlan sp = q4::plan_decode_sk(M, h->K, h->N, q4::device_sm_count());
-        if (sp.ok) {
+    q4::DecodeSkPlan sp{};
+    q4::DecodeRingPlan rp{};
+    const bool tc_ok = h->zsplit == 0 && v.out_bf16 == q4::kOutF16;
+    switch (kernel_for(path, M, h->K, h->N, h->geff, tc_ok, small_layer, q4::device_sm_count(), &sp, &rp)) {
+        case Kern::Prefill: {
+            const q4::PrefillPlan pp = q4::plan_prefill(M, h->K, h->N);
+            if (int r = ensure_decode_work(h, pp.ws_floats, pp.n_tickets, stream, false)) return r;
+            Q4_CUDA(q4::launch_prefill(v, pp, h->ws, h->tickets, xin, M, out, stream), "prefill launch");
+            break;
+        }
+        case Kern::Tc:
+            Q4_CUDA(q4::launch_decode_tc(v, xin, M, out, stream), "decode launch");
+            break;
+        case Kern::Stream:
             if (int r = ensure_decode_work(h, sp.ws_floats, sp.n_tickets, stream, false)) return r;
             Q4_CUDA(q4::launch_decode_sk(v, sp, h->ws, h->tickets, xin, M, out, stream), "decode launch");
-            ++g_launches;
-            return ok();
-        }
-    }
-    if ((path == GPTQ_Q4_PATH_DECODE && !small_layer) || path == GPTQ_Q4_PATH_DECODE_RING) {
-        const q4::DecodeRingPlan rp = q4::plan_decode_ring(M, h->K, h->N, h->geff, q4::device_sm_count());
-        if (rp.ok) {
+            break;
+        case Kern::Ring:
             Q4_CUDA(q4::launch_decode_ring(v, rp, xin, M, out, stream), "decode launch");
-            ++g_launches;
-            return ok();
+            break;
+        case Kern::Reg: {
+            const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N, h->geff);
+            if (int r = ensure_decode_work(h, p.ws_floats, p.n_tickets, stream, false)) return r;
+            q4::DecodeWork w{h->ws, h->ws_floats, h->tickets, h->n_tickets};
+            Q4_CUDA(q4::launch_decode(v, p, w, xin, M, out, stream), "decode launch");
+            break;
         }
     }
-    const q4::DecodePlan p = q4::plan_decode(M, h->K, h->N, h->geff);
-    if (int r = ensure_decode_work(h, p.ws_floats, p.n_tickets, stream, false)) return r;
-    q4::DecodeWork w{h->ws, h->ws_floats, h->tickets, h->n_tickets};
-    Q4_CUDA(q4::launch_decode(v, p, w, xin, M, out, stream), "decode launch");
     ++g_launches;
     return ok();
 }
@@ -687,31 +704,33 @@ static int run_path(gptq_q4_handle h, const q4::HandleView &v, const uint16_t *x
 // other kernels leave SMs short of warps: at one row with groups of at most
 // 128 rows, at two rows with 32-row groups, and at 3-8 rows with groups of
 // 128 rows or more (28672 x 8192 g128 M = 8: 42.1 against 45.8 us).
-static bool prefer_stream(const gptq_q4_s *h, int M) {
-    const long long tiles = h->N / 32, sms = q4::device_sm_count();
-    const bool tall = h->K >= 2LL * h->N && tiles < 2 * sms &&
-                      static_cast<size_t>(h->K) * h->N >= (size_t{100} << 20);
+static bool prefer_stream(int K, int N, int geff, int M, int sms) {
+    const long long tiles = N / 32;
+    const bool tall = K >= 2LL * N && tiles < 2LL * sms && static_cast<size_t>(K) * N >= (size_t{100} << 20);
     if (!tall || M > 8) return false;
-    if (M == 1) return h->geff <= 128;
-    if (M == 2) return h->geff <= 32;
-    return h->geff >= 128;
+    if (M == 1) return geff <= 128;
+    if (M == 2) return geff <= 32;
+    return geff >= 128;
+}
+
+// Which decode kernel: measured on GB300 (CUDA-graph replays over more
+// weights than L2), the register-streaming kernel (with its shared weight
+// ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on layers
+// below 64 Mi weights or with groups of at most 64 rows (8192 x 28672 g32
+// M = 8: 45.0 against 89.3 us) and at any M on layers below 24 Mi weights;
+// the TMA-ring kernel is ahead everywhere else it applies.
+static bool small_layer_for(int K, int N, int geff, int M) {
+    const size_t weights = static_cast<size_t>(K) * N;
+    return M <= 4 || weights < (size_t{24} << 20) || (M <= 8 && (weights < (size_t{64} << 20) || geff <= 64));
 }
 
 static int run_matmul(gptq_q4_handle h, const void *x, int M, void *out, cudaStream_t stream, int path) {
     // fp32 activations: the kernels see 2M fp16 rows (each row's hi and lo
     // parts) and write raw fp32 sums; a last pass adds each row's two parts
     const int Mk = h->act_f32 ? 2 * M : M;
-    if (path == GPTQ_Q4_PATH_DECODE && prefer_stream(h, Mk)) path = GPTQ_Q4_PATH_DECODE_STREAM;
-    // Which decode kernel: measured on GB300 (CUDA-graph replays over more
-    // weights than L2), the register-streaming kernel (with its shared
-    // weight ring at M <= 8) is ahead at M <= 4 on every layer, at M <= 8 on
-    // layers below 64 Mi weights or with groups of at most 64 rows
-    // (8192 x 28672 g32 M = 8: 45.0 against 89.3 us) and at any M on layers
-    // below 24 Mi weights; the TMA-ring kernel is ahead everywhere else it
-    // applies.
-    const size_t weights = static_cast<size_t>(h->K) * h->N;
-    const bool small_layer = Mk <= 4 || weights < (size_t{24} << 20) ||
-                             (Mk <= 8 && (weights < (size_t{64} << 20) || h->geff <= 64));
+    if (path == GPTQ_Q4_PATH_DECODE && prefer_stream(h->K, h->N, h->geff, Mk, q4::device_sm_count()))
+        path = GPTQ_Q4_PATH_DECODE_STREAM;
+    const bool small_layer = small_layer_for(h->K, h->N, h->geff, Mk);
     // the activation kernel lets the decode grid start early when that grid
     // is the register-streaming kernel at M <= 8, or the stream-K kernel at
     // one row (28672x8192 act-order M = 1: 39.0 -> 37.0 us; measured slower
@@ -906,6 +925,25 @@ int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream
         return set_status(GPTQ_Q4_INVALID_ARGUMENT, "limit_us=%u outside [1, 2000000]", limit_us);
     Q4_CUDA(q4::launch_wait_probe(status, static_cast<uint64_t>(limit_us) * 1000ull, stream), "wait probe launch");
     ++g_launches;
+    return ok();
+}
+
+int gptq_q4_debug_dispatch(int M, int K, int N, int groupsize, int path, int sms, int *kernel) {
+    if (!kernel) return set_status(GPTQ_Q4_INVALID_ARGUMENT, "kernel must not be NULL");
+    const int geff = groupsize == -1 ? K : groupsize;
+    if (M < 1 || K <= 0 || N <= 0 || K % 64 || N % 64 || sms < 1 || geff <= 0 || geff % 32 || K % geff)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT,
+                          "M=%d K=%d N=%d groupsize=%d sms=%d: need M >= 1, K and N positive multiples of 64, a "
+                          "group size that is -1 or a multiple of 32 dividing K, sms >= 1",
+                          M, K, N, groupsize, sms);
+    if (path < GPTQ_Q4_PATH_AUTO || path > GPTQ_Q4_PATH_DECODE_STREAM)
+        return set_status(GPTQ_Q4_INVALID_ARGUMENT, "path=%d is not a GPTQ_Q4_PATH_* value", path);
+    if (path == GPTQ_Q4_PATH_AUTO)
+        path = M >= q4::prefill_default_min_m(K, N, geff) ? GPTQ_Q4_PATH_PREFILL : GPTQ_Q4_PATH_DECODE;
+    if (path == GPTQ_Q4_PATH_DECODE && prefer_stream(K, N, geff, M, sms)) path = GPTQ_Q4_PATH_DECODE_STREAM;
+    q4::DecodeSkPlan sp{};
+    q4::DecodeRingPlan rp{};
+    *kernel = static_cast<int>(kernel_for(path, M, K, N, geff, true, small_layer_for(K, N, geff, M), sms, &sp, &rp));
     return ok();
 }
 

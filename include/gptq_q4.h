@@ -304,6 +304,17 @@ int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream
  * (NULL out, M < 1, K or N not a positive multiple of 64, sms < 1). */
 int gptq_q4_debug_prefill_plan(int M, int K, int N, int sms, int *out);
 
+/* Test hook, host only (no device call): the kernel that gptq_q4_matmul runs
+ * for M fp16 rows on a K x N layer with this group size (-1: one group; no
+ * padding, GPTQ zero points), with `path` as the handle's
+ * GPTQ_Q4_PATH_* setting (AUTO resolved by the default prefill threshold)
+ * on a GPU with `sms` SMs.  *kernel (caller-owned host int) = 0 the fused
+ * prefill, 1 the register-streaming decode, 2 the stream-K decode, 3 the
+ * TMA-ring decode, 4 the tcgen05 decode.  Errors: INVALID_ARGUMENT (NULL
+ * kernel, M < 1, K or N not a positive multiple of 64, a group size that is
+ * not -1 or a multiple of 32 dividing K, sms < 1, an unknown path). */
+int gptq_q4_debug_dispatch(int M, int K, int N, int groupsize, int path, int sms, int *kernel);
+
 /* Projection fusion ("Inference Backends", "How AUTO selection works":
  * post-quantization QKV or gate/up projections that read the same input are
  * combined into one call).  One handle over `parts` GPTQ layers that share
