@@ -217,10 +217,10 @@ def gptq_q4_debug_dispatch(M: int, K: int, N: int, groupsize: int, path: int, sm
 
 
 def gptq_q4_debug_prefill_plan(M: int, K: int, N: int, sms: int) -> dict:
-    out = (ctypes.c_int * 6)()
+    out = (ctypes.c_int * 7)()
     _check(_lib.gptq_q4_debug_prefill_plan(M, K, N, sms, out))
     return {"bm": out[0], "bn": out[1], "stream_k": out[2], "grid": out[3], "max_pieces": out[4],
-            "piece0_finishes": out[5]}
+            "piece0_finishes": out[5], "stage_rows": out[6]}
 
 
 def gptq_q4_info(h: int) -> dict:

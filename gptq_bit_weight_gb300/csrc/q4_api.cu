@@ -959,6 +959,7 @@ int gptq_q4_debug_prefill_plan(int M, int K, int N, int sms, int *out) {
     out[3] = p.sk ? p.grid : 0;
     out[4] = p.sk ? p.pmax : 1;
     out[5] = p.fin0;
+    out[6] = p.bk;
     return ok();
 }
 

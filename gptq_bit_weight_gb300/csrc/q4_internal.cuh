@@ -325,6 +325,7 @@ bool pdl_enabled();
 // fused prefill (q4_prefill.cu): tile shape, K split and split workspace
 struct PrefillPlan {
     int bm, bn;        // tile
+    int bk;            // rows of K per pipeline stage (64, or 128 for M <= 64)
     int sk;            // 1: stream-K over the tiles x k-blocks space (cooperative launch)
     int grid;          // stream-K: CTAs
     int pmax;          // stream-K: most pieces of one tile

@@ -40,6 +40,10 @@
 //                the accumulator back, so the epilogue of one tile overlaps
 //                the main loop of the next.
 //
+// Up to 64 rows of x a stage is 128 rows of K instead of 64 (two 64-row
+// chunks; x tiles of 64 rows, whose shared memory pays for the 64 KB B
+// stages), and every dequantizer takes one n16 tile of both chunks.
+//
 // Every mbarrier wait is bounded (~2 s); a wait that runs out records an
 // error bit in the handle's status word, the CTA lets its copies land, frees
 // its TMEM and returns.
@@ -69,6 +73,10 @@
 #ifndef Q4_PF_SP
 #define Q4_PF_SP 4
 #endif
+// most rows of x for which 128-row stages are used
+#ifndef Q4_PF_BK128_MAXM
+#define Q4_PF_BK128_MAXM 64
+#endif
 
 namespace q4 {
 
@@ -79,7 +87,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int BK = 64;
 constexpr int kEpiWarps = 4;
 // Stream-K pieces.  With one range per CTA over the tiles x k-blocks space,
 // a tile is cut into at most three pieces, and all but piece 0 (the tile's
@@ -101,20 +108,27 @@ constexpr int kFinishMax = 3;
 // Three rings: x tiles (BM x 64 fp16, 128-byte swizzle), packed-word stages
 // {packed words BN*32 B, scale pairs of up to two groups (BN*2 B each), their
 // zero words (BN/2 B each)}, and fp16 B tiles (K-major, 128-byte swizzle).
-template <int BM_, int BN_>
+template <int BM_, int BN_, int BK_ = 64>
 struct PfCfg {
-    static constexpr int BM = BM_, BN = BN_;
+    static constexpr int BM = BM_, BN = BN_, BK = BK_;
+    static_assert(BK == 64 || (BK == 128 && BM == 128), "128-row stages: 128-row tiles only");
+    static constexpr int kKC = BK / 64;                // 64-row chunks per stage
+    static constexpr int kBlk = BK / 32;               // 32-row blocks per stage
+    // 128-row stages serve M <= 64: x tiles of 64 rows (the MMA's rows 64..127
+    // read whatever follows in shared memory and are never stored)
+    static constexpr int kXRows = BK == 128 ? 64 : BM;
     static constexpr int kHalves = BM / 128;           // M = 128 MMAs per k step
     static constexpr int kAccBufs = BM == 128 ? 2 : 1; // accumulator sets (double-buffered when they fit)
-    static constexpr int kSX = BM == 128 ? Q4_PF_SX128 : Q4_PF_SX256;   // x-tile ring (released by the MMAs)
-    static constexpr int kSP = Q4_PF_SP;               // packed-word ring (released by the dequantizers)
-    static constexpr int kSB = BM == 128 ? Q4_PF_SB128 : Q4_PF_SB256;   // fp16 B ring
-    static constexpr int kXStage = BM * BK * 2;
+    static constexpr int kSX = BK == 128 ? 3 : (BM == 128 ? Q4_PF_SX128 : Q4_PF_SX256);   // x-tile ring (released by the MMAs)
+    static constexpr int kSP = BK == 128 ? 2 : Q4_PF_SP;   // packed-word ring (released by the dequantizers)
+    static constexpr int kSB = BK == 128 ? 2 : (BM == 128 ? Q4_PF_SB128 : Q4_PF_SB256);   // fp16 B ring
+    static constexpr int kXStage = kXRows * BK * 2;    // kKC sub-tiles of kXRows x 64
+    static constexpr int kMaxG = kBlk;                 // groups a stage can touch (a group is whole blocks)
     static constexpr int kSGroup = BN * 2, kZGroup = BN / 2;
-    static constexpr int kSzOff = BN * 32;             // within a packed stage
-    static constexpr int kZOff = 2 * kSGroup;          // zero words after both groups' scales
-    static constexpr int kPStage = (kSzOff + 2 * kSGroup + 2 * kZGroup + 127) / 128 * 128;
-    static constexpr int kBStage = BN * BK * 2;
+    static constexpr int kSzOff = BN * 32 * kKC;       // within a packed stage
+    static constexpr int kZOff = kMaxG * kSGroup;      // zero words after all groups' scales
+    static constexpr int kPStage = (kSzOff + kMaxG * (kSGroup + kZGroup) + 127) / 128 * 128;
+    static constexpr int kBStage = BN * BK * 2;        // kKC sub-tiles of BN x 64
     static constexpr int kRingP = kSX * kXStage;
     static constexpr int kRingB = (kRingP + kSP * kPStage + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kRingB + kSB * kBStage;
@@ -122,8 +136,10 @@ struct PfCfg {
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr int kDqWarps = BN / 16;
     // 128-row tiles: two dequant groups on alternate stages, two n16 tiles
-    // per warp (measured 5-7 % faster there, 3 % slower with 256-row tiles)
-    static constexpr int kDqGroups = BM == 128 ? 2 : 1;
+    // per warp (measured 5-7 % faster there, 3 % slower with 256-row tiles);
+    // 128-row stages: every warp one n16 tile of every stage, both chunks
+    static constexpr int kDqGroups = BM == 128 && BK == 64 ? 2 : 1;
+    static constexpr int kUnits = BK == 128 ? 2 : kDqGroups;   // (n16 tile, chunk) pairs per warp and stage
     static constexpr int kDqHalf = kDqWarps / kDqGroups;   // warps per dequant group
     static constexpr int kDq0 = 4;                     // first dequant warp
     static constexpr int kThreads = 32 * (kDq0 + kDqWarps + kEpiWarps);
@@ -306,10 +322,11 @@ struct RingPos {
     }
 };
 
-template <int BMT, int BNT>
-__global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
+template <int BMT, int BNT, int BKT>
+__global__ void __launch_bounds__(PfCfg<BMT, BNT, BKT>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, PfArgs a) {
-    using P = PfCfg<BMT, BNT>;
+    using P = PfCfg<BMT, BNT, BKT>;
+    constexpr int BK = P::BK, kKC = P::kKC, kBlk = P::kBlk, kXRows = P::kXRows, kUnits = P::kUnits;
     constexpr int BM = P::BM, BN = P::BN, kSzOff = P::kSzOff, kZOff = P::kZOff;
     constexpr int kSX = P::kSX, kSP = P::kSP, kSB = P::kSB, kHalves = P::kHalves, kAccBufs = P::kAccBufs;
     constexpr int kXStage = P::kXStage, kPStage = P::kPStage, kBStage = P::kBStage;
@@ -379,19 +396,21 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 const int tiles16 = min(BN / 16, NT16 - nt0);
                 const uint32_t sbytes = tiles16 * 32u, zbytes = tiles16 * 8u;
                 // group of the first 32-row block and the blocks left in it (itself included)
-                int gcur = (2 * kbeg) / a.bpg, left = a.bpg - (2 * kbeg - gcur * a.bpg);
+                int gcur = (kBlk * kbeg) / a.bpg, left = a.bpg - (kBlk * kbeg - gcur * a.bpg);
                 for (int kb = kbeg; kb < kend; ++kb) {
                     if (aborted(abort_flag)) { ok = false; break; }
                     if (!mbar_wait(emptyP(r.s), r.ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
-                    if (left == 0) { ++gcur; left = a.bpg; }
-                    const int g_first = gcur;
-                    --left;
-                    if (left == 0) { ++gcur; left = a.bpg; }
-                    --left;
+                    int g_first = gcur;
+#pragma unroll
+                    for (int b = 0; b < kBlk; ++b) {
+                        if (left == 0) { ++gcur; left = a.bpg; }
+                        if (b == 0) g_first = gcur;
+                        --left;
+                    }
                     const int ng = gcur - g_first + 1;
                     const uint32_t st = base + kRingP + r.s * kPStage;
-                    mbar_arrive_expect_tx(fullP(r.s), BN * 32u + ng * (sbytes + zbytes));
-                    tma_load_2d(st, &tmW, fullP(r.s), kb * 128, nt0);
+                    mbar_arrive_expect_tx(fullP(r.s), BN * 32u * kKC + ng * (sbytes + zbytes));
+                    tma_load_2d(st, &tmW, fullP(r.s), kb * 128 * kKC, nt0);
                     for (int gi = 0; gi < ng; ++gi) {
                         const size_t gr = static_cast<size_t>(g_first + gi);
                         bulk_load(st + kSzOff + gi * P::kSGroup, a.s2 + (gr * NT16 + nt0) * 8, sbytes, fullP(r.s));
@@ -420,7 +439,9 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     if (aborted(abort_flag)) { ok = false; break; }
                     if (!mbar_wait(emptyX(r.s), r.ph ^ 1)) { fail(a.status, 0x10, abort_flag); ok = false; break; }
                     mbar_arrive_expect_tx(fullX(r.s), static_cast<uint32_t>(kXStage));
-                    tma_load_2d(base + r.s * kXStage, &tmA, fullX(r.s), kb * BK, m0);
+#pragma unroll
+                    for (int j = 0; j < kKC; ++j)
+                        tma_load_2d(base + r.s * kXStage + j * kXRows * 128, &tmA, fullX(r.s), kb * BK + j * 64, m0);
                     ++issued;
                     r.next(kSX);
                 }
@@ -473,8 +494,8 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                     for (int kk = 0; kk < BK / 16; ++kk)
 #pragma unroll
                         for (int hm = 0; hm < kHalves; ++hm)    // rows 128*hm.. of the x tile, same B tile
-                            umma_f16(d + hm * BN, da + ((hm * 16384 + kk * 32) >> 4), db + ((kk * 32) >> 4), idesc,
-                                     (kb != kbeg) || (kk != 0));
+                            umma_f16(d + hm * BN, da + ((hm * 16384 + (kk / 4) * kXRows * 128 + (kk % 4) * 32) >> 4),
+                                     db + (((kk / 4) * BN * 128 + (kk % 4) * 32) >> 4), idesc, (kb != kbeg) || (kk != 0));
                     umma_commit(emptyX(rx.s));
                     umma_commit(emptyB(rb.s));
                 }
@@ -505,17 +526,19 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         const int ls = 4 * gq + tq;
         const uint32_t sw0 = static_cast<uint32_t>((tq ^ gq) << 4);
         const uint32_t sw1 = static_cast<uint32_t>(((4 + tq) ^ gq) << 4);
-        // one n16 tile of a stage: the constants of the stage's one or two
-        // groups, the words, and the scaled fp16 pairs (four 16-byte vectors)
-        auto dequant_tile = [&](const uint8_t *st, int nt, int g0, bool gl1, uint4 (&bv)[4]) {
+        // one n16 tile and 64-row chunk kc of a stage: the constants of the
+        // chunk's one or two groups (global group g0, stage slot s0; gl1: the
+        // second 32-row block starts the next group), the words, and the
+        // scaled fp16 pairs (four 16-byte vectors)
+        auto dequant_tile = [&](const uint8_t *st, int nt, int kc, int g0, int s0, bool gl1, uint4 (&bv)[4]) {
             const uint8_t *sz = st + kSzOff;
             uint32_t c_s[2][2], c_nl[2][2], c_nh[2][2];   // [group slot][column gq / gq+8]
 #pragma unroll
             for (int gl = 0; gl < 2; ++gl) {
                 if (gl == 1 && !gl1) break;
                 const int g = g0 + gl;
-                const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + gl * P::kSGroup + (nt * 8 + gq) * 4);
-                const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + gl * P::kZGroup + nt * 8);
+                const uint32_t sp = *reinterpret_cast<const uint32_t *>(sz + (s0 + gl) * P::kSGroup + (nt * 8 + gq) * 4);
+                const uint2 zw = *reinterpret_cast<const uint2 *>(sz + kZOff + (s0 + gl) * P::kZGroup + nt * 8);
                 c_s[gl][0] = __byte_perm(sp, sp, 0x1010);
                 c_s[gl][1] = __byte_perm(sp, sp, 0x3232);
                 // effective zero points minus one (stored + zero offset - 1)
@@ -527,7 +550,7 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                 c_nl[gl][1] = neg_zlo(z1);
                 c_nh[gl][1] = neg_zhi(z1);
             }
-            const uint4 wv = *reinterpret_cast<const uint4 *>(st + (nt * 32 + ls) * 16);
+            const uint4 wv = *reinterpret_cast<const uint4 *>(st + ((nt * kKC + kc) * 32 + ls) * 16);
             const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -546,18 +569,19 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
         PfUnit un;
         for (int ui = 0; ok && pf_unit(a, KB, ui, un); ++ui) {
             const int kbeg = un.kb0, kend = un.kb1;
-            int left = 0;                             // 32-row blocks left in the current group
-            int gcur = 0;                             // group of the stage's first block
+            // group of the unit's first 32-row block (a slice may start inside a
+            // group) and the blocks left in it, itself included
+            int gcur = (kBlk * kbeg) / a.bpg, left = a.bpg - (kBlk * kbeg - gcur * a.bpg);
             for (int kb = kbeg; kb < kend; ++kb, ++si) {
-                if (left == 0 || kb == kbeg) {        // a slice may start inside a group
-                    gcur = kb == kbeg ? (2 * kbeg) / a.bpg : gcur + 1;
-                    left = kb == kbeg ? a.bpg - (2 * kbeg - gcur * a.bpg) : a.bpg;
+                // the stage's first group and each block's group slot (as the producer loads them)
+                int g_first = gcur, gsl[kBlk];
+#pragma unroll
+                for (int b = 0; b < kBlk; ++b) {
+                    if (left == 0) { ++gcur; left = a.bpg; }
+                    if (b == 0) g_first = gcur;
+                    gsl[b] = gcur - g_first;
+                    --left;
                 }
-                --left;
-                const bool gl1 = left == 0;           // the second block starts a new group
-                const int g0 = gcur;
-                if (gl1) left = a.bpg;
-                --left;
                 if (si % kDqGroups == grp) {
                     if (aborted(abort_flag)) { ok = false; break; }
                     // The B slot is freed only when the MMAs of the stage kSB back
@@ -570,9 +594,12 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                         break;
                     }
                     const uint8_t *st = sbase + kRingP + rp.s * kPStage;
-                    uint4 bv[kDqGroups][4];
+                    uint4 bv[kUnits][4];
 #pragma unroll
-                    for (int i = 0; i < kDqGroups; ++i) dequant_tile(st, kDqGroups * wg + i, g0, gl1, bv[i]);
+                    for (int u = 0; u < kUnits; ++u) {
+                        const int nt = BK == 128 ? wg : kDqGroups * wg + u, kc = BK == 128 ? u : 0;
+                        dequant_tile(st, nt, kc, g_first + gsl[2 * kc], gsl[2 * kc], gsl[2 * kc + 1] != gsl[2 * kc], bv[u]);
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(emptyP(rp.s));   // every value read from it is in registers
                     if (!mbar_wait(emptyB(rb.s), rb.ph ^ 1)) {
@@ -581,17 +608,17 @@ __global__ void __launch_bounds__(PfCfg<BMT, BNT>::kThreads, 1)
                         break;
                     }
 #pragma unroll
-                    for (int i = 0; i < kDqGroups; ++i) {
-                        uint8_t *brow = sbase + kRingB + rb.s * kBStage + 2 * (kDqGroups * wg + i) * 1024 + gq * 128;
+                    for (int u = 0; u < kUnits; ++u) {
+                        const int nt = BK == 128 ? wg : kDqGroups * wg + u, kc = BK == 128 ? u : 0;
+                        uint8_t *brow = sbase + kRingB + rb.s * kBStage + kc * BN * 128 + 2 * nt * 1024 + gq * 128;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            *reinterpret_cast<uint4 *>(brow + (j & 1) * 1024 + ((j >> 1) ? sw1 : sw0)) = bv[i][j];
+                            *reinterpret_cast<uint4 *>(brow + (j & 1) * 1024 + ((j >> 1) ? sw1 : sw0)) = bv[u][j];
                     }
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(fullB(rb.s));
                 }
-                if (gl1) ++gcur;                      // that group continues into the next stage
                 rp.next(kSP);
                 rb.next(kSB);
             }
@@ -833,22 +860,25 @@ int sm_count() {
 }
 
 
-template <int BM, int BN>
+template <int BM, int BN, int BKS>
 cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets,
                                 const uint16_t *x, int M, uint16_t *out, cudaStream_t s) {
-    using P = PfCfg<BM, BN>;
+    using P = PfCfg<BM, BN, BKS>;
+    // 128-row stages load 64 rows of x: M <= 64 only; their k blocks are whole
+    if ((BKS == 128 && M > P::kXRows) || h.K % BKS) return cudaErrorInvalidValue;
     CUtensorMap tmA, tmW;
     cudaError_t e;
     const int KC = h.K / 64;
-    if ((e = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, h.K, M, static_cast<uint64_t>(h.K) * 2, BK, BM,
+    if ((e = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, h.K, M, static_cast<uint64_t>(h.K) * 2, 64, P::kXRows,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
         return e;
     if ((e = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, h.wp, static_cast<uint64_t>(KC) * 128, h.N / 16,
-                       static_cast<uint64_t>(KC) * 512, 128, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+                       static_cast<uint64_t>(KC) * 512, 128 * P::kKC, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+        cudaSuccess)
         return e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = dyn_smem_optin(reinterpret_cast<const void *>(prefill_kernel<BM, BN>), dev, P::kSmem, nullptr)) !=
+    if ((e = dyn_smem_optin(reinterpret_cast<const void *>(prefill_kernel<BM, BN, BKS>), dev, P::kSmem, nullptr)) !=
         cudaSuccess)
         return e;
     PfArgs args{M, h.N, h.K, h.bias, out, h.status, h.s2, h.zeros, h.geff / 32, (M + BM - 1) / BM,
@@ -865,7 +895,7 @@ cudaError_t launch_prefill_tile(const HandleView &h, const PrefillPlan &p, float
     at.val.cooperative = 1;
     cfg.attrs = &at;
     cfg.numAttrs = p.sk ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<BM, BN>, tmA, tmW, args);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<BM, BN, BKS>, tmA, tmW, args);
 }
 
 }  // namespace
@@ -886,8 +916,7 @@ PrefillPlan plan_prefill(int M, int K, int N, int sms) {
     const long long c = sms > 0 ? sms : sm_count();
     const long long n256 = (N + 255) / 256;
     const long long t256x256 = static_cast<long long>((M + 255) / 256) * n256;
-    const int KB = K / BK;
-    p.bm = 256, p.bn = 256;
+    p.bm = 256, p.bn = 256, p.bk = 64;
     // whole 256 x 256 tiles round robin while the rounds are at least three
     // quarters full; stream-K when the last round would leave SMs idle
     // (8192 x 10240 at M = 1024: 160 tiles, 186 -> 134 us; at M = 2048: 293
@@ -897,18 +926,23 @@ PrefillPlan plan_prefill(int M, int K, int N, int sms) {
     // up to 128 rows: one 128-row tile holds them all (256-row MMAs would
     // spend half or more of the tensor pipe on rows that do not exist)
     if (M <= 128) p.bm = 128;
+    // up to 64 rows: 128-row stages (twice the weights per stage hand-off;
+    // x tiles of 64 rows leave the shared memory for it)
+    if (M <= Q4_PF_BK128_MAXM && K % 128 == 0) p.bk = 128;
     const long long tiles = static_cast<long long>((M + p.bm - 1) / p.bm) * n256;
+    // the split is decided in 64-row blocks, the work walked in stages
+    const int KB64 = K / 64, KB = K / p.bk;
     const long long W = tiles * KB;
     p.sk = 1;
-    if (c / tiles >= 2 && KB / 2 >= 8) {
+    if (c / tiles >= 2 && KB64 / 2 >= 8) {
         int S = static_cast<int>(std::min<long long>(8, c / tiles));
-        while (S > 2 && KB / S < 8) --S;
+        while (S > 2 && KB64 / S < 8) --S;
         p.grid = static_cast<int>(tiles) * S;
     } else {
         // (measured against round robin over 128-row tiles, the choice before
         // stream-K: 1.4x-1.9x faster on 8192 x 28672 at M <= 256, 8192 x 10240
         // and 4096 x 11008 at M = 512, the same elsewhere)
-        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(c, W / 8)));
+        p.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(c, tiles * KB64 / 8)));
         p.fin0 = 1;
     }
     auto owner = [&](long long w) { return static_cast<int>(((w + 1) * p.grid - 1) / W); };
@@ -925,8 +959,9 @@ PrefillPlan plan_prefill(int M, int K, int N, int sms) {
 cudaError_t launch_prefill(const HandleView &h, const PrefillPlan &p, float *ws, int *tickets, const uint16_t *x,
                            int M, uint16_t *out, cudaStream_t s) {
     if (p.bn != 256) return cudaErrorInvalidValue;
-    if (p.bm == 128) return launch_prefill_tile<128, 256>(h, p, ws, tickets, x, M, out, s);
-    return launch_prefill_tile<256, 256>(h, p, ws, tickets, x, M, out, s);
+    if (p.bm == 128 && p.bk == 128) return launch_prefill_tile<128, 256, 128>(h, p, ws, tickets, x, M, out, s);
+    if (p.bm == 128) return launch_prefill_tile<128, 256, 64>(h, p, ws, tickets, x, M, out, s);
+    return launch_prefill_tile<256, 256, 64>(h, p, ws, tickets, x, M, out, s);
 }
 
 // Rows from which the fused prefill beats the decode kernels, measured on

@@ -296,11 +296,12 @@ int gptq_q4_debug_wait_probe(int *status, unsigned limit_us, cudaStream_t stream
 /* Test hook, host only (no device call): the work split that the fused
  * prefill ("Inference Backends", "How AUTO selection works": the prefill
  * path for larger M) plans for an M x K x N call on a GPU with `sms` SMs.
- * out[0..5] (caller-owned host ints) = tile rows BM, tile columns BN,
+ * out[0..6] (caller-owned host ints) = tile rows BM, tile columns BN,
  * stream-K (1) or whole tiles round robin (0), CTAs of the stream-K launch
- * (0 for round robin), the most pieces any tile is cut into, and whether
- * each cut tile is finished by the CTA holding its first k blocks (1) or by
- * every piece's CTA, a share of the rows each (0).  Errors: INVALID_ARGUMENT
+ * (0 for round robin), the most pieces any tile is cut into, whether each
+ * cut tile is finished by the CTA holding its first k blocks (1) or by every
+ * piece's CTA, a share of the rows each (0), and the rows of K per pipeline
+ * stage (64, or 128).  Errors: INVALID_ARGUMENT
  * (NULL out, M < 1, K or N not a positive multiple of 64, sms < 1). */
 int gptq_q4_debug_prefill_plan(int M, int K, int N, int sms, int *out);
 

@@ -32,13 +32,14 @@ def plan(q4, M, K, N, sms=SMS):
     (512, 4096, 4096, dict(bm=256, stream_k=1, grid=128, max_pieces=4, piece0_finishes=0)),
     (1024, 4096, 4096, dict(bm=256, stream_k=1, grid=128, max_pieces=2, piece0_finishes=0)),
     (512, 11008, 4096, dict(bm=256, stream_k=1, grid=128, max_pieces=4, piece0_finishes=0)),
-    (64, 28672, 8192, dict(bm=128, stream_k=1, grid=128, max_pieces=4, piece0_finishes=0)),
+    (64, 28672, 8192, dict(bm=128, stream_k=1, grid=128, max_pieces=4, piece0_finishes=0, stage_rows=128)),
     # stream-K ranges, one per SM: piece 0's CTA finishes each cut tile
     (512, 4096, 11008, dict(bm=256, stream_k=1, grid=SMS, piece0_finishes=1)),
     (1024, 8192, 10240, dict(bm=256, stream_k=1, grid=SMS, piece0_finishes=1)),
     (2048, 8192, 10240, dict(bm=256, stream_k=1, grid=SMS, piece0_finishes=1)),   # 320 tiles, rounds 70 % full
-    (64, 8192, 28672, dict(bm=128, stream_k=1, grid=SMS, piece0_finishes=1)),
-    (256, 8192, 28672, dict(bm=256, stream_k=1, grid=SMS, piece0_finishes=1)),
+    (64, 8192, 28672, dict(bm=128, stream_k=1, grid=SMS, piece0_finishes=1, stage_rows=128)),
+    (100, 8192, 28672, dict(bm=128, stream_k=1, grid=SMS, piece0_finishes=1, stage_rows=64)),
+    (256, 8192, 28672, dict(bm=256, stream_k=1, grid=SMS, piece0_finishes=1, stage_rows=64)),
 ])
 def test_llama_workloads(q4, M, K, N, want):
     p = plan(q4, M, K, N)
@@ -60,6 +61,8 @@ def test_planner_invariants(q4, sms):
                 t = tiles_of(p, M, N)
                 KB = K // 64
                 assert p["bm"] == (128 if M <= 128 and p["stream_k"] else 256), (M, K, N, p)
+                # 128-row stages (x tiles of 64 rows) exactly for M <= 64 off round robin
+                assert p["stage_rows"] == (128 if p["stream_k"] and M <= 64 and K % 128 == 0 else 64), (M, K, N, p)
                 if not p["stream_k"]:
                     # round robin over 256 x 256 tiles: the rounds at least three quarters full
                     rounds = -(-t // sms)
