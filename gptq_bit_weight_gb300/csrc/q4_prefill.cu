@@ -73,9 +73,15 @@
 #ifndef Q4_PF_SP
 #define Q4_PF_SP 4
 #endif
-// most rows of x for which 128-row stages are used
+// most rows of x for which 128-row stages are used, and their x and packed rings
 #ifndef Q4_PF_BK128_MAXM
 #define Q4_PF_BK128_MAXM 64
+#endif
+#ifndef Q4_PF_SXK128
+#define Q4_PF_SXK128 2
+#endif
+#ifndef Q4_PF_SPK128
+#define Q4_PF_SPK128 3
 #endif
 
 namespace q4 {
@@ -119,8 +125,8 @@ struct PfCfg {
     static constexpr int kXRows = BK == 128 ? 64 : BM;
     static constexpr int kHalves = BM / 128;           // M = 128 MMAs per k step
     static constexpr int kAccBufs = BM == 128 ? 2 : 1; // accumulator sets (double-buffered when they fit)
-    static constexpr int kSX = BK == 128 ? 3 : (BM == 128 ? Q4_PF_SX128 : Q4_PF_SX256);   // x-tile ring (released by the MMAs)
-    static constexpr int kSP = BK == 128 ? 2 : Q4_PF_SP;   // packed-word ring (released by the dequantizers)
+    static constexpr int kSX = BK == 128 ? Q4_PF_SXK128 : (BM == 128 ? Q4_PF_SX128 : Q4_PF_SX256);   // x-tile ring (released by the MMAs)
+    static constexpr int kSP = BK == 128 ? Q4_PF_SPK128 : Q4_PF_SP;   // packed-word ring (released by the dequantizers)
     static constexpr int kSB = BK == 128 ? 2 : (BM == 128 ? Q4_PF_SB128 : Q4_PF_SB256);   // fp16 B ring
     static constexpr int kXStage = kXRows * BK * 2;    // kKC sub-tiles of kXRows x 64
     static constexpr int kMaxG = kBlk;                 // groups a stage can touch (a group is whole blocks)
