@@ -58,7 +58,10 @@ namespace q4 {
 
 namespace {
 
-constexpr int kWarps = 8;
+#ifndef Q4_SK_WARPS
+#define Q4_SK_WARPS 8
+#endif
+constexpr int kWarps = Q4_SK_WARPS;
 constexpr int kThreads = 32 * kWarps;
 // ring slots per warp (depth - 1 units in flight), a power of two: 8, or 4
 // with eight rows of x per slot (two CTAs per SM must fit in shared memory)
