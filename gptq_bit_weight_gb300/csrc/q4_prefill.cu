@@ -111,9 +111,11 @@ constexpr int kFinishMax = 3;
 // dequant warp per 16 columns); BM = 128, or 256 (two M = 128 MMAs per k step
 // on the same fp16 B tile, halving the dequantization per flop, with the one
 // accumulator pair filling tensor memory) when there are tiles enough.
-// Three rings: x tiles (BM x 64 fp16, 128-byte swizzle), packed-word stages
-// {packed words BN*32 B, scale pairs of up to two groups (BN*2 B each), their
-// zero words (BN/2 B each)}, and fp16 B tiles (K-major, 128-byte swizzle).
+// Three rings, per stage of BK rows of K (64, or 128 up to 64 rows of x): x
+// tiles (BM x 64 fp16 per 64-row chunk, 128-byte swizzle), packed-word stages
+// {packed words BN*32 B per chunk, scale pairs of up to BK/32 groups (BN*2 B
+// each), their zero words (BN/2 B each)}, and fp16 B tiles (K-major, 128-byte
+// swizzle, one BN x 64 sub-tile per chunk).
 template <int BM_, int BN_, int BK_ = 64>
 struct PfCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_;
